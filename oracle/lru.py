@@ -1,0 +1,150 @@
+"""Global LRU expert-cache simulator: which (layer, expert) keys hit, miss, get bypassed,
+and which GPU slot each resident key occupies.
+
+What the pages fix: during decode "a shared LRU expert cache spanning all MoE layers
+follows the router instead of a placement frozen at load time" ([MTP] §Three mechanisms,
+semantic-aware caching); the cache starts cold ("the first request is served with a cold
+cache") and is rebuilt under a revised VRAM budget at safe points without reloading the
+host pool ([MTP] §Three mechanisms, elastic memory management); the measured quantity is
+the fraction of "decode-time expert reads" that miss ([MTP] §Results; [LN]).
+
+Readings taken where the pages are silent (each is listed in the design doc):
+
+* key = (layer, expert); one global recency order over all keys of all layers;
+* the unit of counting is one unique key per forward call (the call's set S, ascending);
+* phase 1: every resident key of S is a hit and moves to MRU, in ascending expert order;
+* phase 2: each non-resident key of S, in ascending expert order, is a miss. It takes the
+  lowest-index free slot if one exists; otherwise it evicts the least recently used
+  resident key that is NOT in S and takes its slot; the new key goes to MRU. If every
+  resident key is in S (|S| > capacity), the miss is BYPASSED: computed from a staging
+  copy, not inserted, state unchanged;
+* resize to C': keep the min(C', resident) most recently used keys, in order. A survivor
+  whose slot is < C' keeps it; the others move, in ascending old-slot order, to the lowest
+  free slots < C'. Growth only adds free slots.
+
+Pins (tests/test_oracle_lru.py): hand-traced sequences (tests/golden/lru_*.txt), textbook
+LRU via functools.lru_cache on single-key calls, compulsory-miss-only behaviour when the
+capacity covers the pool, total bypass at capacity 0, and bijection/size invariants.
+"""
+import heapq
+from collections import OrderedDict
+
+
+class CallResult:
+    """Outcome of one forward call's cache step."""
+
+    __slots__ = ("hits", "misses", "bypassed", "evicted", "slot_of")
+
+    def __init__(self):
+        self.hits = []        # expert ids (ascending) resident at call start
+        self.misses = []      # [(expert, slot)] filled into a slot, ascending expert
+        self.bypassed = []    # expert ids computed from staging, ascending
+        self.evicted = []     # [(old_key, slot)] in the order the evictions happened
+        self.slot_of = {}     # expert -> slot for hits and filled misses
+
+
+class LRUCache:
+    """List-based simulator. Keys are ints key = layer * experts + expert."""
+
+    def __init__(self, capacity, experts):
+        if capacity < 0:
+            raise ValueError("capacity must be >= 0")
+        self.capacity = int(capacity)
+        self.experts = int(experts)
+        self.order = OrderedDict()            # key -> slot, least recent first
+        self.key_of_slot = [None] * self.capacity
+        self.free = list(range(self.capacity))   # min-heap of free slot indices
+        self.stats = dict(calls=0, hits=0, misses=0, bypassed=0, evictions=0)
+
+    # -- queries -----------------------------------------------------------------------
+    def resident(self):
+        return len(self.order)
+
+    def slot_of_key(self, key):
+        return self.order.get(key, -1)
+
+    def lru_keys(self):
+        """Resident keys from least to most recently used."""
+        return list(self.order.keys())
+
+    # -- one forward call ----------------------------------------------------------------
+    def call(self, layer, experts):
+        """Apply one forward call of ``layer`` that selected ``experts`` (any order/dups)."""
+        S = sorted(set(int(e) for e in experts))
+        keys = {e: layer * self.experts + e for e in S}
+        in_S = set(keys.values())
+        res = CallResult()
+        # phase 1: hits move to MRU in ascending expert order
+        for e in S:
+            key = keys[e]
+            if key in self.order:
+                slot = self.order.pop(key)
+                self.order[key] = slot
+                res.hits.append(e)
+                res.slot_of[e] = slot
+        # phase 2: misses in ascending expert order
+        for e in S:
+            key = keys[e]
+            if e in res.slot_of:
+                continue
+            slot = self._free_slot()
+            if slot is None:
+                victim = None
+                for k in self.order:          # least recent first
+                    if k not in in_S:
+                        victim = k
+                        break
+                if victim is None:
+                    res.bypassed.append(e)
+                    continue
+                slot = self.order.pop(victim)
+                res.evicted.append((victim, slot))
+            self.order[key] = slot
+            self.key_of_slot[slot] = key
+            res.misses.append((e, slot))
+            res.slot_of[e] = slot
+        st = self.stats
+        st["calls"] += 1
+        st["hits"] += len(res.hits)
+        st["misses"] += len(res.misses) + len(res.bypassed)
+        st["bypassed"] += len(res.bypassed)
+        st["evictions"] += len(res.evicted)
+        return res
+
+    def _free_slot(self):
+        """Lowest-index free slot, or None."""
+        return heapq.heappop(self.free) if self.free else None
+
+    # -- resize at a safe point ----------------------------------------------------------
+    def resize(self, new_capacity):
+        new_capacity = int(new_capacity)
+        if new_capacity < 0:
+            raise ValueError("capacity must be >= 0")
+        keep = list(self.order.items())[max(0, len(self.order) - new_capacity):]
+        new_slot = {}
+        taken = set()
+        for key, slot in keep:
+            if slot < new_capacity:
+                new_slot[key] = slot
+                taken.add(slot)
+        movers = sorted((slot, key) for key, slot in keep if slot >= new_capacity)
+        free = [s for s in range(new_capacity) if s not in taken]
+        for (old_slot, key), s in zip(movers, free):
+            new_slot[key] = s
+        self.capacity = new_capacity
+        self.key_of_slot = [None] * new_capacity
+        self.order = OrderedDict()
+        for key, _ in keep:
+            self.order[key] = new_slot[key]
+            self.key_of_slot[new_slot[key]] = key
+        self.free = [s for s in range(new_capacity) if self.key_of_slot[s] is None]
+        heapq.heapify(self.free)
+        return new_slot
+
+    def snapshot(self, num_keys):
+        """(slot_of_key [num_keys], lru_keys [capacity] least->most recent, -1 padded)."""
+        slot_of_key = [-1] * num_keys
+        for key, slot in self.order.items():
+            slot_of_key[key] = slot
+        lru = self.lru_keys()
+        return slot_of_key, lru + [-1] * (self.capacity - len(lru))

@@ -1,0 +1,138 @@
+"""Pins for the oracle's global-LRU simulator (CPU only)."""
+import functools
+import os
+
+import numpy as np
+import pytest
+
+from oracle.lru import LRUCache
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "lru_hand_traces.txt")
+
+
+def _ints(s):
+    return [int(v) for v in s.split(",") if v.strip() != ""]
+
+
+def _pairs(s):
+    out = []
+    for item in s.split(","):
+        item = item.strip()
+        if item:
+            a, b = item.split(":")
+            out.append((int(a), int(b)))
+    return out
+
+
+def _field(part):
+    return part.split("=", 1)[1].strip()
+
+
+def _load_traces():
+    traces, cur = [], None
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("trace"):
+            _, name, cap, exp = line.split()
+            cur = dict(name=name, capacity=int(cap.split("=")[1]),
+                       experts=int(exp.split("=")[1]), ops=[])
+            traces.append(cur)
+        else:
+            cur["ops"].append(line)
+    return traces
+
+
+@pytest.mark.parametrize("trace", _load_traces(), ids=lambda t: t["name"])
+def test_hand_traces(trace):
+    c = LRUCache(trace["capacity"], trace["experts"])
+    for op in trace["ops"]:
+        if op.startswith("resize"):
+            c.resize(int(op.split()[1]))
+        elif op.startswith("call"):
+            head, hits, misses, byp, ev = [p.strip() for p in op.split("|")]
+            _, layer, S = head.split()
+            r = c.call(int(layer), _ints(S))
+            assert r.hits == _ints(_field(hits)), op
+            assert r.misses == _pairs(_field(misses)), op
+            assert r.bypassed == _ints(_field(byp)), op
+            assert r.evicted == _pairs(_field(ev)), op
+        elif op.startswith("final"):
+            slots, lru, counts = [p.strip() for p in op.split("|")]
+            E, C = trace["experts"], c.capacity
+            num_keys = 16 * E
+            want_slots = dict(_pairs(_field(slots)))
+            slot_of_key, lru_keys = c.snapshot(num_keys)
+            assert {k: s for k, s in enumerate(slot_of_key) if s >= 0} == want_slots
+            assert lru_keys == _ints(_field(lru)) + [-1] * (C - len(_ints(_field(lru))))
+            for kv in counts.split():
+                k, v = kv.split("=")
+                assert c.stats[k] == int(v), (k, c.stats)
+
+
+def test_single_key_calls_match_textbook_lru():
+    """With one key per call, the policy is textbook LRU: compare with functools.lru_cache."""
+    rng = np.random.default_rng(7)
+    for C in (0, 1, 3, 10):
+        keys = rng.integers(0, 24, size=2000)
+        seen = []
+
+        @functools.lru_cache(maxsize=C)
+        def touch(k):
+            seen.append(k)
+            return k
+
+        c = LRUCache(C, 24)
+        for k in keys:
+            touch(int(k))
+            c.call(0, [int(k)])
+        info = touch.cache_info()
+        assert c.stats["hits"] == info.hits
+        assert c.stats["misses"] == info.misses
+
+
+def test_compulsory_misses_only_when_capacity_covers_pool():
+    L, E = 3, 16
+    rng = np.random.default_rng(3)
+    c = LRUCache(L * E, E)
+    touched = set()
+    for step in range(200):
+        layer = step % L
+        S = rng.choice(E, size=rng.integers(1, 8), replace=False)
+        r = c.call(layer, S)
+        for e in S:
+            key = layer * E + int(e)
+            if key in touched:
+                assert e in r.hits
+            else:
+                assert (int(e), c.slot_of_key(key)) in r.misses
+            touched.add(key)
+    assert c.stats["misses"] == len(touched)
+    assert c.stats["evictions"] == 0 and c.stats["bypassed"] == 0
+
+
+def test_invariants_random():
+    rng = np.random.default_rng(11)
+    L, E = 2, 32
+    for C in (0, 1, 5, 17, 40):
+        c = LRUCache(C, E)
+        for step in range(300):
+            layer = int(rng.integers(0, L))
+            S = sorted(set(int(e) for e in rng.integers(0, E, size=rng.integers(1, 24))))
+            before = c.resident()
+            r = c.call(layer, S)
+            assert len(r.hits) + len(r.misses) + len(r.bypassed) == len(S)
+            assert c.resident() <= C
+            assert c.resident() == min(C, before + len(r.misses))
+            slots = [s for s in c.order.values()]
+            assert len(set(slots)) == len(slots) and all(0 <= s < C for s in slots)
+            for key, s in c.order.items():
+                assert c.key_of_slot[s] == key
+            # bypass only when every resident key is in S
+            if r.bypassed:
+                assert all(k // E == layer and k % E in S for k in c.order)
+            if step == 150 and C > 2:
+                c.resize(C // 2)
+                C = C // 2
+                assert c.resident() <= C
