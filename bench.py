@@ -1,0 +1,369 @@
+"""Benchmark: MoE-layer decode tokens/s through the GPU expert cache (libftmoe, sm_103a).
+
+Workload (default): the 35B-A3B-shaped decode layer — hidden 2048, 128 experts, expert
+intermediate 768, top-8, BF16 weights, 1..16 tokens per step (seeded length mix),
+Zipf(1.1) expert popularity with 0.6 step-to-step reuse, one LRU cache holding 37% of the
+pool (47 slots); the pool sits in pinned host memory and misses are filled over PCIe.
+
+One step = one forward call of the layer on one decode step of the trace: top-k, cache
+lookup + LRU update, expert FFN on resident experts, miss fills (copy stream), expert FFN
+on filled / staged experts, combine. Inputs (x, logits of every timed step) are resident in
+HBM before timing starts; L2 is flushed (256 MB write) before every step, outside the
+per-step CUDA-event bracket.
+
+Usage:
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (no data-path collective).
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+WORKLOAD = "decode_bf16"
+REF_TOKENS = 2          # tokens per step the CPU reference arm computes (bounded sample)
+METRIC = "MoE-layer decode tokens/s (35B-A3B-shaped BF16 layer, LRU cache 37% of pool)"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, path):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q, "--format=csv,noheader",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx = float(parts[2].split()[0])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return {}
+
+
+def oracle_baseline(cfg, pool_arr, budget_s=15.0, max_steps=64):
+    """The oracle as it stands on this host's cores: LRU simulator + fp64 MoE layer over the
+    first steps of the same trace until ~budget_s of CPU work."""
+    import workloads as W
+    from oracle import formats, lru, moe
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = 1
+    P = pool_arr.shape[0]
+    sim = lru.LRUCache(W.cache_capacity(cfg), cfg.experts)
+    tokens, steps = 0, 0
+    t0 = time.perf_counter()
+    for step in W.decode_trace(cfg, steps=max_steps):
+        d = step[0]
+        idx = moe.topk(d["logits"], cfg.top_k)
+        w = moe.gate_weights(d["logits"], idx)
+        sim.call(0, idx.reshape(-1))
+        moe.layer_forward(formats.bf16_to_f64(d["x"]), idx, w,
+                          lambda e: formats.decode_blob(pool_arr[e % P], cfg.fmt, cfg.hidden,
+                                                        cfg.inter))
+        tokens += d["T"]
+        steps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": int(threads), "kind": "oracle",
+            "sample": "first %d steps (%d tokens) of the same seeded trace, fp64 numpy oracle + "
+                      "LRU simulator" % (steps, tokens)}, tokens, dt
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import workloads as W
+    cfg = W.config(WORKLOAD)
+    pool = W.expert_pool(cfg)
+    from oracle import formats, lru, moe
+    sim = lru.LRUCache(W.cache_capacity(cfg), cfg.experts)
+    tr = W.decode_trace(cfg, steps=args.warmup + args.steps)
+    times, toks = [], []
+    for i, step in enumerate(tr):
+        d = step[0]
+        n = min(d["T"], REF_TOKENS)     # bounded sample: the step's first tokens
+        t0 = time.perf_counter()
+        idx = moe.topk(d["logits"], cfg.top_k)
+        w = moe.gate_weights(d["logits"], idx)
+        sim.call(0, idx.reshape(-1))
+        moe.layer_forward(formats.bf16_to_f64(d["x"][:n]), idx[:n], w[:n],
+                          lambda e: formats.decode_blob(pool[e], cfg.fmt, cfg.hidden, cfg.inter))
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            toks.append(n)
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = 1
+    value = sum(toks) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "hidden": cfg.hidden, "experts": cfg.experts,
+                   "inter": cfg.inter, "top_k": cfg.top_k, "tokens_per_step": "1..16",
+                   "cache_slots": W.cache_capacity(cfg), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": int(threads),
+                         "kind": "oracle",
+                         "sample": "steps %d..%d of the seeded trace; per step the cache "
+                                   "simulator on all tokens and the fp64 layer on the first "
+                                   "min(T, %d) tokens" % (args.warmup, args.warmup + args.steps - 1,
+                                                           REF_TOKENS)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import workloads as W
+    from workloads.host import HostPool
+    from expert_cached_sparse_top_b300 import build as b
+    b.build()
+    from expert_cached_sparse_top_b300 import ftmoe
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    cfg = W.config(WORKLOAD)
+    C = W.cache_capacity(cfg)
+    pool = HostPool(cfg)
+    K, Wm = args.steps, args.warmup
+    nsteps = Wm + K
+    if nsteps > cfg.steps:
+        raise SystemExit("steps + warmup must be <= %d (trace length)" % cfg.steps)
+    trace = [st[0] for st in W.decode_trace(cfg, steps=nsteps)]
+    xs = [torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev) for d in trace]
+    ls = [torch.from_numpy(d["logits"]).to(dev) for d in trace]
+    Ts = [d["T"] for d in trace]
+    out = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def make(capacity):
+        c = ftmoe.make_config(cfg.layers, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
+                              cfg.t_max, cfg.wfmt, capacity, device=local)
+        return ftmoe.MoECache(c, pool.ptrs, None)
+
+    def timed_pass(cache, record_clocks=False):
+        for i in range(Wm):
+            cache.forward(0, xs[i], Ts[i], out, logits=ls[i], stream=stream)
+        torch.cuda.synchronize()
+        s0 = cache.stats()
+        cache.set_timing(True)
+        cache.timing(reset=True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk = Clocks(local, os.path.join(ROOT, "gpurun_out", "clocks_r%d.csv" % rank)) \
+            if record_clocks else None
+        t_wall = time.perf_counter()
+        for j in range(K):
+            i = Wm + j
+            flush.zero_()
+            evs[j][0].record(stream)
+            cache.forward(0, xs[i], Ts[i], out, logits=ls[i], stream=stream)
+            evs[j][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        clocks = clk.stop() if clk else None
+        if ws > 1:
+            dist.barrier()
+        step_ms = [a.elapsed_time(b_) for a, b_ in evs]
+        tim = cache.timing(reset=True)
+        cache.set_timing(False)
+        s1 = cache.stats()
+        return step_ms, t_wall, tim, s0, s1, clocks
+
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    cache = make(C)
+    step_ms, t_wall, tim, s0, s1, clocks = timed_pass(cache, record_clocks=True)
+    cache.close()
+    tokens = sum(Ts[Wm:])
+    dev_s = sum(step_ms) / 1e3
+    # max over ranks of the timed duration; all ranks process the same number of tokens
+    t_max = dev_s
+    if ws > 1:
+        tt = torch.tensor([dev_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = tokens * ws / t_max
+
+    # all experts resident (capacity = pool): the HBM-bound ceiling of the same step
+    cache_r = make(cfg.experts)
+    for i in range(Wm + K):   # touch every selected expert once
+        cache_r.forward(0, xs[i], Ts[i], out, logits=ls[i], stream=stream)
+    rs_ms, _, rtim, _, _, _ = timed_pass(cache_r)
+    cache_r.close()
+
+    # end to end through the C ABI with host buffers: H2D of x + logits, forward, D2H of out
+    xh = [torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory() for d in trace]
+    lh = [torch.from_numpy(d["logits"]).pin_memory() for d in trace]
+    oh = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    ld = torch.empty((cfg.t_max, cfg.experts), dtype=torch.float32, device=dev)
+    cache_e = make(C)
+    h2d = d2h = 0
+    e2e_s = 0.0
+    for i in range(Wm + K):
+        T = Ts[i]
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        xd[:T].copy_(xh[i], non_blocking=True)
+        ld[:T].copy_(lh[i], non_blocking=True)
+        cache_e.forward(0, xd, T, out, logits=ld, stream=stream)
+        oh[:T].copy_(out[:T], non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if i >= Wm:
+            e2e_s += dt
+            h2d += xh[i].numel() * 2 + lh[i].numel() * 4
+            d2h += T * cfg.hidden * 2
+    cache_e.close()
+    if ws > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    hbm = peaks.get("hbm_gbs")
+    ffn_ms = tim["ffn_hit_ms"] + tim["ffn_miss_ms"]
+    ffn_passes = tim["ffn_launches"] // 2
+    achieved = tim["ffn_weight_bytes"] / (ffn_ms * 1e-3) / 1e9 if ffn_ms > 0 else None
+    rffn_ms = rtim["ffn_hit_ms"] + rtim["ffn_miss_ms"]
+    r_achieved = rtim["ffn_weight_bytes"] / (rffn_ms * 1e-3) / 1e9 if rffn_ms > 0 else None
+    misses = s1["misses"] - s0["misses"]
+    hits = s1["hits"] - s0["hits"]
+    fill_b = (s1["fill_bytes"] - s0["fill_bytes"]) + (s1["stage_bytes"] - s0["stage_bytes"])
+    base, _, _ = oracle_baseline(cfg, pool.arr, budget_s=args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": Wm, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "hidden": cfg.hidden, "experts": cfg.experts,
+                   "inter": cfg.inter, "top_k": cfg.top_k, "tokens_per_step": "1..16 (seeded mix)",
+                   "cache_slots": C, "pool": "pinned host, %d blobs x %d B" % (cfg.keys, pool.blob_bytes),
+                   "l2": "flushed (256 MB write) before every step, outside the step's events",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "expert FFN GEMV (W13+SwiGLU, W2), per pass",
+                     "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": (achieved / hbm) if (achieved and hbm) else None,
+                     "traffic": None, "peak_source": "MEASURED_PEAKS.json hbm_gbs" if hbm else None,
+                     "algorithmic_bytes_per_launch": tim["ffn_weight_bytes"] / max(ffn_passes, 1),
+                     "avg_launch_ms": ffn_ms / max(ffn_passes, 1)},
+        "cpu_baseline": base,
+        "e2e": {"value": tokens * ws / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d // K, "d2h_bytes_per_step": d2h // K},
+        "gpu_launches": int(tim["kernel_launches"]),
+        "clocks": clocks,
+        "extras": {
+            "miss_rate": misses / max(hits + misses, 1),
+            "pcie_fill_GBps": (fill_b / (tim["fill_ms"] * 1e-3) / 1e9) if tim["fill_ms"] > 0 else None,
+            "fill_ms_per_step": tim["fill_ms"] / K,
+            "wall_ms_per_step": 1e3 * t_wall / K,
+            "all_resident_tokens_per_s": tokens / (sum(rs_ms) / 1e3),
+            "all_resident_ffn_GBps": r_achieved,
+            "all_resident_ffn_frac": (r_achieved / hbm) if (r_achieved and hbm) else None,
+            "stage_ms": {k2: tim[k2] / K for k2 in ("route_ms", "ffn_hit_ms", "fill_ms",
+                                                     "ffn_miss_ms", "combine_ms", "total_ms")},
+        },
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.steps + args.warmup > 512:
+        raise SystemExit("steps + warmup must be <= 512 (trace length)")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,93 @@
+// Internal declarations shared by the libftmoe CUDA translation units (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace ftmoe {
+
+constexpr int kMaxExperts = 1024;   // router / lookup tables are indexed per expert in smem
+constexpr int kMaxTopK = 32;        // one lane per chosen expert in the top-k warp
+
+// Per-call routing result written by the lookup kernel (device copy and host-mapped copy).
+struct RouteCounts {
+    int32_t n_unique;   // U = |S|
+    int32_t n_hits;     // entries [0, n_hits) are resident at call start
+    int32_t n_miss;     // entries [n_hits, U) are misses (filled, then bypassed)
+    int32_t n_fill;     // misses that took a slot
+    int32_t n_bypass;   // misses computed from staging
+    int32_t n_evict;    // victims that held a key
+    int32_t err;        // bit 0: NaN logit seen, bit 1: expert index out of range,
+                        // bit 2: table/slot inconsistency
+    int32_t pad;
+};
+
+// Device scratch of one forward call. Entries are the call's unique experts: hits first
+// (ascending expert id), then misses (ascending expert id).
+struct RouteBuffers {
+    RouteCounts* counts;   // dev
+    int32_t* entry_e;      // [max_u] expert id of entry u
+    int32_t* entry_dst;    // [max_u] weight location: slot (< C) or C + staging index
+    int32_t* entry_off;    // [max_u + 1] pair-list offsets
+    int32_t* pairs;        // [max_pairs] pair index p = t*k + j, grouped by entry, ascending p
+    int32_t* miss_key;     // [max_u] key of miss j (ascending expert id)
+    int32_t* miss_dst;     // [max_u] destination of miss j
+};
+
+// Host-mapped mirror of the fill list (the host issues one copy per miss).
+struct RouteHostView {
+    RouteCounts* counts;   // device-side address of the mapped struct
+    int32_t* miss_key;
+    int32_t* miss_dst;
+};
+
+struct LookupParams {
+    const int32_t* idx;    // [T*k]
+    int32_t n_pairs;       // T*k
+    int32_t layer;
+    int32_t experts;
+    int64_t capacity;      // C
+    int32_t* table;        // [L*E] slot or -1
+    int32_t* slot_key;     // [C] key or -1
+    const int32_t* order_in;   // [C] slots, least recent first
+    int32_t* order_out;        // [C]
+    int32_t* nan_flag;         // set by the top-k kernel, cleared here (may be null)
+    RouteBuffers rb;
+    RouteHostView hv;
+};
+
+// Weight-section offsets inside one expert blob.
+struct BlobLayout {
+    int64_t blob_bytes;
+    int64_t off_w13, off_w2, off_s13, off_s2, off_ts;
+};
+
+struct FfnParams {
+    const uint8_t* arena;        // slot s / staging i at arena + dst * blob_bytes
+    BlobLayout lay;
+    int32_t hidden, inter, top_k;
+    const RouteCounts* counts;
+    const int32_t* entry_dst;
+    const int32_t* entry_off;
+    const int32_t* pairs;
+    int32_t pass;                // 0: entries [0, n_hits), 1: entries [n_hits, n_unique)
+    const __nv_bfloat16* x;      // [T][H]
+    __nv_bfloat16* act;          // [T*k][I]  SwiGLU activation, bf16
+    float* y;                    // [T*k][H]  expert outputs, fp32
+};
+
+// ---- launchers (defined in route.cu / ffn.cu) ------------------------------------------
+cudaError_t launch_router_logits(const __nv_bfloat16* x, int T, int H, const float* wr, int E,
+                                 float* logits, cudaStream_t s);
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx,
+                                float* w, int32_t* idx2, float* w2, int32_t* nan_flag,
+                                cudaStream_t s);
+cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s);
+cudaError_t launch_ffn(int fmt, const FfnParams& p, int max_tokens, cudaStream_t s,
+                       int* kernels_launched);
+cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H,
+                           __nv_bfloat16* out, cudaStream_t s);
+int ffn_supported(int fmt, int hidden, int inter);
+
+}  // namespace ftmoe

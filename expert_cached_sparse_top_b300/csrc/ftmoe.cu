@@ -1,0 +1,723 @@
+// Host runtime of libftmoe: the C ABI declared in include/ftmoe.h.
+//
+// One handle owns, on one device:
+//   - the slot arena: C cache slots followed by staging slots (one expert blob each);
+//   - the global LRU state: table[key] -> slot, slot_key[slot] -> key, and the recency
+//     order of slots (two buffers, the lookup kernel reads one and writes the other);
+//   - per-call scratch (logits, top-k, entry lists, SwiGLU activations, expert outputs);
+//   - a copy stream for miss fills and a host-mapped buffer the lookup kernel writes the
+//     miss list into.
+// "Meet FreeToken: An Edge-Native MoE Serving Engine ..." (MarkTechPost), section "Three
+// mechanisms": decode uses one LRU across all MoE layers; experts live in pinned host memory
+// in their final layout and enter the GPU on demand; the cache is rebuilt under a new
+// budget at safe points without reloading the host pool; the first request is served cold.
+#include "common.cuh"
+#include "../../include/ftmoe.h"
+
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace ftmoe;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+struct StageEvents {
+    cudaEvent_t ev[8];
+    bool has_fill;
+    bool has_miss;
+    cudaEvent_t fill_begin, fill_end;
+};
+
+}  // namespace
+
+struct ft_moe {
+    ft_moe_config cfg{};
+    int dev = 0;
+    size_t blob_bytes = 0;
+    BlobLayout lay{};
+    int32_t max_u = 0, max_pairs = 0;
+    std::vector<const uint8_t*> blobs;
+    std::vector<void*> pinned;            // ranges registered by this handle
+
+    float* d_router = nullptr;            // [L][E][H]
+    uint8_t* d_arena = nullptr;           // (C + n_stage) blobs
+    int64_t C = 0, n_stage = 0;
+    int32_t* d_table = nullptr;           // [L*E]
+    int32_t* d_slot_key = nullptr;        // [C]
+    int32_t* d_order[2] = {nullptr, nullptr};
+    int cur = 0;
+
+    float* d_logits = nullptr;            // [max_tokens][E]
+    int32_t* d_idx = nullptr;             // [max_pairs]
+    float* d_w = nullptr;                 // [max_pairs]
+    int32_t* d_nan = nullptr;
+    RouteBuffers rb{};
+    uint8_t* d_route_mem = nullptr;
+    __nv_bfloat16* d_act = nullptr;       // [max_pairs][I]
+    float* d_y = nullptr;                 // [max_pairs][H]
+
+    uint8_t* h_mapped = nullptr;          // host-mapped RouteCounts + miss lists
+    RouteHostView hv_dev{};
+    RouteCounts* h_counts = nullptr;
+    int32_t* h_miss_key = nullptr;
+    int32_t* h_miss_dst = nullptr;
+
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_done = nullptr;
+
+    ft_cache_stats_t stats{};
+    bool broken = false;
+    std::string err;
+    int fault_fill = 0, fault_alloc = 0;
+    int64_t wait_ms = 20000;
+
+    bool timing = false;
+    std::vector<StageEvents> pending;
+    std::vector<cudaEvent_t> event_pool;
+    ft_timing_t tsum{};
+};
+
+namespace {
+
+ft_status fail(ft_moe* h, ft_status s, const std::string& msg) {
+    if (h) h->err = msg; else g_create_error = msg;
+    return s;
+}
+
+ft_status cuda_fail(ft_moe* h, cudaError_t e, const char* where) {
+    std::string m = std::string(where) + ": " + cudaGetErrorString(e);
+    return fail(h, e == cudaErrorMemoryAllocation ? FT_ERR_OOM : FT_ERR_CUDA, m);
+}
+
+#define FT_CUDA(h, call)                                                  \
+    do {                                                                  \
+        cudaError_t e_ = (call);                                          \
+        if (e_ != cudaSuccess) return cuda_fail((h), e_, #call);          \
+    } while (0)
+
+bool valid_config(const ft_moe_config* c, std::string* why) {
+    if (!c) { *why = "null config"; return false; }
+    if (c->layers < 1 || c->experts < 1 || c->experts > kMaxExperts) { *why = "layers/experts out of range"; return false; }
+    if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->experts) { *why = "top_k out of range"; return false; }
+    if (c->max_tokens < 1) { *why = "max_tokens must be >= 1"; return false; }
+    if (c->wfmt < 0 || c->wfmt > 2) { *why = "unknown weight format"; return false; }
+    if (!ffn_supported(c->wfmt, c->hidden, c->inter)) { *why = "hidden/inter must be positive multiples of 64"; return false; }
+    if (c->cache_slots < 0 || c->cache_slots > (int64_t)c->layers * c->experts * 4 + 1024) { *why = "cache_slots out of range"; return false; }
+    if ((int64_t)c->layers * c->experts >= (1LL << 31)) { *why = "too many keys"; return false; }
+    if (c->flags != 0) { *why = "flags must be 0"; return false; }
+    return true;
+}
+
+int64_t up256(int64_t n) { return (n + 255) / 256 * 256; }
+
+BlobLayout make_layout(int fmt, int64_t H, int64_t I) {
+    BlobLayout L{};
+    int64_t off = 0;
+    auto sec = [&](int64_t size) { off = up256(off); int64_t o = off; off += size; return o; };
+    if (fmt == FT_W_BF16) {
+        L.off_w13 = sec(2 * I * H * 2);
+        L.off_w2 = sec(H * I * 2);
+    } else {
+        L.off_w13 = sec(2 * I * H / 2);
+        L.off_w2 = sec(H * I / 2);
+        const int64_t blk = (fmt == FT_W_MXFP4) ? 32 : 16;
+        L.off_s13 = sec(2 * I * H / blk);
+        L.off_s2 = sec(H * I / blk);
+        if (fmt == FT_W_NVFP4) L.off_ts = sec(8);
+    }
+    L.blob_bytes = up256(off);
+    return L;
+}
+
+int64_t stage_slots_for(const ft_moe* h, int64_t C) {
+    int64_t need = (int64_t)h->max_u - C;
+    return need > 0 ? need : 0;
+}
+
+// Pin the distinct page ranges covering every blob (merged), skipping memory that is
+// already page-locked.
+ft_status pin_pool(ft_moe* h) {
+    const int64_t page = 4096;
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    r.reserve(h->blobs.size());
+    for (const uint8_t* b : h->blobs) {
+        uintptr_t a = (uintptr_t)b & ~(uintptr_t)(page - 1);
+        uintptr_t e = ((uintptr_t)b + h->blob_bytes + page - 1) & ~(uintptr_t)(page - 1);
+        r.emplace_back(a, e);
+    }
+    std::sort(r.begin(), r.end());
+    std::vector<std::pair<uintptr_t, uintptr_t>> m;
+    for (auto& x : r) {
+        if (!m.empty() && x.first <= m.back().second) m.back().second = std::max(m.back().second, x.second);
+        else m.push_back(x);
+    }
+    for (auto& x : m) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, (void*)x.first) == cudaSuccess &&
+            (at.type == cudaMemoryTypeHost)) {
+            continue;   // already page-locked by the caller
+        }
+        cudaGetLastError();
+        cudaError_t e = cudaHostRegister((void*)x.first, x.second - x.first, cudaHostRegisterDefault);
+        if (e == cudaErrorHostMemoryAlreadyRegistered) { cudaGetLastError(); continue; }
+        if (e != cudaSuccess) return cuda_fail(h, e, "cudaHostRegister(expert pool)");
+        h->pinned.push_back((void*)x.first);
+    }
+    return FT_OK;
+}
+
+ft_status alloc_state(ft_moe* h, int64_t C, uint8_t** arena, int32_t** slot_key,
+                      int32_t** o0, int32_t** o1, int64_t* n_stage) {
+    *arena = nullptr; *slot_key = nullptr; *o0 = nullptr; *o1 = nullptr;
+    *n_stage = stage_slots_for(h, C);
+    const int64_t nblobs = C + *n_stage;
+    if (h->fault_alloc) return fail(h, FT_ERR_OOM, "injected allocation failure (FTMOE_FAULT=alloc_fail)");
+    cudaError_t e = cudaSuccess;
+    if (nblobs > 0) e = cudaMalloc((void**)arena, (size_t)nblobs * h->blob_bytes);
+    if (e == cudaSuccess && C > 0) e = cudaMalloc((void**)slot_key, (size_t)C * 4);
+    if (e == cudaSuccess && C > 0) e = cudaMalloc((void**)o0, (size_t)C * 4);
+    if (e == cudaSuccess && C > 0) e = cudaMalloc((void**)o1, (size_t)C * 4);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(*arena); cudaFree(*slot_key); cudaFree(*o0); cudaFree(*o1);
+        *arena = nullptr; *slot_key = nullptr; *o0 = nullptr; *o1 = nullptr;
+        return cuda_fail(h, e, "cudaMalloc(cache arena)");
+    }
+    return FT_OK;
+}
+
+void free_all(ft_moe* h) {
+    cudaSetDevice(h->dev);
+    if (h->copy_stream) cudaStreamSynchronize(h->copy_stream);
+    if (h->ev_done) cudaEventSynchronize(h->ev_done);
+    cudaFree(h->d_router); cudaFree(h->d_arena); cudaFree(h->d_table); cudaFree(h->d_slot_key);
+    cudaFree(h->d_order[0]); cudaFree(h->d_order[1]); cudaFree(h->d_logits); cudaFree(h->d_idx);
+    cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
+    cudaFree(h->d_y);
+    if (h->h_mapped) cudaFreeHost(h->h_mapped);
+    if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+    if (h->ev_route) cudaEventDestroy(h->ev_route);
+    if (h->ev_fill) cudaEventDestroy(h->ev_fill);
+    if (h->ev_done) cudaEventDestroy(h->ev_done);
+    for (auto& se : h->pending) {
+        for (auto ev : se.ev) h->event_pool.push_back(ev);
+        h->event_pool.push_back(se.fill_begin);
+        h->event_pool.push_back(se.fill_end);
+    }
+    h->pending.clear();
+    for (auto ev : h->event_pool) if (ev) cudaEventDestroy(ev);
+    for (void* p : h->pinned) cudaHostUnregister(p);
+    cudaGetLastError();
+}
+
+ft_status init_lru_state(ft_moe* h) {
+    std::vector<int32_t> tab((size_t)h->cfg.layers * h->cfg.experts, -1);
+    FT_CUDA(h, cudaMemcpy(h->d_table, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice));
+    if (h->C > 0) {
+        std::vector<int32_t> sk((size_t)h->C, -1), ord((size_t)h->C);
+        for (int64_t i = 0; i < h->C; ++i) ord[(size_t)i] = (int32_t)i;
+        FT_CUDA(h, cudaMemcpy(h->d_slot_key, sk.data(), sk.size() * 4, cudaMemcpyHostToDevice));
+        FT_CUDA(h, cudaMemcpy(h->d_order[0], ord.data(), ord.size() * 4, cudaMemcpyHostToDevice));
+    }
+    h->cur = 0;
+    return FT_OK;
+}
+
+// Wait for an event with a deadline (polling), so a wedged device turns into an error.
+ft_status wait_event(ft_moe* h, cudaEvent_t ev, const char* what) {
+    auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t e = cudaEventQuery(ev);
+        if (e == cudaSuccess) return FT_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(h, e, what);
+        auto dt = std::chrono::duration_cast<std::chrono::milliseconds>(
+            std::chrono::steady_clock::now() - t0).count();
+        if (dt > h->wait_ms) {
+            h->broken = true;
+            return fail(h, FT_ERR_TIMEOUT, std::string(what) + ": host wait exceeded FTMOE_WAIT_MS");
+        }
+    }
+}
+
+ft_status sync_handle(ft_moe* h) {
+    cudaSetDevice(h->dev);
+    ft_status s = wait_event(h, h->ev_done, "synchronise handle");
+    if (s != FT_OK) return s;
+    FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+    return FT_OK;
+}
+
+cudaEvent_t get_event(ft_moe* h) {
+    if (!h->event_pool.empty()) {
+        cudaEvent_t e = h->event_pool.back();
+        h->event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+float ev_ms(cudaEvent_t a, cudaEvent_t b) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) { cudaGetLastError(); return 0.f; }
+    return ms;
+}
+
+void collect_timing(ft_moe* h) {
+    for (auto& se : h->pending) {
+        cudaEventSynchronize(se.ev[5]);
+        h->tsum.route_ms += ev_ms(se.ev[0], se.ev[1]);
+        h->tsum.ffn_hit_ms += ev_ms(se.ev[1], se.ev[2]);
+        if (se.has_miss) h->tsum.ffn_miss_ms += ev_ms(se.ev[3], se.ev[4]);
+        h->tsum.combine_ms += ev_ms(se.ev[4], se.ev[5]);
+        h->tsum.total_ms += ev_ms(se.ev[0], se.ev[5]);
+        if (se.has_fill) {
+            cudaEventSynchronize(se.fill_end);
+            float f = ev_ms(se.fill_begin, se.fill_end);
+            h->tsum.fill_ms += f;
+            h->stats.fill_ns += (uint64_t)(f * 1e6);
+        }
+        for (auto ev : se.ev) h->event_pool.push_back(ev);
+        h->event_pool.push_back(se.fill_begin);
+        h->event_pool.push_back(se.fill_end);
+    }
+    h->pending.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ft_status_str(ft_status s) {
+    switch (s) {
+        case FT_OK: return "FT_OK";
+        case FT_ERR_INVALID: return "FT_ERR_INVALID";
+        case FT_ERR_OOM: return "FT_ERR_OOM";
+        case FT_ERR_CUDA: return "FT_ERR_CUDA";
+        case FT_ERR_TIMEOUT: return "FT_ERR_TIMEOUT";
+        case FT_ERR_STATE: return "FT_ERR_STATE";
+        default: return "FT_ERR_UNKNOWN";
+    }
+}
+
+size_t ft_expert_blob_bytes(const ft_moe_config* cfg) {
+    if (!cfg || cfg->wfmt < 0 || cfg->wfmt > 2 || !ffn_supported(cfg->wfmt, cfg->hidden, cfg->inter)) return 0;
+    return (size_t)make_layout(cfg->wfmt, cfg->hidden, cfg->inter).blob_bytes;
+}
+
+const char* ft_moe_last_error(const ft_moe* h) {
+    return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blobs,
+                        const float* router_w, ft_moe** out) {
+    g_create_error.clear();
+    if (!out) return fail(nullptr, FT_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    std::string why;
+    if (!valid_config(cfg, &why)) return fail(nullptr, FT_ERR_INVALID, why);
+    if (!expert_blobs) return fail(nullptr, FT_ERR_INVALID, "expert_blobs is NULL");
+    const int64_t nkeys = (int64_t)cfg->layers * cfg->experts;
+    for (int64_t i = 0; i < nkeys; ++i)
+        if (!expert_blobs[i]) return fail(nullptr, FT_ERR_INVALID, "an expert blob pointer is NULL");
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device < 0 || cfg->device >= ndev) {
+        cudaGetLastError();
+        return fail(nullptr, FT_ERR_INVALID, "no such CUDA device");
+    }
+
+    ft_moe* h = new ft_moe();
+    h->cfg = *cfg;
+    h->dev = cfg->device;
+    h->lay = make_layout(cfg->wfmt, cfg->hidden, cfg->inter);
+    h->blob_bytes = (size_t)h->lay.blob_bytes;
+    h->max_pairs = cfg->max_tokens * cfg->top_k;
+    h->max_u = std::min<int32_t>(h->max_pairs, cfg->experts);
+    h->blobs.assign((const uint8_t* const*)expert_blobs, (const uint8_t* const*)expert_blobs + nkeys);
+    if (const char* f = getenv("FTMOE_FAULT")) {
+        h->fault_alloc = strstr(f, "alloc_fail") != nullptr;
+        h->fault_fill = strstr(f, "fill_fail") != nullptr;
+    }
+    if (const char* w = getenv("FTMOE_WAIT_MS")) h->wait_ms = std::max<int64_t>(1, atoll(w));
+
+    auto bail = [&](ft_status s) {
+        g_create_error = h->err;
+        free_all(h);
+        delete h;
+        return s;
+    };
+    if (cudaSetDevice(h->dev) != cudaSuccess) { cuda_fail(h, cudaGetLastError(), "cudaSetDevice"); return bail(FT_ERR_CUDA); }
+
+    ft_status st = pin_pool(h);
+    if (st != FT_OK) return bail(st);
+
+    const int fault_alloc = h->fault_alloc;
+    h->fault_alloc = 0;   // the injected fault targets resize only
+    h->C = cfg->cache_slots;
+    st = alloc_state(h, h->C, &h->d_arena, &h->d_slot_key, &h->d_order[0], &h->d_order[1], &h->n_stage);
+    h->fault_alloc = fault_alloc;
+    if (st != FT_OK) return bail(st);
+
+    const int L = cfg->layers, E = cfg->experts, H = cfg->hidden, I = cfg->inter;
+    auto dmalloc = [&](void** p, size_t n) -> bool {
+        cudaError_t e = cudaMalloc(p, n > 0 ? n : 16);
+        if (e != cudaSuccess) { cuda_fail(h, e, "cudaMalloc(scratch)"); return false; }
+        return true;
+    };
+    if (!dmalloc((void**)&h->d_table, (size_t)nkeys * 4)) return bail(FT_ERR_OOM);
+    if (router_w) {
+        if (!dmalloc((void**)&h->d_router, (size_t)L * E * H * 4)) return bail(FT_ERR_OOM);
+        if (cudaMemcpy(h->d_router, router_w, (size_t)L * E * H * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "copy router"); return bail(FT_ERR_CUDA);
+        }
+    }
+    if (!dmalloc((void**)&h->d_logits, (size_t)cfg->max_tokens * E * 4)) return bail(FT_ERR_OOM);
+    if (!dmalloc((void**)&h->d_idx, (size_t)h->max_pairs * 4)) return bail(FT_ERR_OOM);
+    if (!dmalloc((void**)&h->d_w, (size_t)h->max_pairs * 4)) return bail(FT_ERR_OOM);
+    if (!dmalloc((void**)&h->d_nan, 16)) return bail(FT_ERR_OOM);
+    if (!dmalloc((void**)&h->d_act, (size_t)h->max_pairs * I * 2)) return bail(FT_ERR_OOM);
+    if (!dmalloc((void**)&h->d_y, (size_t)h->max_pairs * H * 4)) return bail(FT_ERR_OOM);
+    {
+        const size_t mu = (size_t)h->max_u;
+        const size_t bytes = 256 + 4 * (mu + mu + (mu + 1) + (size_t)h->max_pairs + mu + mu) + 64;
+        if (!dmalloc((void**)&h->d_route_mem, bytes)) return bail(FT_ERR_OOM);
+        uint8_t* p = h->d_route_mem;
+        h->rb.counts = (RouteCounts*)p; p += 256;
+        h->rb.entry_e = (int32_t*)p; p += 4 * mu;
+        h->rb.entry_dst = (int32_t*)p; p += 4 * mu;
+        h->rb.entry_off = (int32_t*)p; p += 4 * (mu + 1);
+        h->rb.pairs = (int32_t*)p; p += 4 * (size_t)h->max_pairs;
+        h->rb.miss_key = (int32_t*)p; p += 4 * mu;
+        h->rb.miss_dst = (int32_t*)p;
+        const size_t hbytes = 256 + 8 * mu + 64;
+        if (cudaHostAlloc((void**)&h->h_mapped, hbytes, cudaHostAllocMapped) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(route view)"); return bail(FT_ERR_OOM);
+        }
+        memset(h->h_mapped, 0, hbytes);
+        uint8_t* dp = nullptr;
+        if (cudaHostGetDevicePointer((void**)&dp, h->h_mapped, 0) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "cudaHostGetDevicePointer"); return bail(FT_ERR_CUDA);
+        }
+        h->h_counts = (RouteCounts*)h->h_mapped;
+        h->h_miss_key = (int32_t*)(h->h_mapped + 256);
+        h->h_miss_dst = (int32_t*)(h->h_mapped + 256 + 4 * mu);
+        h->hv_dev.counts = (RouteCounts*)dp;
+        h->hv_dev.miss_key = (int32_t*)(dp + 256);
+        h->hv_dev.miss_dst = (int32_t*)(dp + 256 + 4 * mu);
+    }
+    if (cudaMemset(h->d_nan, 0, 16) != cudaSuccess) { cuda_fail(h, cudaGetLastError(), "memset"); return bail(FT_ERR_CUDA); }
+    if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_route, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess) {
+        cuda_fail(h, cudaGetLastError(), "stream/event create"); return bail(FT_ERR_CUDA);
+    }
+    st = init_lru_state(h);
+    if (st != FT_OK) return bail(st);
+    if (cudaEventRecord(h->ev_done, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cuda_fail(h, cudaGetLastError(), "create sync"); return bail(FT_ERR_CUDA);
+    }
+    h->stats.capacity = h->C;
+    *out = h;
+    return FT_OK;
+}
+
+ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, const float* logits,
+                         void* out, int32_t* topk_idx, float* topk_w, void* stream_) {
+    if (!h) return FT_ERR_INVALID;
+    if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
+    const ft_moe_config& c = h->cfg;
+    if (layer < 0 || layer >= c.layers) return fail(h, FT_ERR_INVALID, "layer out of range");
+    if (T < 0 || T > c.max_tokens) return fail(h, FT_ERR_INVALID, "T out of range");
+    if (T == 0) { h->stats.calls++; return FT_OK; }
+    if (!x || !out) return fail(h, FT_ERR_INVALID, "x/out is NULL");
+    if (!logits && !h->d_router) return fail(h, FT_ERR_INVALID, "no logits given and no router weights");
+    {
+        const uintptr_t xb = (uintptr_t)x, ob = (uintptr_t)out;
+        const uintptr_t n = (uintptr_t)T * c.hidden * 2;
+        if (xb < ob + n && ob < xb + n) return fail(h, FT_ERR_INVALID, "out overlaps x");
+        if ((xb | ob) & 15) return fail(h, FT_ERR_INVALID, "x/out must be 16-byte aligned");
+    }
+    cudaStream_t s = (cudaStream_t)stream_;
+    cudaSetDevice(h->dev);
+    cudaError_t pe = cudaGetLastError();
+    if (pe != cudaSuccess) return cuda_fail(h, pe, "earlier asynchronous error");
+
+    const int E = c.experts, k = c.top_k, H = c.hidden;
+    StageEvents se{};
+    if (h->timing) {
+        for (auto& ev : se.ev) ev = get_event(h);
+        se.fill_begin = get_event(h);
+        se.fill_end = get_event(h);
+    }
+    int launches = 0;
+    FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_done, 0));      // one call at a time per handle
+    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[0], s));
+    const float* lg = logits;
+    if (!lg) {
+        FT_CUDA(h, launch_router_logits((const __nv_bfloat16*)x, T, H,
+                                        h->d_router + (size_t)layer * E * H, E, h->d_logits, s));
+        lg = h->d_logits;
+        ++launches;
+    }
+    FT_CUDA(h, launch_topk_softmax(lg, T, E, k, h->d_idx, h->d_w, topk_idx, topk_w, h->d_nan, s));
+    ++launches;
+    LookupParams lp{};
+    lp.idx = h->d_idx;
+    lp.n_pairs = T * k;
+    lp.layer = layer;
+    lp.experts = E;
+    lp.capacity = h->C;
+    lp.table = h->d_table;
+    lp.slot_key = h->d_slot_key;
+    lp.order_in = h->d_order[h->cur];
+    lp.order_out = h->d_order[h->cur ^ 1];
+    lp.nan_flag = h->d_nan;
+    lp.rb = h->rb;
+    lp.hv = h->hv_dev;
+    FT_CUDA(h, launch_lookup(lp, s));
+    ++launches;
+    h->cur ^= 1;
+    FT_CUDA(h, cudaEventRecord(h->ev_route, s));
+    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
+
+    FfnParams fp{};
+    fp.arena = h->d_arena;
+    fp.lay = h->lay;
+    fp.hidden = H;
+    fp.inter = c.inter;
+    fp.top_k = k;
+    fp.counts = h->rb.counts;
+    fp.entry_dst = h->rb.entry_dst;
+    fp.entry_off = h->rb.entry_off;
+    fp.pairs = h->rb.pairs;
+    fp.x = (const __nv_bfloat16*)x;
+    fp.act = h->d_act;
+    fp.y = h->d_y;
+    fp.pass = 0;
+    FT_CUDA(h, launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches));
+    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[2], s));
+
+    // The one host wait: the miss list of this call.
+    ft_status ws = wait_event(h, h->ev_route, "cache lookup");
+    if (ws != FT_OK) return ws;
+    RouteCounts rc;
+    {
+        volatile int32_t* vc = (volatile int32_t*)h->h_counts;
+        rc.n_unique = vc[0]; rc.n_hits = vc[1]; rc.n_miss = vc[2]; rc.n_fill = vc[3];
+        rc.n_bypass = vc[4]; rc.n_evict = vc[5]; rc.err = vc[6]; rc.pad = 0;
+    }
+    if (rc.err & 6) { h->broken = true; return fail(h, FT_ERR_STATE, "cache lookup found inconsistent state"); }
+
+    if (rc.n_miss > 0) {
+        if (h->fault_fill) {
+            h->broken = true;
+            return fail(h, FT_ERR_CUDA, "injected fill failure (FTMOE_FAULT=fill_fail)");
+        }
+        if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_begin, h->copy_stream));
+        for (int j = 0; j < rc.n_miss; ++j) {
+            const int key = h->h_miss_key[j];
+            const int dst = h->h_miss_dst[j];
+            if (key < 0 || key >= c.layers * E || dst < 0 || dst >= h->C + h->n_stage) {
+                h->broken = true;
+                return fail(h, FT_ERR_STATE, "miss list out of range");
+            }
+            FT_CUDA(h, cudaMemcpyAsync(h->d_arena + (size_t)dst * h->blob_bytes, h->blobs[(size_t)key],
+                                       h->blob_bytes, cudaMemcpyHostToDevice, h->copy_stream));
+        }
+        FT_CUDA(h, cudaEventRecord(h->ev_fill, h->copy_stream));
+        if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_end, h->copy_stream));
+        FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_fill, 0));
+        if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[3], s));
+        fp.pass = 1;
+        FT_CUDA(h, launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches));
+        se.has_miss = true;
+        se.has_fill = true;
+    } else if (h->timing) {
+        FT_CUDA(h, cudaEventRecord(se.ev[3], s));
+    }
+    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[4], s));
+    FT_CUDA(h, launch_combine(h->d_y, h->d_w, T, k, H, (__nv_bfloat16*)out, s));
+    ++launches;
+    FT_CUDA(h, cudaEventRecord(h->ev_done, s));
+    if (h->timing) {
+        FT_CUDA(h, cudaEventRecord(se.ev[5], s));
+        h->pending.push_back(se);
+        h->tsum.forwards++;
+        h->tsum.ffn_launches += rc.n_miss > 0 ? 4 : 2;
+        uint64_t wbytes = (uint64_t)rc.n_unique * (uint64_t)(h->lay.blob_bytes);
+        h->tsum.ffn_weight_bytes += wbytes;
+        h->tsum.kernel_launches += (uint64_t)launches;
+    }
+
+    ft_cache_stats_t& st = h->stats;
+    st.calls++;
+    st.hits += (uint64_t)rc.n_hits;
+    st.misses += (uint64_t)rc.n_miss;
+    st.bypassed += (uint64_t)rc.n_bypass;
+    st.evictions += (uint64_t)rc.n_evict;
+    st.fill_bytes += (uint64_t)rc.n_fill * h->blob_bytes;
+    st.stage_bytes += (uint64_t)rc.n_bypass * h->blob_bytes;
+    st.resident += rc.n_fill - rc.n_evict;
+    if (rc.err & 1) return fail(h, FT_ERR_INVALID, "NaN router logit");
+    return FT_OK;
+}
+
+ft_status ft_cache_resize(ft_moe* h, int64_t new_slots) {
+    if (!h) return FT_ERR_INVALID;
+    if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
+    if (new_slots < 0 || new_slots > (int64_t)h->cfg.layers * h->cfg.experts * 4 + 1024)
+        return fail(h, FT_ERR_INVALID, "new_slots out of range");
+    ft_status s = sync_handle(h);
+    if (s != FT_OK) return s;
+    const int64_t C = h->C, C2 = new_slots;
+    std::vector<int32_t> order((size_t)C), slot_key((size_t)C);
+    if (C > 0) {
+        FT_CUDA(h, cudaMemcpy(order.data(), h->d_order[h->cur], (size_t)C * 4, cudaMemcpyDeviceToHost));
+        FT_CUDA(h, cudaMemcpy(slot_key.data(), h->d_slot_key, (size_t)C * 4, cudaMemcpyDeviceToHost));
+    }
+    // resident keys least -> most recent
+    std::vector<std::pair<int32_t, int32_t>> res;   // (key, old slot)
+    for (int64_t i = 0; i < C; ++i) {
+        int32_t sl = order[(size_t)i];
+        if (slot_key[(size_t)sl] >= 0) res.emplace_back(slot_key[(size_t)sl], sl);
+    }
+    const size_t nkeep = (size_t)std::min<int64_t>(C2, (int64_t)res.size());
+    std::vector<std::pair<int32_t, int32_t>> keep(res.end() - nkeep, res.end());
+    std::vector<int32_t> new_slot(keep.size(), -1);
+    std::vector<char> taken((size_t)C2, 0);
+    for (size_t i = 0; i < keep.size(); ++i)
+        if (keep[i].second < C2) { new_slot[i] = keep[i].second; taken[(size_t)keep[i].second] = 1; }
+    std::vector<std::pair<int32_t, size_t>> movers;   // (old slot, index in keep)
+    for (size_t i = 0; i < keep.size(); ++i)
+        if (keep[i].second >= C2) movers.emplace_back(keep[i].second, i);
+    std::sort(movers.begin(), movers.end());
+    {
+        int64_t f = 0;
+        for (auto& mv : movers) {
+            while (taken[(size_t)f]) ++f;
+            new_slot[mv.second] = (int32_t)f;
+            taken[(size_t)f] = 1;
+        }
+    }
+    uint8_t* arena2 = nullptr;
+    int32_t *sk2 = nullptr, *o0 = nullptr, *o1 = nullptr;
+    int64_t ns2 = 0;
+    s = alloc_state(h, C2, &arena2, &sk2, &o0, &o1, &ns2);
+    if (s != FT_OK) return s;
+    auto undo = [&](cudaError_t e, const char* what) {
+        cudaFree(arena2); cudaFree(sk2); cudaFree(o0); cudaFree(o1);
+        return cuda_fail(h, e, what);
+    };
+    for (size_t i = 0; i < keep.size(); ++i) {
+        cudaError_t e = cudaMemcpyAsync(arena2 + (size_t)new_slot[i] * h->blob_bytes,
+                                        h->d_arena + (size_t)keep[i].second * h->blob_bytes,
+                                        h->blob_bytes, cudaMemcpyDeviceToDevice, h->copy_stream);
+        if (e != cudaSuccess) return undo(e, "resize copy");
+    }
+    std::vector<int32_t> sk((size_t)C2, -1), ord;
+    ord.reserve((size_t)C2);
+    std::vector<int32_t> table((size_t)h->cfg.layers * h->cfg.experts, -1);
+    for (size_t i = 0; i < keep.size(); ++i) {
+        sk[(size_t)new_slot[i]] = keep[i].first;
+        table[(size_t)keep[i].first] = new_slot[i];
+    }
+    for (int64_t sl = 0; sl < C2; ++sl) if (sk[(size_t)sl] < 0) ord.push_back((int32_t)sl);
+    for (size_t i = 0; i < keep.size(); ++i) ord.push_back(new_slot[i]);
+    cudaError_t e = cudaStreamSynchronize(h->copy_stream);
+    if (e == cudaSuccess && C2 > 0) e = cudaMemcpy(sk2, sk.data(), (size_t)C2 * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && C2 > 0) e = cudaMemcpy(o0, ord.data(), (size_t)C2 * 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return undo(e, "resize state upload");
+    // commit: from here on the new state replaces the old one
+    e = cudaMemcpy(h->d_table, table.data(), table.size() * 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) { h->broken = true; undo(e, "resize table upload"); return FT_ERR_STATE; }
+    cudaFree(h->d_arena); cudaFree(h->d_slot_key); cudaFree(h->d_order[0]); cudaFree(h->d_order[1]);
+    h->d_arena = arena2; h->d_slot_key = sk2; h->d_order[0] = o0; h->d_order[1] = o1;
+    h->cur = 0;
+    h->C = C2;
+    h->n_stage = ns2;
+    h->stats.capacity = C2;
+    h->stats.resident = (int64_t)keep.size();
+    return FT_OK;
+}
+
+ft_status ft_cache_stats(ft_moe* h, ft_cache_stats_t* out) {
+    if (!h || !out) return FT_ERR_INVALID;
+    ft_status s = sync_handle(h);
+    if (s != FT_OK) return s;
+    if (h->timing) collect_timing(h);
+    *out = h->stats;
+    return FT_OK;
+}
+
+ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys) {
+    if (!h) return FT_ERR_INVALID;
+    ft_status s = sync_handle(h);
+    if (s != FT_OK) return s;
+    const size_t nkeys = (size_t)h->cfg.layers * h->cfg.experts;
+    if (slot_of_key) FT_CUDA(h, cudaMemcpy(slot_of_key, h->d_table, nkeys * 4, cudaMemcpyDeviceToHost));
+    if (lru_keys && h->C > 0) {
+        std::vector<int32_t> order((size_t)h->C), sk((size_t)h->C);
+        FT_CUDA(h, cudaMemcpy(order.data(), h->d_order[h->cur], (size_t)h->C * 4, cudaMemcpyDeviceToHost));
+        FT_CUDA(h, cudaMemcpy(sk.data(), h->d_slot_key, (size_t)h->C * 4, cudaMemcpyDeviceToHost));
+        int64_t n = 0;
+        for (int64_t i = 0; i < h->C; ++i) {
+            int32_t key = sk[(size_t)order[(size_t)i]];
+            if (key >= 0) lru_keys[n++] = key;
+        }
+        for (; n < h->C; ++n) lru_keys[n] = -1;
+    }
+    return FT_OK;
+}
+
+ft_status ft_moe_set_timing(ft_moe* h, int32_t enable) {
+    if (!h) return FT_ERR_INVALID;
+    h->timing = enable != 0;
+    return FT_OK;
+}
+
+ft_status ft_moe_timing(ft_moe* h, ft_timing_t* out, int32_t reset) {
+    if (!h || !out) return FT_ERR_INVALID;
+    ft_status s = sync_handle(h);
+    if (s != FT_OK) return s;
+    collect_timing(h);
+    *out = h->tsum;
+    if (reset) h->tsum = ft_timing_t{};
+    return FT_OK;
+}
+
+void ft_moe_destroy(ft_moe* h) {
+    if (!h) return;
+    free_all(h);
+    delete h;
+}
+
+ft_status ft_router_logits(const void* x, int32_t T, int32_t H, const float* wr, int32_t E,
+                           float* logits, void* stream) {
+    if (T < 0 || H <= 0 || H % 8 || E <= 0) return FT_ERR_INVALID;
+    if (T == 0) return FT_OK;
+    if (!x || !wr || !logits) return FT_ERR_INVALID;
+    if (((uintptr_t)x | (uintptr_t)wr) & 15) return FT_ERR_INVALID;
+    cudaError_t e = launch_router_logits((const __nv_bfloat16*)x, T, H, wr, E, logits, (cudaStream_t)stream);
+    return e == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+ft_status ft_topk_softmax(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* idx,
+                          float* w, void* stream) {
+    if (T < 0 || E <= 0 || E > kMaxExperts || k < 1 || k > kMaxTopK || k > E) return FT_ERR_INVALID;
+    if (T == 0) return FT_OK;
+    if (!logits || !idx || !w) return FT_ERR_INVALID;
+    cudaError_t e = launch_topk_softmax(logits, T, E, k, idx, w, nullptr, nullptr, nullptr,
+                                        (cudaStream_t)stream);
+    return e == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+/*
+ * ftmoe.h — C ABI of libftmoe.so: the routed Mixture-of-Experts layer forward with a
+ * GPU-resident, globally-LRU expert cache (B300 / sm_103a).
+ *
+ * What the calls compute. The pages describing the edge-native MoE serving engine
+ * ("Meet FreeToken: An Edge-Native MoE Serving Engine that Runs 753B GLM-5.2 on a Single
+ * Workstation GPU", MarkTechPost) state the problem this library serves:
+ *   - "The gap it targets": the expert pool does not fit the GPU, so inactive experts sit
+ *     in host memory and enter the execution path on demand; prefill routes thousands of
+ *     tokens to nearly every expert.
+ *   - "Three mechanisms", semantic-aware caching: during decode one shared LRU expert cache
+ *     spans all MoE layers and follows the router; during prefill, full layers are double
+ *     buffered (layer l+1 streams while layer l computes).
+ *   - "Three mechanisms", elastic memory management: experts are read into their final host
+ *     layout and then pinned; the GPU cache is rebuilt under a revised VRAM budget at safe
+ *     points without reloading the host pool; the first request is served cold.
+ *   - "Key Takeaways": expert output is exact — no router changes, no expert substitution,
+ *     no precision relaxation. Where an expert's bytes live never changes the result.
+ * The CPU-side execution of misses (the pages' q* split) is not part of this library;
+ * every miss is filled over PCIe and its bytes are reported in the statistics.
+ *
+ * Conventions for every call:
+ *   - Every call returns an ft_status; no C++ exception crosses this boundary.
+ *   - Arguments are validated before anything is enqueued; a call that returns
+ *     FT_ERR_INVALID has enqueued no work and changed no state.
+ *   - "dev" pointers are CUDA device memory on the handle's device; "host" pointers are
+ *     ordinary host memory. `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream). Work is stream-ordered; a handle serialises its own calls.
+ *   - An asynchronous CUDA error surfaces as FT_ERR_CUDA from the next call that observes
+ *     it; ft_moe_last_error() returns the text.
+ *   - A handle is not thread-safe: one host thread at a time.
+ *
+ * Expert blob layout (one contiguous blob per (layer, expert), the "final host layout";
+ * each section starts on a 256-byte boundary, the blob size is rounded up to 256 bytes):
+ *     section          BF16             MXFP4                  NVFP4
+ *     s0 W13           [2I][H] bf16     [2I][H/2] E2M1 x2      [2I][H/2] E2M1 x2
+ *     s1 W2            [H][I] bf16      [H][I/2]  E2M1 x2      [H][I/2]  E2M1 x2
+ *     s2 W13 scales    -                [2I][H/32] E8M0        [2I][H/16] E4M3
+ *     s3 W2 scales     -                [H][I/32]  E8M0        [H][I/16]  E4M3
+ *     s4 tensor scale  -                -                      fp32[2] (W13, W2)
+ *   Row 2i of W13 is the gate row W1[i], row 2i+1 the up row W3[i]; W2 is [out=H][in=I].
+ *   Two E2M1 codes per byte, the low nibble holding the even-indexed element.
+ *   The expert computes y = W2 (silu(W1 x) * (W3 x)) with fp32 accumulation; the SwiGLU
+ *   activation is rounded to bf16 before W2, the combined output to bf16.
+ */
+#ifndef FTMOE_H
+#define FTMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FT_API __attribute__((visibility("default")))
+#else
+#define FT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FT_OK = 0,
+    FT_ERR_INVALID = 1,   /* bad argument / precondition; nothing was enqueued */
+    FT_ERR_OOM = 2,       /* a device or pinned allocation failed; state unchanged */
+    FT_ERR_CUDA = 3,      /* a CUDA call or an earlier asynchronous kernel failed */
+    FT_ERR_TIMEOUT = 4,   /* a bounded host wait on the device ran out */
+    FT_ERR_STATE = 5      /* handle unusable (an earlier failure left it inconsistent) */
+} ft_status;
+
+typedef enum { FT_W_BF16 = 0, FT_W_MXFP4 = 1, FT_W_NVFP4 = 2 } ft_wfmt;
+
+typedef struct {
+    int32_t layers;       /* MoE layers sharing the one global cache (>= 1) */
+    int32_t experts;      /* routed experts per layer E (1..1024) */
+    int32_t hidden;       /* H, multiple of 64 */
+    int32_t inter;        /* expert intermediate size I, multiple of 64 */
+    int32_t top_k;        /* k, 1..min(E, 32) */
+    int32_t max_tokens;   /* largest T passed to ft_moe_forward (>= 1) */
+    int32_t wfmt;         /* ft_wfmt */
+    int32_t device;       /* CUDA device ordinal */
+    int64_t cache_slots;  /* C: GPU expert slots, one global LRU over all layers (>= 0) */
+    int32_t flags;        /* reserved, must be 0 */
+    int32_t reserved;
+} ft_moe_config;
+
+typedef struct {
+    uint64_t calls;       /* ft_moe_forward calls with T >= 1 (T = 0 calls count too) */
+    uint64_t hits;        /* unique (layer, expert) reads found resident */
+    uint64_t misses;      /* unique reads not resident (filled + bypassed) */
+    uint64_t bypassed;    /* misses computed from staging because |S| > free capacity */
+    uint64_t evictions;   /* resident keys displaced by a miss */
+    uint64_t fill_bytes;  /* host->device bytes copied into cache slots */
+    uint64_t stage_bytes; /* host->device bytes copied into staging (bypassed misses) */
+    uint64_t fill_ns;     /* device time of the copy batches (timing enabled only) */
+    int64_t capacity;     /* current C */
+    int64_t resident;     /* keys resident now */
+} ft_cache_stats_t;
+
+/* Accumulated device time per stage, in milliseconds, measured with CUDA events on the
+ * stream each stage runs on (ft_moe_set_timing(h, 1) enables recording). */
+typedef struct {
+    double route_ms;      /* router logits (if computed) + top-k + cache lookup/permute */
+    double ffn_hit_ms;    /* expert FFN over entries resident at call start */
+    double fill_ms;       /* H2D miss copies on the copy stream */
+    double ffn_miss_ms;   /* expert FFN over filled / staged entries */
+    double combine_ms;    /* gate-weighted combine */
+    double total_ms;      /* whole forward call, first to last event on the caller's stream */
+    uint64_t forwards;    /* forward calls recorded */
+    uint64_t ffn_launches;/* expert-FFN kernel launches recorded (hit and miss passes) */
+    uint64_t ffn_weight_bytes; /* expert weight bytes those launches were given to stream */
+    uint64_t kernel_launches;  /* all kernels launched by the recorded calls */
+} ft_timing_t;
+
+typedef struct ft_moe ft_moe;
+
+/* Status name ("FT_OK", ...). Never NULL. */
+FT_API const char* ft_status_str(ft_status s);
+
+/* Bytes of one expert blob in the layout above for cfg's (wfmt, hidden, inter); 0 if the
+ * shape is invalid. */
+FT_API size_t ft_expert_blob_bytes(const ft_moe_config* cfg);
+
+/* Create a handle ("Three mechanisms", elastic memory management: host pool in its final
+ * layout, pinned in place; cold start).
+ *   cfg            host, copied.
+ *   expert_blobs   host array of layers*experts host pointers; entry (l*E + e) points at the
+ *                  blob of expert e of layer l. Entries may alias (several keys may share one
+ *                  blob). Caller-owned: every blob must stay valid and unmodified until
+ *                  ft_moe_destroy. The library pins the distinct page ranges in place with
+ *                  cudaHostRegister (memory that is already pinned is used as is) and unpins
+ *                  what it pinned at destroy.
+ *   router_w       host fp32 [layers][experts][hidden], copied to the device; may be NULL,
+ *                  in which case every forward must be given logits.
+ *   out            receives the handle.
+ * All cache slots start empty. Errors: FT_ERR_INVALID (shape/pointers), FT_ERR_OOM,
+ * FT_ERR_CUDA. On error *out is NULL and nothing leaks. */
+FT_API ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blobs,
+                        const float* router_w, ft_moe** out);
+
+/* One MoE layer forward through the cache (decode path; "Three mechanisms", semantic-aware
+ * caching: one LRU over all layers).
+ *   layer      0 <= layer < layers.
+ *   x          dev bf16 [T][H], row-major.
+ *   T          0 <= T <= max_tokens (T = 0 returns FT_OK and touches nothing).
+ *   logits     dev fp32 [T][E] router logits, or NULL to compute x . Wr[layer]^T.
+ *   out        dev bf16 [T][H]; must not overlap x.
+ *   topk_idx   optional dev int32 [T][k]: chosen experts in rank order (logit descending,
+ *              ties to the lower index).
+ *   topk_w     optional dev fp32 [T][k]: softmax of the chosen logits.
+ *   stream     caller's stream; every kernel of the call runs on it, miss copies run on the
+ *              handle's copy stream and are joined back with an event.
+ * The call blocks the host once, until the cache lookup of this call has run on the device
+ * (it needs the miss list to issue the copies); expert compute on resident experts is
+ * already enqueued by then. Errors: FT_ERR_INVALID (arguments, or a NaN logit seen by the
+ * device: outputs are then undefined), FT_ERR_TIMEOUT (the lookup did not finish within the
+ * host wait limit, FTMOE_WAIT_MS, default 20000 ms), FT_ERR_CUDA. */
+FT_API ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T,
+                         const float* logits, void* out, int32_t* topk_idx, float* topk_w,
+                         void* stream);
+
+/* Rebuild the cache under a new slot budget at a safe point ("Three mechanisms", elastic
+ * memory management). Synchronises the handle. The min(new_slots, resident) most recently
+ * used keys survive in recency order; a survivor keeps its slot if that slot is
+ * < new_slots, the others move (device-to-device) in ascending old-slot order to the lowest
+ * free slots. The host pool is not read. On FT_ERR_OOM the old cache is intact. */
+FT_API ft_status ft_cache_resize(ft_moe* h, int64_t new_slots);
+
+/* Cache statistics since create (safe point: synchronises the handle). */
+FT_API ft_status ft_cache_stats(ft_moe* h, ft_cache_stats_t* out);
+
+/* Cache state (safe point: synchronises the handle).
+ *   slot_of_key  host int32 [layers*experts]: slot of each key, -1 if not resident.
+ *   lru_keys     host int32 [capacity]: resident keys least- to most-recently used, -1 pad.
+ * Either pointer may be NULL. */
+FT_API ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys);
+
+/* Enable (1) or disable (0) per-stage event timing; ft_moe_timing synchronises and returns
+ * the sums since the last reset (reset = 1 clears them after reading). */
+FT_API ft_status ft_moe_set_timing(ft_moe* h, int32_t enable);
+FT_API ft_status ft_moe_timing(ft_moe* h, ft_timing_t* out, int32_t reset);
+
+/* Text of the last error on this handle (or of the last failed create when h is NULL). */
+FT_API const char* ft_moe_last_error(const ft_moe* h);
+
+/* Destroy: synchronises, frees device memory, unpins what create pinned. NULL is a no-op. */
+FT_API void ft_moe_destroy(ft_moe* h);
+
+/* ---- stage entry points (stateless; the same kernels ft_moe_forward runs) ---------- */
+
+/* Router logits logits[t][e] = sum_h x[t][h] * wr[e][h], fp32 accumulation.
+ *   x dev bf16 [T][H]; wr dev fp32 [E][H]; logits dev fp32 [T][E]. H multiple of 8. */
+FT_API ft_status ft_router_logits(const void* x, int32_t T, int32_t H, const float* wr, int32_t E,
+                           float* logits, void* stream);
+
+/* Top-k and gate weights, one warp per token: idx dev int32 [T][k] in rank order (logit
+ * descending, ties to the lower index), w dev fp32 [T][k] = softmax over the chosen
+ * logits. E <= 1024, 1 <= k <= min(E, 32). NaN logits are a precondition violation. */
+FT_API ft_status ft_topk_softmax(const float* logits, int32_t T, int32_t E, int32_t k,
+                          int32_t* idx, float* w, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FTMOE_H */
