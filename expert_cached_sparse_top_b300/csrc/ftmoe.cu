@@ -12,6 +12,7 @@
 // in their final layout and enter the GPU on demand; the cache is rebuilt under a new
 // budget at safe points without reloading the host pool; the first request is served cold.
 #include "common.cuh"
+#include "tc_ffn.cuh"
 #include "../../include/ftmoe.h"
 
 #include <algorithm>
@@ -77,6 +78,16 @@ struct ft_moe {
     std::string err;
     int fault_fill = 0, fault_alloc = 0;
     int64_t wait_ms = 20000;
+
+    // tcgen05 expert FFN (BF16 weights)
+    bool use_tc = false;
+    int tc_bn = 16;
+    int64_t act_rows = 0;                 // rows allocated for d_act / d_xp
+    __nv_bfloat16* d_xp = nullptr;        // [act_rows][H] activations in grouped-row order
+    CUtensorMap tmA13{}, tmA2{}, tmB13{}, tmB2{};
+    int* h_ffn_err = nullptr;             // host view of the kernels' error word (mapped)
+    int* d_ffn_err = nullptr;             // device address of the same word
+    int num_sms = 148;
 
     bool timing = false;
     std::vector<StageEvents> pending;
@@ -200,7 +211,7 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_router); cudaFree(h->d_arena); cudaFree(h->d_table); cudaFree(h->d_slot_key);
     cudaFree(h->d_order[0]); cudaFree(h->d_order[1]); cudaFree(h->d_logits); cudaFree(h->d_idx);
     cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
-    cudaFree(h->d_y);
+    cudaFree(h->d_y); cudaFree(h->d_xp);
     if (h->h_mapped) cudaFreeHost(h->h_mapped);
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     if (h->ev_route) cudaEventDestroy(h->ev_route);
@@ -230,6 +241,19 @@ ft_status init_lru_state(ft_moe* h) {
     return FT_OK;
 }
 
+// (Re)build the TMA tensor maps of the tensor-core FFN: weights as (K, row, slot) over the
+// slot arena, activations as (K, row).
+ft_status encode_tc_maps(ft_moe* h) {
+    if (!h->use_tc) return FT_OK;
+    const int H = h->cfg.hidden, I = h->cfg.inter;
+    const int64_t nslots = std::max<int64_t>(1, h->C + h->n_stage);
+    FT_CUDA(h, tc_encode_weights(&h->tmA13, h->d_arena + h->lay.off_w13, H, 2 * I, nslots, h->lay.blob_bytes));
+    FT_CUDA(h, tc_encode_weights(&h->tmA2, h->d_arena + h->lay.off_w2, I, H, nslots, h->lay.blob_bytes));
+    FT_CUDA(h, tc_encode_acts(&h->tmB13, h->d_xp, H, (int)h->act_rows, h->tc_bn));
+    FT_CUDA(h, tc_encode_acts(&h->tmB2, h->d_act, I, (int)h->act_rows, h->tc_bn));
+    return FT_OK;
+}
+
 // Wait for an event with a deadline (polling), so a wedged device turns into an error.
 ft_status wait_event(ft_moe* h, cudaEvent_t ev, const char* what) {
     auto t0 = std::chrono::steady_clock::now();
@@ -251,6 +275,10 @@ ft_status sync_handle(ft_moe* h) {
     ft_status s = wait_event(h, h->ev_done, "synchronise handle");
     if (s != FT_OK) return s;
     FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+    if (h->h_ffn_err && *(volatile int*)h->h_ffn_err) {
+        h->broken = true;
+        return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait");
+    }
     return FT_OK;
 }
 
@@ -383,7 +411,17 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (!dmalloc((void**)&h->d_idx, (size_t)h->max_pairs * 4)) return bail(FT_ERR_OOM);
     if (!dmalloc((void**)&h->d_w, (size_t)h->max_pairs * 4)) return bail(FT_ERR_OOM);
     if (!dmalloc((void**)&h->d_nan, 16)) return bail(FT_ERR_OOM);
-    if (!dmalloc((void**)&h->d_act, (size_t)h->max_pairs * I * 2)) return bail(FT_ERR_OOM);
+    {
+        const char* ffn = getenv("FTMOE_FFN");
+        h->use_tc = cfg->wfmt == FT_W_BF16 && !(ffn && strcmp(ffn, "simt") == 0);
+        h->tc_bn = tc_pick_bn(cfg->max_tokens);
+        h->act_rows = ((int64_t)h->max_pairs + h->tc_bn - 1) / h->tc_bn * h->tc_bn + h->tc_bn;
+        int dev_sms = 0;
+        cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, h->dev);
+        if (dev_sms > 0) h->num_sms = dev_sms;
+    }
+    if (!dmalloc((void**)&h->d_act, (size_t)h->act_rows * I * 2)) return bail(FT_ERR_OOM);
+    if (h->use_tc && !dmalloc((void**)&h->d_xp, (size_t)h->act_rows * H * 2)) return bail(FT_ERR_OOM);
     if (!dmalloc((void**)&h->d_y, (size_t)h->max_pairs * H * 4)) return bail(FT_ERR_OOM);
     {
         const size_t mu = (size_t)h->max_u;
@@ -397,7 +435,7 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->rb.pairs = (int32_t*)p; p += 4 * (size_t)h->max_pairs;
         h->rb.miss_key = (int32_t*)p; p += 4 * mu;
         h->rb.miss_dst = (int32_t*)p;
-        const size_t hbytes = 256 + 8 * mu + 64;
+        const size_t hbytes = 256 + 8 * mu + 64 + 64;
         if (cudaHostAlloc((void**)&h->h_mapped, hbytes, cudaHostAllocMapped) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(route view)"); return bail(FT_ERR_OOM);
         }
@@ -412,6 +450,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->hv_dev.counts = (RouteCounts*)dp;
         h->hv_dev.miss_key = (int32_t*)(dp + 256);
         h->hv_dev.miss_dst = (int32_t*)(dp + 256 + 4 * mu);
+        h->h_ffn_err = (int*)(h->h_mapped + 256 + 8 * mu + 64);
+        h->d_ffn_err = (int*)(dp + 256 + 8 * mu + 64);
     }
     if (cudaMemset(h->d_nan, 0, 16) != cudaSuccess) { cuda_fail(h, cudaGetLastError(), "memset"); return bail(FT_ERR_CUDA); }
     if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
@@ -421,6 +461,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         cuda_fail(h, cudaGetLastError(), "stream/event create"); return bail(FT_ERR_CUDA);
     }
     st = init_lru_state(h);
+    if (st != FT_OK) return bail(st);
+    st = encode_tc_maps(h);
     if (st != FT_OK) return bail(st);
     if (cudaEventRecord(h->ev_done, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cuda_fail(h, cudaGetLastError(), "create sync"); return bail(FT_ERR_CUDA);
@@ -448,6 +490,11 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     }
     cudaStream_t s = (cudaStream_t)stream_;
     cudaSetDevice(h->dev);
+    if (*(volatile int*)h->h_ffn_err) {
+        h->broken = true;
+        return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait (code " +
+                                    std::to_string(*(volatile int*)h->h_ffn_err) + ")");
+    }
     cudaError_t pe = cudaGetLastError();
     if (pe != cudaSuccess) return cuda_fail(h, pe, "earlier asynchronous error");
 
@@ -502,8 +549,35 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     fp.x = (const __nv_bfloat16*)x;
     fp.act = h->d_act;
     fp.y = h->d_y;
-    fp.pass = 0;
-    FT_CUDA(h, launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches));
+    TcParams tp{};
+    if (h->use_tc) {
+        FT_CUDA(h, tc_gather_rows((const __nv_bfloat16*)x, h->rb.pairs, nullptr, T * k, k, H, h->d_xp, s));
+        ++launches;
+        tp.counts = h->rb.counts;
+        tp.entry_off = h->rb.entry_off;
+        tp.entry_dst = h->rb.entry_dst;
+        tp.pairs = h->rb.pairs;
+        tp.act = h->d_act;
+        tp.act_ld = c.inter;
+        tp.y = h->d_y;
+        tp.y_ld = H;
+        tp.err = h->d_ffn_err;
+    }
+    auto run_ffn = [&](int pass) -> cudaError_t {
+        if (!h->use_tc) {
+            fp.pass = pass;
+            return launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches);
+        }
+        tp.pass = pass;
+        tp.m_rows = 2 * c.inter; tp.k_dim = H;
+        cudaError_t e = tc_launch(13, h->tc_bn, tp, h->tmA13, h->tmB13, h->num_sms, s);
+        if (e != cudaSuccess) return e;
+        tp.m_rows = H; tp.k_dim = c.inter;
+        e = tc_launch(2, h->tc_bn, tp, h->tmA2, h->tmB2, h->num_sms, s);
+        launches += 2;
+        return e;
+    };
+    FT_CUDA(h, run_ffn(0));
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[2], s));
 
     // The one host wait: the miss list of this call.
@@ -537,8 +611,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_end, h->copy_stream));
         FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_fill, 0));
         if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[3], s));
-        fp.pass = 1;
-        FT_CUDA(h, launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches));
+        FT_CUDA(h, run_ffn(1));
         se.has_miss = true;
         se.has_fill = true;
     } else if (h->timing) {
@@ -646,6 +719,8 @@ ft_status ft_cache_resize(ft_moe* h, int64_t new_slots) {
     h->n_stage = ns2;
     h->stats.capacity = C2;
     h->stats.resident = (int64_t)keep.size();
+    ft_status es = encode_tc_maps(h);
+    if (es != FT_OK) { h->broken = true; return es; }
     return FT_OK;
 }
 

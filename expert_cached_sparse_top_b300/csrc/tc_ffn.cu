@@ -1,0 +1,471 @@
+// Expert SwiGLU FFN on the 5th-generation tensor cores (tcgen05) for BF16 weights: one
+// persistent grouped-GEMM kernel per matrix (W13 with a fused SwiGLU epilogue, then W2),
+// used for decode (a handful of tokens per expert, N = 16) and prefill (~100-256 tokens per
+// expert, N up to 256).
+//
+// Orientation ("swap AB"): the expert's weight rows are the M = 128 operand A (K-major, as
+// stored in the blob), the expert's tokens are the N operand B (K-major activation rows,
+// gathered per expert), and the fp32 accumulator D[128 x N] lives in tensor memory. So a
+// weight tile is read from HBM once however few tokens the expert has.
+//
+//   warp 0      TMA producer: weights through a 3-D tensor map over the slot arena
+//               (K, row, slot) and activations through a 2-D map, 128-byte swizzled,
+//               into an S-stage shared-memory ring (mbarrier complete_tx).
+//   warp 1      allocates TMEM (2 accumulators of N columns) and issues tcgen05.mma
+//               (kind::f16, bf16 x bf16 -> fp32) from one lane; tcgen05.commit frees ring
+//               stages and publishes finished accumulators.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows; W13 pairs gate/up rows
+//               (adjacent TMEM lanes) into silu(g)*u and writes the bf16 activation; W2
+//               writes fp32 expert outputs to their (token, rank) rows.
+//
+// Every mbarrier wait is bounded; a wait that runs out records an error code in global
+// memory, and all roles leave their loops, so the kernel always ends and frees its TMEM.
+#include "common.cuh"
+#include "tc_ffn.cuh"
+
+#include <cuda.h>
+
+namespace ftmoe {
+namespace tc {
+
+constexpr int kThreads = 192;          // 6 warps
+constexpr int kBK = 64;                // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kBM = 128;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false (and an error code recorded) if the barrier never flips.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 1023u) == 1023u && *(volatile int*)err) return false;
+    }
+    atomicCAS(err, 0, code);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
+           "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
+           "r"(c0), "r"(c1) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1u << 16;                         // leading byte offset (unused: SW128 K-major)
+    d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1u << 46;                         // descriptor version (sm_100 family)
+    d |= (uint64_t)2u << 61;                         // layout: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TileMap {
+    int u_begin, n_entries;
+    int m_tiles;
+    int total;
+};
+
+// Locate tile t: entries are visited in order; within an entry, N tiles, then M tiles
+// (M innermost so that concurrently running CTAs share the entry's activation rows in L2).
+__device__ __forceinline__ void locate(const int* s_prefix, int n_entries, int m_tiles, int t,
+                                       int* u_rel, int* mt, int* nt) {
+    int lo = 0, hi = n_entries - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    int r = t - s_prefix[lo];
+    *u_rel = lo;
+    *nt = r / m_tiles;
+    *mt = r % m_tiles;
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
+    TcParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    constexpr int A_BYTES = kBM * kBK * 2;            // 16 KB
+    constexpr int B_BYTES = BN * kBK * 2;
+    constexpr int STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;       // [2]
+    uint64_t* tempty = tfull + 2;      // [2]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+    int* s_prefix = reinterpret_cast<int*>(s_tmem + 4);   // [kMaxExperts + 1]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const RouteCounts rc = *p.counts;
+    const int u_begin = p.pass == 0 ? 0 : rc.n_hits;
+    const int u_end = p.pass == 0 ? rc.n_hits : rc.n_unique;
+    const int n_entries = u_end - u_begin;
+    if (n_entries <= 0) return;
+    const int m_tiles = (p.m_rows + kBM - 1) / kBM;
+    const int k_steps = p.k_dim / kBK;
+
+    // tile prefix over this pass's entries
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int i = 0; i < n_entries; ++i) {
+            s_prefix[i] = acc;
+            const int n = p.entry_off[u_begin + i + 1] - p.entry_off[u_begin + i];
+            acc += m_tiles * ((n + BN - 1) / BN);
+        }
+        s_prefix[n_entries] = acc;
+    }
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(s_tmem)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int total = s_prefix[n_entries];
+    int* err = p.err;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int ur, mt, nt;
+                locate(s_prefix, n_entries, m_tiles, t, &ur, &mt, &nt);
+                const int u = u_begin + ur;
+                const int slot = p.entry_dst[u];
+                const int row_b = p.entry_off[u] + nt * BN;
+                for (int kb = 0; kb < k_steps; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, err, 1)) { ok = false; break; }
+                    uint8_t* sa = smem + s * STAGE;
+                    mbar_expect_tx(&full[s], STAGE);
+                    tma_load_3d(sa, &tmA, &full[s], kb * kBK, mt * kBM, slot);
+                    tma_load_2d(sa + A_BYTES, &tmB, &full[s], kb * kBK, row_b);
+                }
+            }
+            // drain: every issued stage must land before the CTA may exit
+            if (!ok) {
+                for (uint32_t j = (it > (uint32_t)S ? it - S : 0); j < it; ++j)
+                    mbar_wait(&full[j % S], (j / S) & 1u, err, 5);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, tl = 0;
+            constexpr uint32_t idesc = idesc_bf16(BN);
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tl) {
+                const uint32_t acc = tl & 1u;
+                const uint32_t aph = (tl >> 1) & 1u;
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, err, 2)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < k_steps; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!mbar_wait(&full[s], ph, err, 3)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * STAGE);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
+                                 idesc, (kb | kk) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+            }
+        }
+    } else {
+        // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        uint32_t tl = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl) {
+            int ur, mt, nt;
+            locate(s_prefix, n_entries, m_tiles, t, &ur, &mt, &nt);
+            const int u = u_begin + ur;
+            const int row_b = p.entry_off[u] + nt * BN;
+            const int n_valid = min(BN, p.entry_off[u + 1] - row_b);
+            const uint32_t acc = tl & 1u;
+            const uint32_t aph = (tl >> 1) & 1u;
+            if (!mbar_wait(&tfull[acc], aph, err, 4)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            const int m = mt * kBM + row_in_tile;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tbase + c0, r);
+                tmem_wait_ld();
+                if (MODE == 13) {
+                    // lanes 2i / 2i+1 hold the gate / up rows of output feature i
+                    float own[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) own[j] = __uint_as_float(r[j]);
+                    const bool odd = lane & 1;
+                    const int feat = m >> 1;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        // even lane computes columns c0+j, odd lane columns c0+8+j
+                        const float send = odd ? own[j] : own[j + 8];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const float g = odd ? recv : own[j];
+                        const float uu = odd ? own[j + 8] : recv;
+                        const int n = c0 + (odd ? 8 + j : j);
+                        if (n < n_valid && m < p.m_rows) {
+                            const float a = g / (1.f + __expf(-g)) * uu;
+                            p.act[(int64_t)(row_b + n) * p.act_ld + feat] = __float2bfloat16_rn(a);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = c0 + j;
+                        if (n < n_valid && m < p.m_rows) {
+                            const int pair = p.pairs[row_b + n];
+                            p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// Gather activation rows into expert-grouped order: xp[r] = x[pairs[r] / k].
+__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pairs,
+                                   const int32_t* __restrict__ n_rows_ptr, int n_rows_fixed, int k,
+                                   int H, __nv_bfloat16* __restrict__ xp) {
+    const int n_rows = n_rows_ptr ? *n_rows_ptr : n_rows_fixed;
+    const int cpr = H / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)n_rows * cpr;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / cpr), c = (int)(i % cpr);
+        const int t = pairs[r] / k;
+        reinterpret_cast<uint4*>(xp + (int64_t)r * H)[c] =
+            __ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * H) + c);
+    }
+}
+
+}  // namespace tc
+
+// ----------------------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------------------
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+template <int BN>
+int stages_for() {
+    const int stage = 128 * 64 * 2 + BN * 64 * 2;
+    int s = (200 * 1024) / stage;
+    return s > 8 ? 8 : s;
+}
+
+template <int BN>
+size_t smem_for(int stages) {
+    const size_t stage = 128 * 64 * 2 + BN * 64 * 2;
+    return 1024 + stages * stage + (2 * stages + 4) * 8 + 16 + (kMaxExperts + 1) * 4;
+}
+
+template <int BN, int MODE>
+cudaError_t launch_bn(const TcParams& p0, const CUtensorMap& a, const CUtensorMap& b, int grid,
+                      cudaStream_t s) {
+    TcParams p = p0;
+    p.stages = stages_for<BN>();
+    const size_t smem = smem_for<BN>(p.stages);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc::tc_ffn_kernel<BN, MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    tc::tc_ffn_kernel<BN, MODE><<<grid, tc::kThreads, smem, s>>>(p, a, b);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_pick_bn(int tokens_per_expert_max) {
+    if (tokens_per_expert_max <= 16) return 16;
+    if (tokens_per_expert_max <= 32) return 32;
+    if (tokens_per_expert_max <= 64) return 64;
+    return 128;
+}
+
+cudaError_t tc_encode_weights(CUtensorMap* map, const void* base, int k_dim, int rows,
+                              int64_t n_slots, int64_t blob_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[3] = {(cuuint64_t)k_dim, (cuuint64_t)rows, (cuuint64_t)(n_slots > 0 ? n_slots : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)k_dim * 2, (cuuint64_t)blob_bytes};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t tc_encode_acts(CUtensorMap* map, const void* base, int k_dim, int rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)k_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)k_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t tc_launch(int mode, int bn, const TcParams& p, const CUtensorMap& a,
+                      const CUtensorMap& b, int grid, cudaStream_t s) {
+#define FT_TC_CASE(BNV)                                                              \
+    case BNV:                                                                        \
+        return mode == 13 ? launch_bn<BNV, 13>(p, a, b, grid, s)                     \
+                          : launch_bn<BNV, 2>(p, a, b, grid, s);
+    switch (bn) {
+        FT_TC_CASE(16)
+        FT_TC_CASE(32)
+        FT_TC_CASE(64)
+        FT_TC_CASE(128)
+        FT_TC_CASE(256)
+        default: return cudaErrorInvalidValue;
+    }
+#undef FT_TC_CASE
+}
+
+cudaError_t tc_gather_rows(const __nv_bfloat16* x, const int32_t* pairs, const int32_t* n_rows_dev,
+                           int n_rows_max, int k, int H, __nv_bfloat16* xp, cudaStream_t s) {
+    const int64_t work = (int64_t)n_rows_max * (H / 8);
+    int blocks = (int)((work + 255) / 256);
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks < 1) blocks = 1;
+    tc::gather_rows_kernel<<<blocks, 256, 0, s>>>(x, pairs, n_rows_dev, n_rows_max, k, H, xp);
+    return cudaGetLastError();
+}
+
+}  // namespace ftmoe
