@@ -20,7 +20,7 @@ EXPORTS = (
     "ft_status_str", "ft_expert_blob_bytes", "ft_moe_create", "ft_moe_forward",
     "ft_cache_resize", "ft_cache_stats", "ft_cache_snapshot", "ft_moe_set_timing",
     "ft_moe_timing", "ft_moe_last_error", "ft_moe_destroy", "ft_router_logits",
-    "ft_topk_softmax",
+    "ft_topk_softmax", "ft_expert_ffn_noalloc",
 )
 
 
@@ -82,6 +82,7 @@ def lib():
         "ft_moe_destroy": (None, [VP]),
         "ft_router_logits": (I32, [P, I32, I32, P, I32, P, P]),
         "ft_topk_softmax": (I32, [P, I32, I32, I32, P, P, P]),
+        "ft_expert_ffn_noalloc": (I32, [P, I32, I32, I32, P, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -214,3 +215,9 @@ def router_logits(x, T, H, wr, E, logits, stream=None):
 def topk_softmax(logits, T, E, k, idx, w, stream=None):
     check(lib().ft_topk_softmax(_ptr(logits), int(T), int(E), int(k), _ptr(idx), _ptr(w),
                                 _stream(stream)))
+
+
+def expert_ffn_noalloc(blob, wfmt, hidden, inter, x, T, y, stream=None):
+    """Single-expert SwiGLU FFN with no device allocation (see include/ftmoe.h)."""
+    check(lib().ft_expert_ffn_noalloc(_ptr(blob), int(WFMT.get(wfmt, wfmt)), int(hidden),
+                                      int(inter), _ptr(x), int(T), _ptr(y), _stream(stream)))

@@ -199,6 +199,37 @@ FT_API ft_status ft_router_logits(const void* x, int32_t T, int32_t H, const flo
 FT_API ft_status ft_topk_softmax(const float* logits, int32_t T, int32_t E, int32_t k,
                           int32_t* idx, float* w, void* stream);
 
+/* ---- allocation-free single-expert FFN --------------------------------------------- */
+
+/* Scratch compiled into the library for ft_expert_ffn_noalloc, and its limits. */
+#define FT_NOALLOC_MAX_TOKENS 1024
+#define FT_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* One expert's SwiGLU FFN, y = W2 (silu(W1 x) * (W3 x)), with no device allocation at all.
+ * The pages have no counterpart to this call: it exists for callers that cannot allocate
+ * device memory when they need an expert's output — an engine that has given its whole
+ * VRAM budget to its own expert arena, a serving loop that forbids cudaMalloc/cudaFree
+ * after start-up because they can stall or synchronise the device mid-step, or a host whose
+ * memory belongs to an allocator this library cannot use. It runs the same CUDA-core
+ * streaming FFN kernels as ft_moe_forward and keeps its scratch (the bf16 activation and a
+ * one-entry work list) in a fixed FT_NOALLOC_SCRATCH_BYTES array built into the library,
+ * which every device that loads the library holds until the process exits.
+ *   blob    dev, one expert blob in the layout above, 256-byte aligned.
+ *   wfmt    ft_wfmt of the blob; hidden, inter: its H and I (multiples of 64).
+ *   x       dev bf16 [T][hidden], 16-byte aligned.
+ *   T       0 <= T <= FT_NOALLOC_MAX_TOKENS and T * inter * 2 <= FT_NOALLOC_SCRATCH_BYTES
+ *           - 4352; larger sizes return FT_ERR_INVALID without launching anything.
+ *   y       dev fp32 [T][hidden], 16-byte aligned, caller-owned.
+ *   stream  cudaStream_t as void*.
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture. All calls on a
+ * device share the array and each overwrites it; calls whose kernels can overlap on the GPU
+ * race, so order them on one stream. Errors: FT_ERR_INVALID (sizes, pointers, alignment),
+ * FT_ERR_CUDA (a launch or the address lookup failed). */
+FT_API ft_status ft_expert_ffn_noalloc(const void* blob, int32_t wfmt, int32_t hidden,
+                                       int32_t inter, const void* x, int32_t T, float* y,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif
