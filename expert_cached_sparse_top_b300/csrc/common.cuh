@@ -89,5 +89,8 @@ cudaError_t launch_ffn(int fmt, const FfnParams& p, int max_tokens, cudaStream_t
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H,
                            __nv_bfloat16* out, cudaStream_t s);
 int ffn_supported(int fmt, int hidden, int inter);
+cudaError_t launch_prefill_group(const int32_t* idx, int n_pairs, int E, int32_t* chunk_counts,
+                                 RouteBuffers rb, int32_t* err, cudaStream_t s);
+int prefill_chunks(int n_pairs);
 
 }  // namespace ftmoe

@@ -36,6 +36,13 @@ struct StageEvents {
     cudaEvent_t fill_begin, fill_end;
 };
 
+struct PrefillEvents {
+    cudaEvent_t c0, c1, g0, g1;          // compute begin/end, grouped GEMMs begin/end
+    cudaEvent_t f0[2], f1[2];            // up to two layer fills issued by the call
+    int n_fill;
+    double flops;
+};
+
 }  // namespace
 
 struct ft_moe {
@@ -89,6 +96,29 @@ struct ft_moe {
     int* d_ffn_err = nullptr;             // device address of the same word
     int num_sms = 148;
 
+    // prefill: two full-layer buffers and their own scratch
+    int32_t max_prefill = 0;
+    uint8_t* d_layerbuf[2] = {nullptr, nullptr};
+    int buf_layer[2] = {-1, -1};
+    bool buf_used[2] = {false, false};
+    cudaEvent_t ev_buf_ready[2] = {nullptr, nullptr};
+    cudaEvent_t ev_buf_free[2] = {nullptr, nullptr};
+    float* d_p_logits = nullptr;
+    int32_t* d_p_idx = nullptr;
+    float* d_p_w = nullptr;
+    int32_t* d_p_chunk = nullptr;
+    int32_t* d_p_err = nullptr;
+    uint8_t* d_p_route_mem = nullptr;
+    RouteBuffers p_rb{};
+    int64_t p_rows = 0;
+    __nv_bfloat16* d_p_xp = nullptr;
+    __nv_bfloat16* d_p_act = nullptr;
+    float* d_p_y = nullptr;
+    CUtensorMap tmP_A13[2]{}, tmP_A2[2]{};
+    CUtensorMap tmP_B13[5]{}, tmP_B2[5]{};     // per N tile width 16..256
+    bool p_b_ok[5] = {false, false, false, false, false};
+    std::vector<PrefillEvents> p_pending;
+
     bool timing = false;
     std::vector<StageEvents> pending;
     std::vector<cudaEvent_t> event_pool;
@@ -123,6 +153,7 @@ bool valid_config(const ft_moe_config* c, std::string* why) {
     if (c->cache_slots < 0 || c->cache_slots > (int64_t)c->layers * c->experts * 4 + 1024) { *why = "cache_slots out of range"; return false; }
     if ((int64_t)c->layers * c->experts >= (1LL << 31)) { *why = "too many keys"; return false; }
     if (c->flags != 0) { *why = "flags must be 0"; return false; }
+    if (c->max_prefill_tokens < 0 || (int64_t)c->max_prefill_tokens * c->top_k >= (1LL << 30)) { *why = "max_prefill_tokens out of range"; return false; }
     return true;
 }
 
@@ -212,6 +243,18 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_order[0]); cudaFree(h->d_order[1]); cudaFree(h->d_logits); cudaFree(h->d_idx);
     cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
     cudaFree(h->d_y); cudaFree(h->d_xp);
+    cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
+    cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
+    cudaFree(h->d_p_route_mem); cudaFree(h->d_p_xp); cudaFree(h->d_p_act); cudaFree(h->d_p_y);
+    for (int b = 0; b < 2; ++b) {
+        if (h->ev_buf_ready[b]) cudaEventDestroy(h->ev_buf_ready[b]);
+        if (h->ev_buf_free[b]) cudaEventDestroy(h->ev_buf_free[b]);
+    }
+    for (auto& pe : h->p_pending) {
+        for (cudaEvent_t ev : {pe.c0, pe.c1, pe.g0, pe.g1, pe.f0[0], pe.f0[1], pe.f1[0], pe.f1[1]})
+            if (ev) h->event_pool.push_back(ev);
+    }
+    h->p_pending.clear();
     if (h->h_mapped) cudaFreeHost(h->h_mapped);
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     if (h->ev_route) cudaEventDestroy(h->ev_route);
@@ -318,6 +361,85 @@ void collect_timing(ft_moe* h) {
         h->event_pool.push_back(se.fill_end);
     }
     h->pending.clear();
+    for (auto& pe : h->p_pending) {
+        cudaEventSynchronize(pe.c1);
+        h->tsum.prefill_calls++;
+        h->tsum.prefill_compute_ms += ev_ms(pe.c0, pe.c1);
+        h->tsum.prefill_ffn_ms += ev_ms(pe.g0, pe.g1);
+        h->tsum.prefill_flops += pe.flops;
+        for (int i = 0; i < pe.n_fill; ++i) {
+            cudaEventSynchronize(pe.f1[i]);
+            h->tsum.prefill_fill_ms += ev_ms(pe.f0[i], pe.f1[i]);
+        }
+        for (cudaEvent_t ev : {pe.c0, pe.c1, pe.g0, pe.g1, pe.f0[0], pe.f0[1], pe.f1[0], pe.f1[1]})
+            if (ev) h->event_pool.push_back(ev);
+    }
+    h->p_pending.clear();
+}
+
+int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
+
+// Prefill buffers: two full layers plus grouping scratch for max_prefill tokens.
+ft_status alloc_prefill(ft_moe* h) {
+    const ft_moe_config& c = h->cfg;
+    const int64_t E = c.experts, H = c.hidden, I = c.inter;
+    const int64_t npairs = (int64_t)h->max_prefill * c.top_k;
+    h->p_rows = (npairs + 255) / 256 * 256 + 256;
+    auto dm = [&](void** p, size_t n) -> cudaError_t { return cudaMalloc(p, n > 0 ? n : 16); };
+    for (int b = 0; b < 2; ++b) {
+        FT_CUDA(h, dm((void**)&h->d_layerbuf[b], (size_t)E * h->blob_bytes));
+        FT_CUDA(h, cudaEventCreateWithFlags(&h->ev_buf_ready[b], cudaEventDisableTiming));
+        FT_CUDA(h, cudaEventCreateWithFlags(&h->ev_buf_free[b], cudaEventDisableTiming));
+    }
+    FT_CUDA(h, dm((void**)&h->d_p_logits, (size_t)h->max_prefill * E * 4));
+    FT_CUDA(h, dm((void**)&h->d_p_idx, (size_t)npairs * 4));
+    FT_CUDA(h, dm((void**)&h->d_p_w, (size_t)npairs * 4));
+    FT_CUDA(h, dm((void**)&h->d_p_chunk, (size_t)prefill_chunks((int)npairs) * E * 4 + 64));
+    FT_CUDA(h, dm((void**)&h->d_p_err, 64));
+    FT_CUDA(h, cudaMemset(h->d_p_err, 0, 64));
+    {
+        const size_t bytes = 256 + 4 * ((size_t)E + (size_t)E + (size_t)E + 1 + (size_t)npairs) + 64;
+        FT_CUDA(h, dm((void**)&h->d_p_route_mem, bytes));
+        uint8_t* p = h->d_p_route_mem;
+        h->p_rb.counts = (RouteCounts*)p; p += 256;
+        h->p_rb.entry_e = (int32_t*)p; p += 4 * E;
+        h->p_rb.entry_dst = (int32_t*)p; p += 4 * E;
+        h->p_rb.entry_off = (int32_t*)p; p += 4 * (E + 1);
+        h->p_rb.pairs = (int32_t*)p;
+    }
+    FT_CUDA(h, dm((void**)&h->d_p_act, (size_t)h->p_rows * I * 2));
+    FT_CUDA(h, dm((void**)&h->d_p_y, (size_t)npairs * H * 4));
+    if (h->use_tc) {
+        FT_CUDA(h, dm((void**)&h->d_p_xp, (size_t)h->p_rows * H * 2));
+        for (int b = 0; b < 2; ++b) {
+            FT_CUDA(h, tc_encode_weights(&h->tmP_A13[b], h->d_layerbuf[b] + h->lay.off_w13, (int)H,
+                                         (int)(2 * I), E, h->lay.blob_bytes));
+            FT_CUDA(h, tc_encode_weights(&h->tmP_A2[b], h->d_layerbuf[b] + h->lay.off_w2, (int)I,
+                                         (int)H, E, h->lay.blob_bytes));
+        }
+    }
+    return FT_OK;
+}
+
+// Copy layer l's E blobs into layer buffer b on the copy stream, behind the last compute
+// that read the buffer.
+ft_status fill_layer(ft_moe* h, int b, int l, PrefillEvents* pe) {
+    if (h->buf_used[b]) FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_buf_free[b], 0));
+    if (h->timing && pe && pe->n_fill < 2) FT_CUDA(h, cudaEventRecord(pe->f0[pe->n_fill], h->copy_stream));
+    const int E = h->cfg.experts;
+    for (int e = 0; e < E; ++e) {
+        FT_CUDA(h, cudaMemcpyAsync(h->d_layerbuf[b] + (size_t)e * h->blob_bytes,
+                                   h->blobs[(size_t)l * E + e], h->blob_bytes,
+                                   cudaMemcpyHostToDevice, h->copy_stream));
+    }
+    FT_CUDA(h, cudaEventRecord(h->ev_buf_ready[b], h->copy_stream));
+    if (h->timing && pe && pe->n_fill < 2) {
+        FT_CUDA(h, cudaEventRecord(pe->f1[pe->n_fill], h->copy_stream));
+        pe->n_fill++;
+    }
+    h->buf_layer[b] = l;
+    h->tsum.prefill_fill_bytes += (uint64_t)E * h->blob_bytes;
+    return FT_OK;
 }
 
 }  // namespace
@@ -464,6 +586,11 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (st != FT_OK) return bail(st);
     st = encode_tc_maps(h);
     if (st != FT_OK) return bail(st);
+    h->max_prefill = cfg->max_prefill_tokens;
+    if (h->max_prefill > 0) {
+        st = alloc_prefill(h);
+        if (st != FT_OK) return bail(st);
+    }
     if (cudaEventRecord(h->ev_done, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cuda_fail(h, cudaGetLastError(), "create sync"); return bail(FT_ERR_CUDA);
     }
@@ -641,6 +768,115 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     st.stage_bytes += (uint64_t)rc.n_bypass * h->blob_bytes;
     st.resident += rc.n_fill - rc.n_evict;
     if (rc.err & 1) return fail(h, FT_ERR_INVALID, "NaN router logit");
+    return FT_OK;
+}
+
+ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, const float* logits,
+                         void* out, void* stream_) {
+    if (!h) return FT_ERR_INVALID;
+    if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
+    const ft_moe_config& c = h->cfg;
+    if (layer < 0 || layer >= c.layers) return fail(h, FT_ERR_INVALID, "layer out of range");
+    if (T < 0) return fail(h, FT_ERR_INVALID, "T out of range");
+    if (h->max_prefill <= 0) return fail(h, FT_ERR_STATE, "handle created without prefill buffers");
+    if (T > h->max_prefill) return fail(h, FT_ERR_INVALID, "T > max_prefill_tokens");
+    if (T == 0) return FT_OK;
+    if (!x || !out) return fail(h, FT_ERR_INVALID, "x/out is NULL");
+    if (!logits && !h->d_router) return fail(h, FT_ERR_INVALID, "no logits given and no router weights");
+    {
+        const uintptr_t xb = (uintptr_t)x, ob = (uintptr_t)out;
+        const uintptr_t n = (uintptr_t)T * c.hidden * 2;
+        if (xb < ob + n && ob < xb + n) return fail(h, FT_ERR_INVALID, "out overlaps x");
+        if ((xb | ob) & 15) return fail(h, FT_ERR_INVALID, "x/out must be 16-byte aligned");
+    }
+    cudaStream_t s = (cudaStream_t)stream_;
+    cudaSetDevice(h->dev);
+    if (*(volatile int*)h->h_ffn_err) {
+        h->broken = true;
+        return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait");
+    }
+    cudaError_t pe0 = cudaGetLastError();
+    if (pe0 != cudaSuccess) return cuda_fail(h, pe0, "earlier asynchronous error");
+    const int E = c.experts, k = c.top_k, H = c.hidden, I = c.inter;
+    const int npairs = T * k;
+    PrefillEvents pe{};
+    if (h->timing) {
+        pe.c0 = get_event(h); pe.c1 = get_event(h); pe.g0 = get_event(h); pe.g1 = get_event(h);
+        for (int i = 0; i < 2; ++i) { pe.f0[i] = get_event(h); pe.f1[i] = get_event(h); }
+    }
+    // the layer's weights: in a buffer already, or copied in now
+    int b = (h->buf_layer[0] == layer) ? 0 : (h->buf_layer[1] == layer) ? 1 : -1;
+    if (b < 0) {
+        b = (h->buf_layer[0] == layer + 1) ? 1 : (h->buf_layer[1] == layer + 1) ? 0 : (layer & 1);
+        ft_status fs = fill_layer(h, b, layer, &pe);
+        if (fs != FT_OK) { h->broken = true; return fs; }
+    }
+    // prefetch the next layer into the other buffer while this one computes
+    if (layer + 1 < c.layers && h->buf_layer[b ^ 1] != layer + 1) {
+        ft_status fs = fill_layer(h, b ^ 1, layer + 1, &pe);
+        if (fs != FT_OK) { h->broken = true; return fs; }
+    }
+    FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_done, 0));
+    FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_buf_ready[b], 0));
+    if (h->timing) FT_CUDA(h, cudaEventRecord(pe.c0, s));
+    const float* lg = logits;
+    if (!lg) {
+        FT_CUDA(h, launch_router_logits((const __nv_bfloat16*)x, T, H, h->d_router + (size_t)layer * E * H,
+                                        E, h->d_p_logits, s));
+        lg = h->d_p_logits;
+    }
+    FT_CUDA(h, launch_topk_softmax(lg, T, E, k, h->d_p_idx, h->d_p_w, nullptr, nullptr, h->d_p_err, s));
+    FT_CUDA(h, launch_prefill_group(h->d_p_idx, npairs, E, h->d_p_chunk, h->p_rb, h->d_p_err, s));
+    if (h->timing) FT_CUDA(h, cudaEventRecord(pe.g0, s));
+    if (h->use_tc) {
+        const int avg = (npairs + E - 1) / E;
+        const int bn = avg >= 160 ? 256 : tc_pick_bn(avg + avg / 2);
+        const int bi = bn_index(bn);
+        if (!h->p_b_ok[bi]) {
+            FT_CUDA(h, tc_encode_acts(&h->tmP_B13[bi], h->d_p_xp, H, (int)h->p_rows, bn));
+            FT_CUDA(h, tc_encode_acts(&h->tmP_B2[bi], h->d_p_act, I, (int)h->p_rows, bn));
+            h->p_b_ok[bi] = true;
+        }
+        FT_CUDA(h, tc_gather_rows((const __nv_bfloat16*)x, h->p_rb.pairs, nullptr, npairs, k, H, h->d_p_xp, s));
+        TcParams tp{};
+        tp.counts = h->p_rb.counts;
+        tp.entry_off = h->p_rb.entry_off;
+        tp.entry_dst = h->p_rb.entry_dst;
+        tp.pairs = h->p_rb.pairs;
+        tp.pass = 0;
+        tp.act = h->d_p_act; tp.act_ld = I;
+        tp.y = h->d_p_y; tp.y_ld = H;
+        tp.err = h->d_ffn_err;
+        tp.m_rows = 2 * I; tp.k_dim = H;
+        FT_CUDA(h, tc_launch(13, bn, tp, h->tmP_A13[b], h->tmP_B13[bi], h->num_sms, s));
+        tp.m_rows = H; tp.k_dim = I;
+        FT_CUDA(h, tc_launch(2, bn, tp, h->tmP_A2[b], h->tmP_B2[bi], h->num_sms, s));
+    } else {
+        FfnParams fp{};
+        fp.arena = h->d_layerbuf[b];
+        fp.lay = h->lay;
+        fp.hidden = H; fp.inter = I; fp.top_k = k;
+        fp.counts = h->p_rb.counts;
+        fp.entry_dst = h->p_rb.entry_dst;
+        fp.entry_off = h->p_rb.entry_off;
+        fp.pairs = h->p_rb.pairs;
+        fp.pass = 0;
+        fp.x = (const __nv_bfloat16*)x;
+        fp.act = h->d_p_act;
+        fp.y = h->d_p_y;
+        int launched = 0;
+        FT_CUDA(h, launch_ffn(c.wfmt, fp, T, s, &launched));
+    }
+    if (h->timing) FT_CUDA(h, cudaEventRecord(pe.g1, s));
+    FT_CUDA(h, launch_combine(h->d_p_y, h->d_p_w, T, k, H, (__nv_bfloat16*)out, s));
+    FT_CUDA(h, cudaEventRecord(h->ev_buf_free[b], s));
+    h->buf_used[b] = true;
+    FT_CUDA(h, cudaEventRecord(h->ev_done, s));
+    if (h->timing) {
+        FT_CUDA(h, cudaEventRecord(pe.c1, s));
+        pe.flops = 6.0 * (double)npairs * (double)H * (double)I;
+        h->p_pending.push_back(pe);
+    } 
     return FT_OK;
 }
 

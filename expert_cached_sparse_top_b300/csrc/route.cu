@@ -331,3 +331,104 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
 }
 
 }  // namespace ftmoe
+
+// ----------------------------------------------------------------------------------------
+// Prefill grouping: a stable counting sort of all T*k (token, rank) pairs by expert, over
+// chunks of kSortChunk pairs (one CTA per chunk), so thousands of tokens group in three
+// short launches: per-chunk histograms, one scan CTA, per-chunk stable scatter.
+// Every expert of the layer is an entry (entry e = expert e, weights in layer-buffer slot e).
+// ----------------------------------------------------------------------------------------
+namespace ftmoe {
+
+constexpr int kSortChunk = 1024;
+
+__global__ void __launch_bounds__(256) sort_count_kernel(const int32_t* __restrict__ idx, int n_pairs,
+                                                         int E, int32_t* __restrict__ chunk_counts,
+                                                         int32_t* __restrict__ err) {
+    __shared__ int hist[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int b = blockIdx.x * kSortChunk;
+    const int n = min(kSortChunk, n_pairs - b);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int e = idx[b + i];
+        if (e < 0 || e >= E) { atomicOr(err, 2); continue; }
+        atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One CTA: per-expert totals and per-chunk bases; entry_off = exclusive scan of totals.
+__global__ void __launch_bounds__(1024, 1) sort_scan_kernel(int32_t* __restrict__ chunk_counts, int n_chunks,
+                                                            int E, int n_pairs, RouteBuffers rb) {
+    __shared__ int s_warp[33];
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < E) {
+        for (int c = 0; c < n_chunks; ++c) {
+            int v = chunk_counts[(int64_t)c * E + e];
+            chunk_counts[(int64_t)c * E + e] = total;   // exclusive within the expert
+            total += v;
+        }
+    }
+    int tot_all = 0;
+    int off = block_excl_scan(e < E ? total : 0, s_warp, &tot_all);
+    if (e < E) {
+        rb.entry_off[e] = off;
+        rb.entry_e[e] = e;
+        rb.entry_dst[e] = e;
+        for (int c = 0; c < n_chunks; ++c) chunk_counts[(int64_t)c * E + e] += off;
+    }
+    if (e == 0) {
+        rb.entry_off[E] = n_pairs;
+        RouteCounts rc;
+        rc.n_unique = E; rc.n_hits = E; rc.n_miss = 0; rc.n_fill = 0; rc.n_bypass = 0;
+        rc.n_evict = 0; rc.err = 0; rc.pad = 0;
+        *rb.counts = rc;
+    }
+}
+
+// One warp per chunk: stable scatter in 32-pair batches (match_any groups equal experts).
+__global__ void __launch_bounds__(32) sort_scatter_kernel(const int32_t* __restrict__ idx, int n_pairs,
+                                                          int E, const int32_t* __restrict__ chunk_base,
+                                                          int32_t* __restrict__ pairs) {
+    __shared__ int cursor[kMaxExperts];
+    const int lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[(int64_t)blockIdx.x * E + e];
+    __syncwarp();
+    const int b = blockIdx.x * kSortChunk;
+    const int n = min(kSortChunk, n_pairs - b);
+    for (int s = 0; s < n; s += 32) {
+        const int i = s + lane;
+        int e = -1;
+        if (i < n) {
+            e = idx[b + i];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned mask = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(mask) - 1;
+        const int rk = __popc(mask & ((1u << lane) - 1u));
+        int base = 0;
+        if (lane == leader && e >= 0) {
+            base = cursor[e];
+            cursor[e] = base + __popc(mask);
+        }
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (e >= 0) pairs[base + rk] = b + i;
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_prefill_group(const int32_t* idx, int n_pairs, int E, int32_t* chunk_counts,
+                                 RouteBuffers rb, int32_t* err, cudaStream_t s) {
+    const int n_chunks = (n_pairs + kSortChunk - 1) / kSortChunk;
+    sort_count_kernel<<<n_chunks, 256, 0, s>>>(idx, n_pairs, E, chunk_counts, err);
+    sort_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, n_chunks, E, n_pairs, rb);
+    sort_scatter_kernel<<<n_chunks, 32, 0, s>>>(idx, n_pairs, E, chunk_counts, rb.pairs);
+    return cudaGetLastError();
+}
+
+int prefill_chunks(int n_pairs) { return (n_pairs + kSortChunk - 1) / kSortChunk; }
+
+}  // namespace ftmoe

@@ -187,15 +187,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
     const int m_tiles = (p.m_rows + kBM - 1) / kBM;
     const int k_steps = p.k_dim / kBK;
 
-    // tile prefix over this pass's entries
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int i = 0; i < n_entries; ++i) {
-            s_prefix[i] = acc;
-            const int n = p.entry_off[u_begin + i + 1] - p.entry_off[u_begin + i];
-            acc += m_tiles * ((n + BN - 1) / BN);
+    // tile prefix over this pass's entries: tiles per entry in parallel, then one warp scans
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
+        const int n = p.entry_off[u_begin + i + 1] - p.entry_off[u_begin + i];
+        s_prefix[i] = m_tiles * ((n + BN - 1) / BN);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (n_entries + 31) / 32;
+        const int i0 = lane * per, i1 = min(n_entries, i0 + per);
+        int local = 0;
+        for (int i = i0; i < i1; ++i) local += s_prefix[i];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        s_prefix[n_entries] = acc;
+        int run = incl - local;
+        for (int i = i0; i < i1; ++i) { const int t = s_prefix[i]; s_prefix[i] = run; run += t; }
+        if (lane == 31) s_prefix[n_entries] = incl;
     }
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -378,8 +389,8 @@ EncodeTiledFn encode_fn() {
 template <int BN>
 int stages_for() {
     const int stage = 128 * 64 * 2 + BN * 64 * 2;
-    int s = (200 * 1024) / stage;
-    return s > 8 ? 8 : s;
+    int s = (216 * 1024) / stage;
+    return s > 12 ? 12 : s;
 }
 
 template <int BN>

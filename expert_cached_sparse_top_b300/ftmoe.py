@@ -20,7 +20,7 @@ EXPORTS = (
     "ft_status_str", "ft_expert_blob_bytes", "ft_moe_create", "ft_moe_forward",
     "ft_cache_resize", "ft_cache_stats", "ft_cache_snapshot", "ft_moe_set_timing",
     "ft_moe_timing", "ft_moe_last_error", "ft_moe_destroy", "ft_router_logits",
-    "ft_topk_softmax", "ft_expert_ffn_noalloc",
+    "ft_topk_softmax", "ft_expert_ffn_noalloc", "ft_moe_prefill",
 )
 
 
@@ -30,7 +30,7 @@ class FtMoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("wfmt", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("cache_slots", ctypes.c_int64), ("flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("max_prefill_tokens", ctypes.c_int32)]
 
 
 class FtCacheStats(ctypes.Structure):
@@ -49,7 +49,10 @@ class FtTiming(ctypes.Structure):
                 ("fill_ms", ctypes.c_double), ("ffn_miss_ms", ctypes.c_double),
                 ("combine_ms", ctypes.c_double), ("total_ms", ctypes.c_double),
                 ("forwards", ctypes.c_uint64), ("ffn_launches", ctypes.c_uint64),
-                ("ffn_weight_bytes", ctypes.c_uint64), ("kernel_launches", ctypes.c_uint64)]
+                ("ffn_weight_bytes", ctypes.c_uint64), ("kernel_launches", ctypes.c_uint64),
+                ("prefill_calls", ctypes.c_uint64), ("prefill_fill_ms", ctypes.c_double),
+                ("prefill_compute_ms", ctypes.c_double), ("prefill_ffn_ms", ctypes.c_double),
+                ("prefill_flops", ctypes.c_double), ("prefill_fill_bytes", ctypes.c_uint64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -83,6 +86,7 @@ def lib():
         "ft_router_logits": (I32, [P, I32, I32, P, I32, P, P]),
         "ft_topk_softmax": (I32, [P, I32, I32, I32, P, P, P]),
         "ft_expert_ffn_noalloc": (I32, [P, I32, I32, I32, P, I32, P, P]),
+        "ft_moe_prefill": (I32, [VP, I32, P, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -115,9 +119,10 @@ def _stream(s):
     return s.cuda_stream
 
 
-def make_config(layers, experts, hidden, inter, top_k, max_tokens, wfmt, cache_slots, device=0):
+def make_config(layers, experts, hidden, inter, top_k, max_tokens, wfmt, cache_slots, device=0,
+                max_prefill_tokens=0):
     return FtMoeConfig(layers, experts, hidden, inter, top_k, max_tokens,
-                       WFMT.get(wfmt, wfmt), device, cache_slots, 0, 0)
+                       WFMT.get(wfmt, wfmt), device, cache_slots, 0, max_prefill_tokens)
 
 
 def blob_bytes(cfg):
@@ -163,6 +168,14 @@ class MoECache:
         """Same call, returning the raw status instead of raising."""
         return lib().ft_moe_forward(self.h, int(layer), _ptr(x), int(T), _ptr(logits),
                                     _ptr(out), _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+
+    def prefill(self, layer, x, T, out, logits=None, stream=None):
+        check(lib().ft_moe_prefill(self.h, int(layer), _ptr(x), int(T), _ptr(logits), _ptr(out),
+                                   _stream(stream)), self.h)
+
+    def prefill_status(self, layer, x, T, out, logits=None, stream=None):
+        return lib().ft_moe_prefill(self.h, int(layer), _ptr(x), int(T), _ptr(logits), _ptr(out),
+                                    _stream(stream))
 
     def resize(self, new_slots):
         check(lib().ft_cache_resize(self.h, int(new_slots)), self.h)

@@ -81,7 +81,7 @@ typedef struct {
     int32_t device;       /* CUDA device ordinal */
     int64_t cache_slots;  /* C: GPU expert slots, one global LRU over all layers (>= 0) */
     int32_t flags;        /* reserved, must be 0 */
-    int32_t reserved;
+    int32_t max_prefill_tokens; /* largest T passed to ft_moe_prefill; 0 = no prefill buffers */
 } ft_moe_config;
 
 typedef struct {
@@ -110,6 +110,13 @@ typedef struct {
     uint64_t ffn_launches;/* expert-FFN kernel launches recorded (hit and miss passes) */
     uint64_t ffn_weight_bytes; /* expert weight bytes those launches were given to stream */
     uint64_t kernel_launches;  /* all kernels launched by the recorded calls */
+    /* ft_moe_prefill calls */
+    uint64_t prefill_calls;
+    double prefill_fill_ms;    /* full-layer H2D copies (copy stream) */
+    double prefill_compute_ms; /* routing + grouping + FFN + combine on the caller's stream */
+    double prefill_ffn_ms;     /* the two grouped-GEMM launches (W13+SwiGLU, W2) */
+    double prefill_flops;      /* 6 * T * k * H * I per call (dense-equivalent FFN flops) */
+    uint64_t prefill_fill_bytes;
 } ft_timing_t;
 
 typedef struct ft_moe ft_moe;
@@ -158,6 +165,24 @@ FT_API ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expe
 FT_API ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T,
                          const float* logits, void* out, int32_t* topk_idx, float* topk_w,
                          void* stream);
+
+/* One MoE layer forward for a prefill-sized batch, with full-layer double buffering
+ * ("Three mechanisms", semantic-aware caching: during prefill, layer l+1 streams while the
+ * GPU computes layer l; "The gap it targets": prefill routes thousands of tokens to nearly
+ * every expert, so the whole layer is needed). The LRU cache is not consulted or changed.
+ *   layer   0 <= layer < layers. If the layer is not already in one of the two layer
+ *           buffers, its E blobs are copied in on the copy stream first; the call then
+ *           prefetches layer + 1 into the other buffer (behind the last compute that read
+ *           it) before enqueuing this layer's compute, so calling layers in order overlaps
+ *           each layer's compute with the next layer's copies.
+ *   x       dev bf16 [T][H]; T <= max_prefill_tokens (T = 0 returns FT_OK).
+ *   logits  dev fp32 [T][E] or NULL (router computed from x).
+ *   out     dev bf16 [T][H], must not overlap x.
+ *   stream  caller's stream; compute is stream-ordered after the layer's copies.
+ * Needs a handle created with max_prefill_tokens > 0 (FT_ERR_STATE otherwise). The call
+ * does not block the host. Errors: FT_ERR_INVALID, FT_ERR_STATE, FT_ERR_CUDA. */
+FT_API ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T,
+                                const float* logits, void* out, void* stream);
 
 /* Rebuild the cache under a new slot budget at a safe point ("Three mechanisms", elastic
  * memory management). Synchronises the handle. The min(new_slots, resident) most recently

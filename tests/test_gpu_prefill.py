@@ -1,0 +1,132 @@
+"""Prefill-sized MoE layer forward with double-buffered full-layer streaming (C ABI) vs the
+oracle: each layer's output within the normwise tolerance, refills bit-identical."""
+import numpy as np
+import pytest
+
+import workloads as W
+from workloads.host import HostPool
+from ref import TOL, OracleExperts, bf16_dev_to_f64, normwise_err, oracle_call, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ft():
+    import torch
+    from expert_cached_sparse_top_b300 import build
+    build.build()
+    from expert_cached_sparse_top_b300 import ftmoe
+    ftmoe.lib()
+    torch.cuda.init()
+    return ftmoe
+
+
+def _make(ft, cfg, pool, T, router=None, capacity=1):
+    c = ft.make_config(cfg.layers, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, 16, cfg.wfmt,
+                       capacity, max_prefill_tokens=T)
+    return ft.MoECache(c, pool.ptrs, router)
+
+
+def _run(cache, cfg, layer, x_bits, logits=None):
+    import torch
+    T = x_bits.shape[0]
+    out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    lg = to_dev(logits) if logits is not None else None
+    cache.prefill(layer, to_dev_bf16(x_bits), T, out, logits=lg)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_prefill_bf16_layers_in_order(ft):
+    """35B-A3B-shaped layer (128 experts, top-8, ~256 tokens per expert), 4096 tokens, four
+    layers streamed in order, then layer 0 again (a refill). Pool aliased onto 131 blobs so
+    every layer has different weights."""
+    import torch
+    cfg = W.config("prefill_bf16")
+    pool = HostPool(cfg, images=131)
+    cache = _make(ft, cfg, pool, cfg.tokens)
+    experts = OracleExperts(pool, max_cached=131)
+    first = None
+    for layer in (0, 1, 2, 3, 0):
+        x, logits = W.prefill_inputs(cfg, layer)
+        out = _run(cache, cfg, layer, x, logits)
+        if layer == 0 and first is not None:
+            assert torch.equal(out, first)            # refilled buffer, same result
+            continue
+        if layer == 0:
+            first = out.clone()
+        tokens = None if layer in (0, 3) else np.arange(0, cfg.tokens, 7)
+        ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=tokens)
+        got = bf16_dev_to_f64(out)
+        if tokens is not None:
+            got = got[tokens]
+        assert normwise_err(got, ref) <= TOL["bf16"], layer
+    st = cache.stats()
+    assert st["hits"] == 0 and st["misses"] == 0          # the LRU is not consulted
+    cache.close()
+
+
+def test_prefill_ragged_token_counts(ft):
+    """T far from a multiple of anything; few tokens per expert (small N tiles)."""
+    cfg = W.config("prefill_bf16", layers=2)
+    pool = HostPool(cfg, images=131)
+    cache = _make(ft, cfg, pool, 1000)
+    experts = OracleExperts(pool, max_cached=131)
+    for layer, T in ((0, 1000), (1, 37), (0, 1)):
+        x, logits = W.prefill_inputs(cfg, layer, tokens=T)
+        out = _run(cache, cfg, layer, x, logits)
+        ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k)
+        assert normwise_err(bf16_dev_to_f64(out), ref) <= TOL["bf16"], (layer, T)
+    cache.close()
+
+
+def test_prefill_mxfp4_shape(ft):
+    """284B-shaped layer (256 experts, top-6, MXFP4) on the CUDA-core FFN path."""
+    cfg = W.config("prefill_mxfp4", layers=2)
+    pool = HostPool(cfg, images=13)
+    T = 512
+    cache = _make(ft, cfg, pool, T)
+    experts = OracleExperts(pool, max_cached=13)
+    for layer in (0, 1):
+        x, logits = W.prefill_inputs(cfg, layer, tokens=T)
+        out = _run(cache, cfg, layer, x, logits)
+        sample = np.arange(0, T, 5)
+        ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample)
+        assert normwise_err(bf16_dev_to_f64(out)[sample], ref) <= TOL["mxfp4"], layer
+    cache.close()
+
+
+def test_prefill_router_in_the_loop(ft):
+    from oracle import formats, moe
+    cfg = W.config("tiny", tokens=64)
+    pool = HostPool(cfg)
+    router = W.router_weights(cfg)
+    cache = _make(ft, cfg, pool, 64, router=router)
+    x = W.tiny_inputs(cfg)
+    ref_logits = moe.router_logits(formats.bf16_to_f64(x), router[0])
+    srt = np.sort(ref_logits, axis=1)[:, ::-1]
+    keep = np.nonzero(srt[:, cfg.top_k - 1] - srt[:, cfg.top_k] > 1e-4)[0]
+    out = _run(cache, cfg, 0, x)
+    experts = OracleExperts(pool)
+    ref, _, _ = oracle_call(experts, 0, x, ref_logits, cfg.top_k, tokens=keep)
+    assert len(keep) > 48
+    assert normwise_err(bf16_dev_to_f64(out)[keep], ref) <= TOL["bf16"]
+    cache.close()
+
+
+def test_prefill_errors(ft):
+    import torch
+    cfg = W.config("tiny")
+    pool = HostPool(cfg)
+    c = ft.make_config(1, 8, 256, 128, 2, 16, "bf16", 4)          # no prefill buffers
+    cache = ft.MoECache(c, pool.ptrs, None)
+    x = torch.zeros((16, 256), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    lg = torch.zeros((16, 8), dtype=torch.float32, device="cuda")
+    assert cache.prefill_status(0, x, 16, out, logits=lg) == ft.FT_ERR_STATE
+    cache.close()
+    cache = _make(ft, cfg, pool, 16)
+    assert cache.prefill_status(0, x, 17, out, logits=lg) == ft.FT_ERR_INVALID
+    assert cache.prefill_status(1, x, 16, out, logits=lg) == ft.FT_ERR_INVALID
+    assert cache.prefill_status(0, x, 0, out, logits=lg) == ft.FT_OK
+    cache.close()
