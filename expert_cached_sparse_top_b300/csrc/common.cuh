@@ -33,6 +33,7 @@ struct RouteBuffers {
     int32_t* pairs;        // [max_pairs] pair index p = t*k + j, grouped by entry, ascending p
     int32_t* miss_key;     // [max_u] key of miss j (ascending expert id)
     int32_t* miss_dst;     // [max_u] destination of miss j
+    int32_t* dep;          // [max_u] per-entry W13 completion counters of the fused FFN (zeroed here)
 };
 
 // Host-mapped mirror of the fill list (the host issues one copy per miss).

@@ -88,6 +88,7 @@ struct ft_moe {
 
     // tcgen05 expert FFN (BF16 weights)
     bool use_tc = false;
+    bool tc_fused = true;                 // W13 and W2 in one launch (FTMOE_TC_FUSED=0: two)
     int tc_bn = 16;
     int64_t act_rows = 0;                 // rows allocated for d_act / d_xp
     __nv_bfloat16* d_xp = nullptr;        // [act_rows][H] activations in grouped-row order
@@ -398,14 +399,15 @@ ft_status alloc_prefill(ft_moe* h) {
     FT_CUDA(h, dm((void**)&h->d_p_err, 64));
     FT_CUDA(h, cudaMemset(h->d_p_err, 0, 64));
     {
-        const size_t bytes = 256 + 4 * ((size_t)E + (size_t)E + (size_t)E + 1 + (size_t)npairs) + 64;
+        const size_t bytes = 256 + 4 * ((size_t)E + (size_t)E + (size_t)E + 1 + (size_t)npairs + (size_t)E) + 64;
         FT_CUDA(h, dm((void**)&h->d_p_route_mem, bytes));
         uint8_t* p = h->d_p_route_mem;
         h->p_rb.counts = (RouteCounts*)p; p += 256;
         h->p_rb.entry_e = (int32_t*)p; p += 4 * E;
         h->p_rb.entry_dst = (int32_t*)p; p += 4 * E;
         h->p_rb.entry_off = (int32_t*)p; p += 4 * (E + 1);
-        h->p_rb.pairs = (int32_t*)p;
+        h->p_rb.pairs = (int32_t*)p; p += 4 * (size_t)npairs;
+        h->p_rb.dep = (int32_t*)p;
     }
     FT_CUDA(h, dm((void**)&h->d_p_act, (size_t)h->p_rows * I * 2));
     FT_CUDA(h, dm((void**)&h->d_p_y, (size_t)npairs * H * 4));
@@ -536,6 +538,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     {
         const char* ffn = getenv("FTMOE_FFN");
         h->use_tc = cfg->wfmt == FT_W_BF16 && !(ffn && strcmp(ffn, "simt") == 0);
+        const char* fz = getenv("FTMOE_TC_FUSED");
+        h->tc_fused = !(fz && strcmp(fz, "0") == 0);
         h->tc_bn = tc_pick_bn(cfg->max_tokens);
         h->act_rows = ((int64_t)h->max_pairs + h->tc_bn - 1) / h->tc_bn * h->tc_bn + h->tc_bn;
         int dev_sms = 0;
@@ -547,7 +551,7 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (!dmalloc((void**)&h->d_y, (size_t)h->max_pairs * H * 4)) return bail(FT_ERR_OOM);
     {
         const size_t mu = (size_t)h->max_u;
-        const size_t bytes = 256 + 4 * (mu + mu + (mu + 1) + (size_t)h->max_pairs + mu + mu) + 64;
+        const size_t bytes = 256 + 4 * (mu + mu + (mu + 1) + (size_t)h->max_pairs + mu + mu + mu) + 64;
         if (!dmalloc((void**)&h->d_route_mem, bytes)) return bail(FT_ERR_OOM);
         uint8_t* p = h->d_route_mem;
         h->rb.counts = (RouteCounts*)p; p += 256;
@@ -556,7 +560,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->rb.entry_off = (int32_t*)p; p += 4 * (mu + 1);
         h->rb.pairs = (int32_t*)p; p += 4 * (size_t)h->max_pairs;
         h->rb.miss_key = (int32_t*)p; p += 4 * mu;
-        h->rb.miss_dst = (int32_t*)p;
+        h->rb.miss_dst = (int32_t*)p; p += 4 * mu;
+        h->rb.dep = (int32_t*)p;
         const size_t hbytes = 256 + 8 * mu + 64 + 64;
         if (cudaHostAlloc((void**)&h->h_mapped, hbytes, cudaHostAllocMapped) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(route view)"); return bail(FT_ERR_OOM);
@@ -696,13 +701,20 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             return launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches);
         }
         tp.pass = pass;
-        tp.m_rows = 2 * c.inter; tp.k_dim = H;
-        cudaError_t e = tc_launch(13, h->tc_bn, tp, h->tmA13, h->tmB13, h->num_sms, s);
+        tp.hidden = H; tp.inter = c.inter;
+        const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};
+        if (h->tc_fused) {
+            tp.phases = 3; tp.dep = h->rb.dep;
+            launches += 1;
+            return tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
+        }
+        tp.dep = nullptr;
+        tp.phases = 1;
+        cudaError_t e = tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
         if (e != cudaSuccess) return e;
-        tp.m_rows = H; tp.k_dim = c.inter;
-        e = tc_launch(2, h->tc_bn, tp, h->tmA2, h->tmB2, h->num_sms, s);
+        tp.phases = 2;
         launches += 2;
-        return e;
+        return tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
     };
     FT_CUDA(h, run_ffn(0));
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[2], s));
@@ -752,7 +764,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         FT_CUDA(h, cudaEventRecord(se.ev[5], s));
         h->pending.push_back(se);
         h->tsum.forwards++;
-        h->tsum.ffn_launches += rc.n_miss > 0 ? 4 : 2;
+        h->tsum.ffn_launches += rc.n_miss > 0 ? 2 : 1;
         uint64_t wbytes = (uint64_t)rc.n_unique * (uint64_t)(h->lay.blob_bytes);
         h->tsum.ffn_weight_bytes += wbytes;
         h->tsum.kernel_launches += (uint64_t)launches;
@@ -847,10 +859,17 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         tp.act = h->d_p_act; tp.act_ld = I;
         tp.y = h->d_p_y; tp.y_ld = H;
         tp.err = h->d_ffn_err;
-        tp.m_rows = 2 * I; tp.k_dim = H;
-        FT_CUDA(h, tc_launch(13, bn, tp, h->tmP_A13[b], h->tmP_B13[bi], h->num_sms, s));
-        tp.m_rows = H; tp.k_dim = I;
-        FT_CUDA(h, tc_launch(2, bn, tp, h->tmP_A2[b], h->tmP_B2[bi], h->num_sms, s));
+        tp.hidden = H; tp.inter = I;
+        const TcMaps maps{&h->tmP_A13[b], &h->tmP_B13[bi], &h->tmP_A2[b], &h->tmP_B2[bi]};
+        if (h->tc_fused) {
+            tp.phases = 3; tp.dep = h->p_rb.dep;
+            FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
+        } else {
+            tp.phases = 1;
+            FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
+            tp.phases = 2;
+            FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
+        }
     } else {
         FfnParams fp{};
         fp.arena = h->d_layerbuf[b];

@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kLookupThreads, 1) lookup_kernel(LookupParams 
     // Entries: hits [0, n_hits), misses [n_hits, U).
     if (e < E && present) {
         int ent = is_hit ? hit_rank : n_hits + s_sub[e];
+        if (p.rb.dep) p.rb.dep[ent] = 0;
         p.rb.entry_e[ent] = e;
         if (is_hit) p.rb.entry_dst[ent] = slot;
         s_cnt[ent] = 0;
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(1024, 1) sort_scan_kernel(int32_t* __restrict_
     if (e < E) {
         rb.entry_off[e] = off;
         rb.entry_e[e] = e;
+        if (rb.dep) rb.dep[e] = 0;
         rb.entry_dst[e] = e;
         for (int c = 0; c < n_chunks; ++c) chunk_counts[(int64_t)c * E + e] += off;
     }

@@ -160,9 +160,64 @@ __device__ __forceinline__ void locate(const int* s_prefix, int n_entries, int m
     *mt = r % m_tiles;
 }
 
-template <int BN, int MODE>
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until every W13 tile of an entry has published its activation rows.
+__device__ __forceinline__ bool wait_dep(const int* dep, int target, int* err) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (ld_acquire(dep) >= target) return true;
+        if ((i & 255u) == 255u && *(volatile int*)err) return false;
+        __nanosleep(64);
+    }
+    atomicCAS(err, 0, 6);
+    return false;
+}
+
+struct Tile {
+    int phase;      // 13: W13 + SwiGLU, 2: W2
+    int u;          // entry
+    int mt, nt;     // 128-row weight tile, BN-token tile
+    int ent_rel;    // entry index within the pass
+};
+
+// Tile t of the launch: W13 tiles of all entries first, then W2 tiles. Within a phase,
+// entries in order, then N tiles, then M tiles (M innermost: concurrently running CTAs share
+// an entry's activation rows in L2).
+__device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, int u_begin,
+                                        int m13, int m2, int phases) {
+    const int nt_total = s_nt[n_entries];
+    Tile r;
+    int m_tiles;
+    if ((phases & 1) && t < m13 * nt_total) { r.phase = 13; m_tiles = m13; }
+    else {
+        if (phases & 1) t -= m13 * nt_total;
+        r.phase = 2; m_tiles = m2;
+    }
+    int lo = 0, hi = n_entries - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_nt[mid] * m_tiles <= t) lo = mid; else hi = mid - 1;
+    }
+    const int rr = t - s_nt[lo] * m_tiles;
+    r.ent_rel = lo;
+    r.u = u_begin + lo;
+    r.nt = rr / m_tiles;
+    r.mt = rr % m_tiles;
+    return r;
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
-    TcParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    TcParams p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
+    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr int A_BYTES = kBM * kBK * 2;            // 16 KB
     constexpr int B_BYTES = BN * kBK * 2;
     constexpr int STAGE = A_BYTES + B_BYTES;
@@ -176,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
     uint64_t* tfull = empty + S;       // [2]
     uint64_t* tempty = tfull + 2;      // [2]
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
-    int* s_prefix = reinterpret_cast<int*>(s_tmem + 4);   // [kMaxExperts + 1]
+    int* s_nt = reinterpret_cast<int*>(s_tmem + 4);   // [kMaxExperts + 1] N-tile prefix
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RouteCounts rc = *p.counts;
@@ -184,20 +239,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
     const int u_end = p.pass == 0 ? rc.n_hits : rc.n_unique;
     const int n_entries = u_end - u_begin;
     if (n_entries <= 0) return;
-    const int m_tiles = (p.m_rows + kBM - 1) / kBM;
-    const int k_steps = p.k_dim / kBK;
+    const int H = p.hidden, I = p.inter;
+    const int m13 = (2 * I + kBM - 1) / kBM, m2 = (H + kBM - 1) / kBM;
+    const int phases = p.phases;
+    const bool fused = phases == 3 && p.dep != nullptr;
 
-    // tile prefix over this pass's entries: tiles per entry in parallel, then one warp scans
+    // N-tile prefix over this pass's entries: counts in parallel, then one warp scans
     for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
         const int n = p.entry_off[u_begin + i + 1] - p.entry_off[u_begin + i];
-        s_prefix[i] = m_tiles * ((n + BN - 1) / BN);
+        s_nt[i] = (n + BN - 1) / BN;
     }
     __syncthreads();
     if (warp == 0) {
         const int per = (n_entries + 31) / 32;
         const int i0 = lane * per, i1 = min(n_entries, i0 + per);
         int local = 0;
-        for (int i = i0; i < i1; ++i) local += s_prefix[i];
+        for (int i = i0; i < i1; ++i) local += s_nt[i];
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -205,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
             if (lane >= o) incl += v;
         }
         int run = incl - local;
-        for (int i = i0; i < i1; ++i) { const int t = s_prefix[i]; s_prefix[i] = run; run += t; }
-        if (lane == 31) s_prefix[n_entries] = incl;
+        for (int i = i0; i < i1; ++i) { const int t = s_nt[i]; s_nt[i] = run; run += t; }
+        if (lane == 31) s_nt[n_entries] = incl;
     }
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -222,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
-    const int total = s_prefix[n_entries];
+    const int nt_total = s_nt[n_entries];
+    const int total = ((phases & 1) ? m13 * nt_total : 0) + ((phases & 2) ? m2 * nt_total : 0);
     int* err = p.err;
 
     if (warp == 0) {
@@ -230,19 +288,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                int ur, mt, nt;
-                locate(s_prefix, n_entries, m_tiles, t, &ur, &mt, &nt);
-                const int u = u_begin + ur;
-                const int slot = p.entry_dst[u];
-                const int row_b = p.entry_off[u] + nt * BN;
-                for (int kb = 0; kb < k_steps; ++kb, ++it) {
+                const Tile tl = tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+                const bool w13 = tl.phase == 13;
+                const CUtensorMap* mA = w13 ? &tmA13 : &tmA2;
+                const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
+                const int k_steps = (w13 ? H : I) / kBK;
+                const int slot = p.entry_dst[tl.u];
+                const int row_b = p.entry_off[tl.u] + tl.nt * BN;
+                int kb0 = 0;
+                if (!w13 && fused) {
+                    // stream this tile's first weight stages while the entry's W13 tiles finish
+                    const int npre = min(S, k_steps);
+                    const uint32_t it0 = it;
+                    for (int kb = 0; kb < npre; ++kb, ++it) {
+                        const int s = it % S;
+                        if (!mbar_wait(&empty[s], ((it / S) & 1u) ^ 1u, err, 1)) { ok = false; break; }
+                        mbar_expect_tx(&full[s], STAGE);
+                        tma_load_3d(smem + s * STAGE, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
+                    }
+                    if (!ok) break;
+                    const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
+                    if (!wait_dep(p.dep + tl.u, target, err)) {
+                        // the stages armed above still expect their activation bytes: load
+                        // them (rows already written or not) so the ring can drain
+                        fence_proxy_async_global();
+                        for (int kb = 0; kb < npre; ++kb) {
+                            const int s = (it0 + kb) % S;
+                            tma_load_2d(smem + s * STAGE + A_BYTES, mB, &full[s], kb * kBK, row_b);
+                        }
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                    for (int kb = 0; kb < npre; ++kb) {
+                        const int s = (it0 + kb) % S;
+                        tma_load_2d(smem + s * STAGE + A_BYTES, mB, &full[s], kb * kBK, row_b);
+                    }
+                    kb0 = npre;
+                }
+                for (int kb = kb0; kb < k_steps; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, err, 1)) { ok = false; break; }
                     uint8_t* sa = smem + s * STAGE;
                     mbar_expect_tx(&full[s], STAGE);
-                    tma_load_3d(sa, &tmA, &full[s], kb * kBK, mt * kBM, slot);
-                    tma_load_2d(sa + A_BYTES, &tmB, &full[s], kb * kBK, row_b);
+                    tma_load_3d(sa, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
+                    tma_load_2d(sa + A_BYTES, mB, &full[s], kb * kBK, row_b);
                 }
             }
             // drain: every issued stage must land before the CTA may exit
@@ -253,12 +344,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t it = 0, tl = 0;
-            constexpr uint32_t idesc = idesc_bf16(BN);
+            uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tl) {
-                const uint32_t acc = tl & 1u;
-                const uint32_t aph = (tl >> 1) & 1u;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+                const Tile tl = tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+                const int k_steps = (tl.phase == 13 ? H : I) / kBK;
+                // N of this tile: its token count rounded up to 16 (a tail tile does no
+                // padded work); the accumulator keeps BN columns
+                const int row_b = p.entry_off[tl.u] + tl.nt * BN;
+                const int n_valid = min(BN, p.entry_off[tl.u + 1] - row_b);
+                const uint32_t idesc = idesc_bf16(min(BN, (n_valid + 15) & ~15));
+                const uint32_t acc = tcount & 1u;
+                const uint32_t aph = (tcount >> 1) & 1u;
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, err, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -284,25 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
         // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
-        uint32_t tl = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl) {
-            int ur, mt, nt;
-            locate(s_prefix, n_entries, m_tiles, t, &ur, &mt, &nt);
-            const int u = u_begin + ur;
-            const int row_b = p.entry_off[u] + nt * BN;
-            const int n_valid = min(BN, p.entry_off[u + 1] - row_b);
-            const uint32_t acc = tl & 1u;
-            const uint32_t aph = (tl >> 1) & 1u;
+        uint32_t tcount = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+            const Tile tl = tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+            const bool w13 = tl.phase == 13;
+            const int m_rows = w13 ? 2 * I : H;
+            const int row_b = p.entry_off[tl.u] + tl.nt * BN;
+            const int n_valid = min(BN, p.entry_off[tl.u + 1] - row_b);
+            const uint32_t acc = tcount & 1u;
+            const uint32_t aph = (tcount >> 1) & 1u;
             if (!mbar_wait(&tfull[acc], aph, err, 4)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            const int m = mt * kBM + row_in_tile;
+            const int m = tl.mt * kBM + row_in_tile;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 16) {
+            for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(tbase + c0, r);
                 tmem_wait_ld();
-                if (MODE == 13) {
+                if (w13) {
                     // lanes 2i / 2i+1 hold the gate / up rows of output feature i
                     float own[16];
 #pragma unroll
@@ -317,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
                         const float g = odd ? recv : own[j];
                         const float uu = odd ? own[j + 8] : recv;
                         const int n = c0 + (odd ? 8 + j : j);
-                        if (n < n_valid && m < p.m_rows) {
+                        if (n < n_valid && m < m_rows) {
                             const float a = g / (1.f + __expf(-g)) * uu;
                             p.act[(int64_t)(row_b + n) * p.act_ld + feat] = __float2bfloat16_rn(a);
                         }
@@ -326,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = c0 + j;
-                        if (n < n_valid && m < p.m_rows) {
+                        if (n < n_valid && m < m_rows) {
                             const int pair = p.pairs[row_b + n];
                             p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
                         }
@@ -334,6 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
                 }
             }
             tc_fence_before();
+            if (w13 && fused) {
+                // publish this warp's activation rows to the entry's W2 tiles (TMA readers)
+                __threadfence();
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.dep + tl.u, 1);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
         }
@@ -389,8 +493,8 @@ EncodeTiledFn encode_fn() {
 template <int BN>
 int stages_for() {
     const int stage = 128 * 64 * 2 + BN * 64 * 2;
-    int s = (216 * 1024) / stage;
-    return s > 12 ? 12 : s;
+    int s = (212 * 1024) / stage;
+    return s > 11 ? 11 : s;
 }
 
 template <int BN>
@@ -399,20 +503,19 @@ size_t smem_for(int stages) {
     return 1024 + stages * stage + (2 * stages + 4) * 8 + 16 + (kMaxExperts + 1) * 4;
 }
 
-template <int BN, int MODE>
-cudaError_t launch_bn(const TcParams& p0, const CUtensorMap& a, const CUtensorMap& b, int grid,
-                      cudaStream_t s) {
+template <int BN>
+cudaError_t launch_bn(const TcParams& p0, const TcMaps& m, int grid, cudaStream_t s) {
     TcParams p = p0;
     p.stages = stages_for<BN>();
     const size_t smem = smem_for<BN>(p.stages);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc::tc_ffn_kernel<BN, MODE>,
+        cudaError_t e = cudaFuncSetAttribute(tc::tc_ffn_kernel<BN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tc::tc_ffn_kernel<BN, MODE><<<grid, tc::kThreads, smem, s>>>(p, a, b);
+    tc::tc_ffn_kernel<BN><<<grid, tc::kThreads, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
     return cudaGetLastError();
 }
 
@@ -452,12 +555,10 @@ cudaError_t tc_encode_acts(CUtensorMap* map, const void* base, int k_dim, int ro
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t tc_launch(int mode, int bn, const TcParams& p, const CUtensorMap& a,
-                      const CUtensorMap& b, int grid, cudaStream_t s) {
+cudaError_t tc_launch(int bn, const TcParams& p, const TcMaps& m, int grid, cudaStream_t s) {
 #define FT_TC_CASE(BNV)                                                              \
     case BNV:                                                                        \
-        return mode == 13 ? launch_bn<BNV, 13>(p, a, b, grid, s)                     \
-                          : launch_bn<BNV, 2>(p, a, b, grid, s);
+        return launch_bn<BNV>(p, m, grid, s);
     switch (bn) {
         FT_TC_CASE(16)
         FT_TC_CASE(32)

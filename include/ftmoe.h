@@ -107,8 +107,9 @@ typedef struct {
     double combine_ms;    /* gate-weighted combine */
     double total_ms;      /* whole forward call, first to last event on the caller's stream */
     uint64_t forwards;    /* forward calls recorded */
-    uint64_t ffn_launches;/* expert-FFN kernel launches recorded (hit and miss passes) */
-    uint64_t ffn_weight_bytes; /* expert weight bytes those launches were given to stream */
+    uint64_t ffn_launches;/* expert-FFN passes recorded: 1 per call, 2 when it had misses
+                             (one launch per pass on the fused tensor-core path) */
+    uint64_t ffn_weight_bytes; /* expert weight bytes those passes were given to stream */
     uint64_t kernel_launches;  /* all kernels launched by the recorded calls */
     /* ft_moe_prefill calls */
     uint64_t prefill_calls;

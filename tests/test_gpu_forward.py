@@ -87,12 +87,14 @@ def test_decode_bf16_trace_parity(ft, bf16_pool):
     cache.close()
 
 
-@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+@pytest.mark.parametrize("path", ["tcgen05", "tcgen05_two_launches", "simt"])
 @pytest.mark.parametrize("T", [1, 16])
 def test_decode_bf16_fixed_T(ft, bf16_pool, T, path, monkeypatch):
     """Both BF16 expert-FFN paths (tcgen05 grouped GEMM, CUDA-core GEMV) against the oracle."""
     if path == "simt":
         monkeypatch.setenv("FTMOE_FFN", "simt")
+    if path == "tcgen05_two_launches":
+        monkeypatch.setenv("FTMOE_TC_FUSED", "0")
     cfg = W.config("decode_bf16", t_min=T, t_max=T)
     C = W.cache_capacity(cfg)
     cache = _make(ft, cfg, bf16_pool, C, max_tokens=16)
