@@ -30,6 +30,7 @@ import numpy as np
 
 WORKLOAD = "decode_bf16"
 REF_TOKENS = 2          # tokens per step the CPU reference arm computes (bounded sample)
+REF_LAYERS = 2          # layers per step the CPU reference arm computes (bounded sample)
 METRIC = "MoE-layer decode tokens/s (35B-A3B-shaped BF16 layer, LRU cache 37% of pool)"
 
 
@@ -93,9 +94,35 @@ def _peaks():
         return {}
 
 
-def oracle_baseline(cfg, pool_arr, budget_s=15.0, max_steps=64):
+# Decode workloads: name -> (metric, host images (None = the whole pool), default steps, warmup)
+DECODE = {
+    "decode_bf16": (METRIC, None, 200, 16),
+    "decode_mxfp4": ("MoE decode tokens/s through 43 MXFP4 layers (284B-shaped, one global "
+                     "LRU cache 20% of pool)", 16, 24, 4),
+    "elastic_nvfp4": ("MoE-layer decode tokens/s (35B-A3B-shaped NVFP4 layer, LRU cache "
+                      "resized 40% -> 15% -> 30%)", None, 300, 16),
+}
+
+
+def resize_plan(cfg, Wm, K):
+    """Elastic workload: the cache budget changes twice inside the timed range, at 1/3 and
+    2/3 of it (the trace's own split points scaled to the run). Resizes are safe points
+    between steps, outside every step's events."""
+    if not cfg.resize:
+        return {}
+    cuts = [Wm + K // 3, Wm + (2 * K) // 3]
+    return {c: W_cap(cfg, f) for c, (_, f) in zip(cuts, cfg.resize)}
+
+
+def W_cap(cfg, frac):
+    import workloads as W
+    return W.cache_capacity(cfg, frac)
+
+
+def oracle_baseline(cfg, pool, budget_s=15.0, max_steps=64):
     """The oracle as it stands on this host's cores: LRU simulator + fp64 MoE layer over the
-    first steps of the same trace until ~budget_s of CPU work."""
+    first calls of the same trace until ~budget_s of CPU work. Returns tokens/s through
+    all of the workload's layers (a 43-layer step counts its tokens once)."""
     import workloads as W
     from oracle import formats, lru, moe
     try:
@@ -103,26 +130,31 @@ def oracle_baseline(cfg, pool_arr, budget_s=15.0, max_steps=64):
         threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
         threads = 1
-    P = pool_arr.shape[0]
     sim = lru.LRUCache(W.cache_capacity(cfg), cfg.experts)
-    tokens, steps = 0, 0
+    layer_tokens, calls = 0, 0
     t0 = time.perf_counter()
+    done = False
     for step in W.decode_trace(cfg, steps=max_steps):
-        d = step[0]
-        idx = moe.topk(d["logits"], cfg.top_k)
-        w = moe.gate_weights(d["logits"], idx)
-        sim.call(0, idx.reshape(-1))
-        moe.layer_forward(formats.bf16_to_f64(d["x"]), idx, w,
-                          lambda e: formats.decode_blob(pool_arr[e % P], cfg.fmt, cfg.hidden,
-                                                        cfg.inter))
-        tokens += d["T"]
-        steps += 1
-        if time.perf_counter() - t0 > budget_s:
+        for d in step:
+            idx = moe.topk(d["logits"], cfg.top_k)
+            w = moe.gate_weights(d["logits"], idx)
+            sim.call(d["layer"], idx.reshape(-1))
+            L = d["layer"]
+            moe.layer_forward(formats.bf16_to_f64(d["x"]), idx, w,
+                              lambda e: formats.decode_blob(pool.blob(L * cfg.experts + e), cfg.fmt,
+                                                            cfg.hidden, cfg.inter))
+            layer_tokens += d["T"]
+            calls += 1
+            if time.perf_counter() - t0 > budget_s:
+                done = True
+                break
+        if done:
             break
     dt = time.perf_counter() - t0
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": int(threads), "kind": "oracle",
-            "sample": "first %d steps (%d tokens) of the same seeded trace, fp64 numpy oracle + "
-                      "LRU simulator" % (steps, tokens)}, tokens, dt
+    return {"value": layer_tokens / cfg.layers / dt, "unit": "tokens/s", "cores": int(threads),
+            "kind": "oracle",
+            "sample": "first %d layer calls (%d layer-tokens) of the same seeded trace, fp64 "
+                      "numpy oracle + LRU simulator" % (calls, layer_tokens)}
 
 
 def run_reference(args):
@@ -130,24 +162,28 @@ def run_reference(args):
     if rank != 0:
         return
     import workloads as W
-    cfg = W.config(WORKLOAD)
-    pool = W.expert_pool(cfg)
+    from workloads.host import HostPool
+    metric, images, _, _ = DECODE[args.workload]
+    cfg = W.config(args.workload)
+    pool = HostPool(cfg, images=images, pinned=False)
     from oracle import formats, lru, moe
     sim = lru.LRUCache(W.cache_capacity(cfg), cfg.experts)
     tr = W.decode_trace(cfg, steps=args.warmup + args.steps)
     times, toks = [], []
     for i, step in enumerate(tr):
-        d = step[0]
-        n = min(d["T"], REF_TOKENS)     # bounded sample: the step's first tokens
+        n = min(step[0]["T"], REF_TOKENS)     # bounded sample: the step's first tokens
         t0 = time.perf_counter()
-        idx = moe.topk(d["logits"], cfg.top_k)
-        w = moe.gate_weights(d["logits"], idx)
-        sim.call(0, idx.reshape(-1))
-        moe.layer_forward(formats.bf16_to_f64(d["x"][:n]), idx[:n], w[:n],
-                          lambda e: formats.decode_blob(pool[e], cfg.fmt, cfg.hidden, cfg.inter))
+        for d in step[:REF_LAYERS]:
+            L = d["layer"]
+            idx = moe.topk(d["logits"], cfg.top_k)
+            w = moe.gate_weights(d["logits"], idx)
+            sim.call(L, idx.reshape(-1))
+            moe.layer_forward(formats.bf16_to_f64(d["x"][:n]), idx[:n], w[:n],
+                              lambda e: formats.decode_blob(pool.blob(L * cfg.experts + e), cfg.fmt,
+                                                            cfg.hidden, cfg.inter))
         dt = time.perf_counter() - t0
         if i >= args.warmup:
-            times.append(dt)
+            times.append(dt * cfg.layers / min(cfg.layers, REF_LAYERS))
             toks.append(n)
     try:
         from threadpoolctl import threadpool_info
@@ -156,23 +192,31 @@ def run_reference(args):
         threads = 1
     value = sum(toks) / sum(times)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": metric, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "hidden": cfg.hidden, "experts": cfg.experts,
-                   "inter": cfg.inter, "top_k": cfg.top_k, "tokens_per_step": "1..16",
-                   "cache_slots": W.cache_capacity(cfg), "l2": "n/a (CPU)"},
+        "config": workload_config(cfg, W.cache_capacity(cfg), "n/a (CPU)"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": int(threads),
                          "kind": "oracle",
                          "sample": "steps %d..%d of the seeded trace; per step the cache "
                                    "simulator on all tokens and the fp64 layer on the first "
-                                   "min(T, %d) tokens" % (args.warmup, args.warmup + args.steps - 1,
-                                                           REF_TOKENS)},
+                                   "min(T, %d) tokens of the first %d layer(s), time scaled to "
+                                   "all %d layers" % (args.warmup, args.warmup + args.steps - 1,
+                                                      REF_TOKENS, min(cfg.layers, REF_LAYERS),
+                                                      cfg.layers)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, C, l2):
+    return {"workload": cfg.name, "layers": cfg.layers, "hidden": cfg.hidden,
+            "experts": cfg.experts, "inter": cfg.inter, "top_k": cfg.top_k,
+            "weights": cfg.wfmt,
+            "tokens_per_step": "%d..%d (seeded mix)" % (cfg.t_min, cfg.t_max),
+            "cache_slots": C, "l2": l2}
 
 
 def run_ours(args):
@@ -189,17 +233,23 @@ def run_ours(args):
     if ws > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
-    cfg = W.config(WORKLOAD)
+    metric, images, _, _ = DECODE[args.workload]
+    cfg = W.config(args.workload)
     C = W.cache_capacity(cfg)
-    pool = HostPool(cfg)
+    pool = HostPool(cfg, images=images)
     K, Wm = args.steps, args.warmup
     nsteps = Wm + K
     if nsteps > cfg.steps:
         raise SystemExit("steps + warmup must be <= %d (trace length)" % cfg.steps)
-    trace = [st[0] for st in W.decode_trace(cfg, steps=nsteps)]
-    xs = [torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev) for d in trace]
-    ls = [torch.from_numpy(d["logits"]).to(dev) for d in trace]
-    Ts = [d["T"] for d in trace]
+    resizes = resize_plan(cfg, Wm, K)
+    trace = list(W.decode_trace(cfg, steps=nsteps))
+    # per step: list over layers of (layer, T, x, logits) resident in HBM
+    calls = [[(d["layer"], d["T"],
+               torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev),
+               torch.from_numpy(d["logits"]).to(dev)) for d in st] for st in trace]
+    Ts = [st[0]["T"] for st in trace]
+    touched = sorted({d["layer"] * cfg.experts + int(e) for st in trace for d in st
+                      for e in np.unique(d["picks"])})
     out = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -209,9 +259,13 @@ def run_ours(args):
                               cfg.t_max, cfg.wfmt, capacity, device=local)
         return ftmoe.MoECache(c, pool.ptrs, None)
 
-    def timed_pass(cache, record_clocks=False):
+    def run_step(cache, i):
+        for (layer, T, x, lg) in calls[i]:
+            cache.forward(layer, x, T, out, logits=lg, stream=stream)
+
+    def timed_pass(cache, record_clocks=False, elastic=True):
         for i in range(Wm):
-            cache.forward(0, xs[i], Ts[i], out, logits=ls[i], stream=stream)
+            run_step(cache, i)
         torch.cuda.synchronize()
         s0 = cache.stats()
         cache.set_timing(True)
@@ -226,9 +280,11 @@ def run_ours(args):
         t_wall = time.perf_counter()
         for j in range(K):
             i = Wm + j
+            if elastic and i in resizes:
+                cache.resize(resizes[i])
             flush.zero_()
             evs[j][0].record(stream)
-            cache.forward(0, xs[i], Ts[i], out, logits=ls[i], stream=stream)
+            run_step(cache, i)
             evs[j][1].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -255,37 +311,41 @@ def run_ours(args):
         t_max = float(tt.item())
     value = tokens * ws / t_max
 
-    # all experts resident (capacity = pool): the HBM-bound ceiling of the same step
-    cache_r = make(cfg.experts)
+    # every expert the run selects resident (no misses): the HBM-bound ceiling of the step
+    cache_r = make(len(touched))
     for i in range(Wm + K):   # touch every selected expert once
-        cache_r.forward(0, xs[i], Ts[i], out, logits=ls[i], stream=stream)
-    rs_ms, _, rtim, _, _, _ = timed_pass(cache_r)
+        run_step(cache_r, i)
+    rs_ms, _, rtim, _, _, _ = timed_pass(cache_r, elastic=False)
     cache_r.close()
 
     # end to end through the C ABI with host buffers: H2D of x + logits, forward, D2H of out
-    xh = [torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory() for d in trace]
-    lh = [torch.from_numpy(d["logits"]).pin_memory() for d in trace]
-    oh = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
-    ld = torch.empty((cfg.t_max, cfg.experts), dtype=torch.float32, device=dev)
+    hx = [[(torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+            torch.from_numpy(d["logits"]).pin_memory()) for d in st] for st in trace]
+    oh = torch.empty((cfg.layers, cfg.t_max, cfg.hidden), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((cfg.layers, cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    ld = torch.empty((cfg.layers, cfg.t_max, cfg.experts), dtype=torch.float32, device=dev)
+    od = torch.empty((cfg.layers, cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
     cache_e = make(C)
     h2d = d2h = 0
     e2e_s = 0.0
     for i in range(Wm + K):
+        if i in resizes:
+            cache_e.resize(resizes[i])
         T = Ts[i]
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        xd[:T].copy_(xh[i], non_blocking=True)
-        ld[:T].copy_(lh[i], non_blocking=True)
-        cache_e.forward(0, xd, T, out, logits=ld, stream=stream)
-        oh[:T].copy_(out[:T], non_blocking=True)
+        for li, (xh, lh) in enumerate(hx[i]):
+            xd[li, :T].copy_(xh, non_blocking=True)
+            ld[li, :T].copy_(lh, non_blocking=True)
+            cache_e.forward(li, xd[li], T, od[li], logits=ld[li], stream=stream)
+            oh[li, :T].copy_(od[li, :T], non_blocking=True)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
         if i >= Wm:
             e2e_s += dt
-            h2d += xh[i].numel() * 2 + lh[i].numel() * 4
-            d2h += T * cfg.hidden * 2
+            h2d += sum(xh.numel() * 2 + lh.numel() * 4 for xh, lh in hx[i])
+            d2h += T * cfg.hidden * 2 * cfg.layers
     cache_e.close()
     if ws > 1:
         tt = torch.tensor([e2e_s], device=dev)
@@ -308,17 +368,21 @@ def run_ours(args):
     misses = s1["misses"] - s0["misses"]
     hits = s1["hits"] - s0["hits"]
     fill_b = (s1["fill_bytes"] - s0["fill_bytes"]) + (s1["stage_bytes"] - s0["stage_bytes"])
-    base, _, _ = oracle_baseline(cfg, pool.arr, budget_s=args.cpu_budget)
+    base = oracle_baseline(cfg, pool, budget_s=args.cpu_budget)
+    kern = ("expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
+            if cfg.wfmt == "bf16" else
+            "expert FFN (CUDA-core %s GEMV, W13+SwiGLU then W2), per pass" % cfg.wfmt.upper())
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": Wm, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "hidden": cfg.hidden, "experts": cfg.experts,
-                   "inter": cfg.inter, "top_k": cfg.top_k, "tokens_per_step": "1..16 (seeded mix)",
-                   "cache_slots": C, "pool": "pinned host, %d blobs x %d B" % (cfg.keys, pool.blob_bytes),
-                   "l2": "flushed (256 MB write) before every step, outside the step's events",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass",
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.wfmt, "data": "synthetic",
+        "config": dict(workload_config(cfg, C, "flushed (256 MB write) before every step, "
+                                                "outside the step's events"),
+                       pool="pinned host, %d keys on %d blobs x %d B" % (cfg.keys, pool.images,
+                                                                        pool.blob_bytes),
+                       resizes={str(k2): v for k2, v in resizes.items()} or None,
+                       parallelism="replicas" if ws > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "kernel": kern,
                      "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": (achieved / hbm) if (achieved and hbm) else None,
                      "traffic": None, "peak_source": "MEASURED_PEAKS.json hbm_gbs" if hbm else None,
@@ -334,6 +398,7 @@ def run_ours(args):
             "pcie_fill_GBps": (fill_b / (tim["fill_ms"] * 1e-3) / 1e9) if tim["fill_ms"] > 0 else None,
             "fill_ms_per_step": tim["fill_ms"] / K,
             "wall_ms_per_step": 1e3 * t_wall / K,
+            "all_resident_slots": len(touched),
             "all_resident_tokens_per_s": tokens / (sum(rs_ms) / 1e3),
             "all_resident_ffn_GBps": r_achieved,
             "all_resident_ffn_frac": (r_achieved / hbm) if (r_achieved and hbm) else None,
@@ -434,18 +499,21 @@ def run_prefill(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "prefill_bf16"])
+                    choices=list(DECODE) + ["prefill_bf16"])
     args = ap.parse_args()
+    dflt = DECODE.get(args.workload, (None, None, 8, 3))
+    if args.steps is None:
+        args.steps = dflt[2]
+    if args.warmup is None:
+        args.warmup = dflt[3]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.steps + args.warmup > 512:
-        raise SystemExit("steps + warmup must be <= 512 (trace length)")
-    if args.workload != WORKLOAD:
+    if args.workload not in DECODE:
         run_prefill(args)
     elif args.impl == "reference":
         run_reference(args)
