@@ -64,6 +64,17 @@ struct BlobLayout {
     int64_t off_w13, off_w2, off_s13, off_s2, off_ts;
 };
 
+// Byte offset of the scale of row r, block j inside a scale section: 128-row x 4-block
+// atoms of 512 bytes (the order the block-scaled tensor-core MMA reads scale factors in);
+// `blocks` is the unpadded number of blocks per row.
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int j, int blocks) {
+    const int64_t atoms_per_band = (blocks + 3) >> 2;
+    return ((r >> 7) * atoms_per_band + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+// Section offsets of one expert blob for a weight format (defined in ftmoe.cu).
+BlobLayout make_layout(int fmt, int64_t H, int64_t I);
+
 struct FfnParams {
     const uint8_t* arena;        // slot s / staging i at arena + dst * blob_bytes
     BlobLayout lay;

@@ -102,11 +102,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) ffn_kernel(FfnParams p) {
         const int row0 = (MODE == 13) ? 2 * item : item * R;
         const uint8_t* wbase = blob + (MODE == 13 ? p.lay.off_w13 : p.lay.off_w2) + row0 * row_bytes;
         const uint8_t* sbase = nullptr;
-        int spr = 0;   // scale bytes per row
+        int spr = 0;   // scale blocks per row
         float tscale = 1.f;
         if (FMT != 0) {
             spr = (FMT == 1) ? K / 32 : K / 16;
-            sbase = blob + (MODE == 13 ? p.lay.off_s13 : p.lay.off_s2) + (int64_t)row0 * spr;
+            sbase = blob + (MODE == 13 ? p.lay.off_s13 : p.lay.off_s2);
             if (FMT == 2) tscale = reinterpret_cast<const float*>(blob + p.lay.off_ts)[MODE == 13 ? 0 : 1];
         }
         const int pb = p.entry_off[u], pe = p.entry_off[u + 1];
@@ -137,10 +137,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) ffn_kernel(FfnParams p) {
                         if (c < KC) {
                             wv[r][i] = ld_stream(wbase + r * row_bytes + (int64_t)c * 16);
                             if (FMT == 1) {
-                                float s = e8m0_to_f32(sbase[(int64_t)r * spr + c]);
+                                float s = e8m0_to_f32(sbase[sf_offset(row0 + r, c, spr)]);
                                 sc[r][i][0] = s; sc[r][i][1] = s;
                             } else if (FMT == 2) {
-                                uint32_t b2 = *reinterpret_cast<const uint16_t*>(sbase + (int64_t)r * spr + 2 * c);
+                                // blocks 2c and 2c+1 are adjacent bytes of one atom word
+                                uint32_t b2 = *reinterpret_cast<const uint16_t*>(sbase + sf_offset(row0 + r, 2 * c, spr));
                                 sc[r][i][0] = e4m3_to_f32(b2 & 0xffu) * tscale;
                                 sc[r][i][1] = e4m3_to_f32(b2 >> 8) * tscale;
                             }

@@ -13,6 +13,7 @@
 // budget at safe points without reloading the host pool; the first request is served cold.
 #include "common.cuh"
 #include "tc_ffn.cuh"
+#include "tc_fp4.cuh"
 #include "../../include/ftmoe.h"
 
 #include <algorithm>
@@ -93,6 +94,17 @@ struct ft_moe {
     int64_t act_rows = 0;                 // rows allocated for d_act / d_xp
     __nv_bfloat16* d_xp = nullptr;        // [act_rows][H] activations in grouped-row order
     CUtensorMap tmA13{}, tmA2{}, tmB13{}, tmB2{};
+    // block-scaled tcgen05 expert FFN (MXFP4 / NVFP4 weights)
+    bool use_fp4 = false;
+    int fp4_pieces = 4;                   // E2M1 pieces per activation row
+    int64_t fp4_tiles = 0;                // tile capacity of the piece buffers
+    uint8_t* d_xq = nullptr;              // W13 activation pieces (codes), tile-major
+    uint8_t* d_xsf = nullptr;             // their scale atoms
+    float* d_xrs = nullptr;               // their row scales
+    uint8_t* d_aq = nullptr;              // W2 activation pieces, scale atoms, row scales
+    uint8_t* d_asf = nullptr;
+    float* d_ars = nullptr;
+    CUtensorMap tmF_A13{}, tmF_A2{}, tmF_B13{}, tmF_B2{};
     int* h_ffn_err = nullptr;             // host view of the kernels' error word (mapped)
     int* d_ffn_err = nullptr;             // device address of the same word
     int num_sms = 148;
@@ -160,7 +172,9 @@ bool valid_config(const ft_moe_config* c, std::string* why) {
 
 int64_t up256(int64_t n) { return (n + 255) / 256 * 256; }
 
-BlobLayout make_layout(int fmt, int64_t H, int64_t I) {
+}  // namespace
+
+BlobLayout ftmoe::make_layout(int fmt, int64_t H, int64_t I) {
     BlobLayout L{};
     int64_t off = 0;
     auto sec = [&](int64_t size) { off = up256(off); int64_t o = off; off += size; return o; };
@@ -171,13 +185,18 @@ BlobLayout make_layout(int fmt, int64_t H, int64_t I) {
         L.off_w13 = sec(2 * I * H / 2);
         L.off_w2 = sec(H * I / 2);
         const int64_t blk = (fmt == FT_W_MXFP4) ? 32 : 16;
-        L.off_s13 = sec(2 * I * H / blk);
-        L.off_s2 = sec(H * I / blk);
+        auto sf_bytes = [](int64_t rows, int64_t blocks) {
+            return (rows + 127) / 128 * 128 * ((blocks + 3) / 4 * 4);
+        };
+        L.off_s13 = sec(sf_bytes(2 * I, H / blk));
+        L.off_s2 = sec(sf_bytes(H, I / blk));
         if (fmt == FT_W_NVFP4) L.off_ts = sec(8);
     }
     L.blob_bytes = up256(off);
     return L;
 }
+
+namespace {
 
 int64_t stage_slots_for(const ft_moe* h, int64_t C) {
     int64_t need = (int64_t)h->max_u - C;
@@ -244,6 +263,8 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_order[0]); cudaFree(h->d_order[1]); cudaFree(h->d_logits); cudaFree(h->d_idx);
     cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
     cudaFree(h->d_y); cudaFree(h->d_xp);
+    cudaFree(h->d_xq); cudaFree(h->d_xsf); cudaFree(h->d_xrs);
+    cudaFree(h->d_aq); cudaFree(h->d_asf); cudaFree(h->d_ars);
     cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
     cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
     cudaFree(h->d_p_route_mem); cudaFree(h->d_p_xp); cudaFree(h->d_p_act); cudaFree(h->d_p_y);
@@ -288,9 +309,16 @@ ft_status init_lru_state(ft_moe* h) {
 // (Re)build the TMA tensor maps of the tensor-core FFN: weights as (K, row, slot) over the
 // slot arena, activations as (K, row).
 ft_status encode_tc_maps(ft_moe* h) {
-    if (!h->use_tc) return FT_OK;
     const int H = h->cfg.hidden, I = h->cfg.inter;
     const int64_t nslots = std::max<int64_t>(1, h->C + h->n_stage);
+    if (h->use_fp4) {
+        const int64_t prow = h->fp4_tiles * h->fp4_pieces * h->tc_bn;
+        FT_CUDA(h, fp4_encode_weights(&h->tmF_A13, h->d_arena + h->lay.off_w13, H, 2 * I, nslots, h->lay.blob_bytes));
+        FT_CUDA(h, fp4_encode_weights(&h->tmF_A2, h->d_arena + h->lay.off_w2, I, H, nslots, h->lay.blob_bytes));
+        FT_CUDA(h, fp4_encode_pieces(&h->tmF_B13, h->d_xq, H, prow, h->tc_bn));
+        FT_CUDA(h, fp4_encode_pieces(&h->tmF_B2, h->d_aq, I, prow, h->tc_bn));
+    }
+    if (!h->use_tc) return FT_OK;
     FT_CUDA(h, tc_encode_weights(&h->tmA13, h->d_arena + h->lay.off_w13, H, 2 * I, nslots, h->lay.blob_bytes));
     FT_CUDA(h, tc_encode_weights(&h->tmA2, h->d_arena + h->lay.off_w2, I, H, nslots, h->lay.blob_bytes));
     FT_CUDA(h, tc_encode_acts(&h->tmB13, h->d_xp, H, (int)h->act_rows, h->tc_bn));
@@ -537,7 +565,9 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (!dmalloc((void**)&h->d_nan, 16)) return bail(FT_ERR_OOM);
     {
         const char* ffn = getenv("FTMOE_FFN");
-        h->use_tc = cfg->wfmt == FT_W_BF16 && !(ffn && strcmp(ffn, "simt") == 0);
+        const bool simt = ffn && strcmp(ffn, "simt") == 0;
+        h->use_tc = cfg->wfmt == FT_W_BF16 && !simt;
+        h->use_fp4 = cfg->wfmt != FT_W_BF16 && !simt && H % 256 == 0 && I % 256 == 0;
         const char* fz = getenv("FTMOE_TC_FUSED");
         h->tc_fused = !(fz && strcmp(fz, "0") == 0);
         h->tc_bn = tc_pick_bn(cfg->max_tokens);
@@ -548,6 +578,23 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     }
     if (!dmalloc((void**)&h->d_act, (size_t)h->act_rows * I * 2)) return bail(FT_ERR_OOM);
     if (h->use_tc && !dmalloc((void**)&h->d_xp, (size_t)h->act_rows * H * 2)) return bail(FT_ERR_OOM);
+    if (h->use_fp4) {
+        // an entry of n rows needs ceil(n / bn) <= n / bn + 1 tiles
+        const int bn = h->tc_bn, P = h->fp4_pieces;
+        h->fp4_tiles = (int64_t)h->max_u + (h->max_pairs + bn - 1) / bn;
+        const size_t xq = fp4_piece_bytes(h->fp4_tiles, P, bn, H), aq = fp4_piece_bytes(h->fp4_tiles, P, bn, I);
+        const size_t xsf = fp4_sf_bytes(h->fp4_tiles, P, H, cfg->wfmt), asf = fp4_sf_bytes(h->fp4_tiles, P, I, cfg->wfmt);
+        const size_t rs = (size_t)h->fp4_tiles * bn * 4;
+        if (!dmalloc((void**)&h->d_xq, xq) || !dmalloc((void**)&h->d_aq, aq) ||
+            !dmalloc((void**)&h->d_xsf, xsf) || !dmalloc((void**)&h->d_asf, asf) ||
+            !dmalloc((void**)&h->d_xrs, rs) || !dmalloc((void**)&h->d_ars, rs)) return bail(FT_ERR_OOM);
+        // rows of a tile past its last token are read by the MMA and ignored; start them at zero
+        if (cudaMemset(h->d_xq, 0, xq) != cudaSuccess || cudaMemset(h->d_aq, 0, aq) != cudaSuccess ||
+            cudaMemset(h->d_xsf, 0, xsf) != cudaSuccess || cudaMemset(h->d_asf, 0, asf) != cudaSuccess ||
+            cudaMemset(h->d_xrs, 0, rs) != cudaSuccess || cudaMemset(h->d_ars, 0, rs) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "memset(fp4 pieces)"); return bail(FT_ERR_CUDA);
+        }
+    }
     if (!dmalloc((void**)&h->d_y, (size_t)h->max_pairs * H * 4)) return bail(FT_ERR_OOM);
     {
         const size_t mu = (size_t)h->max_u;
@@ -695,7 +742,69 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         tp.y_ld = H;
         tp.err = h->d_ffn_err;
     }
+    Fp4Params f4{};
+    SplitParams sp{};
+    if (h->use_fp4) {
+        sp.counts = h->rb.counts;
+        sp.entry_off = h->rb.entry_off;
+        sp.pairs = h->rb.pairs;
+        sp.pass = 2;
+        sp.top_k = k;
+        sp.src = (const __nv_bfloat16*)x;
+        sp.src_ld = H;
+        sp.K = H;
+        sp.pieces = h->fp4_pieces;
+        sp.bn = h->tc_bn;
+        sp.fmt = c.wfmt;
+        sp.codes = h->d_xq;
+        sp.sf = h->d_xsf;
+        sp.rs = h->d_xrs;
+        FT_CUDA(h, fp4_split(sp, T * k, s));
+        ++launches;
+        f4.counts = h->rb.counts;
+        f4.entry_off = h->rb.entry_off;
+        f4.entry_dst = h->rb.entry_dst;
+        f4.pairs = h->rb.pairs;
+        f4.hidden = H;
+        f4.inter = c.inter;
+        f4.pieces = h->fp4_pieces;
+        f4.arena = h->d_arena;
+        f4.blob_bytes = h->lay.blob_bytes;
+        f4.off_ts = h->lay.off_ts;
+        f4.act = h->d_act;
+        f4.act_ld = c.inter;
+        f4.y = h->d_y;
+        f4.y_ld = H;
+        f4.err = h->d_ffn_err;
+    }
     auto run_ffn = [&](int pass) -> cudaError_t {
+        if (h->use_fp4) {
+            // W13 + SwiGLU -> bf16 activation rows -> pieces -> W2
+            f4.pass = pass;
+            f4.phase = 13;
+            f4.off_sf = h->lay.off_s13;
+            f4.b_sf = h->d_xsf;
+            f4.b_rs = h->d_xrs;
+            cudaError_t e = fp4_launch(c.wfmt, h->tc_bn, f4, &h->tmF_A13, &h->tmF_B13, h->num_sms, s);
+            if (e != cudaSuccess) return e;
+            SplitParams sa = sp;
+            sa.pass = pass;
+            sa.top_k = 0;
+            sa.src = h->d_act;
+            sa.src_ld = c.inter;
+            sa.K = c.inter;
+            sa.codes = h->d_aq;
+            sa.sf = h->d_asf;
+            sa.rs = h->d_ars;
+            e = fp4_split(sa, T * k, s);
+            if (e != cudaSuccess) return e;
+            f4.phase = 2;
+            f4.off_sf = h->lay.off_s2;
+            f4.b_sf = h->d_asf;
+            f4.b_rs = h->d_ars;
+            launches += 3;
+            return fp4_launch(c.wfmt, h->tc_bn, f4, &h->tmF_A2, &h->tmF_B2, h->num_sms, s);
+        }
         if (!h->use_tc) {
             fp.pass = pass;
             return launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches);

@@ -79,24 +79,7 @@ extern "C" ft_status ft_expert_ffn_noalloc(const void* blob, int32_t wfmt, int32
     if (cudaGetLastError() != cudaSuccess) return FT_ERR_CUDA;
 
     const int64_t H = hidden, I = inter;
-    BlobLayout lay{};
-    {
-        auto up = [](int64_t n) { return (n + 255) / 256 * 256; };
-        int64_t off = 0;
-        auto sec = [&](int64_t size) { off = up(off); int64_t o = off; off += size; return o; };
-        if (wfmt == FT_W_BF16) {
-            lay.off_w13 = sec(2 * I * H * 2);
-            lay.off_w2 = sec(H * I * 2);
-        } else {
-            lay.off_w13 = sec(2 * I * H / 2);
-            lay.off_w2 = sec(H * I / 2);
-            const int64_t blk = (wfmt == FT_W_MXFP4) ? 32 : 16;
-            lay.off_s13 = sec(2 * I * H / blk);
-            lay.off_s2 = sec(H * I / blk);
-            if (wfmt == FT_W_NVFP4) lay.off_ts = sec(8);
-        }
-        lay.blob_bytes = up(off);
-    }
+    const BlobLayout lay = make_layout(wfmt, H, I);
     FfnParams fp{};
     fp.arena = static_cast<const uint8_t*>(blob);
     fp.lay = lay;

@@ -35,9 +35,15 @@
  *     section          BF16             MXFP4                  NVFP4
  *     s0 W13           [2I][H] bf16     [2I][H/2] E2M1 x2      [2I][H/2] E2M1 x2
  *     s1 W2            [H][I] bf16      [H][I/2]  E2M1 x2      [H][I/2]  E2M1 x2
- *     s2 W13 scales    -                [2I][H/32] E8M0        [2I][H/16] E4M3
- *     s3 W2 scales     -                [H][I/32]  E8M0        [H][I/16]  E4M3
+ *     s2 W13 scales    -                SF(2I, H/32) E8M0      SF(2I, H/16) E4M3
+ *     s3 W2 scales     -                SF(H, I/32)  E8M0      SF(H, I/16)  E4M3
  *     s4 tensor scale  -                -                      fp32[2] (W13, W2)
+ *   SF(R, S): the scale of row r, block j (32 or 16 consecutive elements along the row),
+ *   stored in 512-byte atoms of 128 rows x 4 blocks; R and S are padded to multiples of
+ *   128 and 4 with zero bytes; atoms run 4 blocks at a time along a 128-row band, then band
+ *   after band; inside an atom, (r, j) is byte (r % 32) * 16 + ((r % 128) / 32) * 4 + j % 4.
+ *   This is the block-scaled tensor-core MMA's own scale-factor order, so a cache slot feeds
+ *   the MMA without rearranging anything.
  *   Row 2i of W13 is the gate row W1[i], row 2i+1 the up row W3[i]; W2 is [out=H][in=I].
  *   Two E2M1 codes per byte, the low nibble holding the even-indexed element.
  *   The expert computes y = W2 (silu(W1 x) * (W3 x)) with fp32 accumulation; the SwiGLU

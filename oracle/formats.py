@@ -10,9 +10,16 @@ so that one DMA fills one cache slot):
     section            BF16               MXFP4                 NVFP4
     s0  W13            [2I][H] bf16       [2I][H/2] E2M1 x2     [2I][H/2] E2M1 x2
     s1  W2             [H][I]  bf16       [H][I/2]  E2M1 x2     [H][I/2]  E2M1 x2
-    s2  W13 scales     -                  [2I][H/32] E8M0       [2I][H/16] E4M3
-    s3  W2 scales      -                  [H][I/32]  E8M0       [H][I/16]  E4M3
+    s2  W13 scales     -                  SF(2I, H/32) E8M0     SF(2I, H/16) E4M3
+    s3  W2 scales      -                  SF(H, I/32)  E8M0     SF(H, I/16)  E4M3
     s4  tensor scales  -                  -                     fp32 [2] (W13, W2)
+
+* SF(R, S) holds the scale of row r, block j (j < S) in tiles ("atoms") of 128 rows x 4
+  blocks, 512 bytes each: R and S are padded to multiples of 128 and 4 (padding bytes are
+  zero), atoms follow each other 4 blocks at a time along a row band, then band after band,
+  and inside an atom the byte of (r, j) sits at (r mod 32) * 16 + ((r mod 128) div 32) * 4
+  + (j mod 4). This is the order in which the block-scaled tensor-core MMA takes its scale
+  factors, so a cache slot can feed them to it without any rearrangement.
 
 * Row 2i of W13 is W1 row i (gate projection), row 2i+1 is W3 row i (up projection).
 * W1, W3 are [I][H] and W2 is [H][I] (out x in, so y = W2 a).
@@ -106,6 +113,19 @@ def unpack_e2m1(packed, k):
     return codes
 
 
+def sf_padded(rows, blocks):
+    """Padded (rows, blocks) of a scale section: multiples of 128 and 4."""
+    return (rows + 127) // 128 * 128, (blocks + 3) // 4 * 4
+
+
+def sf_offset(r, j, blocks):
+    """Byte offset of the scale of row r, block j in a scale section with `blocks` blocks
+    per row (before padding). Works elementwise on integer arrays."""
+    s_pad = (blocks + 3) // 4 * 4
+    atom = (r // 128) * (s_pad // 4) + j // 4
+    return atom * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4
+
+
 def blob_sections(fmt, hidden, inter):
     """Byte offsets and sizes of the sections of one expert blob, and the blob size."""
     H, I = hidden, inter
@@ -115,13 +135,14 @@ def blob_sections(fmt, hidden, inter):
     off = 0
     if fmt == FMT_BF16:
         sizes = [("w13", 2 * I * H * 2), ("w2", H * I * 2)]
-    elif fmt == FMT_MXFP4:
+    elif fmt in (FMT_MXFP4, FMT_NVFP4):
+        B = 32 if fmt == FMT_MXFP4 else 16
+        r13, s13 = sf_padded(2 * I, H // B)
+        r2, s2 = sf_padded(H, I // B)
         sizes = [("w13", 2 * I * H // 2), ("w2", H * I // 2),
-                 ("w13_scale", 2 * I * H // 32), ("w2_scale", H * I // 32)]
-    elif fmt == FMT_NVFP4:
-        sizes = [("w13", 2 * I * H // 2), ("w2", H * I // 2),
-                 ("w13_scale", 2 * I * H // 16), ("w2_scale", H * I // 16),
-                 ("tensor_scale", 8)]
+                 ("w13_scale", r13 * s13), ("w2_scale", r2 * s2)]
+        if fmt == FMT_NVFP4:
+            sizes.append(("tensor_scale", 8))
     else:
         raise ValueError("unknown format %r" % (fmt,))
     for name, size in sizes:
@@ -135,14 +156,21 @@ def blob_bytes(fmt, hidden, inter):
     return blob_sections(fmt, hidden, inter)[1]
 
 
+def read_scales(section, rows, blocks):
+    """Scale section (atom order) -> [rows][blocks] bytes."""
+    r = np.arange(rows)[:, None]
+    j = np.arange(blocks)[None, :]
+    return np.asarray(section, dtype=np.uint8)[sf_offset(r, j, blocks)]
+
+
 def _dequant_fp4(codes_packed, scales, rows, k, fmt, tensor_scale):
     codes = unpack_e2m1(codes_packed.reshape(rows, k // 2), k)
     vals = E2M1_TABLE[codes]
     if fmt == FMT_MXFP4:
-        s = E8M0_TABLE[scales.reshape(rows, k // 32)]
+        s = E8M0_TABLE[read_scales(scales, rows, k // 32)]
         vals = vals * np.repeat(s, 32, axis=1)
     else:
-        s = E4M3_TABLE[scales.reshape(rows, k // 16)]
+        s = E4M3_TABLE[read_scales(scales, rows, k // 16)]
         vals = vals * np.repeat(s, 16, axis=1) * tensor_scale
     return vals
 

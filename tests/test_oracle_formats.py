@@ -123,18 +123,28 @@ def test_fp4_blob_parse_bytewise(fmt):
         else:
             blob[off] = (blob[off] & 0x0F) | (code << 4)
 
+    def put_scales(base, get, rows, blocks):
+        # walk the section byte by byte: band, atom, r0 (32), r1 (4), j (4)
+        pos = base
+        for band in range((rows + 127) // 128):
+            for atom in range((blocks + 3) // 4):
+                for r0 in range(32):
+                    for r1 in range(4):
+                        for jj in range(4):
+                            r, j = band * 128 + r1 * 32 + r0, atom * 4 + jj
+                            if r < rows and j < blocks:
+                                blob[pos] = get(r, j)
+                            pos += 1
+
     for i in range(I):
         for h in range(H):
             put_codes(secs["w13"][0], 2 * i, H, h, c1[i, h])
             put_codes(secs["w13"][0], 2 * i + 1, H, h, c3[i, h])
-        for b in range(H // B):
-            blob[secs["w13_scale"][0] + (2 * i) * (H // B) + b] = s1[i, b]
-            blob[secs["w13_scale"][0] + (2 * i + 1) * (H // B) + b] = s3[i, b]
+    put_scales(secs["w13_scale"][0], lambda r, j: (s1 if r % 2 == 0 else s3)[r // 2, j], 2 * I, H // B)
     for h in range(H):
         for i in range(I):
             put_codes(secs["w2"][0], h, I, i, c2[h, i])
-        for b in range(I // B):
-            blob[secs["w2_scale"][0] + h * (I // B) + b] = s2[h, b]
+    put_scales(secs["w2_scale"][0], lambda r, j: s2[r, j], H, I // B)
     if fmt == formats.FMT_NVFP4:
         blob[secs["tensor_scale"][0]:secs["tensor_scale"][0] + 8] = np.array([t13, t2], np.float32).tobytes()
     d1, d3, d2 = formats.decode_blob(bytes(blob), fmt, H, I)
@@ -145,14 +155,28 @@ def test_fp4_blob_parse_bytewise(fmt):
             assert d2[h, i] == val(c2[h, i]) * sval(s2[h, i // B]) * t2
 
 
+def test_scale_atom_offsets_hand_traced():
+    """Scale-section offsets worked out by hand for a section with 8 blocks per row (two
+    atoms per 128-row band, 1024 bytes per band)."""
+    cases = {(0, 0): 0, (0, 1): 1, (0, 3): 3, (1, 0): 16, (31, 2): 31 * 16 + 2,
+             (32, 0): 4, (64, 1): 9, (127, 3): 31 * 16 + 12 + 3, (0, 4): 512, (5, 6): 512 + 80 + 2,
+             (128, 0): 1024, (200, 5): 1024 + 512 + 8 * 16 + 2 * 4 + 1}
+    for (r, j), off in cases.items():
+        assert formats.sf_offset(r, j, 8) == off, (r, j)
+    # padding: 6 blocks per row pad to 8, 130 rows pad to 256
+    assert formats.sf_padded(130, 6) == (256, 8)
+    assert formats.sf_offset(129, 5, 6) == 1024 + 512 + 16 + 1
+
+
 def test_generator_blobs_roundtrip_through_oracle():
     """The generator's packer and the oracle's parser are separate code; they must agree."""
     import workloads as W
     cfg = W.config("tiny")
     pool = W.expert_pool(cfg, images=1)
     assert pool.shape[1] == formats.blob_bytes(cfg.fmt, cfg.hidden, cfg.inter)
-    for name in ("decode_mxfp4", "elastic_nvfp4"):
-        c = W.config(name, hidden=128, inter=64)
+    for name, hh, ii in (("decode_mxfp4", 128, 64), ("elastic_nvfp4", 128, 64),
+                         ("decode_mxfp4", 64, 64), ("elastic_nvfp4", 320, 192)):
+        c = W.config(name, hidden=hh, inter=ii)
         p = W.expert_pool(c, images=1)
         assert p.shape[1] == formats.blob_bytes(c.fmt, c.hidden, c.inter)
         w1, w3, w2 = formats.decode_blob(p[0], c.fmt, c.hidden, c.inter)

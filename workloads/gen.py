@@ -108,18 +108,37 @@ def blob_layout(fmt, H, I):
     """Section offsets {name: (offset, size)} and the blob size for one expert."""
     if fmt == 0:
         sizes = [("w13", 4 * I * H), ("w2", 2 * H * I)]
-    elif fmt == 1:
-        sizes = [("w13", I * H), ("w2", H * I // 2), ("w13_scale", I * H // 16),
-                 ("w2_scale", H * I // 32)]
     else:
-        sizes = [("w13", I * H), ("w2", H * I // 2), ("w13_scale", I * H // 8),
-                 ("w2_scale", H * I // 16), ("tensor_scale", 8)]
+        B = 32 if fmt == 1 else 16
+        sizes = [("w13", I * H), ("w2", H * I // 2),
+                 ("w13_scale", _pad(2 * I, 128) * _pad(H // B, 4)),
+                 ("w2_scale", _pad(H, 128) * _pad(I // B, 4))]
+        if fmt == 2:
+            sizes.append(("tensor_scale", 8))
     out, off = {}, 0
     for name, size in sizes:
         off = _up(off)
         out[name] = (off, size)
         off += size
     return out, _up(off)
+
+
+def _pad(n, a):
+    return (n + a - 1) // a * a
+
+
+def scale_atoms(s):
+    """[R][S] scale bytes -> the blob's scale-section bytes: 128-row x 4-block tiles of 512
+    bytes (row band by row band, 4 blocks at a time), inside a tile byte
+    (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4; padding is zero."""
+    s = np.asarray(s, dtype=np.uint8)
+    R, S = s.shape
+    Rp, Sp = _pad(R, 128), _pad(S, 4)
+    full = np.zeros((Rp, Sp), dtype=np.uint8)
+    full[:R, :S] = s
+    # [band][r1 (128//32)][r0 (32)][atom][j (4)] -> [band][atom][r0][r1][j]
+    t = full.reshape(Rp // 128, 4, 32, Sp // 4, 4).transpose(0, 3, 2, 1, 4)
+    return np.ascontiguousarray(t).reshape(-1)
 
 
 def _interleave_rows(w1, w3):
@@ -166,8 +185,8 @@ def pack_blob_fp4(fmt, c1, c3, c2, s1, s3, s2, tensor_scales=None):
 
     put("w13", _pack_nibbles(_interleave_rows(c1, c3)))
     put("w2", _pack_nibbles(c2))
-    put("w13_scale", _interleave_rows(s1, s3).astype(np.uint8))
-    put("w2_scale", np.asarray(s2, dtype=np.uint8))
+    put("w13_scale", scale_atoms(_interleave_rows(s1, s3)))
+    put("w2_scale", scale_atoms(s2))
     if fmt == 2:
         put("tensor_scale", np.asarray(tensor_scales, dtype=np.float32))
     return blob
