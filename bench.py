@@ -371,7 +371,8 @@ def run_ours(args):
     base = oracle_baseline(cfg, pool, budget_s=args.cpu_budget)
     kern = ("expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
             if cfg.wfmt == "bf16" else
-            "expert FFN (CUDA-core %s GEMV, W13+SwiGLU then W2), per pass" % cfg.wfmt.upper())
+            "expert FFN (block-scaled tcgen05 grouped GEMM on %s codes: W13+SwiGLU, activation "
+            "pieces, W2), per pass" % cfg.wfmt.upper())
     line = {
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": Wm, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True,

@@ -34,6 +34,8 @@ struct RouteBuffers {
     int32_t* miss_key;     // [max_u] key of miss j (ascending expert id)
     int32_t* miss_dst;     // [max_u] destination of miss j
     int32_t* dep;          // [max_u] per-entry W13 completion counters of the fused FFN (zeroed here)
+    int32_t* dep_x;        // [max_u] per-entry split-row counters of the fused FP4 FFN (zeroed here)
+    int32_t* dep_a;        // [max_u] per-entry W2-pieces-ready flags of the fused FP4 FFN (zeroed here)
 };
 
 // Host-mapped mirror of the fill list (the host issues one copy per miss).

@@ -97,13 +97,13 @@ struct ft_moe {
     // block-scaled tcgen05 expert FFN (MXFP4 / NVFP4 weights)
     bool use_fp4 = false;
     int fp4_pieces = 4;                   // E2M1 pieces per activation row
+    int fp4_bn = 16;                      // activation rows per tile (fp4_pieces * fp4_bn <= 128)
     int64_t fp4_tiles = 0;                // tile capacity of the piece buffers
     uint8_t* d_xq = nullptr;              // W13 activation pieces (codes), tile-major
     uint8_t* d_xsf = nullptr;             // their scale atoms
     float* d_xrs = nullptr;               // their row scales
-    uint8_t* d_aq = nullptr;              // W2 activation pieces, scale atoms, row scales
+    uint8_t* d_aq = nullptr;              // W2 activation pieces and scale atoms
     uint8_t* d_asf = nullptr;
-    float* d_ars = nullptr;
     CUtensorMap tmF_A13{}, tmF_A2{}, tmF_B13{}, tmF_B2{};
     int* h_ffn_err = nullptr;             // host view of the kernels' error word (mapped)
     int* d_ffn_err = nullptr;             // device address of the same word
@@ -264,7 +264,7 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
     cudaFree(h->d_y); cudaFree(h->d_xp);
     cudaFree(h->d_xq); cudaFree(h->d_xsf); cudaFree(h->d_xrs);
-    cudaFree(h->d_aq); cudaFree(h->d_asf); cudaFree(h->d_ars);
+    cudaFree(h->d_aq); cudaFree(h->d_asf);
     cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
     cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
     cudaFree(h->d_p_route_mem); cudaFree(h->d_p_xp); cudaFree(h->d_p_act); cudaFree(h->d_p_y);
@@ -312,11 +312,12 @@ ft_status encode_tc_maps(ft_moe* h) {
     const int H = h->cfg.hidden, I = h->cfg.inter;
     const int64_t nslots = std::max<int64_t>(1, h->C + h->n_stage);
     if (h->use_fp4) {
-        const int64_t prow = h->fp4_tiles * h->fp4_pieces * h->tc_bn;
+        const int64_t prow = h->fp4_tiles * h->fp4_pieces * h->fp4_bn;
+        const int box = 16;                       // piece rows are loaded 16 at a time
         FT_CUDA(h, fp4_encode_weights(&h->tmF_A13, h->d_arena + h->lay.off_w13, H, 2 * I, nslots, h->lay.blob_bytes));
         FT_CUDA(h, fp4_encode_weights(&h->tmF_A2, h->d_arena + h->lay.off_w2, I, H, nslots, h->lay.blob_bytes));
-        FT_CUDA(h, fp4_encode_pieces(&h->tmF_B13, h->d_xq, H, prow, h->tc_bn));
-        FT_CUDA(h, fp4_encode_pieces(&h->tmF_B2, h->d_aq, I, prow, h->tc_bn));
+        FT_CUDA(h, fp4_encode_pieces(&h->tmF_B13, h->d_xq, H, prow, box));
+        FT_CUDA(h, fp4_encode_pieces(&h->tmF_B2, h->d_aq, I, prow, box));
     }
     if (!h->use_tc) return FT_OK;
     FT_CUDA(h, tc_encode_weights(&h->tmA13, h->d_arena + h->lay.off_w13, H, 2 * I, nslots, h->lay.blob_bytes));
@@ -580,25 +581,27 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (h->use_tc && !dmalloc((void**)&h->d_xp, (size_t)h->act_rows * H * 2)) return bail(FT_ERR_OOM);
     if (h->use_fp4) {
         // an entry of n rows needs ceil(n / bn) <= n / bn + 1 tiles
-        const int bn = h->tc_bn, P = h->fp4_pieces;
+        const int P = h->fp4_pieces;
+        h->fp4_bn = std::min(h->tc_bn, 128 / P);
+        const int bn = h->fp4_bn;
         h->fp4_tiles = (int64_t)h->max_u + (h->max_pairs + bn - 1) / bn;
         const size_t xq = fp4_piece_bytes(h->fp4_tiles, P, bn, H), aq = fp4_piece_bytes(h->fp4_tiles, P, bn, I);
-        const size_t xsf = fp4_sf_bytes(h->fp4_tiles, P, H, cfg->wfmt), asf = fp4_sf_bytes(h->fp4_tiles, P, I, cfg->wfmt);
+        const size_t xsf = fp4_sf_bytes(h->fp4_tiles, H, cfg->wfmt), asf = fp4_sf_bytes(h->fp4_tiles, I, cfg->wfmt);
         const size_t rs = (size_t)h->fp4_tiles * bn * 4;
         if (!dmalloc((void**)&h->d_xq, xq) || !dmalloc((void**)&h->d_aq, aq) ||
             !dmalloc((void**)&h->d_xsf, xsf) || !dmalloc((void**)&h->d_asf, asf) ||
-            !dmalloc((void**)&h->d_xrs, rs) || !dmalloc((void**)&h->d_ars, rs)) return bail(FT_ERR_OOM);
+            !dmalloc((void**)&h->d_xrs, rs)) return bail(FT_ERR_OOM);
         // rows of a tile past its last token are read by the MMA and ignored; start them at zero
         if (cudaMemset(h->d_xq, 0, xq) != cudaSuccess || cudaMemset(h->d_aq, 0, aq) != cudaSuccess ||
             cudaMemset(h->d_xsf, 0, xsf) != cudaSuccess || cudaMemset(h->d_asf, 0, asf) != cudaSuccess ||
-            cudaMemset(h->d_xrs, 0, rs) != cudaSuccess || cudaMemset(h->d_ars, 0, rs) != cudaSuccess) {
+            cudaMemset(h->d_xrs, 0, rs) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "memset(fp4 pieces)"); return bail(FT_ERR_CUDA);
         }
     }
     if (!dmalloc((void**)&h->d_y, (size_t)h->max_pairs * H * 4)) return bail(FT_ERR_OOM);
     {
         const size_t mu = (size_t)h->max_u;
-        const size_t bytes = 256 + 4 * (mu + mu + (mu + 1) + (size_t)h->max_pairs + mu + mu + mu) + 64;
+        const size_t bytes = 256 + 4 * (mu + mu + (mu + 1) + (size_t)h->max_pairs + mu + mu + 3 * mu) + 64;
         if (!dmalloc((void**)&h->d_route_mem, bytes)) return bail(FT_ERR_OOM);
         uint8_t* p = h->d_route_mem;
         h->rb.counts = (RouteCounts*)p; p += 256;
@@ -608,7 +611,9 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->rb.pairs = (int32_t*)p; p += 4 * (size_t)h->max_pairs;
         h->rb.miss_key = (int32_t*)p; p += 4 * mu;
         h->rb.miss_dst = (int32_t*)p; p += 4 * mu;
-        h->rb.dep = (int32_t*)p;
+        h->rb.dep = (int32_t*)p; p += 4 * mu;
+        h->rb.dep_x = (int32_t*)p; p += 4 * mu;
+        h->rb.dep_a = (int32_t*)p;
         const size_t hbytes = 256 + 8 * mu + 64 + 64;
         if (cudaHostAlloc((void**)&h->h_mapped, hbytes, cudaHostAllocMapped) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(route view)"); return bail(FT_ERR_OOM);
@@ -743,67 +748,36 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         tp.err = h->d_ffn_err;
     }
     Fp4Params f4{};
-    SplitParams sp{};
     if (h->use_fp4) {
-        sp.counts = h->rb.counts;
-        sp.entry_off = h->rb.entry_off;
-        sp.pairs = h->rb.pairs;
-        sp.pass = 2;
-        sp.top_k = k;
-        sp.src = (const __nv_bfloat16*)x;
-        sp.src_ld = H;
-        sp.K = H;
-        sp.pieces = h->fp4_pieces;
-        sp.bn = h->tc_bn;
-        sp.fmt = c.wfmt;
-        sp.codes = h->d_xq;
-        sp.sf = h->d_xsf;
-        sp.rs = h->d_xrs;
-        FT_CUDA(h, fp4_split(sp, T * k, s));
-        ++launches;
         f4.counts = h->rb.counts;
         f4.entry_off = h->rb.entry_off;
         f4.entry_dst = h->rb.entry_dst;
         f4.pairs = h->rb.pairs;
         f4.hidden = H;
         f4.inter = c.inter;
+        f4.top_k = k;
         f4.pieces = h->fp4_pieces;
         f4.arena = h->d_arena;
         f4.blob_bytes = h->lay.blob_bytes;
+        f4.off_s13 = h->lay.off_s13;
+        f4.off_s2 = h->lay.off_s2;
         f4.off_ts = h->lay.off_ts;
+        f4.x = (const __nv_bfloat16*)x;
+        f4.xq = h->d_xq; f4.xsf = h->d_xsf; f4.xrs = h->d_xrs;
+        f4.aq = h->d_aq; f4.asf = h->d_asf;
         f4.act = h->d_act;
-        f4.act_ld = c.inter;
         f4.y = h->d_y;
-        f4.y_ld = H;
+        f4.cnt_x = h->rb.dep_x;
+        f4.cnt_w13 = h->rb.dep;
         f4.err = h->d_ffn_err;
     }
     auto run_ffn = [&](int pass) -> cudaError_t {
         if (h->use_fp4) {
-            // W13 + SwiGLU -> bf16 activation rows -> pieces -> W2
+            // one launch: activation pieces, W13 + SwiGLU, W2 pieces, W2
             f4.pass = pass;
-            f4.phase = 13;
-            f4.off_sf = h->lay.off_s13;
-            f4.b_sf = h->d_xsf;
-            f4.b_rs = h->d_xrs;
-            cudaError_t e = fp4_launch(c.wfmt, h->tc_bn, f4, &h->tmF_A13, &h->tmF_B13, h->num_sms, s);
-            if (e != cudaSuccess) return e;
-            SplitParams sa = sp;
-            sa.pass = pass;
-            sa.top_k = 0;
-            sa.src = h->d_act;
-            sa.src_ld = c.inter;
-            sa.K = c.inter;
-            sa.codes = h->d_aq;
-            sa.sf = h->d_asf;
-            sa.rs = h->d_ars;
-            e = fp4_split(sa, T * k, s);
-            if (e != cudaSuccess) return e;
-            f4.phase = 2;
-            f4.off_sf = h->lay.off_s2;
-            f4.b_sf = h->d_asf;
-            f4.b_rs = h->d_ars;
-            launches += 3;
-            return fp4_launch(c.wfmt, h->tc_bn, f4, &h->tmF_A2, &h->tmF_B2, h->num_sms, s);
+            launches += 1;
+            const Fp4Maps maps{&h->tmF_A13, &h->tmF_B13, &h->tmF_A2, &h->tmF_B2};
+            return fp4_launch(c.wfmt, h->fp4_bn, f4, maps, h->num_sms, s);
         }
         if (!h->use_tc) {
             fp.pass = pass;

@@ -263,6 +263,8 @@ __global__ void __launch_bounds__(kLookupThreads, 1) lookup_kernel(LookupParams 
     if (e < E && present) {
         int ent = is_hit ? hit_rank : n_hits + s_sub[e];
         if (p.rb.dep) p.rb.dep[ent] = 0;
+        if (p.rb.dep_x) p.rb.dep_x[ent] = 0;
+        if (p.rb.dep_a) p.rb.dep_a[ent] = 0;
         p.rb.entry_e[ent] = e;
         if (is_hit) p.rb.entry_dst[ent] = slot;
         s_cnt[ent] = 0;
@@ -379,6 +381,8 @@ __global__ void __launch_bounds__(1024, 1) sort_scan_kernel(int32_t* __restrict_
         rb.entry_off[e] = off;
         rb.entry_e[e] = e;
         if (rb.dep) rb.dep[e] = 0;
+        if (rb.dep_x) rb.dep_x[e] = 0;
+        if (rb.dep_a) rb.dep_a[e] = 0;
         rb.entry_dst[e] = e;
         for (int c = 0; c < n_chunks; ++c) chunk_counts[(int64_t)c * E + e] += off;
     }

@@ -10,19 +10,20 @@
 // `split_kernel` writes every activation row as the sum of P E2M1 "pieces", each with its own
 // power-of-two block scale (piece p quantises the residual left by pieces 0..p-1, its scale
 // chosen from the residual's block maximum so no code saturates). Each piece gains at least two
-// bits, so four pieces carry a bf16 row to within about 2^-9 of its block maximum. The MMA
-// accumulates all P pieces into one fp32 accumulator in tensor memory, so the product equals
-// W * (sum of pieces) without any extra pass. A per-row power-of-two prescale keeps the piece
+// bits, so four pieces carry a bf16 row to within about 2^-9 of its block maximum. The pieces
+// of a tile's BN rows are P x BN rows of the MMA's N operand (piece-major), so one MMA per K
+// step covers all of them and the epilogue adds the P column groups of the fp32 accumulator:
+// the result equals W * (sum of pieces). A per-row power-of-two prescale keeps the piece
 // scales inside the E4M3 range; the epilogue undoes it (and applies the NVFP4 tensor scale)
 // per accumulator column.
 //
 // Kernel roles per CTA (persistent, one CTA per SM, 6 warps):
 //   warp 0      producer: per 256-element K stage, the 128-row weight tile (3-D tensor map
-//               over the slot arena), its scale atoms (bulk copy from the slot), and for each
-//               piece the BN-row activation tile (2-D map) and its scale atoms.
+//               over the slot arena), its scale atoms (bulk copy from the slot), the tile's
+//               P x BN activation-piece rows (2-D map) and their scale atoms.
 //   warp 1      TMEM allocation; one lane copies the stage's scale atoms into tensor memory
-//               and issues 4 x P block-scaled MMAs (K = 64 each); commits free ring stages
-//               and publish finished accumulators.
+//               and issues 4 block-scaled MMAs (K = 64, N = P x BN); commits free ring
+//               stages and publishes finished accumulators.
 //   warps 2..5  epilogue: W13 tiles -> silu(g) * u -> bf16 activation rows; W2 tiles -> fp32
 //               expert outputs per (token, rank).
 // Every wait is bounded; a wait that runs out records an error code and all roles leave.
@@ -36,8 +37,8 @@ namespace fp4 {
 
 using namespace tc;
 
-constexpr int kSplitWarps = 8;
 constexpr int kStageK = 256;                 // K elements per stage: 128 bytes of E2M1
+constexpr int kFp4Threads = 224;             // producer, MMA issuer A, 4 epilogue warps, MMA issuer B
 constexpr int kABytes = 128 * 128;           // one 128-row weight tile of a stage
 
 __device__ __forceinline__ int exp_of(float v) {
@@ -51,24 +52,40 @@ __device__ __forceinline__ float pow2(int n) {   // n in [-126, 127]
     return __int_as_float((n + 127) << 23);
 }
 
-// Round m >= 0 to the nearest E2M1 magnitude (ties to the even code), saturating at 6.
-__device__ __forceinline__ uint32_t e2m1_rne(float m, float* q) {
-    float r;
-    uint32_t c;
-    if (m < 2.f) { r = rintf(m * 2.f) * 0.5f; c = (uint32_t)(r * 2.f); }
-    else if (m < 4.f) { r = rintf(m); c = (uint32_t)r + 2u; }
-    else { r = fminf(2.f * rintf(m * 0.5f), 6.f); c = r < 5.f ? 6u : 7u; }
-    *q = r;
-    return c;
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
 }
 
-template <int BS>
-__device__ __forceinline__ void split_block(float (&v)[BS], int pieces, int fmt, uint8_t* codes0,
-                                            int64_t piece_stride, uint8_t* sf0, int64_t sf_stride) {
-    for (int pc = 0; pc < pieces; ++pc) {
+// Two floats -> one byte of E2M1 codes (round to nearest even, saturating at +-6): the low
+// nibble takes `lo`, the high nibble `hi`.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint16_t b;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(b) : "f"(hi), "f"(lo));
+    return b;
+}
+
+// One byte of E2M1 codes -> its two values (low nibble first), exactly.
+__device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
+    uint32_t h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h) : "h"((uint16_t)byte));
+    return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// P pieces of 8 consecutive elements held by this thread. G adjacent lanes (G = block / 8)
+// share one scale block; all 32 lanes of the warp must call this together. Piece pc's codes go
+// to codes0 + pc * piece_stride (4 bytes); the block's scale byte of piece pc is written by the
+// group's first lane into the tile's atom at N-operand row n0 + pc, block jb.
+template <int G>
+__device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* codes0, int64_t piece_stride,
+                                       uint8_t* sf_atom, int n0, int jb, bool store, bool lead) {
+    for (int pc = 0; pc < P; ++pc) {
         float bmax = 0.f;
 #pragma unroll
-        for (int j = 0; j < BS; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
+        for (int j = 0; j < 8; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
         const int be = exp_of(bmax);
         int e;
         uint8_t sfb;
@@ -80,106 +97,95 @@ __device__ __forceinline__ void split_block(float (&v)[BS], int pieces, int fmt,
             sfb = e >= -6 ? (uint8_t)((e + 7) << 3) : (uint8_t)(1 << (e + 9));   // power-of-two E4M3
         }
         const float inv = pow2(-e), step = pow2(e);
-        uint32_t w[BS / 8];
+        uint32_t word = 0;
 #pragma unroll
-        for (int g = 0; g < BS / 8; ++g) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float x = v[g * 8 + j];
-                float q;
-                uint32_t c = e2m1_rne(fabsf(x) * inv, &q);
-                const float d = q * step;
-                if (x < 0.f) { if (c) c |= 8u; v[g * 8 + j] = x + d; }
-                else v[g * 8 + j] = x - d;
-                word |= c << (4 * j);
-            }
-            w[g] = word;
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t byte = e2m1x2(v[2 * j] * inv, v[2 * j + 1] * inv);
+            word |= byte << (8 * j);
+            const float2 q = e2m1x2_decode(byte);
+            v[2 * j] -= q.x * step;
+            v[2 * j + 1] -= q.y * step;
         }
-        uint8_t* dst = codes0 + pc * piece_stride;
-        if (BS == 32) *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        else *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-        sf0[pc * sf_stride] = sfb;
+        if (store) {
+            *reinterpret_cast<uint32_t*>(codes0 + pc * piece_stride) = word;
+            if (lead) {
+                const int n = n0 + pc;
+                sf_atom[(n & 31) * 16 + (n >> 5) * 4 + (jb & 3)] = sfb;
+            }
+        }
     }
 }
 
+// Split one bf16 row into P pieces with nt threads (whole warps, tid = 0..nt-1, named barrier
+// `bar`), each thread taking 8 elements at a time. The row is read through L2 (another CTA of
+// the launch may have written it). The row is prescaled by 2^t so that its largest magnitude
+// lands in [64, 128); the piece scales stay inside the E4M3 range that way, and 2^-t goes to
+// rs_out for the epilogue.
 template <int BS>
-__global__ void __launch_bounds__(kSplitWarps * 32) split_kernel(SplitParams p) {
-    __shared__ int s_tp[kMaxExperts + 1];
-    const RouteCounts rc = *p.counts;
-    const int U = rc.n_unique;
-    const int u_begin = p.pass == 1 ? rc.n_hits : 0;
-    const int u_end = p.pass == 0 ? rc.n_hits : U;
-    if (u_end <= u_begin) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < u_end; i += blockDim.x)
-        s_tp[i] = (p.entry_off[i + 1] - p.entry_off[i] + p.bn - 1) / p.bn;
-    __syncthreads();
-    if (warp == 0) {
-        const int per = (u_end + 31) / 32;
-        const int i0 = lane * per, i1 = min(u_end, i0 + per);
-        int local = 0;
-        for (int i = i0; i < i1; ++i) local += s_tp[i];
-        int incl = local;
+__device__ void split_row(const __nv_bfloat16* row, int K, int P, int fmt, uint8_t* codes_row,
+                          int64_t piece_stride, uint8_t* sf_tile, int n0, float* rs_out, int tid, int nt,
+                          int bar, float* s_red) {
+    constexpr int G = BS / 8;
+    float amax = 0.f;
+    for (int c = tid; c < K / 8; c += nt) {
+        const uint4 u4 = __ldcg(reinterpret_cast<const uint4*>(row) + c);
+        const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        int run = incl - local;
-        for (int i = i0; i < i1; ++i) { const int t = s_tp[i]; s_tp[i] = run; run += t; }
-        if (lane == 31) s_tp[u_end] = incl;
-    }
-    __syncthreads();
-    const int K = p.K, P = p.pieces, bn = p.bn;
-    const int nblk = K / BS;
-    const int atoms = nblk / 4;                        // scale atoms per (tile, piece)
-    const int r0 = p.entry_off[u_begin], r1 = p.entry_off[u_end];
-    for (int r = r0 + blockIdx.x * kSplitWarps + warp; r < r1; r += gridDim.x * kSplitWarps) {
-        int lo = u_begin, hi = u_end - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.entry_off[mid] <= r) lo = mid; else hi = mid - 1;
-        }
-        const int i = r - p.entry_off[lo];
-        const int tile = s_tp[lo] + i / bn, rin = i % bn;
-        const int64_t srow = p.top_k > 0 ? p.pairs[r] / p.top_k : r;
-        const __nv_bfloat16* row = p.src + srow * p.src_ld;
-        float amax = 0.f;
-        for (int c = lane; c < K / 8; c += 32) {
-            const uint4 u4 = __ldg(reinterpret_cast<const uint4*>(row) + c);
-            const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] << 16)));
-                amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] & 0xffff0000u)));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const int ex = exp_of(amax);
-        const int t = (ex <= -1000 || ex > 127) ? 0 : max(-100, min(100, 6 - ex));
-        const float pre = pow2(t);
-        if (lane == 0) p.rs[(int64_t)tile * bn + rin] = pow2(-t);
-        const int64_t prow = (int64_t)tile * P * bn + rin;          // piece 0's code row
-        for (int b = lane; b < nblk; b += 32) {
-            float v[BS];
-#pragma unroll
-            for (int g = 0; g < BS / 8; ++g) {
-                const uint4 u4 = __ldg(reinterpret_cast<const uint4*>(row + b * BS) + g);
-                const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    v[g * 8 + 2 * q] = __uint_as_float(w4[q] << 16) * pre;
-                    v[g * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u) * pre;
-                }
-            }
-            uint8_t* codes0 = p.codes + prow * (K / 2) + b * (BS / 2);
-            uint8_t* sf0 = p.sf + ((int64_t)tile * P * atoms + b / 4) * 512 + (rin & 31) * 16 +
-                           (rin >> 5) * 4 + (b & 3);
-            split_block<BS>(v, P, p.fmt, codes0, (int64_t)bn * (K / 2), sf0, (int64_t)atoms * 512);
+        for (int q = 0; q < 4; ++q) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] & 0xffff0000u)));
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((tid & 31) == 0) s_red[tid >> 5] = amax;
+    named_bar(bar, nt);
+    amax = s_red[0];
+    for (int w = 1; w < nt / 32; ++w) amax = fmaxf(amax, s_red[w]);
+    named_bar(bar, nt);
+    const int ex = exp_of(amax);
+    const int t = (ex <= -1000 || ex > 127) ? 0 : max(-100, min(100, 6 - ex));
+    const float pre = pow2(t);
+    if (tid == 0) *rs_out = pow2(-t);
+    // K / 8 is a multiple of 32, so every warp runs the same number of iterations
+    for (int c = tid; c < K / 8; c += nt) {
+        const uint4 u4 = __ldcg(reinterpret_cast<const uint4*>(row) + c);
+        const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[2 * q] = __uint_as_float(w4[q] << 16) * pre;
+            v[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u) * pre;
+        }
+        const int jb = c / G;
+        split8<G>(v, P, fmt, codes_row + c * 4, piece_stride, sf_tile + (jb / 4) * 512, n0, jb, true,
+                  (c % G) == 0);
+    }
+}
+
+__device__ __forceinline__ int ld_acquire_s32(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until *flag >= target (written by other CTAs of this launch).
+__device__ __forceinline__ bool wait_count(const int* flag, int target, int* err, int code) {
+    // back off to ~1 us between polls: many CTAs poll a few flags, and a tight loop floods
+    // the L2 slice that also serves the writers
+    uint32_t ns = 64;
+    for (uint32_t i = 0; i < (kWaitLimit >> 4); ++i) {
+        if (ld_acquire_s32(flag) >= target) return true;
+        if ((i & 63u) == 63u && *(volatile int*)err) return false;
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+    }
+    atomicCAS(err, 0, code);
+    return false;
 }
 
 template <int FMT>
@@ -207,10 +213,16 @@ __device__ __forceinline__ uint32_t idesc_fp4(int n, uint32_t id) {
            ((FMT == FT_W_MXFP4 ? 1u : 0u) << 23) | ((uint32_t)(128 >> 4) << 24) | (id << 29);
 }
 
-struct FTile { int u, g, mt; };
+struct FTile { int u, g, mt; bool w13; };
 
-__device__ __forceinline__ FTile fp4_tile(int t, const int* s_tp, int u_begin, int u_end, int m_tiles) {
+// Tile t of the launch: W13 tiles of the pass's entries first, then W2 tiles; within a phase
+// entry by entry, then N tiles, then the 128-row M tiles (innermost).
+__device__ __forceinline__ FTile fp4_tile(int t, const int* s_tp, int u_begin, int u_end, int m13, int m2) {
     FTile r;
+    const int nt_pass = s_tp[u_end] - s_tp[u_begin];
+    int m_tiles = m13;
+    r.w13 = t < nt_pass * m13;
+    if (!r.w13) { t -= nt_pass * m13; m_tiles = m2; }
     r.g = s_tp[u_begin] + t / m_tiles;
     r.mt = t % m_tiles;
     int lo = u_begin, hi = u_end - 1;
@@ -222,37 +234,52 @@ __device__ __forceinline__ FTile fp4_tile(int t, const int* s_tp, int u_begin, i
     return r;
 }
 
-template <int BN, int FMT>
-__global__ void __launch_bounds__(kThreads, 1) fp4_ffn_kernel(
-    Fp4Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+__device__ __forceinline__ int entry_of_row(const int* s_eoff, int u_begin, int u_end, int r) {
+    int lo = u_begin, hi = u_end - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_eoff[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int BN, int FMT, int P>
+__global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
+    Fp4Params p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
+    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr int BS = FMT == FT_W_MXFP4 ? 32 : 16;
     constexpr int APS = kStageK / (BS * 4);           // scale atoms per operand per stage
     constexpr int SF_BYTES = APS * 512;
-    constexpr int B_BYTES = BN * 128;
-    constexpr uint32_t SF_COL0 = 256;                 // scale-factor columns (two buffers of 128)
+    constexpr uint32_t SF_COL0 = 256;                 // scale-factor columns: one buffer of 64 per issuer
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int S = p.stages, STAGE = p.stage_bytes, P = p.pieces;
+    const int S = p.stages, STAGE = p.stage_bytes;
+    constexpr int NC = P * BN;                        // rows of a tile's N operand: BN tokens x P pieces
+    constexpr int B_BYTES = NC * 128;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
-    int* s_tp = reinterpret_cast<int*>(s_tmem + 4);
+    int* s_flag = reinterpret_cast<int*>(s_tmem + 1);
+    int* s_eoff = reinterpret_cast<int*>(s_tmem + 4);          // [kMaxExperts + 1]
+    int* s_tp = s_eoff + (kMaxExperts + 1);                      // [kMaxExperts + 1]
+    float* s_red = reinterpret_cast<float*>(s_tp + (kMaxExperts + 1));   // [8]
+    float* s_stage = s_red + 8;                                          // [32][65] SwiGLU values
+    int* s_got = reinterpret_cast<int*>(s_stage + 32 * 65);                // [2][4] epilogue votes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RouteCounts rc = *p.counts;
     const int u_begin = p.pass == 1 ? rc.n_hits : 0;
     const int u_end = p.pass == 0 ? rc.n_hits : rc.n_unique;
     if (u_end <= u_begin) return;
-    const bool w13 = p.phase == 13;
-    const int K = w13 ? p.hidden : p.inter;
-    const int rows = w13 ? 2 * p.inter : p.hidden;
-    const int m_tiles = rows / 128, k_stages = K / kStageK;
-    const int atoms_k = K / BS / 4;                  // scale atoms per 128-row band / per tile piece
+    const int H = p.hidden, I = p.inter;
+    const int m13 = 2 * I / 128, m2 = H / 128;
+    const int ak13 = H / BS / 4, ak2 = I / BS / 4;   // scale atoms per 128-row band / per tile
 
-    for (int i = threadIdx.x; i < u_end; i += blockDim.x)
-        s_tp[i] = (p.entry_off[i + 1] - p.entry_off[i] + BN - 1) / BN;
+    for (int i = threadIdx.x; i <= u_end; i += blockDim.x) s_eoff[i] = p.entry_off[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < u_end; i += blockDim.x) s_tp[i] = (s_eoff[i + 1] - s_eoff[i] + BN - 1) / BN;
     __syncthreads();
     if (warp == 0) {
         const int per = (u_end + 31) / 32;
@@ -270,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_ffn_kernel(
         if (lane == 31) s_tp[u_end] = incl;
     }
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+        // a stage is free, and an accumulator full, once both MMA issuers have committed
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 2); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 2); mbar_init(&tempty[a], 4); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -283,33 +311,84 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_ffn_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
-    const int total = (s_tp[u_end] - s_tp[u_begin]) * m_tiles;
+    const int nt_pass = s_tp[u_end] - s_tp[u_begin];
+    const int total = nt_pass * (m13 + m2);
     int* err = p.err;
+
+    // 1. W13 activation pieces: the launch's CTAs split the pass's token rows between them
+    {
+        const int r0 = s_eoff[u_begin], r1 = s_eoff[u_end];
+        for (int r = r0 + blockIdx.x; r < r1; r += gridDim.x) {
+            const int u = entry_of_row(s_eoff, u_begin, u_end, r);
+            const int i = r - s_eoff[u];
+            const int tile = s_tp[u] + i / BN, rin = i % BN;
+            const __nv_bfloat16* src = p.x + (int64_t)(p.pairs[r] / p.top_k) * H;
+            split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
+                          p.xsf + (int64_t)tile * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
+                          threadIdx.x, kFp4Threads, 2, s_red);
+            fence_proxy_async_global();
+            __threadfence();
+            named_bar(2, kFp4Threads);
+            if (threadIdx.x == 0) atomicAdd(p.cnt_x + u, 1);
+        }
+    }
 
     if (warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m_tiles);
+                const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
+                const int K = tl.w13 ? H : I;
+                const int k_stages = K / kStageK;
+                const int ak = tl.w13 ? ak13 : ak2;
+                const CUtensorMap* mA = tl.w13 ? &tmA13 : &tmA2;
+                const CUtensorMap* mB = tl.w13 ? &tmB13 : &tmB2;
+                const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * ak * 512;
                 const int slot = p.entry_dst[tl.u];
-                const uint8_t* sfa = p.arena + (int64_t)slot * p.blob_bytes + p.off_sf +
-                                     (int64_t)tl.mt * atoms_k * 512;
-                for (int kb = 0; kb < k_stages; ++kb, ++it) {
+                const uint8_t* sfa = p.arena + (int64_t)slot * p.blob_bytes + (tl.w13 ? p.off_s13 : p.off_s2) +
+                                     (int64_t)tl.mt * ak * 512;
+                // the tile's rows are token-major (token i, piece pc at row i * P + pc): only the
+                // first P * n_valid rows carry data, loaded as 16-row boxes
+                const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
+                const int nbox = (P * n_valid + 15) / 16;
+                const uint32_t stage_tx = (uint32_t)(kABytes + 2 * SF_BYTES + nbox * 2048);
+                // weights (and their scales) of the first stages go out before the activation
+                // pieces of this entry are known to be ready
+                const int npre = min(S, k_stages);
+                const uint32_t it0 = it;
+                for (int kb = 0; kb < npre; ++kb, ++it) {
                     const int s = it % S;
                     if (!mbar_wait(&empty[s], ((it / S) & 1u) ^ 1u, err, 1)) { ok = false; break; }
                     uint8_t* st = smem + (size_t)s * STAGE;
-                    uint8_t* st_sf = st + kABytes + P * B_BYTES;
-                    mbar_expect_tx(&full[s], STAGE);
-                    tma_load_3d(st, &tmA, &full[s], kb * 128, tl.mt * 128, slot);
-                    bulk_load(st_sf, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
-                    for (int pc = 0; pc < P; ++pc) {
-                        const int brow = (tl.g * P + pc) * BN;
-                        tma_load_2d(st + kABytes + pc * B_BYTES, &tmB, &full[s], kb * 128, brow);
-                        bulk_load(st_sf + (1 + pc) * SF_BYTES,
-                                  p.b_sf + ((int64_t)(tl.g * P + pc) * atoms_k + kb * APS) * 512,
-                                  SF_BYTES, &full[s]);
-                    }
+                    mbar_expect_tx(&full[s], stage_tx);
+                    tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
+                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
+                }
+                if (!ok) break;
+                const bool ready = tl.w13 ? wait_count(p.cnt_x + tl.u, s_eoff[tl.u + 1] - s_eoff[tl.u], err, 6)
+                                          : wait_count(p.cnt_w13 + tl.u, m13 * (s_tp[tl.u + 1] - s_tp[tl.u]), err, 7);
+                fence_proxy_async_global();
+                // the armed stages expect their activation bytes: load them in any case so the
+                // ring drains if the wait ran out
+                for (int kb = 0; kb < npre; ++kb) {
+                    uint8_t* st = smem + (size_t)((it0 + kb) % S) * STAGE;
+                    uint64_t* fb = &full[(it0 + kb) % S];
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_load_2d(st + kABytes + bx * 2048, mB, fb, kb * 128, tl.g * NC + bx * 16);
+                    bulk_load(st + kABytes + B_BYTES + SF_BYTES, bsf + (int64_t)kb * SF_BYTES, SF_BYTES, fb);
+                }
+                if (!ready) { ok = false; break; }
+                for (int kb = npre; kb < k_stages; ++kb, ++it) {
+                    const int s = it % S;
+                    if (!mbar_wait(&empty[s], ((it / S) & 1u) ^ 1u, err, 1)) { ok = false; break; }
+                    uint8_t* st = smem + (size_t)s * STAGE;
+                    mbar_expect_tx(&full[s], stage_tx);
+                    tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
+                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_load_2d(st + kABytes + bx * 2048, mB, &full[s], kb * 128, tl.g * NC + bx * 16);
+                    bulk_load(st + kABytes + B_BYTES + SF_BYTES, bsf + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
                 }
             }
             if (!ok) {
@@ -317,44 +396,50 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_ffn_kernel(
                     mbar_wait(&full[j % S], (j / S) & 1u, err, 5);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
+        // Two issuers: in every stage warp 1 issues K steps 0-1 and warp 6 K steps 2-3 (with the
+        // scale atoms those steps read), each into its own accumulator; the epilogue adds the
+        // two. One thread issuing every tcgen05.mma / cp of a decode tile (N = 16) cannot keep
+        // up with the weight stream; two can.
+        const uint32_t par = warp == 6 ? 1u : 0u;
+        constexpr int HA = APS / 2;                   // scale atoms per operand per issuer
         if (lane == 0) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
-                const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m_tiles);
-                const int nt = tl.g - s_tp[tl.u];
-                const int row_b = p.entry_off[tl.u] + nt * BN;
-                const int n_valid = min(BN, p.entry_off[tl.u + 1] - row_b);
-                const int n_mma = min(BN, (n_valid + 15) & ~15);
+                const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
+                const int k_stages = (tl.w13 ? H : I) / kStageK;
+                const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
+                const int n_mma = (P * n_valid + 15) & ~15;
                 const uint32_t acc = tcount & 1u;
                 if (!mbar_wait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, err, 2)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + (acc * 2u + par) * (uint32_t)NC;
                 for (int kb = 0; kb < k_stages; ++kb, ++it) {
                     const int s = it % S;
                     if (!mbar_wait(&full[s], (it / S) & 1u, err, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + (size_t)s * STAGE);
-                    const uint32_t ssf = sa + kABytes + P * B_BYTES;
-                    const uint32_t tsf = tmem_base + SF_COL0 + (it & 1u) * 128u;
-                    // scale atoms -> TMEM: A at tsf + 4a, piece pc at tsf + 4 * APS * (1 + pc) + 4a
-                    for (int q = 0; q < 1 + P; ++q)
+                    const uint32_t ssf = sa + kABytes + B_BYTES;
+                    // this issuer's scale atoms -> TMEM (double-buffered by stage parity):
+                    // weights at tsf + 4a, activation pieces at tsf + 4 (HA + a)
+                    const uint32_t tsf = tmem_base + SF_COL0 + par * 64u + (it & 1u) * 32u;
 #pragma unroll
-                        for (int a = 0; a < APS; ++a)
-                            tmem_cp_sf(tsf + (uint32_t)(4 * (q * APS + a)),
-                                       smem_desc_sf(ssf + q * SF_BYTES + a * 512));
+                    for (int a = 0; a < HA; ++a) {
+                        const int ga = (int)par * HA + a;     // atom within the stage
+                        tmem_cp_sf(tsf + (uint32_t)(4 * a), smem_desc_sf(ssf + ga * 512));
+                        tmem_cp_sf(tsf + (uint32_t)(4 * (HA + a)), smem_desc_sf(ssf + (APS + ga) * 512));
+                    }
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const int ai = FMT == FT_W_MXFP4 ? (kk >> 1) : kk;
-                        const uint32_t id = FMT == FT_W_MXFP4 ? (uint32_t)((kk & 1) * 2) : 0u;
-                        const uint32_t idesc = idesc_fp4<FMT>(n_mma, id);
-                        const uint64_t da = smem_desc_sw128(sa + kk * 32);
-                        for (int pc = 0; pc < P; ++pc) {
-                            mma_bs<FMT>(d_tmem, da, smem_desc_sw128(sa + kABytes + pc * B_BYTES + kk * 32), idesc,
-                                        tsf + 4 * ai, tsf + 4 * (APS * (1 + pc) + ai),
-                                        (kb | kk | pc) ? 1u : 0u);
-                        }
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const int kk = (int)par * 2 + k2;
+                        // MXFP4: one atom (4 blocks of 32) per two K steps, byte pair 0 or 2;
+                        // NVFP4: one atom (4 blocks of 16) per K step
+                        const int ai = FMT == FT_W_MXFP4 ? 0 : k2;
+                        const uint32_t id = FMT == FT_W_MXFP4 ? (uint32_t)(k2 * 2) : 0u;
+                        mma_bs<FMT>(d_tmem, smem_desc_sw128(sa + kk * 32),
+                                    smem_desc_sw128(sa + kABytes + kk * 32), idesc_fp4<FMT>(n_mma, id),
+                                    tsf + 4 * ai, tsf + 4 * (HA + ai), (kb == 0 && k2 == 0) ? 0u : 1u);
                     }
                     mma_commit(&empty[s]);
                 }
@@ -364,58 +449,112 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_ffn_kernel(
         }
     } else {
         const int q = warp & 3;
+        const int etid = threadIdx.x - 64;                 // 0..127 over the epilogue warps
         const int row_in_tile = q * 32 + lane;
         uint32_t tcount = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-            const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m_tiles);
+            const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
             const int nt = tl.g - s_tp[tl.u];
-            const int row_b = p.entry_off[tl.u] + nt * BN;
-            const int n_valid = min(BN, p.entry_off[tl.u + 1] - row_b);
+            const int row_b = s_eoff[tl.u] + nt * BN;
+            const int n_valid = min(BN, s_eoff[tl.u + 1] - row_b);
             const uint32_t acc = tcount & 1u;
-            if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1u, err, 4)) break;
-            tc_fence_after();
-            float ts = 1.f;
-            if (FMT == FT_W_NVFP4) {
-                const int slot = p.entry_dst[tl.u];
-                ts = reinterpret_cast<const float*>(p.arena + (int64_t)slot * p.blob_bytes + p.off_ts)[w13 ? 0 : 1];
-            }
-            const float* rsp = p.b_rs + (int64_t)tl.g * BN;
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            const int m = tl.mt * 128 + row_in_tile;
+            // the four epilogue warps agree on the outcome of the wait, so that they always meet
+            // at the same named barriers (votes are double-buffered by tile parity); after a
+            // wait runs out they keep looping without work, and later waits return at once
+            // because the error word is set
+            const bool mine = mbar_wait(&tfull[acc], (tcount >> 1) & 1u, err, 4);
+            int* vote = s_got + (tcount & 1u) * 4;
+            if (lane == 0) vote[q] = mine ? 1 : 0;
+            named_bar(1, 128);
+            const bool got = vote[0] && vote[1] && vote[2] && vote[3];
+            if (got) {
+                tc_fence_after();
+                float ts = 1.f;
+                if (FMT == FT_W_NVFP4) {
+                    const int slot = p.entry_dst[tl.u];
+                    ts = reinterpret_cast<const float*>(p.arena + (int64_t)slot * p.blob_bytes + p.off_ts)[tl.w13 ? 0 : 1];
+                }
+                const float* rsp = p.xrs + (int64_t)tl.g * BN;     // W13 only: the x rows' prescale
+                // accumulator pair of this tile: issuer A at (2 acc) NC, issuer B at (2 acc + 1) NC
+                const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 2u * (uint32_t)NC;
+                const int m = tl.mt * 128 + row_in_tile;
+                // columns are token-major: token i's pieces are columns i * P .. i * P + P - 1,
+                // so a 16-column load holds 16 / P whole tokens
+                constexpr int tpc = 16 / P;
+                const int ncols = (P * n_valid + 15) & ~15;
 #pragma unroll 1
-            for (int c0 = 0; c0 < n_valid; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tbase + c0, r);
-                tmem_wait_ld();
-                float own[16];
+                for (int c0 = 0; c0 < ncols; c0 += 16) {
+                    uint32_t r[16], r2[16];
+                    tmem_ld16(tbase + c0, r);
+                    tmem_ld16(tbase + NC + c0, r2);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) own[j] = __uint_as_float(r[j]) * (ts * __ldg(rsp + c0 + j));
-                if (w13) {
-                    const bool odd = lane & 1;
-                    const int feat = m >> 1;
+                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                    const int i0 = c0 / P;                     // first token of the chunk
+                    float tok[tpc];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float send = odd ? own[j] : own[j + 8];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                        const float g = odd ? recv : own[j];
-                        const float uu = odd ? own[j + 8] : recv;
-                        const int n = c0 + (odd ? 8 + j : j);
-                        if (n < n_valid) {
+                    for (int j = 0; j < tpc; ++j) {
+                        float sum = 0.f;
+#pragma unroll
+                        for (int pc = 0; pc < P; ++pc) sum += __uint_as_float(r[j * P + pc]);
+                        tok[j] = sum * (tl.w13 ? ts * __ldcg(rsp + min(i0 + j, BN - 1)) : ts);
+                    }
+                    if (tl.w13) {
+                        // lanes 2f / 2f+1 hold the gate / up rows of feature f: the even lane
+                        // finishes the first half of the chunk's tokens, the odd lane the rest
+                        const bool odd = lane & 1;
+                        const int feat = m >> 1;
+                        const int lf = feat - tl.mt * 64;      // feature within the tile, 0..63
+                        constexpr int half = tpc / 2;
+#pragma unroll
+                        for (int jj = 0; jj < half; ++jj) {
+                            const float send = odd ? tok[jj] : tok[jj + half];
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                            const float g = odd ? recv : tok[jj];
+                            const float uu = odd ? tok[jj + half] : recv;
+                            const int i = i0 + (odd ? jj + half : jj);
                             const float a = g / (1.f + __expf(-g)) * uu;
-                            p.act[(int64_t)(row_b + n) * p.act_ld + feat] = __float2bfloat16_rn(a);
+                            const __nv_bfloat16 ab = __float2bfloat16_rn(a);
+                            if (i < n_valid) p.act[(int64_t)(row_b + i) * I + feat] = ab;
+                            s_stage[i * 65 + lf] = __bfloat162float(ab);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < tpc; ++j) {
+                            const int i = i0 + j;
+                            if (i < n_valid) p.y[(int64_t)p.pairs[row_b + i] * H + m] = tok[j];
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = c0 + j;
-                        if (n < n_valid) p.y[(int64_t)p.pairs[row_b + n] * p.y_ld + m] = own[j];
-                    }
                 }
+                if (tl.w13) {
+                    // the tile's 64 features of its tokens -> W2 activation pieces; item = token
+                    // i (item / 8) x features (item % 8) * 8 .. + 7
+                    named_bar(1, 128);
+                    constexpr int G = BS / 8;
+                    for (int item = etid; item < BN * 8; item += 128) {
+                        const int i = item >> 3, f8 = (item & 7) * 8;
+                        float v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[j] = s_stage[i * 65 + f8 + j];
+                        const int f0 = tl.mt * 64 + f8;             // first feature of the 8
+                        const int jb = f0 / BS;                     // scale block along K = I
+                        split8<G>(v, P, FMT, p.aq + ((int64_t)tl.g * NC + i * P) * (I / 2) + f0 / 2, I / 2,
+                                  p.asf + ((int64_t)tl.g * ak2 + jb / 4) * 512, i * P, jb, i < n_valid,
+                                  (f8 % BS) == 0);
+                    }
+                    named_bar(1, 128);
+                }
+                tc_fence_before();
             }
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (lane == 0 && got) mbar_arrive(&tempty[acc]);
+            if (tl.w13) {
+                // publish this tile's activation pieces to the entry's W2 tiles (TMA readers)
+                fence_proxy_async_global();
+                __threadfence();
+                named_bar(1, 128);
+                if (etid == 0) atomicAdd(p.cnt_w13 + tl.u, 1);
+            }
         }
     }
     tc_fence_before();
@@ -451,32 +590,31 @@ EncodeTiledFn encode_fn() {
 }
 
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kStageBudget = 212 * 1024;
 
 int stage_bytes_for(int fmt, int bn, int pieces) {
     const int aps = fmt == FT_W_MXFP4 ? 2 : 4;
-    return fp4::kABytes + pieces * bn * 128 + (1 + pieces) * aps * 512;
+    return fp4::kABytes + pieces * bn * 128 + 2 * aps * 512;
 }
 
 template <int BN, int FMT>
-cudaError_t launch_t(const Fp4Params& p0, const CUtensorMap* a, const CUtensorMap* b, int grid,
-                     cudaStream_t s) {
+cudaError_t launch_t(const Fp4Params& p0, const Fp4Maps& m, int grid, cudaStream_t s) {
+    constexpr int P = kFp4MaxPieces;
     Fp4Params p = p0;
     p.stage_bytes = stage_bytes_for(FMT, BN, p.pieces);
-    p.stages = kStageBudget / p.stage_bytes;
-    if (p.stages > 12) p.stages = 12;
+    const size_t fixed = 1024 + 4 * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + 32 * 65 * 4 + 32 + 64;
+    p.stages = (int)((kSmemLimit - fixed) / (p.stage_bytes + 16));
+    if (p.stages > 8) p.stages = 8;
     if (p.stages < 2) return cudaErrorInvalidValue;
-    const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + (2 * p.stages + 4) * 8 + 16 +
-                        (kMaxExperts + 1) * 4;
+    const size_t smem = fixed + (size_t)p.stages * (p.stage_bytes + 16);
     if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(fp4::fp4_ffn_kernel<BN, FMT>,
+        cudaError_t e = cudaFuncSetAttribute(fp4::fp4_ffn_kernel<BN, FMT, P>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    fp4::fp4_ffn_kernel<BN, FMT><<<grid, tc::kThreads, smem, s>>>(p, *a, *b);
+    fp4::fp4_ffn_kernel<BN, FMT, P><<<grid, fp4::kFp4Threads, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
     return cudaGetLastError();
 }
 
@@ -486,9 +624,9 @@ size_t fp4_piece_bytes(int64_t tiles, int pieces, int bn, int K) {
     return (size_t)tiles * pieces * bn * (K / 2);
 }
 
-size_t fp4_sf_bytes(int64_t tiles, int pieces, int K, int fmt) {
+size_t fp4_sf_bytes(int64_t tiles, int K, int fmt) {
     const int bs = fmt == FT_W_MXFP4 ? 32 : 16;
-    return (size_t)tiles * pieces * (K / bs / 4) * 512;
+    return (size_t)tiles * (K / bs / 4) * 512;
 }
 
 cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, int rows,
@@ -505,12 +643,12 @@ cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, in
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int64_t rows, int bn) {
+cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int64_t rows, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)(k_dim / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(k_dim / 2)};
-    cuuint32_t box[2] = {128, (cuuint32_t)bn};
+    cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -518,29 +656,18 @@ cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t fp4_split(const SplitParams& p, int rows_max, cudaStream_t s) {
-    if (rows_max <= 0) return cudaSuccess;
-    if (p.K % fp4::kStageK || p.pieces < 1 || p.pieces > kFp4MaxPieces) return cudaErrorInvalidValue;
-    int blocks = (rows_max + fp4::kSplitWarps - 1) / fp4::kSplitWarps;
-    if (blocks > 148 * 8) blocks = 148 * 8;
-    if (p.fmt == FT_W_MXFP4) fp4::split_kernel<32><<<blocks, fp4::kSplitWarps * 32, 0, s>>>(p);
-    else fp4::split_kernel<16><<<blocks, fp4::kSplitWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const CUtensorMap* a,
-                       const CUtensorMap* b, int grid, cudaStream_t s) {
-    if (p.pieces < 1 || p.pieces > kFp4MaxPieces) return cudaErrorInvalidValue;
+cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, int grid, cudaStream_t s) {
+    // the kernel is built for kFp4MaxPieces pieces (a divisor of 16: one 16-column accumulator
+    // load holds whole tokens), P * bn <= 128 rows of scale atoms
+    if (p.pieces != kFp4MaxPieces || p.pieces * bn > 128 || p.top_k < 1) return cudaErrorInvalidValue;
     if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK) return cudaErrorInvalidValue;
 #define FT_FP4_CASE(BNV)                                                                   \
     case BNV:                                                                              \
-        return fmt == FT_W_MXFP4 ? launch_t<BNV, FT_W_MXFP4>(p, a, b, grid, s)             \
-                                 : launch_t<BNV, FT_W_NVFP4>(p, a, b, grid, s);
+        return fmt == FT_W_MXFP4 ? launch_t<BNV, FT_W_MXFP4>(p, m, grid, s)                \
+                                 : launch_t<BNV, FT_W_NVFP4>(p, m, grid, s);
     switch (bn) {
         FT_FP4_CASE(16)
         FT_FP4_CASE(32)
-        FT_FP4_CASE(64)
-        FT_FP4_CASE(128)
         default: return cudaErrorInvalidValue;
     }
 #undef FT_FP4_CASE
