@@ -427,7 +427,9 @@ def run_prefill(args):
     from expert_cached_sparse_top_b300 import ftmoe
     cfg = W.config(args.workload)
     torch.cuda.set_device(0)
-    pool = HostPool(cfg, images=cfg.experts + 3)
+    fp4 = cfg.wfmt != "bf16"
+    # the 256-expert MXFP4 layer aliases 16 physical blobs (keys and PCIe bytes unchanged)
+    pool = HostPool(cfg, images=16 if fp4 else cfg.experts + 3)
     T = cfg.tokens
     c = ftmoe.make_config(cfg.layers, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, 16, cfg.wfmt,
                           1, max_prefill_tokens=T)
@@ -468,23 +470,41 @@ def run_prefill(args):
     layer_ms = sum(a.elapsed_time(e) for a, e in evs) / len(evs)
     peaks = _peaks()
     bf16 = peaks.get("bf16_tflops")
+    hbm = peaks.get("hbm_gbs", 6487.4)
+    ffn_ms = tc["prefill_ffn_ms"] / max(tc["prefill_calls"], 1)
     ffn_tflops = tc["prefill_flops"] / (tc["prefill_ffn_ms"] * 1e-3) / 1e12
     wbytes = cfg.experts * pool.blob_bytes
+    ceiling = (6.0 * T * cfg.top_k * cfg.hidden * cfg.inter) / (wbytes / (hbm * 1e9)) / 1e12
+    if fp4:
+        # ~96 tokens per expert: the layer's weights bound it (the HBM ceiling is far below the
+        # FP4 tensor peak), so the roofline is weight bytes per FFN second against HBM
+        gbs = wbytes / (ffn_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "block-scaled tcgen05 grouped GEMM (MXFP4 x MXFP4: W13+SwiGLU, W2)",
+                "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs", "tflops": ffn_tflops,
+                "hbm_bound_ceiling_tflops": ceiling, "frac_of_hbm_ceiling": ffn_tflops / ceiling}
+        metric = ("MoE-layer prefill tokens/s (284B-shaped MXFP4 layer, 256 experts top-6, 4096 tokens, "
+                  "layers streamed)")
+    else:
+        roof = {"bound": "tensor", "kernel": "tcgen05 grouped GEMM (W13+SwiGLU, W2)",
+                "achieved": ffn_tflops, "peak": bf16, "unit": "TFLOP/s",
+                "frac": ffn_tflops / bf16 if bf16 else None, "traffic": None,
+                "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)",
+                "hbm_bound_ceiling_tflops": ceiling}
+        metric = "MoE-layer prefill tokens/s (35B-A3B-shaped BF16 layer, 4096 tokens, layers streamed)"
     line = {
-        "metric": "MoE-layer prefill tokens/s (35B-A3B-shaped BF16 layer, 4096 tokens, layers streamed)",
+        "metric": metric,
         "value": T * cfg.layers / stream_s, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * stream_s / cfg.layers,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 weights x mxfp4 activations" if fp4 else "bf16",
         "data": "synthetic",
         "config": {"workload": args.workload, "tokens": T, "experts": cfg.experts, "top_k": cfg.top_k,
                    "hidden": cfg.hidden, "inter": cfg.inter, "layers": cfg.layers,
+                   "pool": "pinned host, %d blobs x %d B%s" % (pool.images, pool.blob_bytes,
+                                                             " (keys aliased)" if fp4 else ""),
                    "l2": "flushed before every compute-only step"},
-        "roofline": {"bound": "tensor", "kernel": "tcgen05 grouped GEMM (W13+SwiGLU, W2)",
-                     "achieved": ffn_tflops, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": ffn_tflops / bf16 if bf16 else None, "traffic": None,
-                     "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)",
-                     "hbm_bound_ceiling_tflops": (6.0 * T * cfg.top_k * cfg.hidden * cfg.inter) /
-                         (wbytes / (peaks.get("hbm_gbs", 6487.4) * 1e9)) / 1e12},
+        "roofline": roof,
         "extras": {"compute_only_layer_ms": layer_ms,
                    "compute_only_tokens_per_s": T / (layer_ms * 1e-3),
                    "ffn_ms_per_layer": tc["prefill_ffn_ms"] / max(tc["prefill_calls"], 1),
@@ -505,7 +525,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=list(DECODE) + ["prefill_bf16"])
+                    choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4"])
     args = ap.parse_args()
     dflt = DECODE.get(args.workload, (None, None, 8, 3))
     if args.steps is None:

@@ -130,6 +130,17 @@ struct ft_moe {
     CUtensorMap tmP_A13[2]{}, tmP_A2[2]{};
     CUtensorMap tmP_B13[5]{}, tmP_B2[5]{};     // per N tile width 16..256
     bool p_b_ok[5] = {false, false, false, false, false};
+    // prefill on the block-scaled tensor cores (MXFP4 weights, MXFP4 activations)
+    bool use_fp4_prefill = false;
+    int64_t p_fp4_tiles = 0;
+    uint8_t* d_p_tq = nullptr;            // token-major activation codes [T][H/2]
+    uint8_t* d_p_tsf = nullptr;           // and scale bytes [T][H/32]
+    uint8_t* d_p_fxq = nullptr;           // W13 N operand (tile-major), scale atoms, row scales
+    uint8_t* d_p_fxsf = nullptr;
+    float* d_p_fxrs = nullptr;
+    uint8_t* d_p_faq = nullptr;           // W2 N operand and scale atoms
+    uint8_t* d_p_fasf = nullptr;
+    CUtensorMap tmPF_A13[2]{}, tmPF_A2[2]{}, tmPF_B13{}, tmPF_B2{};
     std::vector<PrefillEvents> p_pending;
 
     bool timing = false;
@@ -268,6 +279,8 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
     cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
     cudaFree(h->d_p_route_mem); cudaFree(h->d_p_xp); cudaFree(h->d_p_act); cudaFree(h->d_p_y);
+    cudaFree(h->d_p_tq); cudaFree(h->d_p_tsf); cudaFree(h->d_p_fxq); cudaFree(h->d_p_fxsf);
+    cudaFree(h->d_p_fxrs); cudaFree(h->d_p_faq); cudaFree(h->d_p_fasf);
     for (int b = 0; b < 2; ++b) {
         if (h->ev_buf_ready[b]) cudaEventDestroy(h->ev_buf_ready[b]);
         if (h->ev_buf_free[b]) cudaEventDestroy(h->ev_buf_free[b]);
@@ -440,6 +453,37 @@ ft_status alloc_prefill(ft_moe* h) {
     }
     FT_CUDA(h, dm((void**)&h->d_p_act, (size_t)h->p_rows * I * 2));
     FT_CUDA(h, dm((void**)&h->d_p_y, (size_t)npairs * H * 4));
+    h->use_fp4_prefill = h->use_fp4 && c.wfmt == FT_W_MXFP4;
+    if (h->use_fp4_prefill) {
+        const int bn = 128;
+        const int64_t T = h->max_prefill;
+        h->p_fp4_tiles = E + (npairs + bn - 1) / bn;
+        const size_t xq = fp4_piece_bytes(h->p_fp4_tiles, 1, bn, (int)H);
+        const size_t aq = fp4_piece_bytes(h->p_fp4_tiles, 1, bn, (int)I);
+        const size_t xsf = fp4_sf_bytes(h->p_fp4_tiles, (int)H, c.wfmt);
+        const size_t asf = fp4_sf_bytes(h->p_fp4_tiles, (int)I, c.wfmt);
+        FT_CUDA(h, dm((void**)&h->d_p_tq, (size_t)T * H / 2));
+        FT_CUDA(h, dm((void**)&h->d_p_tsf, (size_t)T * H / 32));
+        FT_CUDA(h, dm((void**)&h->d_p_fxq, xq));
+        FT_CUDA(h, dm((void**)&h->d_p_fxsf, xsf));
+        FT_CUDA(h, dm((void**)&h->d_p_fxrs, (size_t)h->p_fp4_tiles * bn * 4));
+        FT_CUDA(h, dm((void**)&h->d_p_faq, aq));
+        FT_CUDA(h, dm((void**)&h->d_p_fasf, asf));
+        // rows of a tile past its last token are read by the MMA and ignored; start them at zero
+        FT_CUDA(h, cudaMemset(h->d_p_fxq, 0, xq));
+        FT_CUDA(h, cudaMemset(h->d_p_faq, 0, aq));
+        FT_CUDA(h, cudaMemset(h->d_p_fxsf, 0, xsf));
+        FT_CUDA(h, cudaMemset(h->d_p_fasf, 0, asf));
+        const int64_t prow = h->p_fp4_tiles * bn;
+        for (int b = 0; b < 2; ++b) {
+            FT_CUDA(h, fp4_encode_weights(&h->tmPF_A13[b], h->d_layerbuf[b] + h->lay.off_w13, (int)H,
+                                          (int)(2 * I), E, h->lay.blob_bytes));
+            FT_CUDA(h, fp4_encode_weights(&h->tmPF_A2[b], h->d_layerbuf[b] + h->lay.off_w2, (int)I, (int)H,
+                                          E, h->lay.blob_bytes));
+        }
+        FT_CUDA(h, fp4_encode_pieces(&h->tmPF_B13, h->d_p_fxq, (int)H, prow, 16));
+        FT_CUDA(h, fp4_encode_pieces(&h->tmPF_B2, h->d_p_faq, (int)I, prow, 16));
+    }
     if (h->use_tc) {
         FT_CUDA(h, dm((void**)&h->d_p_xp, (size_t)h->p_rows * H * 2));
         for (int b = 0; b < 2; ++b) {
@@ -953,6 +997,38 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             tp.phases = 2;
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
         }
+    } else if (h->use_fp4_prefill) {
+        // MXFP4 activations once per token, gathered per routed row into 128-token tiles; one
+        // launch then runs W13 + SwiGLU (+ the SwiGLU activation's MXFP4 codes) and W2
+        const int bn = 128;
+        FT_CUDA(h, fp4_quant_tokens((const __nv_bfloat16*)x, T, H, h->d_p_tq, h->d_p_tsf, s));
+        FT_CUDA(h, fp4_gather_tiles(h->p_rb.counts, h->p_rb.entry_off, h->p_rb.pairs, k, H, bn, h->d_p_tq,
+                                    h->d_p_tsf, h->d_p_fxq, h->d_p_fxsf, h->d_p_fxrs, npairs, s));
+        Fp4Params f4{};
+        f4.counts = h->p_rb.counts;
+        f4.entry_off = h->p_rb.entry_off;
+        f4.entry_dst = h->p_rb.entry_dst;
+        f4.pairs = h->p_rb.pairs;
+        f4.pass = 0;
+        f4.hidden = H;
+        f4.inter = I;
+        f4.top_k = k;
+        f4.pieces = 1;
+        f4.x_ready = 1;
+        f4.arena = h->d_layerbuf[b];
+        f4.blob_bytes = h->lay.blob_bytes;
+        f4.off_s13 = h->lay.off_s13;
+        f4.off_s2 = h->lay.off_s2;
+        f4.off_ts = h->lay.off_ts;
+        f4.x = (const __nv_bfloat16*)x;
+        f4.xq = h->d_p_fxq; f4.xsf = h->d_p_fxsf; f4.xrs = h->d_p_fxrs;
+        f4.aq = h->d_p_faq; f4.asf = h->d_p_fasf;
+        f4.act = h->d_p_act;
+        f4.y = h->d_p_y;
+        f4.cnt_w13 = h->p_rb.dep;
+        f4.err = h->d_ffn_err;
+        const Fp4Maps maps{&h->tmPF_A13[b], &h->tmPF_B13, &h->tmPF_A2[b], &h->tmPF_B2};
+        FT_CUDA(h, fp4_launch(c.wfmt, bn, f4, maps, h->num_sms, s));
     } else {
         FfnParams fp{};
         fp.arena = h->d_layerbuf[b];

@@ -104,15 +104,24 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
     return r;
 }
 
+// Decode-sized tiles (N <= 64) are issued by two MMA warps, each taking two of a stage's four
+// K steps into its own accumulator (the epilogue adds them): a single thread issuing every
+// small-N tcgen05.mma cannot keep up with the weight stream.
+template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
+template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 32 : kThreads; }
+
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
+__global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
     TcParams p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
+    constexpr bool DUAL = TcDual<BN>::value;
+    constexpr int NI = DUAL ? 2 : 1;                  // MMA issuers
     constexpr int A_BYTES = kBM * kBK * 2;            // 16 KB
     constexpr int B_BYTES = BN * kBK * 2;
     constexpr int STAGE = A_BYTES + B_BYTES;
-    constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                   : (2 * BN <= 256) ? 256 : 512;
+    constexpr int COLS = 2 * NI * BN;                 // two tiles in flight x issuers
+    constexpr uint32_t TMEM_COLS = (COLS <= 32) ? 32 : (COLS <= 64) ? 64 : (COLS <= 128) ? 128
+                                   : (COLS <= 256) ? 256 : 512;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
@@ -156,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
         if (lane == 31) s_nt[n_entries] = incl;
     }
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NI); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -232,7 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
                     mbar_wait(&full[j % S], (j / S) & 1u, err, 5);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (DUAL && warp == 6)) {
+        const int par = warp == 6 ? 1 : 0;
+        constexpr int KK = 4 / NI;                    // K steps per stage for this issuer
         if (lane == 0) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
                 const uint32_t aph = (tcount >> 1) & 1u;
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, err, 2)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + (acc * NI + par) * BN;
                 for (int kb = 0; kb < k_steps; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1u;
@@ -257,9 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
                     const uint32_t sa = smem_u32(smem + s * STAGE);
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                    for (int k2 = 0; k2 < KK; ++k2) {
+                        const int kk = par * KK + k2;
                         mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
-                                 idesc, (kb | kk) ? 1u : 0u);
+                                 idesc, (kb | k2) ? 1u : 0u);
                     }
                     mma_commit(&empty[s]);
                 }
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
                 mma_commit(&tfull[acc]);
             }
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
@@ -282,13 +294,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ffn_kernel(
             const uint32_t aph = (tcount >> 1) & 1u;
             if (!mbar_wait(&tfull[acc], aph, err, 4)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * NI * BN;
             const int m = tl.mt * kBM + row_in_tile;
 #pragma unroll 1
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(tbase + c0, r);
-                tmem_wait_ld();
+                if (DUAL) {
+                    uint32_t r2[16];
+                    tmem_ld16(tbase + BN + c0, r2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                } else {
+                    tmem_wait_ld();
+                }
                 if (w13) {
                     // lanes 2i / 2i+1 hold the gate / up rows of output feature i
                     float own[16];
@@ -405,7 +425,7 @@ cudaError_t launch_bn(const TcParams& p0, const TcMaps& m, int grid, cudaStream_
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tc::tc_ffn_kernel<BN><<<grid, tc::kThreads, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
+    tc::tc_ffn_kernel<BN><<<grid, tc::tc_threads<BN>(), smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
     return cudaGetLastError();
 }
 

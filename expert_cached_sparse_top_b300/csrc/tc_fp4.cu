@@ -38,7 +38,13 @@ namespace fp4 {
 using namespace tc;
 
 constexpr int kStageK = 256;                 // K elements per stage: 128 bytes of E2M1
-constexpr int kFp4Threads = 224;             // producer, MMA issuer A, 4 epilogue warps, MMA issuer B
+// Tiles whose MMA has N <= 64 (decode) get two MMA-issuing warps (warps 1 and 6): a single
+// thread issuing every small-N tcgen05.mma / cp cannot keep up with the weight stream. Larger
+// tiles (prefill, N = 128) keep one issuer.
+template <int P, int BN> struct Fp4Cfg {
+    static constexpr int NI = P * BN <= 64 ? 2 : 1;
+    static constexpr int THREADS = NI == 2 ? 224 : 192;
+};
 constexpr int kABytes = 128 * 128;           // one 128-row weight tile of a stage
 
 __device__ __forceinline__ int exp_of(float v) {
@@ -77,7 +83,10 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
 // share one scale block; all 32 lanes of the warp must call this together. Piece pc's codes go
 // to codes0 + pc * piece_stride (4 bytes); the block's scale byte of piece pc is written by the
 // group's first lane into the tile's atom at N-operand row n0 + pc, block jb.
-template <int G>
+//
+// OCP = true is the single-piece MXFP4 activation quantisation of the FP4 prefill path:
+// scale exponent floor(log2(block max)) - 2 and codes saturating at +-6 (OCP Microscaling).
+template <int G, bool OCP = false>
 __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* codes0, int64_t piece_stride,
                                        uint8_t* sf_atom, int n0, int jb, bool store, bool lead) {
     for (int pc = 0; pc < P; ++pc) {
@@ -89,7 +98,10 @@ __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* c
         const int be = exp_of(bmax);
         int e;
         uint8_t sfb;
-        if (fmt == FT_W_MXFP4) {
+        if (OCP) {
+            e = be <= -1000 ? -126 : max(-126, min(126, be - 2));
+            sfb = (uint8_t)(e + 127);
+        } else if (fmt == FT_W_MXFP4) {
             e = be <= -1000 ? -126 : max(-126, min(126, be - 1));
             sfb = (uint8_t)(e + 127);
         } else {
@@ -102,9 +114,11 @@ __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* c
         for (int j = 0; j < 4; ++j) {
             const uint32_t byte = e2m1x2(v[2 * j] * inv, v[2 * j + 1] * inv);
             word |= byte << (8 * j);
-            const float2 q = e2m1x2_decode(byte);
-            v[2 * j] -= q.x * step;
-            v[2 * j + 1] -= q.y * step;
+            if (!OCP) {
+                const float2 q = e2m1x2_decode(byte);
+                v[2 * j] -= q.x * step;
+                v[2 * j + 1] -= q.y * step;
+            }
         }
         if (store) {
             *reinterpret_cast<uint32_t*>(codes0 + pc * piece_stride) = word;
@@ -244,13 +258,15 @@ __device__ __forceinline__ int entry_of_row(const int* s_eoff, int u_begin, int 
 }
 
 template <int BN, int FMT, int P>
-__global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
+__global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
     Fp4Params p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr int BS = FMT == FT_W_MXFP4 ? 32 : 16;
     constexpr int APS = kStageK / (BS * 4);           // scale atoms per operand per stage
     constexpr int SF_BYTES = APS * 512;
     constexpr uint32_t SF_COL0 = 256;                 // scale-factor columns: one buffer of 64 per issuer
+    constexpr int NI = Fp4Cfg<P, BN>::NI;             // MMA issuers
+    constexpr int NTH = Fp4Cfg<P, BN>::THREADS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages, STAGE = p.stage_bytes;
@@ -265,8 +281,8 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
     int* s_eoff = reinterpret_cast<int*>(s_tmem + 4);          // [kMaxExperts + 1]
     int* s_tp = s_eoff + (kMaxExperts + 1);                      // [kMaxExperts + 1]
     float* s_red = reinterpret_cast<float*>(s_tp + (kMaxExperts + 1));   // [8]
-    float* s_stage = s_red + 8;                                          // [32][65] SwiGLU values
-    int* s_got = reinterpret_cast<int*>(s_stage + 32 * 65);                // [2][4] epilogue votes
+    float* s_stage = s_red + 8;                                          // [BN][65] SwiGLU values
+    int* s_got = reinterpret_cast<int*>(s_stage + BN * 65);                // [2][4] epilogue votes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RouteCounts rc = *p.counts;
@@ -297,9 +313,9 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
         if (lane == 31) s_tp[u_end] = incl;
     }
     if (warp == 0 && lane == 0) {
-        // a stage is free, and an accumulator full, once both MMA issuers have committed
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 2); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 2); mbar_init(&tempty[a], 4); }
+        // a stage is free, and an accumulator full, once every MMA issuer has committed
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NI); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -316,7 +332,8 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
     int* err = p.err;
 
     // 1. W13 activation pieces: the launch's CTAs split the pass's token rows between them
-    {
+    // (unless the caller has already written them)
+    if (!p.x_ready) {
         const int r0 = s_eoff[u_begin], r1 = s_eoff[u_end];
         for (int r = r0 + blockIdx.x; r < r1; r += gridDim.x) {
             const int u = entry_of_row(s_eoff, u_begin, u_end, r);
@@ -325,10 +342,10 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
             const __nv_bfloat16* src = p.x + (int64_t)(p.pairs[r] / p.top_k) * H;
             split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
                           p.xsf + (int64_t)tile * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
-                          threadIdx.x, kFp4Threads, 2, s_red);
+                          threadIdx.x, NTH, 2, s_red);
             fence_proxy_async_global();
             __threadfence();
-            named_bar(2, kFp4Threads);
+            named_bar(2, NTH);
             if (threadIdx.x == 0) atomicAdd(p.cnt_x + u, 1);
         }
     }
@@ -354,8 +371,12 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                 const int nbox = (P * n_valid + 15) / 16;
                 const uint32_t stage_tx = (uint32_t)(kABytes + 2 * SF_BYTES + nbox * 2048);
                 // weights (and their scales) of the first stages go out before the activation
-                // pieces of this entry are known to be ready
-                const int npre = min(S, k_stages);
+                // pieces of this entry are known to be ready (if they are not ready yet)
+                const int* dep = tl.w13 ? p.cnt_x + tl.u : p.cnt_w13 + tl.u;
+                const int target = tl.w13 ? (p.x_ready ? 0 : s_eoff[tl.u + 1] - s_eoff[tl.u])
+                                          : m13 * (s_tp[tl.u + 1] - s_tp[tl.u]);
+                const bool ready_now = target == 0 || ld_acquire_s32(dep) >= target;
+                const int npre = ready_now ? 0 : min(S, k_stages);
                 const uint32_t it0 = it;
                 for (int kb = 0; kb < npre; ++kb, ++it) {
                     const int s = it % S;
@@ -366,8 +387,7 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                     bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
                 }
                 if (!ok) break;
-                const bool ready = tl.w13 ? wait_count(p.cnt_x + tl.u, s_eoff[tl.u + 1] - s_eoff[tl.u], err, 6)
-                                          : wait_count(p.cnt_w13 + tl.u, m13 * (s_tp[tl.u + 1] - s_tp[tl.u]), err, 7);
+                const bool ready = ready_now || wait_count(dep, target, err, tl.w13 ? 6 : 7);
                 fence_proxy_async_global();
                 // the armed stages expect their activation bytes: load them in any case so the
                 // ring drains if the wait ran out
@@ -396,13 +416,14 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                     mbar_wait(&full[j % S], (j / S) & 1u, err, 5);
             }
         }
-    } else if (warp == 1 || warp == 6) {
+    } else if (warp == 1 || (NI == 2 && warp == 6)) {
         // Two issuers: in every stage warp 1 issues K steps 0-1 and warp 6 K steps 2-3 (with the
         // scale atoms those steps read), each into its own accumulator; the epilogue adds the
         // two. One thread issuing every tcgen05.mma / cp of a decode tile (N = 16) cannot keep
         // up with the weight stream; two can.
         const uint32_t par = warp == 6 ? 1u : 0u;
-        constexpr int HA = APS / 2;                   // scale atoms per operand per issuer
+        constexpr int HA = APS / NI;                  // scale atoms per operand per issuer
+        constexpr int KK = 4 / NI;                    // K steps per stage per issuer
         if (lane == 0) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
@@ -414,7 +435,7 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                 const uint32_t acc = tcount & 1u;
                 if (!mbar_wait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, err, 2)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (acc * 2u + par) * (uint32_t)NC;
+                const uint32_t d_tmem = tmem_base + (acc * NI + par) * (uint32_t)NC;
                 for (int kb = 0; kb < k_stages; ++kb, ++it) {
                     const int s = it % S;
                     if (!mbar_wait(&full[s], (it / S) & 1u, err, 3)) { ok = false; break; }
@@ -431,12 +452,12 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                         tmem_cp_sf(tsf + (uint32_t)(4 * (HA + a)), smem_desc_sf(ssf + (APS + ga) * 512));
                     }
 #pragma unroll
-                    for (int k2 = 0; k2 < 2; ++k2) {
-                        const int kk = (int)par * 2 + k2;
+                    for (int k2 = 0; k2 < KK; ++k2) {
+                        const int kk = (int)par * KK + k2;
                         // MXFP4: one atom (4 blocks of 32) per two K steps, byte pair 0 or 2;
                         // NVFP4: one atom (4 blocks of 16) per K step
-                        const int ai = FMT == FT_W_MXFP4 ? 0 : k2;
-                        const uint32_t id = FMT == FT_W_MXFP4 ? (uint32_t)(k2 * 2) : 0u;
+                        const int ai = (FMT == FT_W_MXFP4 ? (kk >> 1) : kk) - (int)par * HA;
+                        const uint32_t id = FMT == FT_W_MXFP4 ? (uint32_t)((kk & 1) * 2) : 0u;
                         mma_bs<FMT>(d_tmem, smem_desc_sw128(sa + kk * 32),
                                     smem_desc_sw128(sa + kABytes + kk * 32), idesc_fp4<FMT>(n_mma, id),
                                     tsf + 4 * ai, tsf + 4 * (HA + ai), (kb == 0 && k2 == 0) ? 0u : 1u);
@@ -475,8 +496,8 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                     ts = reinterpret_cast<const float*>(p.arena + (int64_t)slot * p.blob_bytes + p.off_ts)[tl.w13 ? 0 : 1];
                 }
                 const float* rsp = p.xrs + (int64_t)tl.g * BN;     // W13 only: the x rows' prescale
-                // accumulator pair of this tile: issuer A at (2 acc) NC, issuer B at (2 acc + 1) NC
-                const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 2u * (uint32_t)NC;
+                // accumulators of this tile: issuer A at (NI acc) NC, issuer B at (NI acc + 1) NC
+                const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)(NI * NC);
                 const int m = tl.mt * 128 + row_in_tile;
                 // columns are token-major: token i's pieces are columns i * P .. i * P + P - 1,
                 // so a 16-column load holds 16 / P whole tokens
@@ -484,12 +505,17 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                 const int ncols = (P * n_valid + 15) & ~15;
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 16) {
-                    uint32_t r[16], r2[16];
+                    uint32_t r[16];
                     tmem_ld16(tbase + c0, r);
-                    tmem_ld16(tbase + NC + c0, r2);
-                    tmem_wait_ld();
+                    if (NI == 2) {
+                        uint32_t r2[16];
+                        tmem_ld16(tbase + NC + c0, r2);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                    } else {
+                        tmem_wait_ld();
+                    }
                     const int i0 = c0 / P;                     // first token of the chunk
                     float tok[tpc];
 #pragma unroll
@@ -538,7 +564,7 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
                         for (int j = 0; j < 8; ++j) v[j] = s_stage[i * 65 + f8 + j];
                         const int f0 = tl.mt * 64 + f8;             // first feature of the 8
                         const int jb = f0 / BS;                     // scale block along K = I
-                        split8<G>(v, P, FMT, p.aq + ((int64_t)tl.g * NC + i * P) * (I / 2) + f0 / 2, I / 2,
+                        split8<G, P == 1>(v, P, FMT, p.aq + ((int64_t)tl.g * NC + i * P) * (I / 2) + f0 / 2, I / 2,
                                   p.asf + ((int64_t)tl.g * ak2 + jb / 4) * 512, i * P, jb, i < n_valid,
                                   (f8 % BS) == 0);
                     }
@@ -562,6 +588,83 @@ __global__ void __launch_bounds__(kFp4Threads, 1) fp4_ffn_kernel(
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem_base) : "memory");
+    }
+}
+
+// Prefill activations, MXFP4 (single piece, OCP rule), token-major: codes [T][H/2], scale
+// bytes [T][H/32]. Thread = 8 consecutive elements, 4 lanes per 32-element block.
+__global__ void __launch_bounds__(128) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int H,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+    const int t = blockIdx.x;
+    const int c = blockIdx.y * 1024 + threadIdx.x * 8;       // H % 256 == 0: warp-uniform
+    if (c >= H) return;
+    const uint4 u4 = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * H + c));
+    const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
+    float v[8];
+    float bmax = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = __uint_as_float(w4[q] << 16);
+        v[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+        bmax = fmaxf(bmax, fmaxf(fabsf(v[2 * q]), fabsf(v[2 * q + 1])));
+    }
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
+    const int be = exp_of(bmax);
+    const int e = be <= -1000 ? -126 : max(-126, min(126, be - 2));
+    const float inv = pow2(-e);
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) word |= e2m1x2(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * j);
+    *reinterpret_cast<uint32_t*>(codes + (int64_t)t * (H / 2) + c / 2) = word;
+    if ((threadIdx.x & 3) == 0) sf[(int64_t)t * (H / 32) + c / 32] = (uint8_t)(e + 127);
+}
+
+// Routed rows -> the W13 N operand of the single-piece MMA: row r (entry u, position i) takes
+// token pairs[r] / top_k's codes into tile tp[u] + i / bn, row i % bn, and scatters its scale
+// bytes into that tile's atoms; its row scale is 1. One warp per row.
+__global__ void __launch_bounds__(256) gather_tiles_kernel(const RouteCounts* __restrict__ counts,
+                                                           const int32_t* __restrict__ entry_off,
+                                                           const int32_t* __restrict__ pairs, int top_k, int H,
+                                                           int bn, const uint8_t* __restrict__ tcodes,
+                                                           const uint8_t* __restrict__ tsf, uint8_t* __restrict__ xq,
+                                                           uint8_t* __restrict__ xsf, float* __restrict__ xrs) {
+    __shared__ int s_eoff[kMaxExperts + 1];
+    __shared__ int s_tp[kMaxExperts + 1];
+    const int U = counts->n_unique;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= U; i += blockDim.x) s_eoff[i] = entry_off[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < U; i += blockDim.x) s_tp[i] = (s_eoff[i + 1] - s_eoff[i] + bn - 1) / bn;
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (U + 31) / 32;
+        const int i0 = lane * per, i1 = min(U, i0 + per);
+        int local = 0;
+        for (int i = i0; i < i1; ++i) local += s_tp[i];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int i = i0; i < i1; ++i) { const int t = s_tp[i]; s_tp[i] = run; run += t; }
+    }
+    __syncthreads();
+    const int rows = s_eoff[U];
+    const int nblk = H / 32, atoms = nblk / 4;
+    for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
+        const int u = entry_of_row(s_eoff, 0, U, r);
+        const int i = r - s_eoff[u];
+        const int tile = s_tp[u] + i / bn, rin = i % bn;
+        const int64_t tok = pairs[r] / top_k;
+        const uint4* src = reinterpret_cast<const uint4*>(tcodes + tok * (H / 2));
+        uint4* dst = reinterpret_cast<uint4*>(xq + ((int64_t)tile * bn + rin) * (H / 2));
+        for (int c = lane; c < H / 32; c += 32) dst[c] = __ldg(src + c);
+        uint8_t* atom0 = xsf + (int64_t)tile * atoms * 512 + (rin & 31) * 16 + (rin >> 5) * 4;
+        for (int j = lane; j < nblk; j += 32) atom0[(j >> 2) * 512 + (j & 3)] = __ldg(tsf + tok * nblk + j);
+        if (lane == 0) xrs[(int64_t)tile * bn + rin] = 1.f;
     }
 }
 
@@ -592,16 +695,16 @@ EncodeTiledFn encode_fn() {
 constexpr int kSmemLimit = 227 * 1024;
 
 int stage_bytes_for(int fmt, int bn, int pieces) {
+    // weights tile + P * bn activation rows + weight and activation scale atoms
     const int aps = fmt == FT_W_MXFP4 ? 2 : 4;
     return fp4::kABytes + pieces * bn * 128 + 2 * aps * 512;
 }
 
-template <int BN, int FMT>
+template <int BN, int FMT, int P>
 cudaError_t launch_t(const Fp4Params& p0, const Fp4Maps& m, int grid, cudaStream_t s) {
-    constexpr int P = kFp4MaxPieces;
     Fp4Params p = p0;
     p.stage_bytes = stage_bytes_for(FMT, BN, p.pieces);
-    const size_t fixed = 1024 + 4 * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + 32 * 65 * 4 + 32 + 64;
+    const size_t fixed = 1024 + 4 * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + BN * 65 * 4 + 32 + 64;
     p.stages = (int)((kSmemLimit - fixed) / (p.stage_bytes + 16));
     if (p.stages > 8) p.stages = 8;
     if (p.stages < 2) return cudaErrorInvalidValue;
@@ -614,7 +717,7 @@ cudaError_t launch_t(const Fp4Params& p0, const Fp4Maps& m, int grid, cudaStream
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    fp4::fp4_ffn_kernel<BN, FMT, P><<<grid, fp4::kFp4Threads, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
+    fp4::fp4_ffn_kernel<BN, FMT, P><<<grid, fp4::Fp4Cfg<P, BN>::THREADS, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
     return cudaGetLastError();
 }
 
@@ -657,20 +760,34 @@ cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int
 }
 
 cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, int grid, cudaStream_t s) {
-    // the kernel is built for kFp4MaxPieces pieces (a divisor of 16: one 16-column accumulator
-    // load holds whole tokens), P * bn <= 128 rows of scale atoms
-    if (p.pieces != kFp4MaxPieces || p.pieces * bn > 128 || p.top_k < 1) return cudaErrorInvalidValue;
-    if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK) return cudaErrorInvalidValue;
-#define FT_FP4_CASE(BNV)                                                                   \
-    case BNV:                                                                              \
-        return fmt == FT_W_MXFP4 ? launch_t<BNV, FT_W_MXFP4>(p, m, grid, s)                \
-                                 : launch_t<BNV, FT_W_NVFP4>(p, m, grid, s);
-    switch (bn) {
-        FT_FP4_CASE(16)
-        FT_FP4_CASE(32)
-        default: return cudaErrorInvalidValue;
-    }
-#undef FT_FP4_CASE
+    if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1) return cudaErrorInvalidValue;
+    if (fmt != FT_W_MXFP4 && fmt != FT_W_NVFP4) return cudaErrorInvalidValue;
+    const bool mx = fmt == FT_W_MXFP4;
+    // decode: four pieces, 16- or 32-token tiles; prefill: one MXFP4 piece, 128-token tiles
+    if (p.pieces == kFp4MaxPieces && bn == 16)
+        return mx ? launch_t<16, FT_W_MXFP4, 4>(p, m, grid, s) : launch_t<16, FT_W_NVFP4, 4>(p, m, grid, s);
+    if (p.pieces == kFp4MaxPieces && bn == 32)
+        return mx ? launch_t<32, FT_W_MXFP4, 4>(p, m, grid, s) : launch_t<32, FT_W_NVFP4, 4>(p, m, grid, s);
+    if (p.pieces == 1 && bn == 128 && mx && p.x_ready) return launch_t<128, FT_W_MXFP4, 1>(p, m, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t fp4_quant_tokens(const __nv_bfloat16* x, int T, int H, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    if (H % fp4::kStageK) return cudaErrorInvalidValue;
+    fp4::quant_tokens_kernel<<<dim3(T, (H + 1023) / 1024), 128, 0, s>>>(x, H, codes, sf);
+    return cudaGetLastError();
+}
+
+cudaError_t fp4_gather_tiles(const RouteCounts* counts, const int32_t* entry_off, const int32_t* pairs,
+                             int top_k, int H, int bn, const uint8_t* tcodes, const uint8_t* tsf,
+                             uint8_t* xq, uint8_t* xsf, float* xrs, int rows_max, cudaStream_t s) {
+    if (rows_max <= 0) return cudaSuccess;
+    int blocks = (rows_max + 7) / 8;
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    fp4::gather_tiles_kernel<<<blocks, 256, 0, s>>>(counts, entry_off, pairs, top_k, H, bn, tcodes, tsf, xq,
+                                                   xsf, xrs);
+    return cudaGetLastError();
 }
 
 }  // namespace ftmoe

@@ -21,7 +21,9 @@ Pins (tests/test_oracle_moe.py): top-k against brute force over all C(E,k) subse
 inputs and crafted ties; gate weights against the closed forms (k=1 gives 1, equal logits
 give 1/k) and the sum-to-one invariant; the FFN at E=1, k=1 against
 torch.nn.functional.silu-based SwiGLU in fp64 (library routine); k=E with all experts
-equal to the dense weighted sum; a hand-worked 3-expert example (tests/golden/).
+equal to the dense weighted sum; a hand-worked 3-expert example (tests/golden/); the
+MXFP4 act-quant step (FP4 prefill reading) against hand-worked blocks, a brute-force nearest-
+even search on random blocks and its fixed points; bf16 rounding against torch's bfloat16.
 """
 import numpy as np
 
@@ -72,6 +74,51 @@ def expert_ffn(w1, w3, w2, x):
     return a @ w2.T, a
 
 
+def bf16_round(v):
+    """Round to the nearest bf16 value (ties to even), returned in fp64."""
+    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def mx_act_quant(v, block=32):
+    """MXFP4 quantisation of activations along the last axis (the act-quant step of the FP4
+    prefill reading): per block of 32 consecutive values, shared scale 2^s with
+    s = floor(log2(max |v|)) - 2 (E2M1's largest exponent), each value divided by 2^s and
+    rounded to the nearest E2M1 magnitude {0, 0.5, 1, 1.5, 2, 3, 4, 6} with ties to the even
+    code, saturating at 6 (OCP Microscaling v1.0, conversion to MX). An all-zero block stays
+    zero. Returns the dequantised values (fp64)."""
+    v = np.asarray(v, dtype=np.float64)
+    shp = v.shape
+    b = v.reshape(-1, block)
+    amax = np.abs(b).max(axis=1, keepdims=True)
+    with np.errstate(divide="ignore"):
+        s = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0.0)
+    scale = 2.0 ** s
+    m = np.abs(b) / scale
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    # nearest grid point; on a tie take the even code (codes 0, 2, 4, 6: 0, 1, 2, 4)
+    d = np.abs(m[..., None] - grid)
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    even = (np.arange(8) % 2) == 0
+    pick = np.where((cand & even).any(axis=-1), np.argmax(cand & even, axis=-1), np.argmax(cand, axis=-1))
+    q = grid[pick] * np.sign(b) * scale
+    return q.reshape(shp)
+
+
+def expert_ffn_w4a4(w1, w3, w2, x):
+    """Step 4 for the FP4 prefill reading (weights FP4, activations MXFP4): x is
+    act-quantised, the SwiGLU activation is rounded to bf16 (the precision the kernel keeps
+    it in) and act-quantised, then y = W2 a_q. Returns y [n][H]."""
+    xq = mx_act_quant(np.asarray(x, dtype=np.float64))
+    g = xq @ w1.T
+    u = xq @ w3.T
+    a = mx_act_quant(bf16_round(silu(g) * u))
+    return a @ w2.T
+
+
 def combine(w, y):
     """Step 5. w [T][k], y [T][k][H] -> out [T][H], summed over j in ascending order."""
     T, k = w.shape
@@ -81,8 +128,9 @@ def combine(w, y):
     return out
 
 
-def layer_forward(x_f64, idx, w, expert_weights):
-    """Steps 4-5 for given routing. expert_weights(e) -> (w1, w3, w2) fp64.
+def layer_forward(x_f64, idx, w, expert_weights, ffn=None):
+    """Steps 4-5 for given routing. expert_weights(e) -> (w1, w3, w2) fp64; ffn (default
+    expert_ffn) maps (w1, w3, w2, x) to y or (y, a).
 
     Returns out [T][H] and y [T][k][H]. Each (token, rank) pair goes through its expert's
     FFN; where the expert's bytes came from (cache slot, staging, host) does not enter.
@@ -94,7 +142,10 @@ def layer_forward(x_f64, idx, w, expert_weights):
     for e in np.unique(idx):
         rows, cols = np.nonzero(idx == e)
         w1, w3, w2 = expert_weights(int(e))
-        ye, _ = expert_ffn(w1, w3, w2, x[rows])
+        if ffn is None:
+            ye, _ = expert_ffn(w1, w3, w2, x[rows])
+        else:
+            ye = ffn(w1, w3, w2, x[rows])
         y[rows, cols, :] = ye
     return combine(w, y), y
 

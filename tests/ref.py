@@ -30,8 +30,9 @@ class OracleExperts:
         return w
 
 
-def oracle_call(experts, layer, x_bits, logits, k, tokens=None):
-    """Expected (out, idx, w) for one forward call; ``tokens`` restricts to a sample."""
+def oracle_call(experts, layer, x_bits, logits, k, tokens=None, ffn=None):
+    """Expected (out, idx, w) for one forward call; ``tokens`` restricts to a sample; ``ffn``
+    replaces the plain expert FFN (e.g. moe.expert_ffn_w4a4 for the FP4 prefill reading)."""
     E = experts.cfg.experts
     x = formats.bf16_to_f64(x_bits)
     l = np.asarray(logits, dtype=np.float64)
@@ -39,7 +40,7 @@ def oracle_call(experts, layer, x_bits, logits, k, tokens=None):
         x, l = x[tokens], l[tokens]
     idx = moe.topk(l, k)
     w = moe.gate_weights(l, idx)
-    out, _ = moe.layer_forward(x, idx, w, lambda e: experts(layer * E + e))
+    out, _ = moe.layer_forward(x, idx, w, lambda e: experts(layer * E + e), ffn=ffn)
     return out, idx, w
 
 

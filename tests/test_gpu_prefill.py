@@ -80,8 +80,14 @@ def test_prefill_ragged_token_counts(ft):
     cache.close()
 
 
-def test_prefill_mxfp4_shape(ft):
-    """284B-shaped layer (256 experts, top-6, MXFP4) on the CUDA-core FFN path."""
+@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+def test_prefill_mxfp4_shape(ft, path, monkeypatch):
+    """284B-shaped layer (256 experts, top-6, MXFP4). tcgen05: block-scaled MMA with MXFP4
+    activations, against the oracle with its act-quant step (the FP4 prefill reading); simt:
+    CUDA-core FFN with bf16 activations, against the plain oracle."""
+    from oracle import moe
+    if path == "simt":
+        monkeypatch.setenv("FTMOE_FFN", "simt")
     cfg = W.config("prefill_mxfp4", layers=2)
     pool = HostPool(cfg, images=13)
     T = 512
@@ -90,9 +96,19 @@ def test_prefill_mxfp4_shape(ft):
     for layer in (0, 1):
         x, logits = W.prefill_inputs(cfg, layer, tokens=T)
         out = _run(cache, cfg, layer, x, logits)
+        got = bf16_dev_to_f64(out)
         sample = np.arange(0, T, 5)
-        ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample)
-        assert normwise_err(bf16_dev_to_f64(out)[sample], ref) <= TOL["mxfp4"], layer
+        if path == "tcgen05":
+            ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample,
+                                    ffn=moe.expert_ffn_w4a4)
+            plain, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample)
+            err = normwise_err(got[sample], ref)
+            print("layer %d: vs act-quant oracle %.3e, vs plain oracle %.3e (information)"
+                  % (layer, err, normwise_err(got[sample], plain)))
+            assert err <= TOL["mxfp4"], (layer, err)
+        else:
+            ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample)
+            assert normwise_err(got[sample], ref) <= TOL["mxfp4"], layer
     cache.close()
 
 
