@@ -234,7 +234,7 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
     metric, images, _, _ = DECODE[args.workload]
-    cfg = W.config(args.workload)
+    cfg = W.config(args.workload, **({"layers": args.layers} if args.layers else {}))
     C = W.cache_capacity(cfg)
     pool = HostPool(cfg, images=images)
     K, Wm = args.steps, args.warmup
@@ -425,7 +425,7 @@ def run_prefill(args):
     from expert_cached_sparse_top_b300 import build as b
     b.build()
     from expert_cached_sparse_top_b300 import ftmoe
-    cfg = W.config(args.workload)
+    cfg = W.config(args.workload, **({"layers": args.layers} if args.layers else {}))
     torch.cuda.set_device(0)
     fp4 = cfg.wfmt != "bf16"
     # the 256-expert MXFP4 layer aliases 16 physical blobs (keys and PCIe bytes unchanged)
@@ -524,6 +524,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="fewer MoE layers than the workload defines (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4"])
     args = ap.parse_args()
