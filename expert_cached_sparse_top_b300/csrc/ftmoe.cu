@@ -762,7 +762,6 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     ++launches;
     h->cur ^= 1;
     FT_CUDA(h, cudaEventRecord(h->ev_route, s));
-    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
 
     FfnParams fp{};
     fp.arena = h->d_arena;
@@ -843,6 +842,8 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         launches += 2;
         return tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
     };
+    // the FFN window opens here: routing, the row gather (BF16) and parameter set-up before
+    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
     FT_CUDA(h, run_ffn(0));
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[2], s));
 

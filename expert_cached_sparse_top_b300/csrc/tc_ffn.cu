@@ -62,10 +62,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 // Bounded wait until every W13 tile of an entry has published its activation rows.
 __device__ __forceinline__ bool wait_dep(const int* dep, int target, int* err) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    // back off to ~1 us between polls: many CTAs poll a few counters
+    uint32_t ns = 64;
+    for (uint32_t i = 0; i < (kWaitLimit >> 4); ++i) {
         if (ld_acquire(dep) >= target) return true;
-        if ((i & 255u) == 255u && *(volatile int*)err) return false;
-        __nanosleep(64);
+        if ((i & 63u) == 63u && *(volatile int*)err) return false;
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
     }
     atomicCAS(err, 0, 6);
     return false;
@@ -195,7 +198,11 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
                 const int slot = p.entry_dst[tl.u];
                 const int row_b = p.entry_off[tl.u] + tl.nt * BN;
                 int kb0 = 0;
-                if (!w13 && fused) {
+                const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
+                if (!w13 && fused && ld_acquire(p.dep + tl.u) >= target) {
+                    // the entry's activation rows are already published: stream A and B together
+                    fence_proxy_async_global();
+                } else if (!w13 && fused) {
                     // stream this tile's first weight stages while the entry's W13 tiles finish
                     const int npre = min(S, k_steps);
                     const uint32_t it0 = it;
@@ -206,7 +213,6 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
                         tma_load_3d(smem + s * STAGE, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
                     }
                     if (!ok) break;
-                    const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
                     if (!wait_dep(p.dep + tl.u, target, err)) {
                         // the stages armed above still expect their activation bytes: load
                         // them (rows already written or not) so the ring can drain

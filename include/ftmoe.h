@@ -115,8 +115,9 @@ typedef struct {
 /* Accumulated device time per stage, in milliseconds, measured with CUDA events on the
  * stream each stage runs on (ft_moe_set_timing(h, 1) enables recording). */
 typedef struct {
-    double route_ms;      /* router logits (if computed) + top-k + cache lookup/permute */
-    double ffn_hit_ms;    /* expert FFN over entries resident at call start */
+    double route_ms;      /* router logits (if computed) + top-k + cache lookup/permute
+                             (+ the BF16 path's activation-row gather) */
+    double ffn_hit_ms;    /* expert FFN kernel over entries resident at call start */
     double fill_ms;       /* H2D miss copies on the copy stream */
     double ffn_miss_ms;   /* expert FFN over filled / staged entries */
     double combine_ms;    /* gate-weighted combine */
