@@ -104,6 +104,23 @@ DECODE = {
 }
 
 
+def host_copy_gbs(nbytes=1 << 30, reps=5):
+    """Host memory bandwidth B_H: a multi-threaded memcpy of 1 GiB between two ordinary
+    (pageable) host buffers; read + write bytes per second, best of `reps`."""
+    import torch
+    a = torch.empty(nbytes, dtype=torch.uint8)
+    b = torch.empty(nbytes, dtype=torch.uint8)
+    a.fill_(1)
+    b.copy_(a)
+    best = 0.0
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        b.copy_(a)
+        dt = time.perf_counter() - t0
+        best = max(best, 2 * nbytes / dt / 1e9)
+    return best, torch.get_num_threads()
+
+
 def resize_plan(cfg, Wm, K):
     """Elastic workload: the cache budget changes twice inside the timed range, at 1/3 and
     2/3 of it (the trace's own split points scaled to the run). Resizes are safe points
@@ -369,6 +386,12 @@ def run_ours(args):
     hits = s1["hits"] - s0["hits"]
     fill_b = (s1["fill_bytes"] - s0["fill_bytes"]) + (s1["stage_bytes"] - s0["stage_bytes"])
     base = oracle_baseline(cfg, pool, budget_s=args.cpu_budget)
+    # q* of the pages' bandwidth-adaptive policy: of a step's m misses, about m * B_P / B_H
+    # would be filled over PCIe and the rest computed in place on the CPU ([MTP] q* policy).
+    # CPU execution is not built; the split is reported from the bandwidths measured here.
+    b_h, h_threads = host_copy_gbs()
+    b_p = (fill_b / (tim["fill_ms"] * 1e-3) / 1e9) if tim["fill_ms"] > 0 else None
+    m_step = misses / K
     kern = ("expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
             if cfg.wfmt == "bf16" else
             "expert FFN (block-scaled tcgen05 grouped GEMM on %s codes: W13+SwiGLU, activation "
@@ -396,7 +419,12 @@ def run_ours(args):
         "clocks": clocks,
         "extras": {
             "miss_rate": misses / max(hits + misses, 1),
-            "pcie_fill_GBps": (fill_b / (tim["fill_ms"] * 1e-3) / 1e9) if tim["fill_ms"] > 0 else None,
+            "pcie_fill_GBps": b_p,
+            "q_star": {"B_P_GBps": b_p, "B_H_GBps": b_h, "host_threads": h_threads,
+                       "misses_per_step": m_step,
+                       "q_star_per_step": (m_step * b_p / b_h) if (b_p and b_h) else None,
+                       "note": "experts per step the pages' policy would fill (m * B_P / B_H); "
+                               "the rest would run on the host CPU, which is not built"},
             "fill_ms_per_step": tim["fill_ms"] / K,
             "wall_ms_per_step": 1e3 * t_wall / K,
             "all_resident_slots": len(touched),
@@ -411,6 +439,83 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_policy_compare(args):
+    """Cache policies on the same decode trace, through the engine: the engine's global LRU
+    against the pages' comparators ([MTP] §The gap it targets, §Results): a per-layer LRU,
+    a static hot subset (KTransformers-style: the C keys selected most often over a
+    calibration window, pinned at load) and static layer placement (llama.cpp-style: every
+    expert of the first C // E layers resident). Miss rates, PCIe bytes and tokens/s over the
+    same measured steps; each policy runs its own warm-up on the calibration steps."""
+    import torch
+    import workloads as W
+    from workloads.host import HostPool
+    from expert_cached_sparse_top_b300 import build as b
+    b.build()
+    from expert_cached_sparse_top_b300 import ftmoe
+    torch.cuda.set_device(0)
+    layers = args.layers or 40
+    cfg = W.config("decode_bf16", layers=layers)          # the 35B-A3B layer shape, 40 layers
+    C = W.cache_capacity(cfg)                              # 37 % of the pool
+    pool = HostPool(cfg, images=16)
+    calib, K = 64, args.steps
+    trace = list(W.decode_trace(cfg, steps=calib + K))
+    dev = torch.device("cuda", 0)
+    calls = [[(d["layer"], d["T"], torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(dev),
+               torch.from_numpy(d["logits"]).to(dev)) for d in st] for st in trace]
+    out = torch.empty((cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    count = np.zeros(cfg.keys, dtype=np.int64)
+    for st in trace[:calib]:
+        for d in st:
+            for e in np.unique(d["picks"]):
+                count[d["layer"] * cfg.experts + int(e)] += 1
+    hot = [int(k) for k in np.lexsort((np.arange(cfg.keys), -count))[:C]]
+    whole = [l * cfg.experts + e for l in range(C // cfg.experts) for e in range(cfg.experts)]
+    plans = [("global_lru", ftmoe.POLICY_GLOBAL_LRU, None), ("layer_lru", ftmoe.POLICY_LAYER_LRU, None),
+             ("static_hot_set", ftmoe.POLICY_STATIC, hot), ("static_layers", ftmoe.POLICY_STATIC, whole)]
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for name, policy, pin in plans:
+        c = ftmoe.make_config(cfg.layers, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, cfg.t_max,
+                              cfg.wfmt, C, policy=policy)
+        cache = ftmoe.MoECache(c, pool.ptrs, None)
+        if pin is not None:
+            cache.pin(pin)
+        else:
+            for st in calls[:calib]:                       # the LRU policies warm up on the
+                for (layer, T, x, lg) in st:               # calibration steps
+                    cache.forward(layer, x, T, out, logits=lg, stream=stream)
+        torch.cuda.synchronize()
+        s0 = cache.stats()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for st in calls[calib:]:
+            for (layer, T, x, lg) in st:
+                cache.forward(layer, x, T, out, logits=lg, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        s1 = cache.stats()
+        cache.close()
+        hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+        pcie = (s1["fill_bytes"] - s0["fill_bytes"]) + (s1["stage_bytes"] - s0["stage_bytes"])
+        tokens = sum(st[0]["T"] for st in trace[calib:])
+        res[name] = {"miss_rate": misses / max(hits + misses, 1), "pcie_GB_per_step": pcie / K / 1e9,
+                     "tokens_per_s": tokens / (e0.elapsed_time(e1) * 1e-3),
+                     "resident_keys": int(s1["resident"])}
+    line = {
+        "metric": "decode tokens/s by cache policy (%d-layer 35B-A3B-shaped BF16 trace, cache 37%% of pool)"
+                  % layers,
+        "value": res["global_lru"]["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": calib, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "policy_compare", "layers": layers, "experts": cfg.experts,
+                   "hidden": cfg.hidden, "inter": cfg.inter, "top_k": cfg.top_k, "cache_slots": C,
+                   "tokens_per_step": "1..16 (seeded mix)", "calibration_steps": calib,
+                   "pool": "pinned host, %d keys on %d blobs" % (cfg.keys, pool.images)},
+        "extras": {"policies": res},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_prefill(args):
@@ -527,7 +632,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer MoE layers than the workload defines (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4"])
+                    choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare"])
     args = ap.parse_args()
     dflt = DECODE.get(args.workload, (None, None, 8, 3))
     if args.steps is None:
@@ -536,7 +641,9 @@ def main():
         args.warmup = dflt[3]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.workload not in DECODE:
+    if args.workload == "policy_compare":
+        run_policy_compare(args)
+    elif args.workload not in DECODE:
         run_prefill(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -50,7 +50,9 @@ struct LookupParams {
     int32_t n_pairs;       // T*k
     int32_t layer;
     int32_t experts;
-    int64_t capacity;      // C
+    int64_t capacity;      // C: slots are < C, staging slots start at C
+    int64_t list_len;      // entries of order_in / order_out (the slots this call may use)
+    int32_t no_insert;     // nonzero: every miss is bypassed (static resident set)
     int32_t* table;        // [L*E] slot or -1
     int32_t* slot_key;     // [C] key or -1
     const int32_t* order_in;   // [C] slots, least recent first

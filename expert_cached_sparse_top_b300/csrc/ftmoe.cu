@@ -62,6 +62,9 @@ struct ft_moe {
     int32_t* d_slot_key = nullptr;        // [C]
     int32_t* d_order[2] = {nullptr, nullptr};
     int cur = 0;
+    int policy = FT_POLICY_GLOBAL_LRU;
+    std::vector<int64_t> lbase, llen;     // FT_POLICY_LAYER_LRU: each layer's slots and list
+    std::vector<int> lcur;                // and its ping-pong side
 
     float* d_logits = nullptr;            // [max_tokens][E]
     int32_t* d_idx = nullptr;             // [max_pairs]
@@ -176,7 +179,7 @@ bool valid_config(const ft_moe_config* c, std::string* why) {
     if (!ffn_supported(c->wfmt, c->hidden, c->inter)) { *why = "hidden/inter must be positive multiples of 64"; return false; }
     if (c->cache_slots < 0 || c->cache_slots > (int64_t)c->layers * c->experts * 4 + 1024) { *why = "cache_slots out of range"; return false; }
     if ((int64_t)c->layers * c->experts >= (1LL << 31)) { *why = "too many keys"; return false; }
-    if (c->flags != 0) { *why = "flags must be 0"; return false; }
+    if (c->flags < FT_POLICY_GLOBAL_LRU || c->flags > FT_POLICY_STATIC) { *why = "unknown cache policy (flags)"; return false; }
     if (c->max_prefill_tokens < 0 || (int64_t)c->max_prefill_tokens * c->top_k >= (1LL << 30)) { *why = "max_prefill_tokens out of range"; return false; }
     return true;
 }
@@ -210,8 +213,54 @@ BlobLayout ftmoe::make_layout(int fmt, int64_t H, int64_t I) {
 namespace {
 
 int64_t stage_slots_for(const ft_moe* h, int64_t C) {
+    // the comparator policies can bypass every miss of a call (a layer's share or a fixed
+    // set may hold none of them)
+    if (h->policy != FT_POLICY_GLOBAL_LRU) return h->max_u;
     int64_t need = (int64_t)h->max_u - C;
     return need > 0 ? need : 0;
+}
+
+// The LRU list(s) as one host array of C slots: the whole cache, or each layer's segment
+// taken from that layer's current ping-pong side.
+cudaError_t read_order(ft_moe* h, std::vector<int32_t>* order) {
+    order->assign((size_t)h->C, 0);
+    if (h->C == 0) return cudaSuccess;
+    if (h->policy != FT_POLICY_LAYER_LRU)
+        return cudaMemcpy(order->data(), h->d_order[h->cur], (size_t)h->C * 4, cudaMemcpyDeviceToHost);
+    for (size_t l = 0; l < h->lbase.size(); ++l) {
+        if (h->llen[l] == 0) continue;
+        cudaError_t e = cudaMemcpy(order->data() + h->lbase[l], h->d_order[h->lcur[l]] + h->lbase[l],
+                                   (size_t)h->llen[l] * 4, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t write_order(ft_moe* h, const std::vector<int32_t>& order) {
+    if (h->C == 0) return cudaSuccess;
+    if (h->policy != FT_POLICY_LAYER_LRU)
+        return cudaMemcpy(h->d_order[h->cur], order.data(), (size_t)h->C * 4, cudaMemcpyHostToDevice);
+    for (size_t l = 0; l < h->lbase.size(); ++l) {
+        if (h->llen[l] == 0) continue;
+        cudaError_t e = cudaMemcpy(h->d_order[h->lcur[l]] + h->lbase[l], order.data() + h->lbase[l],
+                                   (size_t)h->llen[l] * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+void layer_partition(ft_moe* h) {
+    const int L = h->cfg.layers;
+    h->lbase.assign((size_t)L, 0);
+    h->llen.assign((size_t)L, 0);
+    h->lcur.assign((size_t)L, 0);
+    int64_t b = 0;
+    for (int l = 0; l < L; ++l) {
+        const int64_t n = h->C / L + (l < h->C % L ? 1 : 0);
+        h->lbase[(size_t)l] = b;
+        h->llen[(size_t)l] = n;
+        b += n;
+    }
 }
 
 // Pin the distinct page ranges covering every blob (merged), skipping memory that is
@@ -316,6 +365,7 @@ ft_status init_lru_state(ft_moe* h) {
         FT_CUDA(h, cudaMemcpy(h->d_order[0], ord.data(), ord.size() * 4, cudaMemcpyHostToDevice));
     }
     h->cur = 0;
+    for (auto& c : h->lcur) c = 0;
     return FT_OK;
 }
 
@@ -587,6 +637,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     const int fault_alloc = h->fault_alloc;
     h->fault_alloc = 0;   // the injected fault targets resize only
     h->C = cfg->cache_slots;
+    h->policy = cfg->flags;
+    layer_partition(h);
     st = alloc_state(h, h->C, &h->d_arena, &h->d_slot_key, &h->d_order[0], &h->d_order[1], &h->n_stage);
     h->fault_alloc = fault_alloc;
     if (st != FT_OK) return bail(st);
@@ -753,14 +805,25 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     lp.capacity = h->C;
     lp.table = h->d_table;
     lp.slot_key = h->d_slot_key;
-    lp.order_in = h->d_order[h->cur];
-    lp.order_out = h->d_order[h->cur ^ 1];
+    lp.list_len = h->C;
+    lp.no_insert = h->policy == FT_POLICY_STATIC;
+    int* curp = &h->cur;
+    if (h->policy == FT_POLICY_LAYER_LRU) {
+        // this layer's share of the slots: its own list segment, its own ping-pong side
+        curp = &h->lcur[(size_t)layer];
+        lp.list_len = h->llen[(size_t)layer];
+        lp.order_in = h->d_order[*curp] + h->lbase[(size_t)layer];
+        lp.order_out = h->d_order[*curp ^ 1] + h->lbase[(size_t)layer];
+    } else {
+        lp.order_in = h->d_order[h->cur];
+        lp.order_out = h->d_order[h->cur ^ 1];
+    }
     lp.nan_flag = h->d_nan;
     lp.rb = h->rb;
     lp.hv = h->hv_dev;
     FT_CUDA(h, launch_lookup(lp, s));
     ++launches;
-    h->cur ^= 1;
+    *curp ^= 1;
     FT_CUDA(h, cudaEventRecord(h->ev_route, s));
 
     FfnParams fp{};
@@ -1064,6 +1127,8 @@ ft_status ft_cache_resize(ft_moe* h, int64_t new_slots) {
     if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
     if (new_slots < 0 || new_slots > (int64_t)h->cfg.layers * h->cfg.experts * 4 + 1024)
         return fail(h, FT_ERR_INVALID, "new_slots out of range");
+    if (h->policy != FT_POLICY_GLOBAL_LRU)
+        return fail(h, FT_ERR_INVALID, "resize supports the global LRU policy only");
     ft_status s = sync_handle(h);
     if (s != FT_OK) return s;
     const int64_t C = h->C, C2 = new_slots;
@@ -1155,9 +1220,10 @@ ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys) 
     const size_t nkeys = (size_t)h->cfg.layers * h->cfg.experts;
     if (slot_of_key) FT_CUDA(h, cudaMemcpy(slot_of_key, h->d_table, nkeys * 4, cudaMemcpyDeviceToHost));
     if (lru_keys && h->C > 0) {
-        std::vector<int32_t> order((size_t)h->C), sk((size_t)h->C);
-        FT_CUDA(h, cudaMemcpy(order.data(), h->d_order[h->cur], (size_t)h->C * 4, cudaMemcpyDeviceToHost));
+        std::vector<int32_t> sk((size_t)h->C);
         FT_CUDA(h, cudaMemcpy(sk.data(), h->d_slot_key, (size_t)h->C * 4, cudaMemcpyDeviceToHost));
+        std::vector<int32_t> order;
+        FT_CUDA(h, read_order(h, &order));
         int64_t n = 0;
         for (int64_t i = 0; i < h->C; ++i) {
             int32_t key = sk[(size_t)order[(size_t)i]];
@@ -1165,6 +1231,52 @@ ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys) 
         }
         for (; n < h->C; ++n) lru_keys[n] = -1;
     }
+    return FT_OK;
+}
+
+ft_status ft_cache_pin(ft_moe* h, const int32_t* keys, int32_t n) {
+    if (!h) return FT_ERR_INVALID;
+    if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
+    if (n < 0 || (n > 0 && !keys)) return fail(h, FT_ERR_INVALID, "keys/n");
+    const int64_t nkeys = (int64_t)h->cfg.layers * h->cfg.experts;
+    for (int32_t i = 0; i < n; ++i)
+        if (keys[i] < 0 || keys[i] >= nkeys) return fail(h, FT_ERR_INVALID, "key out of range");
+    ft_status s = sync_handle(h);
+    if (s != FT_OK) return s;
+    const int64_t C = h->C;
+    std::vector<int32_t> table((size_t)nkeys), sk((size_t)C), order;
+    FT_CUDA(h, cudaMemcpy(table.data(), h->d_table, (size_t)nkeys * 4, cudaMemcpyDeviceToHost));
+    if (C > 0) FT_CUDA(h, cudaMemcpy(sk.data(), h->d_slot_key, (size_t)C * 4, cudaMemcpyDeviceToHost));
+    FT_CUDA(h, read_order(h, &order));
+    // plan on host copies first, so a key that does not fit changes nothing
+    const bool per_layer = h->policy == FT_POLICY_LAYER_LRU;
+    std::vector<std::pair<int32_t, int32_t>> copies;   // (key, slot)
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t key = keys[i];
+        const int l = per_layer ? key / h->cfg.experts : 0;
+        const int64_t b0 = per_layer ? h->lbase[(size_t)l] : 0;
+        const int64_t len = per_layer ? h->llen[(size_t)l] : C;
+        int32_t slot = table[(size_t)key];
+        if (slot < 0) {
+            for (int64_t j = b0; j < b0 + len; ++j)
+                if (sk[(size_t)j] < 0 && (slot < 0 || j < slot)) slot = (int32_t)j;
+            if (slot < 0) return fail(h, FT_ERR_INVALID, "no free slot left for a pinned key");
+            sk[(size_t)slot] = key;
+            table[(size_t)key] = slot;
+            copies.emplace_back(key, slot);
+        }
+        // most recent end of the key's list
+        auto first = order.begin() + b0, last = order.begin() + b0 + len;
+        auto it = std::find(first, last, slot);
+        std::rotate(it, it + 1, last);
+    }
+    for (auto& kc : copies)
+        FT_CUDA(h, cudaMemcpy(h->d_arena + (size_t)kc.second * h->blob_bytes, h->blobs[(size_t)kc.first],
+                              h->blob_bytes, cudaMemcpyHostToDevice));
+    FT_CUDA(h, cudaMemcpy(h->d_table, table.data(), (size_t)nkeys * 4, cudaMemcpyHostToDevice));
+    if (C > 0) FT_CUDA(h, cudaMemcpy(h->d_slot_key, sk.data(), (size_t)C * 4, cudaMemcpyHostToDevice));
+    FT_CUDA(h, write_order(h, order));
+    h->stats.resident += (int64_t)copies.size();
     return FT_OK;
 }
 

@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(kLookupThreads, 1) lookup_kernel(LookupParams 
 
     const int tid = threadIdx.x;
     const int E = p.experts;
-    const int64_t C = p.capacity;
+    const int64_t C = p.capacity;        // slot bound and staging base
+    const int64_t NL = p.list_len;       // this call's LRU list (all C slots, or a layer's share)
     const int key0 = p.layer * E;
 
     for (int e = tid; e < E; e += blockDim.x) s_present[e] = 0;
@@ -213,15 +214,15 @@ __global__ void __launch_bounds__(kLookupThreads, 1) lookup_kernel(LookupParams 
     }
     __syncthreads();
 
-    const int64_t n_nonS = C - n_hits;
-    const int n_fill = (int)((int64_t)n_miss < n_nonS ? n_miss : n_nonS);
+    const int64_t n_nonS = NL - n_hits;
+    const int n_fill = p.no_insert ? 0 : (int)((int64_t)n_miss < n_nonS ? n_miss : n_nonS);
     const int n_bypass = n_miss - n_fill;
 
     // Reorder the LRU list; assign victims to misses.
-    if (C > 0) {
-        const int64_t per = (C + blockDim.x - 1) / blockDim.x;
+    if (NL > 0) {
+        const int64_t per = (NL + blockDim.x - 1) / blockDim.x;
         const int64_t i0 = (int64_t)tid * per;
-        const int64_t i1 = (i0 + per < C) ? i0 + per : C;
+        const int64_t i1 = (i0 + per < NL) ? i0 + per : NL;
         int cnt = 0;
         for (int64_t i = i0; i < i1; ++i) {
             int s = p.order_in[i];

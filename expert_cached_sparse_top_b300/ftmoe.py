@@ -20,7 +20,7 @@ EXPORTS = (
     "ft_status_str", "ft_expert_blob_bytes", "ft_moe_create", "ft_moe_forward",
     "ft_cache_resize", "ft_cache_stats", "ft_cache_snapshot", "ft_moe_set_timing",
     "ft_moe_timing", "ft_moe_last_error", "ft_moe_destroy", "ft_router_logits",
-    "ft_topk_softmax", "ft_expert_ffn_noalloc", "ft_moe_prefill",
+    "ft_topk_softmax", "ft_expert_ffn_noalloc", "ft_moe_prefill", "ft_cache_pin",
 )
 
 
@@ -87,6 +87,7 @@ def lib():
         "ft_topk_softmax": (I32, [P, I32, I32, I32, P, P, P]),
         "ft_expert_ffn_noalloc": (I32, [P, I32, I32, I32, P, I32, P, P]),
         "ft_moe_prefill": (I32, [VP, I32, P, I32, P, P, P]),
+        "ft_cache_pin": (I32, [VP, P, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -119,10 +120,13 @@ def _stream(s):
     return s.cuda_stream
 
 
+POLICY_GLOBAL_LRU, POLICY_LAYER_LRU, POLICY_STATIC = 0, 1, 2
+
+
 def make_config(layers, experts, hidden, inter, top_k, max_tokens, wfmt, cache_slots, device=0,
-                max_prefill_tokens=0):
+                max_prefill_tokens=0, policy=POLICY_GLOBAL_LRU):
     return FtMoeConfig(layers, experts, hidden, inter, top_k, max_tokens,
-                       WFMT.get(wfmt, wfmt), device, cache_slots, 0, max_prefill_tokens)
+                       WFMT.get(wfmt, wfmt), device, cache_slots, int(policy), max_prefill_tokens)
 
 
 def blob_bytes(cfg):
@@ -176,6 +180,12 @@ class MoECache:
     def prefill_status(self, layer, x, T, out, logits=None, stream=None):
         return lib().ft_moe_prefill(self.h, int(layer), _ptr(x), int(T), _ptr(logits), _ptr(out),
                                     _stream(stream))
+
+    def pin(self, keys):
+        """Place keys (layer * experts + expert) into the cache, first key least recent."""
+        import numpy as np
+        k = np.ascontiguousarray(keys, dtype=np.int32)
+        check(lib().ft_cache_pin(self.h, k.ctypes.data if k.size else None, int(k.size)), self.h)
 
     def resize(self, new_slots):
         check(lib().ft_cache_resize(self.h, int(new_slots)), self.h)

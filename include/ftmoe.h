@@ -85,6 +85,20 @@ typedef enum {
 
 typedef enum { FT_W_BF16 = 0, FT_W_MXFP4 = 1, FT_W_NVFP4 = 2 } ft_wfmt;
 
+/* Cache policy (ft_moe_config.flags). The engine's policy is the global LRU: one recency
+ * order over every (layer, expert) key of all layers ("FreeToken Runs 753B GLM-5.2 on One
+ * Workstation GPU" / MarkTechPost, Three mechanisms: semantic-aware caching). The other two
+ * are the comparators those pages measure it against, kept so the comparison runs through
+ * the same kernels on the same traces:
+ *   FT_POLICY_LAYER_LRU  the C slots split evenly between layers (layer l owns slots
+ *                        [sum_{j<l} C_j, ...), C_l = C / L, the first C % L layers one more),
+ *                        each layer its own LRU; a layer's misses evict only its own keys.
+ *   FT_POLICY_STATIC     a resident set fixed by ft_cache_pin (e.g. a hot subset chosen by
+ *                        profiling, or whole layers placed at load time); misses are computed
+ *                        from staging and never inserted; nothing is evicted.
+ * ft_cache_resize supports the global LRU only. */
+typedef enum { FT_POLICY_GLOBAL_LRU = 0, FT_POLICY_LAYER_LRU = 1, FT_POLICY_STATIC = 2 } ft_policy;
+
 typedef struct {
     int32_t layers;       /* MoE layers sharing the one global cache (>= 1) */
     int32_t experts;      /* routed experts per layer E (1..1024) */
@@ -95,7 +109,7 @@ typedef struct {
     int32_t wfmt;         /* ft_wfmt */
     int32_t device;       /* CUDA device ordinal */
     int64_t cache_slots;  /* C: GPU expert slots, one global LRU over all layers (>= 0) */
-    int32_t flags;        /* reserved, must be 0 */
+    int32_t flags;        /* cache policy, ft_policy (0 = the global LRU) */
     int32_t max_prefill_tokens; /* largest T passed to ft_moe_prefill; 0 = no prefill buffers */
 } ft_moe_config;
 
@@ -202,7 +216,8 @@ FT_API ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t
                                 const float* logits, void* out, void* stream);
 
 /* Rebuild the cache under a new slot budget at a safe point ("Three mechanisms", elastic
- * memory management). Synchronises the handle. The min(new_slots, resident) most recently
+ * memory management). Synchronises the handle. Global LRU policy only (FT_ERR_INVALID
+ * otherwise). The min(new_slots, resident) most recently
  * used keys survive in recency order; a survivor keeps its slot if that slot is
  * < new_slots, the others move (device-to-device) in ascending old-slot order to the lowest
  * free slots. The host pool is not read. On FT_ERR_OOM the old cache is intact. */
@@ -213,9 +228,21 @@ FT_API ft_status ft_cache_stats(ft_moe* h, ft_cache_stats_t* out);
 
 /* Cache state (safe point: synchronises the handle).
  *   slot_of_key  host int32 [layers*experts]: slot of each key, -1 if not resident.
- *   lru_keys     host int32 [capacity]: resident keys least- to most-recently used, -1 pad.
+ *   lru_keys     host int32 [capacity]: resident keys least- to most-recently used, -1 pad
+ *                (FT_POLICY_LAYER_LRU: layer 0's list, then layer 1's, ..., then the pad).
  * Either pointer may be NULL. */
 FT_API ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys);
+
+/* Place keys (layer * experts + expert, host int32[n]) into the cache at a safe point, the
+ * first key least recent: a key already resident moves to the most recent end; a missing key
+ * takes the lowest free slot of its list (the whole cache, or its layer's share under
+ * FT_POLICY_LAYER_LRU) and its blob is copied from the pinned host pool before the call
+ * returns. This is how a FT_POLICY_STATIC handle gets its resident set; for the LRU policies
+ * it pre-warms the cache. The copies are load-time placement: they do not count in the
+ * per-call statistics (only `resident` changes). Synchronises the handle.
+ * Errors: FT_ERR_INVALID for a key out of range or no free slot left in its list (nothing
+ * changed in that case); FT_ERR_CUDA on a copy failure. */
+FT_API ft_status ft_cache_pin(ft_moe* h, const int32_t* keys, int32_t n);
 
 /* Enable (1) or disable (0) per-stage event timing; ft_moe_timing synchronises and returns
  * the sums since the last reset (reset = 1 clears them after reading). */

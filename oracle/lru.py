@@ -22,6 +22,10 @@ Readings taken where the pages are silent (each is listed in the design doc):
   whose slot is < C' keeps it; the others move, in ascending old-slot order, to the lowest
   free slots < C'. Growth only adds free slots.
 
+Comparator policies (the engine's FT_POLICY_LAYER_LRU / FT_POLICY_STATIC) are in
+``policies.py``: per-layer LRU is one of these caches per layer; a static resident set is
+one with ``no_insert`` after ``pin``.
+
 Pins (tests/test_oracle_lru.py): hand-traced sequences (tests/golden/lru_*.txt), textbook
 LRU via functools.lru_cache on single-key calls, compulsory-miss-only behaviour when the
 capacity covers the pool, total bypass at capacity 0, and bijection/size invariants.
@@ -46,11 +50,12 @@ class CallResult:
 class LRUCache:
     """List-based simulator. Keys are ints key = layer * experts + expert."""
 
-    def __init__(self, capacity, experts):
+    def __init__(self, capacity, experts, no_insert=False):
         if capacity < 0:
             raise ValueError("capacity must be >= 0")
         self.capacity = int(capacity)
         self.experts = int(experts)
+        self.no_insert = bool(no_insert)      # static resident set: every miss is bypassed
         self.order = OrderedDict()            # key -> slot, least recent first
         self.key_of_slot = [None] * self.capacity
         self.free = list(range(self.capacity))   # min-heap of free slot indices
@@ -87,6 +92,9 @@ class LRUCache:
             key = keys[e]
             if e in res.slot_of:
                 continue
+            if self.no_insert:
+                res.bypassed.append(e)
+                continue
             slot = self._free_slot()
             if slot is None:
                 victim = None
@@ -110,6 +118,20 @@ class LRUCache:
         st["bypassed"] += len(res.bypassed)
         st["evictions"] += len(res.evicted)
         return res
+
+    def pin(self, keys):
+        """Place keys at a safe point, the first least recent: a resident key moves to MRU,
+        a missing key takes the lowest free slot (ValueError if none is free)."""
+        for key in keys:
+            key = int(key)
+            if key in self.order:
+                self.order[key] = self.order.pop(key)
+                continue
+            slot = self._free_slot()
+            if slot is None:
+                raise ValueError("no free slot for pinned key %d" % key)
+            self.order[key] = slot
+            self.key_of_slot[slot] = key
 
     def _free_slot(self):
         """Lowest-index free slot, or None."""

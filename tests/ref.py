@@ -69,10 +69,10 @@ class Runner:
     """Drives one MoECache and a mirror oracle LRU over calls, checking per-call cache
     counts bit-exactly."""
 
-    def __init__(self, cache, cfg, capacity):
+    def __init__(self, cache, cfg, capacity, sim=None):
         self.cache = cache
         self.cfg = cfg
-        self.sim = lru.LRUCache(capacity, cfg.experts)
+        self.sim = sim if sim is not None else lru.LRUCache(capacity, cfg.experts)
         self.prev = cache.stats()
 
     def call(self, layer, x_bits, logits=None, T=None, check=True):

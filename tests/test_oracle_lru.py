@@ -136,3 +136,67 @@ def test_invariants_random():
                 c.resize(C // 2)
                 C = C // 2
                 assert c.resident() <= C
+
+
+# ---- comparator policies (per-layer LRU, static resident set) ---------------------------
+from oracle import lru, policies
+
+
+def test_layer_shares_split_evenly():
+    assert policies.layer_shares(10, 3) == [(0, 4), (4, 3), (7, 3)]
+    assert policies.layer_shares(2, 3) == [(0, 1), (1, 1), (2, 0)]
+
+
+def test_layer_lru_with_one_layer_is_the_global_lru():
+    import numpy as np
+    rng = np.random.default_rng(5)
+    g = lru.LRUCache(6, 16)
+    p = policies.LayerLRU(6, 16, 1)
+    for _ in range(200):
+        sel = rng.integers(0, 16, size=rng.integers(1, 9))
+        a, b = g.call(0, sel), p.call(0, sel)
+        assert (a.hits, a.misses, a.bypassed, a.evicted) == (b.hits, b.misses, b.bypassed, b.evicted)
+    assert g.snapshot(16) == p.snapshot(16)
+
+
+def test_layer_lru_hand_trace():
+    """Two layers, 4 slots (2 each), 3 experts per layer. Layer 0 fills its share; layer 1's
+    misses go to slots 2, 3 and evict only layer-1 keys, where a global LRU would have
+    evicted layer 0's least recent key."""
+    p = policies.LayerLRU(4, 3, 2)
+    r = p.call(0, [0, 1]);  assert r.misses == [(0, 0), (1, 1)]
+    r = p.call(1, [0, 1]);  assert r.misses == [(0, 2), (1, 3)]
+    r = p.call(1, [2]);     assert r.misses == [(2, 2)] and r.evicted == [(3, 2)]
+    r = p.call(0, [0, 1]);  assert r.hits == [0, 1] and not r.misses
+    slots, order = p.snapshot(6)
+    assert slots == [0, 1, -1, -1, 3, 2]
+    assert order == [0, 1, 4, 5]          # layer 0 LRU->MRU, then layer 1
+    g = lru.LRUCache(4, 3)
+    for layer, sel in ((0, [0, 1]), (1, [0, 1]), (1, [2])):
+        g.call(layer, sel)
+    assert g.snapshot(6)[0][0] == -1      # the global LRU evicted layer 0's key 0 instead
+
+
+def test_static_set_never_changes_and_bypasses_misses():
+    c = policies.static_set(4, 8, [3, 5, 9])   # keys: layer 0 experts 3, 5; layer 1 expert 1
+    before = c.snapshot(16)[0]
+    assert before[3] == 0 and before[5] == 1 and before[9] == 2
+    r = c.call(0, [3, 4, 5, 6])
+    assert r.hits == [3, 5] and r.bypassed == [4, 6] and not r.misses and not r.evicted
+    r = c.call(1, [1, 2])
+    assert r.hits == [1] and r.bypassed == [2]
+    assert c.snapshot(16)[0] == before          # a free slot stays free
+    assert c.stats["misses"] == 3 and c.stats["bypassed"] == 3
+
+
+def test_pin_order_and_capacity():
+    c = lru.LRUCache(3, 4)
+    c.pin([2, 0])
+    assert c.lru_keys() == [2, 0] and c.slot_of_key(2) == 0 and c.slot_of_key(0) == 1
+    c.pin([2, 3])
+    assert c.lru_keys() == [0, 2, 3] and c.slot_of_key(3) == 2
+    try:
+        c.pin([1])
+        raise AssertionError("pin into a full cache must fail")
+    except ValueError:
+        pass
