@@ -94,6 +94,50 @@ def _peaks():
         return {}
 
 
+# DRAM traffic of the decode FFN kernel: an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum over every FFN launch of a `--ffn-traffic` run) divided by the
+# algorithmic bytes of the same launches, kept in a profile summary together with a hash of
+# the kernel's sources; a kernel changed since the capture reports no traffic.
+TRAFFIC = {
+    "bf16": ("tc_ffn_decode_bf16_traffic.md", ["tc_ffn.cu", "tc_ffn.cuh", "tc_ptx.cuh"]),
+    "mxfp4": ("fp4_ffn_decode_mxfp4_traffic.md", ["tc_fp4.cu", "tc_fp4.cuh", "tc_ptx.cuh"]),
+    "nvfp4": ("fp4_ffn_decode_nvfp4_traffic.md", ["tc_fp4.cu", "tc_fp4.cuh", "tc_ptx.cuh"]),
+}
+
+
+def kernel_sources_sha256(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "expert_cached_sparse_top_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_ratio(wfmt):
+    """DRAM bytes per algorithmic byte of the decode FFN kernel, or None (no capture, or the
+    kernel's sources changed since)."""
+    if wfmt not in TRAFFIC:
+        return None
+    name, files = TRAFFIC[wfmt]
+    try:
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in text.splitlines():
+        ln = ln.strip().strip("-").strip()
+        if ln.startswith("`") and "`:" in ln:
+            key, _, v = ln[1:].partition("`:")
+            vals[key] = v.strip().strip("`")
+    try:
+        if vals.get("kernel_sources_sha256") != kernel_sources_sha256(files):
+            return None
+        return float(vals["traffic_per_algorithmic_byte"])
+    except (KeyError, ValueError, OSError):
+        return None
+
+
 # Decode workloads: name -> (metric, host images (None = the whole pool), default steps, warmup)
 DECODE = {
     "decode_bf16": (METRIC, None, 200, 16),
@@ -315,6 +359,24 @@ def run_ours(args):
         return step_ms, t_wall, tim, s0, s1, clocks
 
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    if args.ffn_traffic:
+        # the cached pass alone, every FFN launch counted from the first call (an ncu capture
+        # of the FFN kernel over this run divides its DRAM bytes by these)
+        cache = make(C)
+        cache.set_timing(True)
+        cache.timing(reset=True)
+        for i in range(Wm + K):
+            if i in resizes:
+                cache.resize(resizes[i])
+            run_step(cache, i)
+        torch.cuda.synchronize()
+        tim = cache.timing(reset=True)
+        cache.close()
+        print(json.dumps({"workload": args.workload, "ffn_launches": int(tim["ffn_launches"]),
+                          "ffn_algorithmic_bytes": int(tim["ffn_weight_bytes"]),
+                          "kernel_sources_sha256": kernel_sources_sha256(TRAFFIC[cfg.wfmt][1])}),
+              flush=True)
+        return
     cache = make(C)
     step_ms, t_wall, tim, s0, s1, clocks = timed_pass(cache, record_clocks=True)
     cache.close()
@@ -392,6 +454,12 @@ def run_ours(args):
     b_h, h_threads = host_copy_gbs()
     b_p = (fill_b / (tim["fill_ms"] * 1e-3) / 1e9) if tim["fill_ms"] > 0 else None
     m_step = misses / K
+    # fill time not hidden under the step's kernels (route, FFN passes, combine)
+    busy = tim["route_ms"] + tim["ffn_hit_ms"] + tim["ffn_miss_ms"] + tim["combine_ms"]
+    exposed = min(max(tim["total_ms"] - busy, 0.0), tim["fill_ms"])
+    overlap = (1.0 - exposed / tim["fill_ms"]) if tim["fill_ms"] > 0 else None
+    ratio = traffic_ratio(cfg.wfmt)
+    bpl = tim["ffn_weight_bytes"] / max(ffn_passes, 1)
     kern = ("expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
             if cfg.wfmt == "bf16" else
             "expert FFN (block-scaled tcgen05 grouped GEMM on %s codes: W13+SwiGLU, activation "
@@ -409,8 +477,12 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": kern,
                      "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": (achieved / hbm) if (achieved and hbm) else None,
-                     "traffic": None, "peak_source": "MEASURED_PEAKS.json hbm_gbs" if hbm else None,
-                     "algorithmic_bytes_per_launch": tim["ffn_weight_bytes"] / max(ffn_passes, 1),
+                     "traffic": ratio * bpl if ratio else None,
+                     "traffic_source": ("ncu dram bytes per algorithmic byte (profiles/%s) x "
+                                        "algorithmic bytes per launch" % TRAFFIC[cfg.wfmt][0])
+                     if ratio else None,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs" if hbm else None,
+                     "algorithmic_bytes_per_launch": bpl,
                      "avg_launch_ms": ffn_ms / max(ffn_passes, 1)},
         "cpu_baseline": base,
         "e2e": {"value": tokens * ws / e2e_s, "unit": "tokens/s",
@@ -426,6 +498,7 @@ def run_ours(args):
                        "note": "experts per step the pages' policy would fill (m * B_P / B_H); "
                                "the rest would run on the host CPU, which is not built"},
             "fill_ms_per_step": tim["fill_ms"] / K,
+            "fill_overlap_fraction": overlap,
             "wall_ms_per_step": 1e3 * t_wall / K,
             "all_resident_slots": len(touched),
             "all_resident_tokens_per_s": tokens / (sum(rs_ms) / 1e3),
@@ -530,7 +603,10 @@ def run_prefill(args):
     from expert_cached_sparse_top_b300 import build as b
     b.build()
     from expert_cached_sparse_top_b300 import ftmoe
-    cfg = W.config(args.workload, **({"layers": args.layers} if args.layers else {}))
+    ov = {"layers": args.layers} if args.layers else {}
+    if args.tokens:
+        ov["tokens"] = args.tokens
+    cfg = W.config(args.workload, **ov)
     torch.cuda.set_device(0)
     fp4 = cfg.wfmt != "bf16"
     # the 256-expert MXFP4 layer aliases 16 physical blobs (keys and PCIe bytes unchanged)
@@ -588,15 +664,15 @@ def run_prefill(args):
                 "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs", "tflops": ffn_tflops,
                 "hbm_bound_ceiling_tflops": ceiling, "frac_of_hbm_ceiling": ffn_tflops / ceiling}
-        metric = ("MoE-layer prefill tokens/s (284B-shaped MXFP4 layer, 256 experts top-6, 4096 tokens, "
-                  "layers streamed)")
+        metric = ("MoE-layer prefill tokens/s (284B-shaped MXFP4 layer, 256 experts top-6, %d tokens, "
+                  "layers streamed)" % T)
     else:
         roof = {"bound": "tensor", "kernel": "tcgen05 grouped GEMM (W13+SwiGLU, W2)",
                 "achieved": ffn_tflops, "peak": bf16, "unit": "TFLOP/s",
                 "frac": ffn_tflops / bf16 if bf16 else None, "traffic": None,
                 "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)",
                 "hbm_bound_ceiling_tflops": ceiling}
-        metric = "MoE-layer prefill tokens/s (35B-A3B-shaped BF16 layer, 4096 tokens, layers streamed)"
+        metric = "MoE-layer prefill tokens/s (35B-A3B-shaped BF16 layer, %d tokens, layers streamed)" % T
     line = {
         "metric": metric,
         "value": T * cfg.layers / stream_s, "unit": "tokens/s", "n_gpus": 1,
@@ -631,6 +707,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer MoE layers than the workload defines (profiling runs)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prefill tokens per layer (default: the workload's 4096)")
+    ap.add_argument("--ffn-traffic", action="store_true",
+                    help="decode: run the cached pass only and print the FFN launches and their "
+                         "algorithmic bytes (the denominator of an ncu traffic capture)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare"])
     args = ap.parse_args()
