@@ -317,7 +317,7 @@ def run_ours(args):
 
     def make(capacity):
         c = ftmoe.make_config(cfg.layers, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
-                              cfg.t_max, cfg.wfmt, capacity, device=local)
+                              cfg.t_max, cfg.wfmt, capacity, device=local, fused_decode=args.fused)
         return ftmoe.MoECache(c, pool.ptrs, None)
 
     def run_step(cache, i):
@@ -457,10 +457,13 @@ def run_ours(args):
     # fill time not hidden under the step's kernels (route, FFN passes, combine)
     busy = tim["route_ms"] + tim["ffn_hit_ms"] + tim["ffn_miss_ms"] + tim["combine_ms"]
     exposed = min(max(tim["total_ms"] - busy, 0.0), tim["fill_ms"])
-    overlap = (1.0 - exposed / tim["fill_ms"]) if tim["fill_ms"] > 0 else None
-    ratio = traffic_ratio(cfg.wfmt)
+    overlap = (1.0 - exposed / tim["fill_ms"]) if tim["fill_ms"] > 0 and not args.fused else None
+    ratio = None if args.fused else traffic_ratio(cfg.wfmt)
     bpl = tim["ffn_weight_bytes"] / max(ffn_passes, 1)
-    kern = ("expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
+    kern = ("fused decode kernel (one cooperative launch per call: top-k, LRU lookup, row gather, "
+            "tcgen05 W13+SwiGLU and W2, combine; missed experts' tiles wait for their PCIe fills)"
+            if args.fused else
+            "expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
             if cfg.wfmt == "bf16" else
             "expert FFN (block-scaled tcgen05 grouped GEMM on %s codes: W13+SwiGLU, activation "
             "pieces, W2), per pass" % cfg.wfmt.upper())
@@ -473,7 +476,8 @@ def run_ours(args):
                        pool="pinned host, %d keys on %d blobs x %d B" % (cfg.keys, pool.images,
                                                                         pool.blob_bytes),
                        resizes={str(k2): v for k2, v in resizes.items()} or None,
-                       parallelism="replicas" if ws > 1 else "single GPU"),
+                       parallelism="replicas" if ws > 1 else "single GPU",
+                       fused_decode=bool(args.fused)),
         "roofline": {"bound": "hbm", "kernel": kern,
                      "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": (achieved / hbm) if (achieved and hbm) else None,
@@ -712,6 +716,8 @@ def main():
     ap.add_argument("--ffn-traffic", action="store_true",
                     help="decode: run the cached pass only and print the FFN launches and their "
                          "algorithmic bytes (the denominator of an ncu traffic capture)")
+    ap.add_argument("--fused", action="store_true",
+                    help="decode through the fused decode kernel (FT_FLAG_FUSED_DECODE; BF16)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare"])
     args = ap.parse_args()

@@ -30,6 +30,23 @@ namespace {
 
 thread_local std::string g_create_error;
 
+// cuStreamWriteValue32: a stream-ordered 32-bit write (with a memory barrier before it) that
+// the stream's front end performs, so it needs no SM while the fused decode kernel holds
+// them all.
+typedef CUresult (*StreamWriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+StreamWriteValue32Fn stream_write_fn() {
+    static StreamWriteValue32Fn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<StreamWriteValue32Fn>(p);
+    }
+    return fn;
+}
+
 struct StageEvents {
     cudaEvent_t ev[8];
     bool has_fill;
@@ -111,6 +128,14 @@ struct ft_moe {
     int* h_ffn_err = nullptr;             // host view of the kernels' error word (mapped)
     int* d_ffn_err = nullptr;             // device address of the same word
     int num_sms = 148;
+    // fused decode: one cooperative launch per forward call
+    bool mega = false;
+    int mega_grid = 0;
+    int32_t mega_epoch = 0;
+    int32_t* d_mega = nullptr;            // [0] route flag, [1] done count, [2] device error word,
+                                          // [64 + j] fill flag of miss j
+    int32_t* h_seq = nullptr;             // host view of the routing-published word (mapped)
+    int32_t* d_seq = nullptr;             // its device address
 
     // prefill: two full-layer buffers and their own scratch
     int32_t max_prefill = 0;
@@ -179,7 +204,7 @@ bool valid_config(const ft_moe_config* c, std::string* why) {
     if (!ffn_supported(c->wfmt, c->hidden, c->inter)) { *why = "hidden/inter must be positive multiples of 64"; return false; }
     if (c->cache_slots < 0 || c->cache_slots > (int64_t)c->layers * c->experts * 4 + 1024) { *why = "cache_slots out of range"; return false; }
     if ((int64_t)c->layers * c->experts >= (1LL << 31)) { *why = "too many keys"; return false; }
-    if (c->flags < FT_POLICY_GLOBAL_LRU || c->flags > FT_POLICY_STATIC) { *why = "unknown cache policy (flags)"; return false; }
+    if ((c->flags & 0xff) > FT_POLICY_STATIC || (c->flags & ~(0xff | FT_FLAG_FUSED_DECODE))) { *why = "unknown cache policy or flag bits (flags)"; return false; }
     if (c->max_prefill_tokens < 0 || (int64_t)c->max_prefill_tokens * c->top_k >= (1LL << 30)) { *why = "max_prefill_tokens out of range"; return false; }
     return true;
 }
@@ -321,6 +346,7 @@ void free_all(ft_moe* h) {
     if (h->ev_done) cudaEventSynchronize(h->ev_done);
     cudaFree(h->d_router); cudaFree(h->d_arena); cudaFree(h->d_table); cudaFree(h->d_slot_key);
     cudaFree(h->d_order[0]); cudaFree(h->d_order[1]); cudaFree(h->d_logits); cudaFree(h->d_idx);
+    cudaFree(h->d_mega);
     cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
     cudaFree(h->d_y); cudaFree(h->d_xp);
     cudaFree(h->d_xq); cudaFree(h->d_xsf); cudaFree(h->d_xrs);
@@ -637,7 +663,7 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     const int fault_alloc = h->fault_alloc;
     h->fault_alloc = 0;   // the injected fault targets resize only
     h->C = cfg->cache_slots;
-    h->policy = cfg->flags;
+    h->policy = cfg->flags & 0xff;
     layer_partition(h);
     st = alloc_state(h, h->C, &h->d_arena, &h->d_slot_key, &h->d_order[0], &h->d_order[1], &h->n_stage);
     h->fault_alloc = fault_alloc;
@@ -710,7 +736,7 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->rb.dep = (int32_t*)p; p += 4 * mu;
         h->rb.dep_x = (int32_t*)p; p += 4 * mu;
         h->rb.dep_a = (int32_t*)p;
-        const size_t hbytes = 256 + 8 * mu + 64 + 64;
+        const size_t hbytes = 256 + 8 * mu + 64 + 64 + 64;
         if (cudaHostAlloc((void**)&h->h_mapped, hbytes, cudaHostAllocMapped) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(route view)"); return bail(FT_ERR_OOM);
         }
@@ -727,6 +753,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->hv_dev.miss_dst = (int32_t*)(dp + 256 + 4 * mu);
         h->h_ffn_err = (int*)(h->h_mapped + 256 + 8 * mu + 64);
         h->d_ffn_err = (int*)(dp + 256 + 8 * mu + 64);
+        h->h_seq = (int32_t*)(h->h_mapped + 256 + 8 * mu + 128);
+        h->d_seq = (int32_t*)(dp + 256 + 8 * mu + 128);
     }
     if (cudaMemset(h->d_nan, 0, 16) != cudaSuccess) { cuda_fail(h, cudaGetLastError(), "memset"); return bail(FT_ERR_CUDA); }
     if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
@@ -739,6 +767,25 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (st != FT_OK) return bail(st);
     st = encode_tc_maps(h);
     if (st != FT_OK) return bail(st);
+    if (cfg->flags & FT_FLAG_FUSED_DECODE) {
+        if (!h->use_tc || !h->tc_fused || h->tc_bn > 32 || E > 256) {
+            fail(h, FT_ERR_INVALID, "FT_FLAG_FUSED_DECODE needs BF16 weights, experts <= 256 and max_tokens <= 32");
+            return bail(FT_ERR_INVALID);
+        }
+        int coop = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->dev);
+        h->mega_grid = std::min(tc_mega_grid(h->tc_bn, h->num_sms), h->num_sms);
+        cudaGetLastError();
+        if (!coop || !stream_write_fn() || h->mega_grid < 1) {
+            fail(h, FT_ERR_INVALID, "FT_FLAG_FUSED_DECODE: no cooperative launch or stream memory writes on this device");
+            return bail(FT_ERR_INVALID);
+        }
+        if (!dmalloc((void**)&h->d_mega, (size_t)(64 + h->max_u) * 4)) return bail(FT_ERR_OOM);
+        if (cudaMemset(h->d_mega, 0, (size_t)(64 + h->max_u) * 4) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "memset(fused decode flags)"); return bail(FT_ERR_CUDA);
+        }
+        h->mega = true;
+    }
     h->max_prefill = cfg->max_prefill_tokens;
     if (h->max_prefill > 0) {
         st = alloc_prefill(h);
@@ -751,6 +798,173 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     *out = h;
     return FT_OK;
 }
+
+namespace {
+
+void count_call(ft_moe* h, const RouteCounts& rc) {
+    ft_cache_stats_t& st = h->stats;
+    st.calls++;
+    st.hits += (uint64_t)rc.n_hits;
+    st.misses += (uint64_t)rc.n_miss;
+    st.bypassed += (uint64_t)rc.n_bypass;
+    st.evictions += (uint64_t)rc.n_evict;
+    st.fill_bytes += (uint64_t)rc.n_fill * h->blob_bytes;
+    st.stage_bytes += (uint64_t)rc.n_bypass * h->blob_bytes;
+    st.resident += rc.n_fill - rc.n_evict;
+}
+
+// The fused decode call (FT_FLAG_FUSED_DECODE): one cooperative launch does top-k, lookup,
+// row gather, the FFN of every entry and the combine. The host waits only for the routing
+// to be published (a mapped word), then enqueues each miss's copy followed by a
+// stream-ordered write of its fill flag on the copy stream; the kernel's tiles of that
+// miss start when the flag shows this call's epoch. On a host-side failure every pending
+// flag gets -epoch, so the kernel ends (with an error code) instead of waiting out its bound.
+ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* out, int32_t* topk_idx,
+                        float* topk_w, cudaStream_t s, const LookupParams& lp, int* curp, StageEvents& se,
+                        int launches) {
+    const ft_moe_config& c = h->cfg;
+    const int E = c.experts, k = c.top_k, H = c.hidden;
+    StreamWriteValue32Fn write_value = stream_write_fn();
+    if (h->mega_epoch >= 0x3fffffff) {
+        // restart the epochs at a safe point (nothing of this handle in flight)
+        ft_status ss = sync_handle(h);
+        if (ss != FT_OK) return ss;
+        FT_CUDA(h, cudaMemset(h->d_mega, 0, (size_t)(64 + h->max_u) * 4));
+        FT_CUDA(h, cudaDeviceSynchronize());
+        *(volatile int32_t*)h->h_seq = 0;
+        h->mega_epoch = 0;
+    }
+    const int32_t epoch = ++h->mega_epoch;
+    TcParams tp{};
+    tp.counts = h->rb.counts;
+    tp.entry_off = h->rb.entry_off;
+    tp.entry_dst = h->rb.entry_dst;
+    tp.pairs = h->rb.pairs;
+    tp.pass = 2;
+    tp.phases = 3;
+    tp.hidden = H;
+    tp.inter = c.inter;
+    tp.act = h->d_act;
+    tp.act_ld = c.inter;
+    tp.y = h->d_y;
+    tp.y_ld = H;
+    tp.err = h->d_ffn_err;
+    tp.dep = h->rb.dep;
+    TcMega mg{};
+    mg.logits = lg;
+    mg.T = T;
+    mg.experts = E;
+    mg.top_k = k;
+    mg.idx = h->d_idx;
+    mg.w = h->d_w;
+    mg.idx_out = topk_idx;
+    mg.w_out = topk_w;
+    mg.nan_flag = h->d_nan;
+    mg.lp = lp;
+    mg.x = (const __nv_bfloat16*)x;
+    mg.xp = h->d_xp;
+    mg.dep_x = h->rb.dep_x;
+    mg.fill_flag = h->d_mega + 64;
+    mg.out = (__nv_bfloat16*)out;
+    mg.route_flag = h->d_mega;
+    mg.host_seq = h->d_seq;
+    mg.done = h->d_mega + 1;
+    mg.err_dev = h->d_mega + 2;
+    mg.epoch = epoch;
+    mg.wait_ns = std::min<int64_t>(h->wait_ms, 4000) * 1000000;
+    const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};
+    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
+    FT_CUDA(h, tc_launch_mega(h->tc_bn, tp, mg, maps, h->mega_grid, s));
+    ++launches;
+    *curp ^= 1;
+    if (h->timing) {
+        for (int i = 2; i <= 5; ++i) FT_CUDA(h, cudaEventRecord(se.ev[i], s));
+    }
+    FT_CUDA(h, cudaEventRecord(h->ev_done, s));
+
+    CUdeviceptr flags = (CUdeviceptr)(h->d_mega + 64);
+    auto abandon = [&](int from, int to) {
+        for (int j = from; j < to; ++j)
+            write_value((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j, (cuuint32_t)(-epoch), 0);
+    };
+    // the one host wait: the kernel publishes this call's routing to mapped memory
+    auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        if (*(volatile int32_t*)h->h_seq == epoch) break;
+        cudaError_t q = cudaEventQuery(h->ev_done);
+        if (q != cudaErrorNotReady) {
+            if (*(volatile int32_t*)h->h_seq == epoch) break;
+            h->broken = true;
+            if (q != cudaSuccess) return cuda_fail(h, q, "fused decode kernel");
+            return fail(h, FT_ERR_CUDA, "fused decode kernel ended without publishing its routing (code " +
+                                        std::to_string(*(volatile int*)h->h_ffn_err) + ")");
+        }
+        auto dt = std::chrono::duration_cast<std::chrono::milliseconds>(
+            std::chrono::steady_clock::now() - t0).count();
+        if (dt > h->wait_ms) {
+            h->broken = true;
+            abandon(0, h->max_u);
+            return fail(h, FT_ERR_TIMEOUT, "fused decode routing: host wait exceeded FTMOE_WAIT_MS");
+        }
+    }
+    RouteCounts rc;
+    {
+        volatile int32_t* vc = (volatile int32_t*)h->h_counts;
+        rc.n_unique = vc[0]; rc.n_hits = vc[1]; rc.n_miss = vc[2]; rc.n_fill = vc[3];
+        rc.n_bypass = vc[4]; rc.n_evict = vc[5]; rc.err = vc[6]; rc.pad = 0;
+    }
+    if (rc.n_miss < 0 || rc.n_miss > h->max_u) {
+        h->broken = true;
+        abandon(0, h->max_u);
+        return fail(h, FT_ERR_STATE, "fused decode: miss count out of range");
+    }
+    if (rc.err & 6) {
+        h->broken = true;
+        abandon(0, rc.n_miss);
+        return fail(h, FT_ERR_STATE, "cache lookup found inconsistent state");
+    }
+    if (rc.n_miss > 0) {
+        if (h->fault_fill) {
+            h->broken = true;
+            abandon(0, rc.n_miss);
+            return fail(h, FT_ERR_CUDA, "injected fill failure (FTMOE_FAULT=fill_fail)");
+        }
+        if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_begin, h->copy_stream));
+        for (int j = 0; j < rc.n_miss; ++j) {
+            const int key = ((volatile int32_t*)h->h_miss_key)[j];
+            const int dst = ((volatile int32_t*)h->h_miss_dst)[j];
+            if (key < 0 || key >= c.layers * E || dst < 0 || dst >= h->C + h->n_stage) {
+                h->broken = true;
+                abandon(j, rc.n_miss);
+                return fail(h, FT_ERR_STATE, "miss list out of range");
+            }
+            cudaError_t ce = cudaMemcpyAsync(h->d_arena + (size_t)dst * h->blob_bytes, h->blobs[(size_t)key],
+                                             h->blob_bytes, cudaMemcpyHostToDevice, h->copy_stream);
+            if (ce != cudaSuccess || write_value((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j,
+                                                 (cuuint32_t)epoch, 0) != CUDA_SUCCESS) {
+                h->broken = true;
+                abandon(j + 1, rc.n_miss);
+                return cuda_fail(h, ce != cudaSuccess ? ce : cudaErrorUnknown, "fused decode fill");
+            }
+        }
+        if (h->timing) {
+            FT_CUDA(h, cudaEventRecord(se.fill_end, h->copy_stream));
+            se.has_fill = true;
+        }
+    }
+    if (h->timing) {
+        h->pending.push_back(se);
+        h->tsum.forwards++;
+        h->tsum.ffn_launches += 1;
+        h->tsum.ffn_weight_bytes += (uint64_t)rc.n_unique * (uint64_t)(h->lay.blob_bytes);
+        h->tsum.kernel_launches += (uint64_t)launches;
+    }
+    count_call(h, rc);
+    if (rc.err & 1) return fail(h, FT_ERR_INVALID, "NaN router logit");
+    return FT_OK;
+}
+
+}  // namespace
 
 ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, const float* logits,
                          void* out, int32_t* topk_idx, float* topk_w, void* stream_) {
@@ -795,8 +1009,10 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         lg = h->d_logits;
         ++launches;
     }
-    FT_CUDA(h, launch_topk_softmax(lg, T, E, k, h->d_idx, h->d_w, topk_idx, topk_w, h->d_nan, s));
-    ++launches;
+    if (!h->mega) {
+        FT_CUDA(h, launch_topk_softmax(lg, T, E, k, h->d_idx, h->d_w, topk_idx, topk_w, h->d_nan, s));
+        ++launches;
+    }
     LookupParams lp{};
     lp.idx = h->d_idx;
     lp.n_pairs = T * k;
@@ -821,6 +1037,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     lp.nan_flag = h->d_nan;
     lp.rb = h->rb;
     lp.hv = h->hv_dev;
+    if (h->mega) return forward_fused(h, x, T, lg, out, topk_idx, topk_w, s, lp, curp, se, launches);
     FT_CUDA(h, launch_lookup(lp, s));
     ++launches;
     *curp ^= 1;
@@ -961,15 +1178,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         h->tsum.kernel_launches += (uint64_t)launches;
     }
 
-    ft_cache_stats_t& st = h->stats;
-    st.calls++;
-    st.hits += (uint64_t)rc.n_hits;
-    st.misses += (uint64_t)rc.n_miss;
-    st.bypassed += (uint64_t)rc.n_bypass;
-    st.evictions += (uint64_t)rc.n_evict;
-    st.fill_bytes += (uint64_t)rc.n_fill * h->blob_bytes;
-    st.stage_bytes += (uint64_t)rc.n_bypass * h->blob_bytes;
-    st.resident += rc.n_fill - rc.n_evict;
+    count_call(h, rc);
     if (rc.err & 1) return fail(h, FT_ERR_INVALID, "NaN router logit");
     return FT_OK;
 }

@@ -23,6 +23,7 @@
 #include "common.cuh"
 #include "tc_ffn.cuh"
 #include "tc_ptx.cuh"
+#include "route_dev.cuh"
 
 #include <cuda.h>
 
@@ -113,9 +114,107 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
 template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
 template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 32 : kThreads; }
 
-template <int BN>
-__global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
-    TcParams p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
+template <int BN, bool MK> constexpr int tc_block() { return MK ? 256 : tc_threads<BN>(); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_sys(int* p, int v) {
+    asm volatile("st.release.sys.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Wait (up to the deadline) until *p >= target, polling with a short back-off; records
+// `code` and returns false on time-out, or as soon as another role recorded an error.
+__device__ __forceinline__ bool wait_ge_until(const int* p, int target, int* err, int code,
+                                              uint64_t deadline, uint32_t max_ns) {
+    uint32_t ns = 32;
+    for (uint32_t i = 0;; ++i) {
+        if (ld_acquire(p) >= target) return true;
+        if ((i & 15u) == 15u) {
+            if (*(volatile int*)err) return false;
+            if (global_ns() > deadline) break;
+        }
+        __nanosleep(ns);
+        if (ns < max_ns) ns <<= 1;
+    }
+    atomicCAS(err, 0, code);
+    return false;
+}
+
+// Fill flag of one missed expert: epoch once its blob is in place, -epoch if the host
+// abandoned the call before copying it.
+__device__ __forceinline__ bool wait_fill_until(const int* p, int epoch, int* err, uint64_t deadline) {
+    uint32_t ns = 64;
+    for (uint32_t i = 0;; ++i) {
+        const int v = ld_acquire(p);
+        if (v == epoch) return true;
+        if (v == -epoch) { atomicCAS(err, 0, 22); return false; }
+        if ((i & 15u) == 15u) {
+            if (*(volatile int*)err) return false;
+            if (global_ns() > deadline) break;
+        }
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+    }
+    atomicCAS(err, 0, 21);
+    return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, int* err, int code,
+                                                uint64_t deadline) {
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 1023u) == 1023u) {
+            if (*(volatile int*)err) return false;
+            if (global_ns() > deadline) break;
+        }
+    }
+    atomicCAS(err, 0, code);
+    return false;
+}
+
+// Tile t of one group of entries [e_lo, e_lo + n) whose N-tile prefix is s_nt (absolute):
+// W13 tiles of the group's entries first, then its W2 tiles (order as in tile_at).
+__device__ __forceinline__ Tile tile_in(int t, const int* s_nt, int e_lo, int n, int m13, int m2) {
+    const int base = s_nt[e_lo];
+    const int nt = s_nt[e_lo + n] - base;
+    Tile r;
+    int m_tiles;
+    if (t < m13 * nt) { r.phase = 13; m_tiles = m13; }
+    else { t -= m13 * nt; r.phase = 2; m_tiles = m2; }
+    int lo = e_lo, hi = e_lo + n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((s_nt[mid] - base) * m_tiles <= t) lo = mid; else hi = mid - 1;
+    }
+    const int rr = t - (s_nt[lo] - base) * m_tiles;
+    r.ent_rel = lo;
+    r.u = lo;
+    r.nt = rr / m_tiles;
+    r.mt = rr % m_tiles;
+    return r;
+}
+
+// Entry of grouped row r: the last u with entry_off[u] <= r.
+__device__ __forceinline__ int entry_of_row(const int32_t* entry_off, int n_entries, int r) {
+    int lo = 0, hi = n_entries - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldcg(entry_off + mid) <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int BN, bool MK>
+__global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
+    TcParams p, TcMega mg, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr bool DUAL = TcDual<BN>::value;
     constexpr int NI = DUAL ? 2 : 1;                  // MMA issuers
@@ -136,19 +235,87 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
     int* s_nt = reinterpret_cast<int*>(s_tmem + 4);   // [kMaxExperts + 1] N-tile prefix
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const RouteCounts rc = *p.counts;
-    const int u_begin = p.pass == 0 ? 0 : rc.n_hits;
-    const int u_end = p.pass == 0 ? rc.n_hits : rc.n_unique;
+    // the fused call's waits poll a device word (the host-mapped p.err would put a PCIe read
+    // in every poll); thread 0 of each CTA copies a code to p.err as the CTA leaves
+    int* err = MK ? mg.err_dev : p.err;
+    auto report = [&]() {
+        if (MK && threadIdx.x == 0) {
+            const int e = *(volatile int*)err;
+            if (e) atomicCAS(p.err, 0, e);
+        }
+    };
+    uint64_t deadline = 0;
+    if constexpr (MK) {
+        volatile uint32_t* s_ok = s_tmem + 2;
+        if (blockIdx.x == 0) {
+            // routing of the call: top-k per token (one warp each), then the lookup, with the
+            // (still unused) stage ring as the lookup's scratch
+            for (int t = warp; t < mg.T; t += blockDim.x >> 5)
+                topk_row(mg.logits, t, mg.experts, mg.top_k, mg.idx, mg.w, mg.idx_out, mg.w_out, mg.nan_flag);
+            __syncthreads();
+            int* sc = reinterpret_cast<int*>(smem);
+            const int E = mg.experts;
+            const LookupScratch ls{sc, sc + E, sc + 2 * E, sc + 3 * E, sc + 4 * E, sc + 5 * E,
+                                   sc + 5 * E + 33, sc + 5 * E + 34};
+            lookup_block(mg.lp, ls);
+            // the scratch is stage ring memory the TMA (async proxy) writes next
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                *mg.done = 0;
+                __threadfence_system();
+                st_release_gpu(mg.route_flag, mg.epoch);
+                st_release_sys(mg.host_seq, mg.epoch);
+            }
+        }
+        if (threadIdx.x == 0) {
+            deadline = global_ns() + (uint64_t)mg.wait_ns;
+            *s_ok = wait_ge_until(mg.route_flag, mg.epoch, err, 20, deadline, 256) ? 1u : 0u;
+            // a later epoch cannot appear while this launch runs: the flag is exact
+        }
+        __syncthreads();
+        if (*s_ok == 0) { report(); return; }
+        if (threadIdx.x != 0) deadline = global_ns() + (uint64_t)mg.wait_ns;
+    }
+    RouteCounts rc;
+    if constexpr (MK) {
+        const int4* c4 = reinterpret_cast<const int4*>(p.counts);
+        const int4 a = __ldcg(c4), b = __ldcg(c4 + 1);
+        rc.n_unique = a.x; rc.n_hits = a.y; rc.n_miss = a.z; rc.n_fill = a.w;
+        rc.n_bypass = b.x; rc.n_evict = b.y; rc.err = b.z; rc.pad = b.w;
+    } else {
+        rc = *p.counts;
+    }
+    const int u_begin = MK ? 0 : (p.pass == 0 ? 0 : rc.n_hits);
+    const int u_end = MK ? rc.n_unique : (p.pass == 0 ? rc.n_hits : rc.n_unique);
     const int n_entries = u_end - u_begin;
-    if (n_entries <= 0) return;
+    if (n_entries <= 0) { report(); return; }
     const int H = p.hidden, I = p.inter;
     const int m13 = (2 * I + kBM - 1) / kBM, m2 = (H + kBM - 1) / kBM;
-    const int phases = p.phases;
+    const int phases = MK ? 3 : p.phases;
     const bool fused = phases == 3 && p.dep != nullptr;
+    const int n_hits = rc.n_hits;
 
-    // N-tile prefix over this pass's entries: counts in parallel, then one warp scans
+    if constexpr (MK) {
+        // gather this CTA's share of the grouped activation rows: xp[r] = x[pairs[r] / k];
+        // each finished row counts toward its entry (the W13 tiles wait for all of them)
+        const int R = __ldcg(p.entry_off + n_entries);
+        const int cpr = H / 8;
+        for (int r = blockIdx.x; r < R; r += gridDim.x) {
+            const int tok = __ldcg(p.pairs + r) / mg.top_k;
+            const uint4* src = reinterpret_cast<const uint4*>(mg.x + (int64_t)tok * H);
+            uint4* dst = reinterpret_cast<uint4*>(mg.xp + (int64_t)r * H);
+            for (int c = threadIdx.x; c < cpr; c += blockDim.x) dst[c] = __ldg(src + c);
+            __threadfence();
+            fence_proxy_async_global();
+            __syncthreads();
+            if (threadIdx.x == 0) atomicAdd(mg.dep_x + entry_of_row(p.entry_off, n_entries, r), 1);
+        }
+    }
+
+    // N-tile prefix over this launch's entries: counts in parallel, then one warp scans
     for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
-        const int n = p.entry_off[u_begin + i + 1] - p.entry_off[u_begin + i];
+        const int n = __ldcg(p.entry_off + u_begin + i + 1) - __ldcg(p.entry_off + u_begin + i);
         s_nt[i] = (n + BN - 1) / BN;
     }
     __syncthreads();
@@ -182,21 +349,48 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
     const int nt_total = s_nt[n_entries];
+    // fused call: hit entries' tiles, then miss entries' tiles (a CTA blocked on a fill never
+    // holds back hit work)
+    const int total0 = MK ? (m13 + m2) * s_nt[n_hits] : 0;
     const int total = ((phases & 1) ? m13 * nt_total : 0) + ((phases & 2) ? m2 * nt_total : 0);
-    int* err = p.err;
+    auto tile = [&](int t) -> Tile {
+        if constexpr (MK) {
+            return t < total0 ? tile_in(t, s_nt, 0, n_hits, m13, m2)
+                              : tile_in(t - total0, s_nt, n_hits, n_entries - n_hits, m13, m2);
+        } else {
+            return tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+        }
+    };
+    auto bar_wait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+        if constexpr (MK) return mbar_wait_until(bar, parity, err, code, deadline);
+        else return mbar_wait(bar, parity, err, code);
+    };
 
     if (warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+                const Tile tl = tile(t);
                 const bool w13 = tl.phase == 13;
                 const CUtensorMap* mA = w13 ? &tmA13 : &tmA2;
                 const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
                 const int k_steps = (w13 ? H : I) / kBK;
-                const int slot = p.entry_dst[tl.u];
-                const int row_b = p.entry_off[tl.u] + tl.nt * BN;
+                const int slot = __ldcg(p.entry_dst + tl.u);
+                const int row_b = __ldcg(p.entry_off + tl.u) + tl.nt * BN;
+                if constexpr (MK) {
+                    // a missed expert's weights are read only once its copy has landed; W13
+                    // activation rows only once the entry's rows are gathered
+                    if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    if (w13) {
+                        const int rows = __ldcg(p.entry_off + tl.u + 1) - __ldcg(p.entry_off + tl.u);
+                        if (!wait_ge_until(mg.dep_x + tl.u, rows, err, 23, deadline, 256)) { ok = false; break; }
+                    }
+                    fence_proxy_async_global();
+                }
                 int kb0 = 0;
                 const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
                 if (!w13 && fused && ld_acquire(p.dep + tl.u) >= target) {
@@ -208,12 +402,15 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
                     const uint32_t it0 = it;
                     for (int kb = 0; kb < npre; ++kb, ++it) {
                         const int s = it % S;
-                        if (!mbar_wait(&empty[s], ((it / S) & 1u) ^ 1u, err, 1)) { ok = false; break; }
+                        if (!bar_wait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
                         mbar_expect_tx(&full[s], STAGE);
                         tma_load_3d(smem + s * STAGE, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
                     }
                     if (!ok) break;
-                    if (!wait_dep(p.dep + tl.u, target, err)) {
+                    bool dep_ok;
+                    if constexpr (MK) dep_ok = wait_ge_until(p.dep + tl.u, target, err, 6, deadline, 1024);
+                    else dep_ok = wait_dep(p.dep + tl.u, target, err);
+                    if (!dep_ok) {
                         // the stages armed above still expect their activation bytes: load
                         // them (rows already written or not) so the ring can drain
                         fence_proxy_async_global();
@@ -234,7 +431,7 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
                 for (int kb = kb0; kb < k_steps; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, err, 1)) { ok = false; break; }
+                    if (!bar_wait(&empty[s], ph ^ 1u, 1)) { ok = false; break; }
                     uint8_t* sa = smem + s * STAGE;
                     mbar_expect_tx(&full[s], STAGE);
                     tma_load_3d(sa, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
@@ -254,22 +451,22 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
-                const Tile tl = tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+                const Tile tl = tile(t);
                 const int k_steps = (tl.phase == 13 ? H : I) / kBK;
                 // N of this tile: its token count rounded up to 16 (a tail tile does no
                 // padded work); the accumulator keeps BN columns
-                const int row_b = p.entry_off[tl.u] + tl.nt * BN;
-                const int n_valid = min(BN, p.entry_off[tl.u + 1] - row_b);
+                const int row_b = __ldcg(p.entry_off + tl.u) + tl.nt * BN;
+                const int n_valid = min(BN, __ldcg(p.entry_off + tl.u + 1) - row_b);
                 const uint32_t idesc = idesc_bf16(min(BN, (n_valid + 15) & ~15));
                 const uint32_t acc = tcount & 1u;
                 const uint32_t aph = (tcount >> 1) & 1u;
-                if (!mbar_wait(&tempty[acc], aph ^ 1u, err, 2)) break;
+                if (!bar_wait(&tempty[acc], aph ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * BN;
                 for (int kb = 0; kb < k_steps; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1u;
-                    if (!mbar_wait(&full[s], ph, err, 3)) { ok = false; break; }
+                    if (!bar_wait(&full[s], ph, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + s * STAGE);
                     const uint32_t sb = sa + A_BYTES;
@@ -291,14 +488,14 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
         const int row_in_tile = q * 32 + lane;
         uint32_t tcount = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-            const Tile tl = tile_at(t, s_nt, n_entries, u_begin, m13, m2, phases);
+            const Tile tl = tile(t);
             const bool w13 = tl.phase == 13;
             const int m_rows = w13 ? 2 * I : H;
-            const int row_b = p.entry_off[tl.u] + tl.nt * BN;
-            const int n_valid = min(BN, p.entry_off[tl.u + 1] - row_b);
+            const int row_b = __ldcg(p.entry_off + tl.u) + tl.nt * BN;
+            const int n_valid = min(BN, __ldcg(p.entry_off + tl.u + 1) - row_b);
             const uint32_t acc = tcount & 1u;
             const uint32_t aph = (tcount >> 1) & 1u;
-            if (!mbar_wait(&tfull[acc], aph, err, 4)) break;
+            if (!bar_wait(&tfull[acc], aph, 4)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * NI * BN;
             const int m = tl.mt * kBM + row_in_tile;
@@ -340,7 +537,7 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
                     for (int j = 0; j < 16; ++j) {
                         const int n = c0 + j;
                         if (n < n_valid && m < m_rows) {
-                            const int pair = p.pairs[row_b + n];
+                            const int pair = __ldcg(p.pairs + row_b + n);
                             p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
                         }
                     }
@@ -354,6 +551,12 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
                 __syncwarp();
                 if (lane == 0) atomicAdd(p.dep + tl.u, 1);
             }
+            if (MK && !w13) {
+                // this quarter of the call's expert outputs is written (read by the combine)
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(mg.done, 1);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
         }
@@ -364,6 +567,40 @@ __global__ void __launch_bounds__(tc_threads<BN>(), 1) tc_ffn_kernel(
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                      :: "r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
+    if constexpr (MK) {
+        // combine, once every W2 tile quarter of the call is written: out[t] = sum_j w[t,j] *
+        // y[t*k + j], in rank order (the same arithmetic as the standalone combine)
+        volatile uint32_t* s_ok = s_tmem + 2;
+        if (threadIdx.x == 0)
+            *s_ok = wait_ge_until(mg.done, 4 * m2 * nt_total, err, 24, deadline, 1024) ? 1u : 0u;
+        __syncthreads();
+        if (*s_ok == 0) { report(); return; }
+        const int k = mg.top_k;
+        const int hv = H / 8;
+        const int64_t items = (int64_t)mg.T * hv;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            const int t = (int)(i / hv), c = (int)(i % hv);
+            float accv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) accv[q] = 0.f;
+            for (int j = 0; j < k; ++j) {
+                const float wj = __ldcg(mg.w + (int64_t)t * k + j);
+                const float4* yr = reinterpret_cast<const float4*>(p.y + ((int64_t)t * k + j) * p.y_ld + c * 8);
+                const float4 a = __ldcg(yr), b = __ldcg(yr + 1);
+                accv[0] = fmaf(wj, a.x, accv[0]); accv[1] = fmaf(wj, a.y, accv[1]);
+                accv[2] = fmaf(wj, a.z, accv[2]); accv[3] = fmaf(wj, a.w, accv[3]);
+                accv[4] = fmaf(wj, b.x, accv[4]); accv[5] = fmaf(wj, b.y, accv[5]);
+                accv[6] = fmaf(wj, b.z, accv[6]); accv[7] = fmaf(wj, b.w, accv[7]);
+            }
+            uint4 o;
+            __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ob[q] = __floats2bfloat162_rn(accv[2 * q], accv[2 * q + 1]);
+            *reinterpret_cast<uint4*>(mg.out + (int64_t)t * H + c * 8) = o;
+        }
+        report();
     }
 }
 
@@ -426,13 +663,59 @@ cudaError_t launch_bn(const TcParams& p0, const TcMaps& m, int grid, cudaStream_
     const size_t smem = smem_for<BN>(p.stages);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc::tc_ffn_kernel<BN>,
+        cudaError_t e = cudaFuncSetAttribute(tc::tc_ffn_kernel<BN, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tc::tc_ffn_kernel<BN><<<grid, tc::tc_threads<BN>(), smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
+    tc::tc_ffn_kernel<BN, false><<<grid, tc::tc_threads<BN>(), smem, s>>>(p, TcMega{}, *m.a13, *m.b13,
+                                                                         *m.a2, *m.b2);
     return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t mega_attr(size_t smem) {
+    static bool attr = false;
+    if (attr) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(tc::tc_ffn_kernel<BN, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) attr = true;
+    return e;
+}
+
+template <int BN>
+int mega_grid(int num_sms) {
+    const size_t smem = smem_for<BN>(stages_for<BN>());
+    if (mega_attr<BN>(smem) != cudaSuccess) return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::tc_ffn_kernel<BN, true>,
+                                                      tc::tc_block<BN, true>(), smem) != cudaSuccess)
+        return 0;
+    return per_sm * num_sms;
+}
+
+template <int BN>
+cudaError_t launch_mega(const TcParams& p0, const TcMega& mg0, const TcMaps& m, int grid, cudaStream_t s) {
+    TcParams p = p0;
+    p.stages = stages_for<BN>();
+    p.pass = 2;
+    p.phases = 3;
+    TcMega mg = mg0;
+    const size_t smem = smem_for<BN>(p.stages);
+    cudaError_t e = mega_attr<BN>(smem);
+    if (e != cudaSuccess) return e;
+    // every CTA waits on CTA 0's routing and on the others' outputs: all must be resident
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(tc::tc_block<BN, true>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc::tc_ffn_kernel<BN, true>, p, mg, *m.a13, *m.b13, *m.a2, *m.b2);
 }
 
 }  // namespace
@@ -484,6 +767,21 @@ cudaError_t tc_launch(int bn, const TcParams& p, const TcMaps& m, int grid, cuda
         default: return cudaErrorInvalidValue;
     }
 #undef FT_TC_CASE
+}
+
+cudaError_t tc_launch_mega(int bn, const TcParams& p, const TcMega& mg, const TcMaps& m, int grid,
+                           cudaStream_t s) {
+    if (mg.experts < 1 || mg.experts > tc::tc_block<16, true>() || mg.epoch <= 0 || grid < 1)
+        return cudaErrorInvalidValue;
+    if (bn == 16) return launch_mega<16>(p, mg, m, grid, s);
+    if (bn == 32) return launch_mega<32>(p, mg, m, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+int tc_mega_grid(int bn, int num_sms) {
+    if (bn == 16) return mega_grid<16>(num_sms);
+    if (bn == 32) return mega_grid<32>(num_sms);
+    return 0;
 }
 
 cudaError_t tc_gather_rows(const __nv_bfloat16* x, const int32_t* pairs, const int32_t* n_rows_dev,

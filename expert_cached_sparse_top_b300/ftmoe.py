@@ -121,12 +121,14 @@ def _stream(s):
 
 
 POLICY_GLOBAL_LRU, POLICY_LAYER_LRU, POLICY_STATIC = 0, 1, 2
+FLAG_FUSED_DECODE = 0x100
 
 
 def make_config(layers, experts, hidden, inter, top_k, max_tokens, wfmt, cache_slots, device=0,
-                max_prefill_tokens=0, policy=POLICY_GLOBAL_LRU):
+                max_prefill_tokens=0, policy=POLICY_GLOBAL_LRU, fused_decode=False):
+    flags = int(policy) | (FLAG_FUSED_DECODE if fused_decode else 0)
     return FtMoeConfig(layers, experts, hidden, inter, top_k, max_tokens,
-                       WFMT.get(wfmt, wfmt), device, cache_slots, int(policy), max_prefill_tokens)
+                       WFMT.get(wfmt, wfmt), device, cache_slots, flags, max_prefill_tokens)
 
 
 def blob_bytes(cfg):

@@ -99,6 +99,22 @@ typedef enum { FT_W_BF16 = 0, FT_W_MXFP4 = 1, FT_W_NVFP4 = 2 } ft_wfmt;
  * ft_cache_resize supports the global LRU only. */
 typedef enum { FT_POLICY_GLOBAL_LRU = 0, FT_POLICY_LAYER_LRU = 1, FT_POLICY_STATIC = 2 } ft_policy;
 
+/* Option bits of ft_moe_config.flags above the policy (which takes the low 8 bits).
+ *
+ * FT_FLAG_FUSED_DECODE: every ft_moe_forward is one cooperative kernel launch (the fused
+ *   decode kernel, a fused form of the per-call steps these pages describe): CTA 0 runs
+ *   the top-k and the cache lookup, every CTA then gathers activation rows, runs the expert
+ *   FFN tiles of the hit experts, then those of the missed experts, and the combine. A
+ *   missed expert's tiles start once its blob has been copied: the host reads the miss list
+ *   from mapped memory while the kernel runs and, per miss, enqueues the copy and a
+ *   stream-ordered write of a device flag on the copy stream. The results (outputs, top-k,
+ *   cache state, statistics) equal those of the default path bit for bit.
+ *   Requires BF16 weights, experts <= 256 and max_tokens <= 32, and a device where the
+ *   kernel's CTAs can all be resident at once; ft_moe_create fails with FT_ERR_INVALID
+ *   otherwise. ft_timing_t then reports the whole kernel as ffn_hit_ms (route_ms covers only
+ *   the router logits, if computed; ffn_miss_ms and combine_ms stay 0). */
+#define FT_FLAG_FUSED_DECODE 0x100
+
 typedef struct {
     int32_t layers;       /* MoE layers sharing the one global cache (>= 1) */
     int32_t experts;      /* routed experts per layer E (1..1024) */
@@ -109,7 +125,7 @@ typedef struct {
     int32_t wfmt;         /* ft_wfmt */
     int32_t device;       /* CUDA device ordinal */
     int64_t cache_slots;  /* C: GPU expert slots, one global LRU over all layers (>= 0) */
-    int32_t flags;        /* cache policy, ft_policy (0 = the global LRU) */
+    int32_t flags;        /* cache policy (ft_policy, low 8 bits; 0 = the global LRU) | FT_FLAG_* */
     int32_t max_prefill_tokens; /* largest T passed to ft_moe_prefill; 0 = no prefill buffers */
 } ft_moe_config;
 

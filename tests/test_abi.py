@@ -76,7 +76,7 @@ def test_blob_bytes_agree_with_oracle_and_generator(ft):
 @pytest.mark.parametrize("field,value", [
     ("layers", 0), ("experts", 0), ("experts", 2000), ("top_k", 0), ("top_k", 9),
     ("max_tokens", 0), ("wfmt", 7), ("hidden", 100), ("inter", 32), ("cache_slots", -1),
-    ("flags", 1),
+    ("flags", 3), ("flags", 0x200), ("flags", 0x101 | 0x400),
 ])
 def test_create_rejects_bad_config_before_touching_the_device(ft, field, value):
     cfg = ft.make_config(1, 8, 256, 128, 2, 16, "bf16", 4)
@@ -87,7 +87,8 @@ def test_create_rejects_bad_config_before_touching_the_device(ft, field, value):
     st = ft.lib().ft_moe_create(ctypes.byref(cfg), ptrs, None, ctypes.byref(h))
     assert st == ft.FT_ERR_INVALID
     assert not h.value
-    assert ft.lib().ft_moe_last_error(None)
+    msg = ft.lib().ft_moe_last_error(None)
+    assert msg and b"no such CUDA device" not in msg      # the config check itself refused it
 
 
 def test_create_rejects_null_blob_pointer(ft):
