@@ -295,7 +295,12 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
     metric, images, _, _ = DECODE[args.workload]
-    cfg = W.config(args.workload, **({"layers": args.layers} if args.layers else {}))
+    ov = {"layers": args.layers} if args.layers else {}
+    if args.tokens:
+        # every step the same number of tokens (e.g. T = 1, single-sequence decode)
+        ov.update(t_min=args.tokens, t_max=args.tokens)
+        metric = metric.replace("(", "(T = %d, " % args.tokens, 1)
+    cfg = W.config(args.workload, **ov)
     C = W.cache_capacity(cfg)
     pool = HostPool(cfg, images=images)
     K, Wm = args.steps, args.warmup
@@ -712,7 +717,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer MoE layers than the workload defines (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0,
-                    help="prefill tokens per layer (default: the workload's 4096)")
+                    help="prefill: tokens per layer (default 4096); decode: a fixed number of "
+                         "tokens per step instead of the seeded 1..16 mix")
     ap.add_argument("--ffn-traffic", action="store_true",
                     help="decode: run the cached pass only and print the FFN launches and their "
                          "algorithmic bytes (the denominator of an ncu traffic capture)")

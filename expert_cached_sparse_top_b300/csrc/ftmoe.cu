@@ -17,11 +17,17 @@
 #include "../../include/ftmoe.h"
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
+#include <condition_variable>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <deque>
+#include <memory>
+#include <mutex>
 #include <string>
+#include <thread>
 #include <vector>
 
 using namespace ftmoe;
@@ -136,6 +142,26 @@ struct ft_moe {
                                           // [64 + j] fill flag of miss j
     int32_t* h_seq = nullptr;             // host view of the routing-published word (mapped)
     int32_t* d_seq = nullptr;             // its device address
+    int32_t* h_wseq = nullptr;            // mapped: epoch of the call rewriting the routing record
+    int32_t* d_wseq = nullptr;
+    int32_t* h_nan = nullptr;             // mapped: a fused call saw a NaN logit
+    int32_t* d_nan_host = nullptr;
+    unsigned long long* d_dstats = nullptr;   // device cache counters of fused calls (in d_mega)
+    // The fill agent: a host thread that, per fused call, waits for the routing record and
+    // enqueues the miss copies and their flag writes, so that ft_moe_forward never blocks.
+    struct FillAgent {
+        struct Job { int32_t epoch; StageEvents* se; };
+        std::thread th;
+        std::mutex mu;
+        std::condition_variable cv;
+        std::deque<Job> jobs;
+        int32_t launched = 0, handled = 0;
+        bool stop = false;
+        ft_status status = FT_OK;     // first failure (reported once, then the handle is broken)
+        bool reported = false;
+        std::string msg;
+    };
+    std::unique_ptr<FillAgent> agent;
 
     // prefill: two full-layer buffers and their own scratch
     int32_t max_prefill = 0;
@@ -172,7 +198,7 @@ struct ft_moe {
     std::vector<PrefillEvents> p_pending;
 
     bool timing = false;
-    std::vector<StageEvents> pending;
+    std::deque<StageEvents> pending;
     std::vector<cudaEvent_t> event_pool;
     ft_timing_t tsum{};
 };
@@ -340,8 +366,18 @@ ft_status alloc_state(ft_moe* h, int64_t C, uint8_t** arena, int32_t** slot_key,
     return FT_OK;
 }
 
+void agent_stop(ft_moe* h);
+
 void free_all(ft_moe* h) {
     cudaSetDevice(h->dev);
+    if (h->agent) {
+        {
+            std::unique_lock<std::mutex> lk(h->agent->mu);
+            h->agent->cv.wait_for(lk, std::chrono::milliseconds(h->wait_ms + 5000),
+                                  [&] { return h->agent->handled == h->agent->launched; });
+        }
+        agent_stop(h);
+    }
     if (h->copy_stream) cudaStreamSynchronize(h->copy_stream);
     if (h->ev_done) cudaEventSynchronize(h->ev_done);
     cudaFree(h->d_router); cudaFree(h->d_arena); cudaFree(h->d_table); cudaFree(h->d_slot_key);
@@ -432,15 +468,203 @@ ft_status wait_event(ft_moe* h, cudaEvent_t ev, const char* what) {
     }
 }
 
+// ---- the fill agent of a fused-decode handle ----
+
+constexpr int32_t kFusedAhead = 2;
+
+// Mark every fill flag abandoned for the calls up to `epoch`: their kernels end (with an
+// error code) instead of waiting out their bound.
+void agent_abandon(ft_moe* h, int32_t epoch) {
+    StreamWriteValue32Fn wv = stream_write_fn();
+    const CUdeviceptr flags = (CUdeviceptr)(h->d_mega + 64);
+    for (int j = 0; j < h->max_u; ++j)
+        wv((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j, (cuuint32_t)(-epoch), 0);
+}
+
+// One fused call: wait for its routing record, then enqueue a copy and a flag write per miss.
+ft_status agent_handle(ft_moe* h, const ft_moe::FillAgent::Job& job, std::string* msg) {
+    const int32_t epoch = job.epoch;
+    const auto t0 = std::chrono::steady_clock::now();
+    volatile int32_t* seq = h->h_seq;
+    uint32_t spins = 0;
+    for (;;) {
+        if (*seq >= epoch) break;
+        if (*(volatile int*)h->h_ffn_err) {
+            *msg = "fused decode kernel failed before publishing its routing (code " +
+                   std::to_string(*(volatile int*)h->h_ffn_err) + ")";
+            return FT_ERR_CUDA;
+        }
+        if ((++spins & 255u) == 0) {
+            const auto dt = std::chrono::duration_cast<std::chrono::milliseconds>(
+                std::chrono::steady_clock::now() - t0).count();
+            if (dt > h->wait_ms) { *msg = "fused decode routing: host wait exceeded FTMOE_WAIT_MS"; return FT_ERR_TIMEOUT; }
+        }
+    }
+    // a later call has routed already: this one had no misses (a call with misses holds the
+    // stream until its fills land)
+    if (*seq != epoch) return FT_OK;
+    std::atomic_thread_fence(std::memory_order_acquire);
+    const int n_miss = ((volatile int32_t*)h->h_counts)[2];
+    std::vector<int32_t> keys, dsts;
+    if (n_miss > 0 && n_miss <= h->max_u) {
+        keys.resize((size_t)n_miss);
+        dsts.resize((size_t)n_miss);
+        for (int j = 0; j < n_miss; ++j) {
+            keys[(size_t)j] = ((volatile int32_t*)h->h_miss_key)[j];
+            dsts[(size_t)j] = ((volatile int32_t*)h->h_miss_dst)[j];
+        }
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
+    // the record may have been rewritten by a later call while it was read: then this call
+    // had no misses either
+    if (*(volatile int32_t*)h->h_wseq != epoch) return FT_OK;
+    if (n_miss < 0 || n_miss > h->max_u) { *msg = "fused decode: miss count out of range"; return FT_ERR_STATE; }
+    if (n_miss == 0) return FT_OK;
+    if (h->fault_fill) { *msg = "injected fill failure (FTMOE_FAULT=fill_fail)"; return FT_ERR_CUDA; }
+    const int nkeys = h->cfg.layers * h->cfg.experts;
+    for (int j = 0; j < n_miss; ++j)
+        if (keys[(size_t)j] < 0 || keys[(size_t)j] >= nkeys || dsts[(size_t)j] < 0 ||
+            dsts[(size_t)j] >= h->C + h->n_stage) {
+            *msg = "miss list out of range";
+            return FT_ERR_STATE;
+        }
+    StreamWriteValue32Fn wv = stream_write_fn();
+    const CUdeviceptr flags = (CUdeviceptr)(h->d_mega + 64);
+    if (job.se) cudaEventRecord(job.se->fill_begin, h->copy_stream);
+    for (int j = 0; j < n_miss; ++j) {
+        cudaError_t ce = cudaMemcpyAsync(h->d_arena + (size_t)dsts[(size_t)j] * h->blob_bytes,
+                                         h->blobs[(size_t)keys[(size_t)j]], h->blob_bytes,
+                                         cudaMemcpyHostToDevice, h->copy_stream);
+        if (ce != cudaSuccess) { *msg = std::string("fused decode fill: ") + cudaGetErrorString(ce); return FT_ERR_CUDA; }
+        if (wv((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j, (cuuint32_t)epoch, 0) != CUDA_SUCCESS) {
+            *msg = "fused decode fill: stream write of a fill flag failed";
+            return FT_ERR_CUDA;
+        }
+    }
+    if (job.se) {
+        cudaEventRecord(job.se->fill_end, h->copy_stream);
+        std::lock_guard<std::mutex> lk(h->agent->mu);
+        job.se->has_fill = true;
+    }
+    return FT_OK;
+}
+
+void agent_main(ft_moe* h) {
+    cudaSetDevice(h->dev);
+    auto& a = *h->agent;
+    int32_t abandoned = 0;
+    for (;;) {
+        ft_moe::FillAgent::Job job{};
+        bool failed;
+        {
+            std::unique_lock<std::mutex> lk(a.mu);
+            a.cv.wait(lk, [&] { return a.stop || !a.jobs.empty(); });
+            if (a.jobs.empty()) return;
+            job = a.jobs.front();
+            failed = a.status != FT_OK;
+        }
+        ft_status st = FT_OK;
+        std::string msg;
+        if (!failed) st = agent_handle(h, job, &msg);
+        if (st != FT_OK || failed) {
+            int32_t upto;
+            {
+                std::lock_guard<std::mutex> lk(a.mu);
+                upto = a.launched;
+            }
+            if (upto > abandoned) {
+                agent_abandon(h, upto);
+                abandoned = upto;
+            }
+        }
+        {
+            std::lock_guard<std::mutex> lk(a.mu);
+            if (st != FT_OK && a.status == FT_OK) { a.status = st; a.msg = msg; }
+            a.jobs.pop_front();
+            a.handled = job.epoch;
+        }
+        a.cv.notify_all();
+    }
+}
+
+// A failure the agent saw, or a NaN logit an earlier fused call saw: reported once.
+ft_status agent_report(ft_moe* h) {
+    auto& a = *h->agent;
+    {
+        std::lock_guard<std::mutex> lk(a.mu);
+        if (a.status != FT_OK && !a.reported) {
+            a.reported = true;
+            h->broken = true;
+            return fail(h, a.status, a.msg);
+        }
+    }
+    if (*(volatile int32_t*)h->h_nan) {
+        *(volatile int32_t*)h->h_nan = 0;
+        return fail(h, FT_ERR_INVALID, "NaN router logit (in an earlier call of the fused decode path)");
+    }
+    return FT_OK;
+}
+
+// Wait until the agent has handled every launched call (bounded).
+ft_status agent_drain(ft_moe* h) {
+    auto& a = *h->agent;
+    {
+        std::unique_lock<std::mutex> lk(a.mu);
+        const bool ok = a.cv.wait_for(lk, std::chrono::milliseconds(h->wait_ms + 5000),
+                                      [&] { return a.handled == a.launched; });
+        if (!ok) {
+            h->broken = true;
+            return fail(h, FT_ERR_TIMEOUT, "fill agent: host wait exceeded FTMOE_WAIT_MS");
+        }
+    }
+    return agent_report(h);
+}
+
+void agent_stop(ft_moe* h) {
+    if (!h->agent) return;
+    {
+        std::lock_guard<std::mutex> lk(h->agent->mu);
+        h->agent->stop = true;
+    }
+    h->agent->cv.notify_all();
+    if (h->agent->th.joinable()) h->agent->th.join();
+    h->agent.reset();
+}
+
+// Fold the fused calls' device cache counters into the handle's statistics (safe point).
+ft_status merge_dstats(ft_moe* h) {
+    unsigned long long d[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    FT_CUDA(h, cudaMemcpy(d, h->d_dstats, sizeof(d), cudaMemcpyDeviceToHost));
+    if (!(d[0] | d[1] | d[5] | d[6])) return FT_OK;
+    ft_cache_stats_t& st = h->stats;
+    st.calls += d[6];
+    st.hits += d[0];
+    st.misses += d[1];
+    st.bypassed += d[2];
+    st.evictions += d[3];
+    st.fill_bytes += d[4] * h->blob_bytes;
+    st.stage_bytes += d[2] * h->blob_bytes;
+    st.resident += (int64_t)d[4] - (int64_t)d[3];
+    if (h->timing) h->tsum.ffn_weight_bytes += d[5] * (uint64_t)h->lay.blob_bytes;
+    FT_CUDA(h, cudaMemset(h->d_dstats, 0, sizeof(d)));
+    return FT_OK;
+}
+
 ft_status sync_handle(ft_moe* h) {
     cudaSetDevice(h->dev);
+    if (h->agent) {
+        ft_status as = agent_drain(h);
+        if (as != FT_OK) return as;
+    }
     ft_status s = wait_event(h, h->ev_done, "synchronise handle");
     if (s != FT_OK) return s;
     FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
     if (h->h_ffn_err && *(volatile int*)h->h_ffn_err) {
         h->broken = true;
-        return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait");
+        return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait (code " +
+                                    std::to_string(*(volatile int*)h->h_ffn_err) + ")");
     }
+    if (h->mega) return merge_dstats(h);
     return FT_OK;
 }
 
@@ -755,6 +979,10 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->d_ffn_err = (int*)(dp + 256 + 8 * mu + 64);
         h->h_seq = (int32_t*)(h->h_mapped + 256 + 8 * mu + 128);
         h->d_seq = (int32_t*)(dp + 256 + 8 * mu + 128);
+        h->h_wseq = (int32_t*)(h->h_mapped + 256 + 8 * mu + 132);
+        h->d_wseq = (int32_t*)(dp + 256 + 8 * mu + 132);
+        h->h_nan = (int32_t*)(h->h_mapped + 256 + 8 * mu + 136);
+        h->d_nan_host = (int32_t*)(dp + 256 + 8 * mu + 136);
     }
     if (cudaMemset(h->d_nan, 0, 16) != cudaSuccess) { cuda_fail(h, cudaGetLastError(), "memset"); return bail(FT_ERR_CUDA); }
     if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
@@ -784,7 +1012,10 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         if (cudaMemset(h->d_mega, 0, (size_t)(64 + h->max_u) * 4) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "memset(fused decode flags)"); return bail(FT_ERR_CUDA);
         }
+        h->d_dstats = (unsigned long long*)(h->d_mega + 16);
         h->mega = true;
+        h->agent.reset(new ft_moe::FillAgent());
+        h->agent->th = std::thread(agent_main, h);
     }
     h->max_prefill = cfg->max_prefill_tokens;
     if (h->max_prefill > 0) {
@@ -814,25 +1045,37 @@ void count_call(ft_moe* h, const RouteCounts& rc) {
 }
 
 // The fused decode call (FT_FLAG_FUSED_DECODE): one cooperative launch does top-k, lookup,
-// row gather, the FFN of every entry and the combine. The host waits only for the routing
-// to be published (a mapped word), then enqueues each miss's copy followed by a
-// stream-ordered write of its fill flag on the copy stream; the kernel's tiles of that
-// miss start when the flag shows this call's epoch. On a host-side failure every pending
-// flag gets -epoch, so the kernel ends (with an error code) instead of waiting out its bound.
+// row gather, the FFN of every entry and the combine; ft_moe_forward only launches it and
+// hands the call to the fill agent, which enqueues the miss copies and their fill flags.
 ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* out, int32_t* topk_idx,
                         float* topk_w, cudaStream_t s, const LookupParams& lp, int* curp, StageEvents& se,
                         int launches) {
     const ft_moe_config& c = h->cfg;
     const int E = c.experts, k = c.top_k, H = c.hidden;
-    StreamWriteValue32Fn write_value = stream_write_fn();
     if (h->mega_epoch >= 0x3fffffff) {
         // restart the epochs at a safe point (nothing of this handle in flight)
         ft_status ss = sync_handle(h);
         if (ss != FT_OK) return ss;
-        FT_CUDA(h, cudaMemset(h->d_mega, 0, (size_t)(64 + h->max_u) * 4));
+        FT_CUDA(h, cudaMemset(h->d_mega, 0, (size_t)(16) * 4));
+        FT_CUDA(h, cudaMemset(h->d_mega + 64, 0, (size_t)h->max_u * 4));
         FT_CUDA(h, cudaDeviceSynchronize());
         *(volatile int32_t*)h->h_seq = 0;
+        *(volatile int32_t*)h->h_wseq = 0;
         h->mega_epoch = 0;
+    }
+    {
+        // at most kFusedAhead calls whose routing the agent has not handled yet: the caller
+        // never queues far ahead of the device (a full launch queue would block the caller
+        // inside the driver while the kernels wait for the agent's copies)
+        auto& a = *h->agent;
+        std::unique_lock<std::mutex> lk(a.mu);
+        const bool ok = a.cv.wait_for(lk, std::chrono::milliseconds(h->wait_ms + 5000), [&] {
+            return a.launched - a.handled < kFusedAhead || a.status != FT_OK;
+        });
+        if (!ok) {
+            h->broken = true;
+            return fail(h, FT_ERR_TIMEOUT, "fill agent: host wait exceeded FTMOE_WAIT_MS");
+        }
     }
     const int32_t epoch = ++h->mega_epoch;
     TcParams tp{};
@@ -868,6 +1111,9 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
     mg.out = (__nv_bfloat16*)out;
     mg.route_flag = h->d_mega;
     mg.host_seq = h->d_seq;
+    mg.host_wseq = h->d_wseq;
+    mg.host_nan = h->d_nan_host;
+    mg.dstats = h->d_dstats;
     mg.done = h->d_mega + 1;
     mg.err_dev = h->d_mega + 2;
     mg.epoch = epoch;
@@ -881,86 +1127,21 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
         for (int i = 2; i <= 5; ++i) FT_CUDA(h, cudaEventRecord(se.ev[i], s));
     }
     FT_CUDA(h, cudaEventRecord(h->ev_done, s));
-
-    CUdeviceptr flags = (CUdeviceptr)(h->d_mega + 64);
-    auto abandon = [&](int from, int to) {
-        for (int j = from; j < to; ++j)
-            write_value((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j, (cuuint32_t)(-epoch), 0);
-    };
-    // the one host wait: the kernel publishes this call's routing to mapped memory
-    auto t0 = std::chrono::steady_clock::now();
-    for (;;) {
-        if (*(volatile int32_t*)h->h_seq == epoch) break;
-        cudaError_t q = cudaEventQuery(h->ev_done);
-        if (q != cudaErrorNotReady) {
-            if (*(volatile int32_t*)h->h_seq == epoch) break;
-            h->broken = true;
-            if (q != cudaSuccess) return cuda_fail(h, q, "fused decode kernel");
-            return fail(h, FT_ERR_CUDA, "fused decode kernel ended without publishing its routing (code " +
-                                        std::to_string(*(volatile int*)h->h_ffn_err) + ")");
-        }
-        auto dt = std::chrono::duration_cast<std::chrono::milliseconds>(
-            std::chrono::steady_clock::now() - t0).count();
-        if (dt > h->wait_ms) {
-            h->broken = true;
-            abandon(0, h->max_u);
-            return fail(h, FT_ERR_TIMEOUT, "fused decode routing: host wait exceeded FTMOE_WAIT_MS");
-        }
-    }
-    RouteCounts rc;
+    auto& a = *h->agent;
     {
-        volatile int32_t* vc = (volatile int32_t*)h->h_counts;
-        rc.n_unique = vc[0]; rc.n_hits = vc[1]; rc.n_miss = vc[2]; rc.n_fill = vc[3];
-        rc.n_bypass = vc[4]; rc.n_evict = vc[5]; rc.err = vc[6]; rc.pad = 0;
-    }
-    if (rc.n_miss < 0 || rc.n_miss > h->max_u) {
-        h->broken = true;
-        abandon(0, h->max_u);
-        return fail(h, FT_ERR_STATE, "fused decode: miss count out of range");
-    }
-    if (rc.err & 6) {
-        h->broken = true;
-        abandon(0, rc.n_miss);
-        return fail(h, FT_ERR_STATE, "cache lookup found inconsistent state");
-    }
-    if (rc.n_miss > 0) {
-        if (h->fault_fill) {
-            h->broken = true;
-            abandon(0, rc.n_miss);
-            return fail(h, FT_ERR_CUDA, "injected fill failure (FTMOE_FAULT=fill_fail)");
-        }
-        if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_begin, h->copy_stream));
-        for (int j = 0; j < rc.n_miss; ++j) {
-            const int key = ((volatile int32_t*)h->h_miss_key)[j];
-            const int dst = ((volatile int32_t*)h->h_miss_dst)[j];
-            if (key < 0 || key >= c.layers * E || dst < 0 || dst >= h->C + h->n_stage) {
-                h->broken = true;
-                abandon(j, rc.n_miss);
-                return fail(h, FT_ERR_STATE, "miss list out of range");
-            }
-            cudaError_t ce = cudaMemcpyAsync(h->d_arena + (size_t)dst * h->blob_bytes, h->blobs[(size_t)key],
-                                             h->blob_bytes, cudaMemcpyHostToDevice, h->copy_stream);
-            if (ce != cudaSuccess || write_value((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j,
-                                                 (cuuint32_t)epoch, 0) != CUDA_SUCCESS) {
-                h->broken = true;
-                abandon(j + 1, rc.n_miss);
-                return cuda_fail(h, ce != cudaSuccess ? ce : cudaErrorUnknown, "fused decode fill");
-            }
-        }
+        std::lock_guard<std::mutex> lk(a.mu);
+        StageEvents* sp = nullptr;
         if (h->timing) {
-            FT_CUDA(h, cudaEventRecord(se.fill_end, h->copy_stream));
-            se.has_fill = true;
+            h->pending.push_back(se);
+            sp = &h->pending.back();
+            h->tsum.forwards++;
+            h->tsum.ffn_launches += 1;
+            h->tsum.kernel_launches += (uint64_t)launches;
         }
+        a.jobs.push_back({epoch, sp});
+        a.launched = epoch;
     }
-    if (h->timing) {
-        h->pending.push_back(se);
-        h->tsum.forwards++;
-        h->tsum.ffn_launches += 1;
-        h->tsum.ffn_weight_bytes += (uint64_t)rc.n_unique * (uint64_t)(h->lay.blob_bytes);
-        h->tsum.kernel_launches += (uint64_t)launches;
-    }
-    count_call(h, rc);
-    if (rc.err & 1) return fail(h, FT_ERR_INVALID, "NaN router logit");
+    a.cv.notify_all();
     return FT_OK;
 }
 
@@ -984,6 +1165,10 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     }
     cudaStream_t s = (cudaStream_t)stream_;
     cudaSetDevice(h->dev);
+    if (h->agent) {
+        ft_status ar = agent_report(h);
+        if (ar != FT_OK) return ar;
+    }
     if (*(volatile int*)h->h_ffn_err) {
         h->broken = true;
         return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait (code " +
@@ -1206,6 +1391,10 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     if (*(volatile int*)h->h_ffn_err) {
         h->broken = true;
         return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait");
+    }
+    if (h->agent) {
+        ft_status ar = agent_drain(h);
+        if (ar != FT_OK) return ar;
     }
     cudaError_t pe0 = cudaGetLastError();
     if (pe0 != cudaSuccess) return cuda_fail(h, pe0, "earlier asynchronous error");

@@ -148,14 +148,14 @@ __device__ __forceinline__ bool wait_ge_until(const int* p, int target, int* err
     return false;
 }
 
-// Fill flag of one missed expert: epoch once its blob is in place, -epoch if the host
-// abandoned the call before copying it.
+// Fill flag of one missed expert: epoch once its blob is in place; -e with e >= epoch once
+// the host abandoned this call (and any later one) before copying it.
 __device__ __forceinline__ bool wait_fill_until(const int* p, int epoch, int* err, uint64_t deadline) {
     uint32_t ns = 64;
     for (uint32_t i = 0;; ++i) {
         const int v = ld_acquire(p);
         if (v == epoch) return true;
-        if (v == -epoch) { atomicCAS(err, 0, 22); return false; }
+        if (v < 0 && -v >= epoch) { atomicCAS(err, 0, 22); return false; }
         if ((i & 15u) == 15u) {
             if (*(volatile int*)err) return false;
             if (global_ns() > deadline) break;
@@ -249,7 +249,12 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         volatile uint32_t* s_ok = s_tmem + 2;
         if (blockIdx.x == 0) {
             // routing of the call: top-k per token (one warp each), then the lookup, with the
-            // (still unused) stage ring as the lookup's scratch
+            // (still unused) stage ring as the lookup's scratch. The mapped routing record is
+            // marked as being rewritten first (the host checks the mark after reading it).
+            if (threadIdx.x == 0) {
+                st_release_sys(mg.host_wseq, mg.epoch);
+                __threadfence_system();
+            }
             for (int t = warp; t < mg.T; t += blockDim.x >> 5)
                 topk_row(mg.logits, t, mg.experts, mg.top_k, mg.idx, mg.w, mg.idx_out, mg.w_out, mg.nan_flag);
             __syncthreads();
@@ -263,6 +268,18 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             __syncthreads();
             if (threadIdx.x == 0) {
                 *mg.done = 0;
+                // per-call cache counters stay on the device (read back at the handle's safe
+                // points); a NaN logit and an inconsistent cache state are reported to the host
+                const RouteCounts c = *mg.lp.rb.counts;
+                atomicAdd(mg.dstats + 0, (unsigned long long)c.n_hits);
+                atomicAdd(mg.dstats + 1, (unsigned long long)c.n_miss);
+                atomicAdd(mg.dstats + 2, (unsigned long long)c.n_bypass);
+                atomicAdd(mg.dstats + 3, (unsigned long long)c.n_evict);
+                atomicAdd(mg.dstats + 4, (unsigned long long)c.n_fill);
+                atomicAdd(mg.dstats + 5, (unsigned long long)c.n_unique);
+                atomicAdd(mg.dstats + 6, 1ull);
+                if (c.err & 1) *(volatile int*)mg.host_nan = 1;
+                if (c.err & 6) atomicCAS(err, 0, 30);
                 __threadfence_system();
                 st_release_gpu(mg.route_flag, mg.epoch);
                 st_release_sys(mg.host_seq, mg.epoch);

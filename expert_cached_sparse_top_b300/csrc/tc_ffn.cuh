@@ -43,10 +43,16 @@ struct TcMega {
     const __nv_bfloat16* x;      // [T][H]
     __nv_bfloat16* xp;           // grouped activation rows, the W13 B operand
     int32_t* dep_x;              // [entry] rows gathered (zeroed by the lookup)
-    const int32_t* fill_flag;    // [miss rank] epoch once the blob is in place; -epoch: abandoned
+    const int32_t* fill_flag;    // [miss rank] epoch once the blob is in place; a negative value
+                                 // -e with e >= epoch: abandoned
     __nv_bfloat16* out;          // [T][H]
     int32_t* route_flag;         // device word: epoch once the routing is published
     int32_t* host_seq;           // host-mapped word: the same, for the host's poll
+    int32_t* host_wseq;          // host-mapped word: epoch before the call rewrites the mapped
+                                 // routing record (counts, miss list)
+    int32_t* host_nan;           // host-mapped word: set to 1 when a call saw a NaN logit
+    unsigned long long* dstats;  // device counters: hits, misses, bypassed, evictions, fills,
+                                 // unique, calls
     int32_t* done;               // W2 tile quarters written in this call (reset by CTA 0)
     int32_t* err_dev;            // device error word the launch's waits poll (0 = none); a
                                  // nonzero code is copied to TcParams::err as the launch ends

@@ -1,9 +1,10 @@
 """The fused decode kernel (FT_FLAG_FUSED_DECODE: one cooperative launch per forward call
-for top-k, lookup, row gather, expert FFN and combine, miss fills signalled by device
-flags) against the oracle and against the default multi-launch path: routing, per-call
-cache counts and snapshots bit-exact against the LRU simulators, outputs within the
-normwise tolerance of the oracle and bit-identical to the default path's; host-side
-failures end the kernel through its flags (no GPU fault)."""
+for top-k, lookup, row gather, expert FFN and combine; a host fill agent copies the misses
+and sets their device flags, so the call never blocks) against the oracle and against the
+default multi-launch path: routing, per-call cache counts and snapshots bit-exact against
+the LRU simulators, outputs within the normwise tolerance of the oracle and bit-identical
+to the default path's. Failures on the host end the kernel through its flags (no GPU
+fault) and are reported by the next call on the handle."""
 import time
 
 import numpy as np
@@ -215,16 +216,19 @@ def test_fused_nan_logit_is_reported(ft):
     lg = np.zeros((16, 8), dtype=np.float32)
     lg[3, 5] = np.nan
     out = torch.empty((16, cfg.hidden), dtype=torch.bfloat16, device="cuda")
-    assert cache.forward_status(0, x, 16, out, logits=to_dev(lg)) == ft.FT_ERR_INVALID
+    assert cache.forward_status(0, x, 16, out, logits=to_dev(lg)) == ft.FT_OK    # asynchronous
+    torch.cuda.synchronize()
     lg[3, 5] = 0.0
+    assert cache.forward_status(0, x, 16, out, logits=to_dev(lg)) == ft.FT_ERR_INVALID   # reported
     assert cache.forward_status(0, x, 16, out, logits=to_dev(lg)) == ft.FT_OK
+    cache.stats()
     cache.close()
 
 
 def test_fused_injected_fill_failure_ends_the_kernel(ft, monkeypatch):
-    """The host refuses to copy (injected): it marks every pending fill flag abandoned, the
-    kernel's miss tiles see that and the kernel ends with an error code well before its
-    wait bound; the handle then reports FT_ERR_STATE."""
+    """The fill agent refuses to copy (injected): it marks every pending fill flag abandoned,
+    the kernel's miss tiles see that and the kernel ends with an error code well before its
+    wait bound; the next call reports the failure, the one after FT_ERR_STATE."""
     import torch
     cfg = W.config("tiny")
     pool = HostPool(cfg)
@@ -234,17 +238,18 @@ def test_fused_injected_fill_failure_ends_the_kernel(ft, monkeypatch):
     out = torch.empty((16, cfg.hidden), dtype=torch.bfloat16, device="cuda")
     lg = to_dev(np.random.default_rng(2).standard_normal((16, 8)).astype(np.float32))
     t0 = time.perf_counter()
-    assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_CUDA
-    torch.cuda.synchronize()
+    assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_OK             # launched
+    torch.cuda.synchronize()                                 # the kernel ends by itself
     assert time.perf_counter() - t0 < 2.0
+    assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_CUDA       # reported
     assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_STATE
     cache.close()
 
 
 def test_fused_host_wait_timeout(ft, monkeypatch):
-    """The device is kept busy (a finite sleep kernel) past the host's wait limit: the forward
-    returns FT_ERR_TIMEOUT and abandons the call's fill flags, so the kernel, once it runs,
-    ends by itself."""
+    """The device is kept busy (a finite sleep kernel) past the host's wait limit: the fill
+    agent gives up on the call's routing, abandons its fill flags (so the kernel, once it
+    runs, ends by itself), and the next call reports FT_ERR_TIMEOUT."""
     import torch
     cfg = W.config("tiny")
     pool = HostPool(cfg)
@@ -254,8 +259,9 @@ def test_fused_host_wait_timeout(ft, monkeypatch):
     out = torch.empty((16, cfg.hidden), dtype=torch.bfloat16, device="cuda")
     lg = to_dev(np.zeros((16, 8), dtype=np.float32))
     torch.cuda._sleep(int(4e8))          # ~0.2 s of device time
-    assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_TIMEOUT
+    assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_OK             # launched
     torch.cuda.synchronize()
+    assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_TIMEOUT    # reported
     assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_STATE
     cache.close()
 
@@ -270,3 +276,27 @@ def test_fused_rejects_unsupported_configs(ft):
     pool = HostPool(cfg, images=4)
     with pytest.raises(ft.FtError):
         _make(ft, cfg, pool, 8, True)          # more than 32 tokens per call
+
+
+def test_fused_calls_queue_without_host_waits(ft, bf16_pool):
+    """Forty calls issued back to back with no synchronisation in between (misses included):
+    the final cache state, the statistics and the last outputs equal the default path's."""
+    import torch
+    cfg = W.config("decode_bf16")
+    C = W.cache_capacity(cfg)
+    caches = [_make(ft, cfg, bf16_pool, C, fused) for fused in (False, True)]
+    steps = list(W.decode_trace(cfg, steps=40))
+    xs = [(to_dev_bf16(st[0]["x"]), to_dev(st[0]["logits"]), st[0]["T"]) for st in steps]
+    outs = [[torch.empty((16, cfg.hidden), dtype=torch.bfloat16, device="cuda") for _ in steps]
+            for _ in caches]
+    for ci, cache in enumerate(caches):
+        for i, (x, lg, T) in enumerate(xs):
+            cache.forward(0, x, T, outs[ci][i], logits=lg)
+    torch.cuda.synchronize()
+    for i, (_, _, T) in enumerate(xs):
+        assert torch.equal(outs[0][i][:T], outs[1][i][:T])
+    assert caches[0].stats() == caches[1].stats()
+    s0, s1 = caches[0].snapshot(), caches[1].snapshot()
+    assert np.array_equal(s0[0], s1[0]) and np.array_equal(s0[1], s1[1])
+    for c in caches:
+        c.close()
