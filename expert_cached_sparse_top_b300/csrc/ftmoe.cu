@@ -1116,6 +1116,10 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
     mg.dstats = h->d_dstats;
     mg.done = h->d_mega + 1;
     mg.err_dev = h->d_mega + 2;
+    mg.arena = h->d_arena;
+    mg.blob_bytes = h->lay.blob_bytes;
+    mg.off_w13 = h->lay.off_w13;
+    mg.off_w2 = h->lay.off_w2;
     mg.epoch = epoch;
     mg.wait_ns = std::min<int64_t>(h->wait_ms, 4000) * 1000000;
     const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};

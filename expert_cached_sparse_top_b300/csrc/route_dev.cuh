@@ -18,6 +18,8 @@ __device__ __forceinline__ bool topk_better(float av, int ai, float bv, int bi) 
 // Top-k + softmax over the chosen for token t, by the calling warp. Lane l holds logits
 // l, l+32, ...; each of the k rounds takes the warp-wide best (value descending, index
 // ascending). NaN logits count as -inf and raise bit 0 of *nan_flag.
+// NV = logits held per lane (E <= 32 * NV).
+template <int NV = kMaxExperts / 32>
 __device__ __forceinline__ void topk_row(const float* __restrict__ logits, int t, int E, int k,
                                          int32_t* __restrict__ idx, float* __restrict__ w,
                                          int32_t* __restrict__ idx2, float* __restrict__ w2,
@@ -25,10 +27,10 @@ __device__ __forceinline__ void topk_row(const float* __restrict__ logits, int t
 
     const int lane = threadIdx.x & 31;
     const float* row = logits + (size_t)t * E;
-    float v[kMaxExperts / 32];
+    float v[NV];
     bool has_nan = false;
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
+    for (int i = 0; i < NV; ++i) {
         int e = lane + 32 * i;
         float val = -INFINITY;
         if (e < E) {
@@ -45,7 +47,7 @@ __device__ __forceinline__ void topk_row(const float* __restrict__ logits, int t
         float bv = -INFINITY;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
+        for (int i = 0; i < NV; ++i) {
             int e = lane + 32 * i;
             if (e < E && !((taken >> i) & 1u) && topk_better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
         }

@@ -56,6 +56,8 @@ struct TcMega {
     int32_t* done;               // W2 tile quarters written in this call (reset by CTA 0)
     int32_t* err_dev;            // device error word the launch's waits poll (0 = none); a
                                  // nonzero code is copied to TcParams::err as the launch ends
+    const uint8_t* arena;        // weight slots (for the L2 prefetch of each CTA's first tile)
+    int64_t blob_bytes, off_w13, off_w2;
     int32_t epoch;               // > 0, increases per call
     int64_t wait_ns;             // bound of every wait in the launch
 };
