@@ -36,6 +36,7 @@ struct RouteBuffers {
     int32_t* dep;          // [max_u] per-entry W13 completion counters of the fused FFN (zeroed here)
     int32_t* dep_x;        // [max_u] per-entry split-row counters of the fused FP4 FFN (zeroed here)
     int32_t* dep_a;        // [max_u] per-entry W2-pieces-ready flags of the fused FP4 FFN (zeroed here)
+    int32_t* tile_ctr;     // [4] tile-claim counters of the BF16 FFN launches of a call (zeroed here)
 };
 
 // Host-mapped mirror of the fill list (the host issues one copy per miss).

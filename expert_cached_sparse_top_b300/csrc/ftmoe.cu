@@ -749,7 +749,8 @@ ft_status alloc_prefill(ft_moe* h) {
         h->p_rb.entry_dst = (int32_t*)p; p += 4 * E;
         h->p_rb.entry_off = (int32_t*)p; p += 4 * (E + 1);
         h->p_rb.pairs = (int32_t*)p; p += 4 * (size_t)npairs;
-        h->p_rb.dep = (int32_t*)p;
+        h->p_rb.dep = (int32_t*)p; p += 4 * E;
+        h->p_rb.tile_ctr = (int32_t*)p;
     }
     FT_CUDA(h, dm((void**)&h->d_p_act, (size_t)h->p_rows * I * 2));
     FT_CUDA(h, dm((void**)&h->d_p_y, (size_t)npairs * H * 4));
@@ -959,7 +960,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->rb.miss_dst = (int32_t*)p; p += 4 * mu;
         h->rb.dep = (int32_t*)p; p += 4 * mu;
         h->rb.dep_x = (int32_t*)p; p += 4 * mu;
-        h->rb.dep_a = (int32_t*)p;
+        h->rb.dep_a = (int32_t*)p; p += 4 * mu;
+        h->rb.tile_ctr = (int32_t*)p;
         const size_t hbytes = 256 + 8 * mu + 64 + 64 + 64;
         if (cudaHostAlloc((void**)&h->h_mapped, hbytes, cudaHostAllocMapped) != cudaSuccess) {
             cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(route view)"); return bail(FT_ERR_OOM);
@@ -1093,6 +1095,7 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
     tp.y_ld = H;
     tp.err = h->d_ffn_err;
     tp.dep = h->rb.dep;
+    tp.tile_ctr = h->rb.tile_ctr;
     TcMega mg{};
     mg.logits = lg;
     mg.T = T;
@@ -1298,6 +1301,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         tp.pass = pass;
         tp.hidden = H; tp.inter = c.inter;
         const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};
+        tp.tile_ctr = h->rb.tile_ctr + 2 * pass;
         if (h->tc_fused) {
             tp.phases = 3; tp.dep = h->rb.dep;
             launches += 1;
@@ -1308,6 +1312,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         cudaError_t e = tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
         if (e != cudaSuccess) return e;
         tp.phases = 2;
+        tp.tile_ctr = h->rb.tile_ctr + 2 * pass + 1;
         launches += 2;
         return tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
     };
@@ -1454,6 +1459,7 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         tp.err = h->d_ffn_err;
         tp.hidden = H; tp.inter = I;
         const TcMaps maps{&h->tmP_A13[b], &h->tmP_B13[bi], &h->tmP_A2[b], &h->tmP_B2[bi]};
+        tp.tile_ctr = h->p_rb.tile_ctr;
         if (h->tc_fused) {
             tp.phases = 3; tp.dep = h->p_rb.dep;
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
@@ -1461,6 +1467,7 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             tp.phases = 1;
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
             tp.phases = 2;
+            tp.tile_ctr = h->p_rb.tile_ctr + 1;
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
         }
     } else if (h->use_fp4_prefill) {

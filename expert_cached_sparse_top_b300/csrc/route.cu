@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(1024, 1) sort_scan_kernel(int32_t* __restrict_
                                                             int E, int n_pairs, RouteBuffers rb) {
     __shared__ int s_warp[33];
     const int e = threadIdx.x;
+    if (e < 4 && rb.tile_ctr) rb.tile_ctr[e] = 0;
     int total = 0;
     if (e < E) {
         for (int c = 0; c < n_chunks; ++c) {

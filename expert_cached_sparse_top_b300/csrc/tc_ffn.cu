@@ -112,6 +112,7 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
 // K steps into its own accumulator (the epilogue adds them): a single thread issuing every
 // small-N tcgen05.mma cannot keep up with the weight stream.
 template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
+constexpr int kTQ = 4;             // claimed-tile ring depth
 template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 32 : kThreads; }
 
 template <int BN, bool MK> constexpr int tc_block() { return MK ? 256 : tc_threads<BN>(); }
@@ -202,6 +203,14 @@ __device__ __forceinline__ Tile tile_in(int t, const int* s_nt, int e_lo, int n,
     return r;
 }
 
+// Routing arrays of the launch: the fused call's CTA 0 writes them during the launch (L2
+// loads); otherwise they were written before it (ordinary cached loads).
+template <bool MK>
+__device__ __forceinline__ int ldr(const int32_t* p) {
+    if constexpr (MK) return __ldcg(p);
+    else return *p;
+}
+
 // Entry of grouped row r: the last u with entry_off[u] <= r.
 __device__ __forceinline__ int entry_of_row(const int32_t* entry_off, int n_entries, int r) {
     int lo = 0, hi = n_entries - 1;
@@ -285,8 +294,11 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;       // [2]
     uint64_t* tempty = tfull + 2;      // [2]
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
-    int* s_nt = reinterpret_cast<int*>(s_tmem + 4);   // [kMaxExperts + 1] N-tile prefix
+    uint64_t* tq_full = tempty + 2;    // [kTQ] claimed tile ids: producer -> MMA, epilogue
+    uint64_t* tq_empty = tq_full + kTQ;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tq_empty + kTQ);
+    int* s_tile = reinterpret_cast<int*>(s_tmem + 4);  // [kTQ]
+    int* s_nt = s_tile + kTQ;                          // [kMaxExperts + 1] N-tile prefix
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the fused call's waits poll a device word (the host-mapped p.err would put a PCIe read
@@ -372,10 +384,10 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     if constexpr (MK) {
         // gather this CTA's share of the grouped activation rows: xp[r] = x[pairs[r] / k];
         // each finished row counts toward its entry (the W13 tiles wait for all of them)
-        const int R = __ldcg(p.entry_off + n_entries);
+        const int R = ldr<MK>(p.entry_off + n_entries);
         const int cpr = H / 8;
         for (int r = blockIdx.x; r < R; r += gridDim.x) {
-            const int tok = __ldcg(p.pairs + r) / mg.top_k;
+            const int tok = ldr<MK>(p.pairs + r) / mg.top_k;
             const uint4* src = reinterpret_cast<const uint4*>(mg.x + (int64_t)tok * H);
             uint4* dst = reinterpret_cast<uint4*>(mg.xp + (int64_t)r * H);
             for (int c = threadIdx.x; c < cpr; c += blockDim.x) dst[c] = __ldg(src + c);
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
 
     // N-tile prefix over this launch's entries: counts in parallel, then one warp scans
     for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
-        const int n = __ldcg(p.entry_off + u_begin + i + 1) - __ldcg(p.entry_off + u_begin + i);
+        const int n = ldr<MK>(p.entry_off + u_begin + i + 1) - ldr<MK>(p.entry_off + u_begin + i);
         s_nt[i] = (n + BN - 1) / BN;
     }
     __syncthreads();
@@ -410,6 +422,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NI); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
+        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 4); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -441,16 +454,26 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
 
     if (warp == 0) {
         if (lane == 0) {
+            // tiles are claimed from the launch's counter when the producer is ready for the
+            // next one (claiming ahead would hand two tiles to one CTA while others idle) and
+            // handed to the MMA and epilogue warps in claim order
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (uint32_t q = 0; ok; ++q) {
+                const int ts = (int)(q % kTQ);
+                if (!bar_wait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 7)) { ok = false; break; }
+                const int claimed = atomicAdd(p.tile_ctr, 1);
+                const int t = claimed < total ? claimed : -1;
+                s_tile[ts] = t;
+                mbar_arrive(&tq_full[ts]);
+                if (t < 0) break;
                 const Tile tl = tile(t);
                 const bool w13 = tl.phase == 13;
                 const CUtensorMap* mA = w13 ? &tmA13 : &tmA2;
                 const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
                 const int k_steps = (w13 ? H : I) / kBK;
-                const int slot = __ldcg(p.entry_dst + tl.u);
-                const int row_b = __ldcg(p.entry_off + tl.u) + tl.nt * BN;
+                const int slot = ldr<MK>(p.entry_dst + tl.u);
+                const int row_b = ldr<MK>(p.entry_off + tl.u) + tl.nt * BN;
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed; W13
                     // activation rows only once the entry's rows are gathered
@@ -459,7 +482,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                         break;
                     }
                     if (w13) {
-                        const int rows = __ldcg(p.entry_off + tl.u + 1) - __ldcg(p.entry_off + tl.u);
+                        const int rows = ldr<MK>(p.entry_off + tl.u + 1) - ldr<MK>(p.entry_off + tl.u);
                         if (!wait_ge_until(mg.dep_x + tl.u, rows, err, 23, deadline, 256)) { ok = false; break; }
                     }
                     fence_proxy_async_global();
@@ -521,15 +544,20 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         const int par = warp == 6 ? 1 : 0;
         constexpr int KK = 4 / NI;                    // K steps per stage for this issuer
         if (lane == 0) {
-            uint32_t it = 0, tcount = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const int ts = (int)(tcount % kTQ);
+                if (!bar_wait(&tq_full[ts], (tcount / kTQ) & 1u, 8)) break;
+                const int t = s_tile[ts];
+                mbar_arrive(&tq_empty[ts]);
+                if (t < 0) break;
                 const Tile tl = tile(t);
                 const int k_steps = (tl.phase == 13 ? H : I) / kBK;
                 // N of this tile: its token count rounded up to 16 (a tail tile does no
                 // padded work); the accumulator keeps BN columns
-                const int row_b = __ldcg(p.entry_off + tl.u) + tl.nt * BN;
-                const int n_valid = min(BN, __ldcg(p.entry_off + tl.u + 1) - row_b);
+                const int row_b = ldr<MK>(p.entry_off + tl.u) + tl.nt * BN;
+                const int n_valid = min(BN, ldr<MK>(p.entry_off + tl.u + 1) - row_b);
                 const uint32_t idesc = idesc_bf16(min(BN, (n_valid + 15) & ~15));
                 const uint32_t acc = tcount & 1u;
                 const uint32_t aph = (tcount >> 1) & 1u;
@@ -559,13 +587,18 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
-        uint32_t tcount = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+        for (uint32_t tcount = 0;; ++tcount) {
+            const int ts = (int)(tcount % kTQ);
+            if (!bar_wait(&tq_full[ts], (tcount / kTQ) & 1u, 9)) break;
+            const int t = s_tile[ts];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tq_empty[ts]);
+            if (t < 0) break;
             const Tile tl = tile(t);
             const bool w13 = tl.phase == 13;
             const int m_rows = w13 ? 2 * I : H;
-            const int row_b = __ldcg(p.entry_off + tl.u) + tl.nt * BN;
-            const int n_valid = min(BN, __ldcg(p.entry_off + tl.u + 1) - row_b);
+            const int row_b = ldr<MK>(p.entry_off + tl.u) + tl.nt * BN;
+            const int n_valid = min(BN, ldr<MK>(p.entry_off + tl.u + 1) - row_b);
             const uint32_t acc = tcount & 1u;
             const uint32_t aph = (tcount >> 1) & 1u;
             if (!bar_wait(&tfull[acc], aph, 4)) break;
@@ -606,13 +639,13 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                         }
                     }
                 } else {
+                    // the chunk's 16 (token, rank) pairs: one load per lane, then broadcast
+                    const int my_pair = (lane < 16 && c0 + lane < n_valid) ? ldr<MK>(p.pairs + row_b + c0 + lane) : 0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = c0 + j;
-                        if (n < n_valid && m < m_rows) {
-                            const int pair = __ldcg(p.pairs + row_b + n);
-                            p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
-                        }
+                        const int pair = __shfl_sync(0xffffffffu, my_pair, j);
+                        if (n < n_valid && m < m_rows) p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
                     }
                 }
             }
@@ -726,7 +759,8 @@ int stages_for() {
 template <int BN>
 size_t smem_for(int stages) {
     const size_t stage = 128 * 64 * 2 + BN * 64 * 2;
-    return 1024 + stages * stage + (2 * stages + 4) * 8 + 16 + (kMaxExperts + 1) * 4;
+    return 1024 + stages * stage + (2 * stages + 4 + 2 * tc::kTQ) * 8 + 16 + tc::kTQ * 4 +
+           (kMaxExperts + 1) * 4;
 }
 
 template <int BN>
@@ -828,6 +862,7 @@ cudaError_t tc_encode_acts(CUtensorMap* map, const void* base, int k_dim, int ro
 }
 
 cudaError_t tc_launch(int bn, const TcParams& p, const TcMaps& m, int grid, cudaStream_t s) {
+    if (!p.tile_ctr) return cudaErrorInvalidValue;
 #define FT_TC_CASE(BNV)                                                              \
     case BNV:                                                                        \
         return launch_bn<BNV>(p, m, grid, s);
@@ -844,7 +879,7 @@ cudaError_t tc_launch(int bn, const TcParams& p, const TcMaps& m, int grid, cuda
 
 cudaError_t tc_launch_mega(int bn, const TcParams& p, const TcMega& mg, const TcMaps& m, int grid,
                            cudaStream_t s) {
-    if (mg.experts < 1 || mg.experts > tc::tc_block<16, true>() || mg.epoch <= 0 || grid < 1)
+    if (mg.experts < 1 || mg.experts > tc::tc_block<16, true>() || mg.epoch <= 0 || grid < 1 || !p.tile_ctr)
         return cudaErrorInvalidValue;
     if (bn == 16) return launch_mega<16>(p, mg, m, grid, s);
     if (bn == 32) return launch_mega<32>(p, mg, m, grid, s);

@@ -22,6 +22,8 @@ struct TcParams {
     int* err;                    // nonzero if a bounded wait ran out
     int32_t* dep;                // per-entry count of published W13 tile quarters (phases 3),
                                  // zeroed by the routing kernels before the launch
+    int32_t* tile_ctr;           // tile-claim counter of this launch, zero at launch (the
+                                 // routing kernels reset it)
 };
 
 // The fused decode call (one cooperative launch of the BF16 FFN kernel with every CTA
