@@ -36,7 +36,7 @@ def _rank(rank, ws, port, out):
 
 def test_two_replicas_max_time_and_whole_job_throughput():
     ws = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(ws, _free_port(), out), nprocs=ws, join=True,
                            start_method="spawn")
