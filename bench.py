@@ -385,12 +385,15 @@ def run_ours(args):
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     if args.ffn_traffic:
         # the cached pass alone, every FFN launch counted from the first call (an ncu capture
-        # of the FFN kernel over this run divides its DRAM bytes by these)
-        cache = make(C)
+        # of the FFN kernel over this run divides its DRAM bytes by these); with --all-resident
+        # every selected expert is placed before the first call (no fill ever)
+        cache = make(len(touched) if args.all_resident else C)
+        if args.all_resident:
+            cache.pin(touched)
         cache.set_timing(True)
         cache.timing(reset=True)
         for i in range(Wm + K):
-            if i in resizes:
+            if i in resizes and not args.all_resident:
                 cache.resize(resizes[i])
             run_step(cache, i)
         torch.cuda.synchronize()
@@ -742,6 +745,8 @@ def main():
     ap.add_argument("--ffn-traffic", action="store_true",
                     help="decode: run the cached pass only and print the FFN launches and their "
                          "algorithmic bytes (the denominator of an ncu traffic capture)")
+    ap.add_argument("--all-resident", action="store_true",
+                    help="with --ffn-traffic: every selected expert resident (no fills)")
     ap.add_argument("--fused", action="store_true",
                     help="decode through the fused decode kernel (FT_FLAG_FUSED_DECODE; BF16)")
     ap.add_argument("--workload", default=WORKLOAD,
