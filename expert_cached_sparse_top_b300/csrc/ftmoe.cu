@@ -1290,6 +1290,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         if (h->use_fp4) {
             // one launch: activation pieces, W13 + SwiGLU, W2 pieces, W2
             f4.pass = pass;
+            f4.tile_ctr = h->rb.tile_ctr + 2 * pass;
             launches += 1;
             const Fp4Maps maps{&h->tmF_A13, &h->tmF_B13, &h->tmF_A2, &h->tmF_B2};
             return fp4_launch(c.wfmt, h->fp4_bn, f4, maps, h->num_sms, s);
@@ -1500,6 +1501,7 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.y = h->d_p_y;
         f4.cnt_w13 = h->p_rb.dep;
         f4.err = h->d_ffn_err;
+        f4.tile_ctr = h->p_rb.tile_ctr;
         const Fp4Maps maps{&h->tmPF_A13[b], &h->tmPF_B13, &h->tmPF_A2[b], &h->tmPF_B2};
         FT_CUDA(h, fp4_launch(c.wfmt, bn, f4, maps, h->num_sms, s));
     } else {

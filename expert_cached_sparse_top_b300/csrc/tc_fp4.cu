@@ -46,6 +46,7 @@ template <int P, int BN> struct Fp4Cfg {
     static constexpr int THREADS = NI == 2 ? 224 : 192;
 };
 constexpr int kABytes = 128 * 128;           // one 128-row weight tile of a stage
+constexpr int kTQ = 4;                        // claimed-tile ring depth
 
 __device__ __forceinline__ int exp_of(float v) {
     // floor(log2|v|) for normal v; a large negative number for zero and subnormals
@@ -276,13 +277,17 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* tq_full = tempty + 2;                              // [kTQ] claimed tile ids
+    uint64_t* tq_empty = tq_full + kTQ;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tq_empty + kTQ);
     int* s_flag = reinterpret_cast<int*>(s_tmem + 1);
     int* s_eoff = reinterpret_cast<int*>(s_tmem + 4);          // [kMaxExperts + 1]
     int* s_tp = s_eoff + (kMaxExperts + 1);                      // [kMaxExperts + 1]
     float* s_red = reinterpret_cast<float*>(s_tp + (kMaxExperts + 1));   // [8]
     float* s_stage = s_red + 8;                                          // [BN][65] SwiGLU values
     int* s_got = reinterpret_cast<int*>(s_stage + BN * 65);                // [2][4] epilogue votes
+    int* s_tile = s_got + 8;                                               // [kTQ] tile ids
+    int* s_tvote = s_tile + kTQ;                                           // [2][4] tile-id votes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RouteCounts rc = *p.counts;
@@ -316,6 +321,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
         // a stage is free, and an accumulator full, once every MMA issuer has committed
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NI); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
+        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 4); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -352,9 +358,20 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
 
     if (warp == 0) {
         if (lane == 0) {
+            // decode: tiles are claimed from the launch's counter when the producer is ready for
+            // the next one; prefill (one piece, ~25 tiles per CTA): a fixed round robin, which
+            // measured faster there. Either way they reach the MMA issuers and the epilogue in
+            // claim order.
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (uint32_t q = 0; ok; ++q) {
+                const int ts = (int)(q % kTQ);
+                if (!mbar_wait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, err, 8)) { ok = false; break; }
+                const int claimed = P > 1 ? atomicAdd(p.tile_ctr, 1) : (int)(blockIdx.x + q * gridDim.x);
+                const int t = claimed < total ? claimed : -1;
+                s_tile[ts] = t;
+                mbar_arrive(&tq_full[ts]);
+                if (t < 0) break;
                 const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
                 const int K = tl.w13 ? H : I;
                 const int k_stages = K / kStageK;
@@ -425,9 +442,14 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
         constexpr int HA = APS / NI;                  // scale atoms per operand per issuer
         constexpr int KK = 4 / NI;                    // K steps per stage per issuer
         if (lane == 0) {
-            uint32_t it = 0, tcount = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const int ts = (int)(tcount % kTQ);
+                if (!mbar_wait(&tq_full[ts], (tcount / kTQ) & 1u, err, 9)) break;
+                const int t = s_tile[ts];
+                mbar_arrive(&tq_empty[ts]);
+                if (t < 0) break;
                 const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
                 const int k_stages = (tl.w13 ? H : I) / kStageK;
                 const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
@@ -472,8 +494,19 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
         const int q = warp & 3;
         const int etid = threadIdx.x - 64;                 // 0..127 over the epilogue warps
         const int row_in_tile = q * 32 + lane;
-        uint32_t tcount = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+        for (uint32_t tcount = 0;; ++tcount) {
+            // the next claimed tile id; the four warps vote on the wait's outcome so that they
+            // leave the loop together (they meet at named barriers below)
+            const int ts = (int)(tcount % kTQ);
+            const bool have = mbar_wait(&tq_full[ts], (tcount / kTQ) & 1u, err, 10);
+            int* tv = s_tvote + (tcount & 1u) * 4;
+            if (lane == 0) tv[q] = have ? 1 : 0;
+            named_bar(1, 128);
+            if (!(tv[0] && tv[1] && tv[2] && tv[3])) break;
+            const int t = s_tile[ts];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tq_empty[ts]);
+            if (t < 0) break;
             const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
             const int nt = tl.g - s_tp[tl.u];
             const int row_b = s_eoff[tl.u] + nt * BN;
@@ -704,7 +737,8 @@ template <int BN, int FMT, int P>
 cudaError_t launch_t(const Fp4Params& p0, const Fp4Maps& m, int grid, cudaStream_t s) {
     Fp4Params p = p0;
     p.stage_bytes = stage_bytes_for(FMT, BN, p.pieces);
-    const size_t fixed = 1024 + 4 * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + BN * 65 * 4 + 32 + 64;
+    const size_t fixed = 1024 + (4 + 2 * fp4::kTQ) * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + BN * 65 * 4 + 32 +
+                         (fp4::kTQ + 8) * 4 + 64;
     p.stages = (int)((kSmemLimit - fixed) / (p.stage_bytes + 16));
     if (p.stages > 8) p.stages = 8;
     if (p.stages < 2) return cudaErrorInvalidValue;
@@ -760,7 +794,7 @@ cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int
 }
 
 cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, int grid, cudaStream_t s) {
-    if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1) return cudaErrorInvalidValue;
+    if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1 || !p.tile_ctr) return cudaErrorInvalidValue;
     if (fmt != FT_W_MXFP4 && fmt != FT_W_NVFP4) return cudaErrorInvalidValue;
     const bool mx = fmt == FT_W_MXFP4;
     // decode: four pieces, 16- or 32-token tiles; prefill: one MXFP4 piece, 128-token tiles

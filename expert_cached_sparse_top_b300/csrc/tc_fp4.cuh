@@ -43,6 +43,7 @@ struct Fp4Params {
     float* y;                    // [pair][hidden] fp32 expert outputs
     int32_t* cnt_x;              // [entry] rows split (zeroed by the routing kernels)
     int32_t* cnt_w13;            // [entry] W13 tiles finished (zeroed by the routing kernels)
+    int32_t* tile_ctr;           // tile-claim counter of this launch (zeroed by the routing kernels)
     int* err;                    // nonzero if a bounded wait ran out
 };
 
