@@ -487,8 +487,10 @@ def run_ours(args):
         roof_gbs, roof_on = r_achieved, "the all-resident pass (the fused kernel waits for fills)"
         bpl = rtim["ffn_weight_bytes"] / max(rtim["ffn_launches"], 1)
         ffn_ms, ffn_passes = rffn_ms, rtim["ffn_launches"]
-    kern = ("fused decode kernel (one cooperative launch per call: top-k, LRU lookup, row gather, "
-            "tcgen05 W13+SwiGLU and W2, combine; missed experts' tiles wait for their PCIe fills)"
+    kern = ("fused decode kernel (one cooperative launch per call: top-k, LRU lookup, %s, combine; "
+            "missed experts' tiles wait for their PCIe fills)"
+            % ("row gather, tcgen05 W13+SwiGLU and W2" if cfg.wfmt == "bf16" else
+               "activation pieces, block-scaled tcgen05 W13+SwiGLU and W2 on %s codes" % cfg.wfmt.upper())
             if args.fused else
             "expert FFN (tcgen05 grouped GEMM, W13+SwiGLU and W2 in one launch), per pass"
             if cfg.wfmt == "bf16" else

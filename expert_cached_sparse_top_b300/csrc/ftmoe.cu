@@ -998,13 +998,17 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     st = encode_tc_maps(h);
     if (st != FT_OK) return bail(st);
     if (cfg->flags & FT_FLAG_FUSED_DECODE) {
-        if (!h->use_tc || !h->tc_fused || h->tc_bn > 32 || E > 256) {
-            fail(h, FT_ERR_INVALID, "FT_FLAG_FUSED_DECODE needs BF16 weights, experts <= 256 and max_tokens <= 32");
+        const bool bf16_ok = h->use_tc && h->tc_fused && h->tc_bn <= 32;
+        const bool fp4_ok = h->use_fp4 && h->fp4_bn == 16 && h->fp4_pieces == kFp4MaxPieces;
+        if (!(bf16_ok || fp4_ok) || E > 256) {
+            fail(h, FT_ERR_INVALID, "FT_FLAG_FUSED_DECODE needs experts <= 256 and max_tokens <= 32 (BF16) "
+                                    "or <= 16 (MXFP4, NVFP4)");
             return bail(FT_ERR_INVALID);
         }
         int coop = 0;
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->dev);
-        h->mega_grid = std::min(tc_mega_grid(h->tc_bn, h->num_sms), h->num_sms);
+        h->mega_grid = std::min(h->use_fp4 ? fp4_mega_grid(cfg->wfmt, h->num_sms)
+                                           : tc_mega_grid(h->tc_bn, h->num_sms), h->num_sms);
         cudaGetLastError();
         if (!coop || !stream_write_fn() || h->mega_grid < 1) {
             fail(h, FT_ERR_INVALID, "FT_FLAG_FUSED_DECODE: no cooperative launch or stream memory writes on this device");
@@ -1125,9 +1129,39 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
     mg.off_w2 = h->lay.off_w2;
     mg.epoch = epoch;
     mg.wait_ns = std::min<int64_t>(h->wait_ms, 4000) * 1000000;
-    const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
-    FT_CUDA(h, tc_launch_mega(h->tc_bn, tp, mg, maps, h->mega_grid, s));
+    if (h->use_fp4) {
+        Fp4Params f4{};
+        f4.counts = h->rb.counts;
+        f4.entry_off = h->rb.entry_off;
+        f4.entry_dst = h->rb.entry_dst;
+        f4.pairs = h->rb.pairs;
+        f4.pass = 2;
+        f4.hidden = H;
+        f4.inter = c.inter;
+        f4.top_k = k;
+        f4.pieces = h->fp4_pieces;
+        f4.x_ready = 0;
+        f4.arena = h->d_arena;
+        f4.blob_bytes = h->lay.blob_bytes;
+        f4.off_s13 = h->lay.off_s13;
+        f4.off_s2 = h->lay.off_s2;
+        f4.off_ts = h->lay.off_ts;
+        f4.x = (const __nv_bfloat16*)x;
+        f4.xq = h->d_xq; f4.xsf = h->d_xsf; f4.xrs = h->d_xrs;
+        f4.aq = h->d_aq; f4.asf = h->d_asf;
+        f4.act = h->d_act;
+        f4.y = h->d_y;
+        f4.cnt_x = h->rb.dep_x;
+        f4.cnt_w13 = h->rb.dep;
+        f4.tile_ctr = h->rb.tile_ctr;
+        f4.err = h->d_ffn_err;
+        const Fp4Maps fmaps{&h->tmF_A13, &h->tmF_B13, &h->tmF_A2, &h->tmF_B2};
+        FT_CUDA(h, fp4_launch_mega(c.wfmt, f4, mg, fmaps, h->mega_grid, s));
+    } else {
+        const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};
+        FT_CUDA(h, tc_launch_mega(h->tc_bn, tp, mg, maps, h->mega_grid, s));
+    }
     ++launches;
     *curp ^= 1;
     if (h->timing) {

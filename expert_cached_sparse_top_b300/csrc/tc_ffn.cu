@@ -24,42 +24,12 @@
 #include "tc_ffn.cuh"
 #include "tc_ptx.cuh"
 #include "route_dev.cuh"
+#include "mk.cuh"
 
 #include <cuda.h>
 
 namespace ftmoe {
 namespace tc {
-
-struct TileMap {
-    int u_begin, n_entries;
-    int m_tiles;
-    int total;
-};
-
-// Locate tile t: entries are visited in order; within an entry, N tiles, then M tiles
-// (M innermost so that concurrently running CTAs share the entry's activation rows in L2).
-__device__ __forceinline__ void locate(const int* s_prefix, int n_entries, int m_tiles, int t,
-                                       int* u_rel, int* mt, int* nt) {
-    int lo = 0, hi = n_entries - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (s_prefix[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    int r = t - s_prefix[lo];
-    *u_rel = lo;
-    *nt = r / m_tiles;
-    *mt = r % m_tiles;
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 // Bounded wait until every W13 tile of an entry has published its activation rows.
 __device__ __forceinline__ bool wait_dep(const int* dep, int target, int* err) {
@@ -117,70 +87,6 @@ template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThrea
 
 template <int BN, bool MK> constexpr int tc_block() { return MK ? 256 : tc_threads<BN>(); }
 
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_release_sys(int* p, int v) {
-    asm volatile("st.release.sys.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
-// Wait (up to the deadline) until *p >= target, polling with a short back-off; records
-// `code` and returns false on time-out, or as soon as another role recorded an error.
-__device__ __forceinline__ bool wait_ge_until(const int* p, int target, int* err, int code,
-                                              uint64_t deadline, uint32_t max_ns) {
-    uint32_t ns = 32;
-    for (uint32_t i = 0;; ++i) {
-        if (ld_acquire(p) >= target) return true;
-        if ((i & 15u) == 15u) {
-            if (*(volatile int*)err) return false;
-            if (global_ns() > deadline) break;
-        }
-        __nanosleep(ns);
-        if (ns < max_ns) ns <<= 1;
-    }
-    atomicCAS(err, 0, code);
-    return false;
-}
-
-// Fill flag of one missed expert: epoch once its blob is in place; -e with e >= epoch once
-// the host abandoned this call (and any later one) before copying it.
-__device__ __forceinline__ bool wait_fill_until(const int* p, int epoch, int* err, uint64_t deadline) {
-    uint32_t ns = 64;
-    for (uint32_t i = 0;; ++i) {
-        const int v = ld_acquire(p);
-        if (v == epoch) return true;
-        if (v < 0 && -v >= epoch) { atomicCAS(err, 0, 22); return false; }
-        if ((i & 15u) == 15u) {
-            if (*(volatile int*)err) return false;
-            if (global_ns() > deadline) break;
-        }
-        __nanosleep(ns);
-        if (ns < 1024) ns <<= 1;
-    }
-    atomicCAS(err, 0, 21);
-    return false;
-}
-
-__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, int* err, int code,
-                                                uint64_t deadline) {
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 1023u) == 1023u) {
-            if (*(volatile int*)err) return false;
-            if (global_ns() > deadline) break;
-        }
-    }
-    atomicCAS(err, 0, code);
-    return false;
-}
-
 // Tile t of one group of entries [e_lo, e_lo + n) whose N-tile prefix is s_nt (absolute):
 // W13 tiles of the group's entries first, then its W2 tiles (order as in tile_at).
 __device__ __forceinline__ Tile tile_in(int t, const int* s_nt, int e_lo, int n, int m13, int m2) {
@@ -201,14 +107,6 @@ __device__ __forceinline__ Tile tile_in(int t, const int* s_nt, int e_lo, int n,
     r.nt = rr / m_tiles;
     r.mt = rr % m_tiles;
     return r;
-}
-
-// Routing arrays of the launch: the fused call's CTA 0 writes them during the launch (L2
-// loads); otherwise they were written before it (ordinary cached loads).
-template <bool MK>
-__device__ __forceinline__ int ldr(const int32_t* p) {
-    if constexpr (MK) return __ldcg(p);
-    else return *p;
 }
 
 // Entry of grouped row r: the last u with entry_off[u] <= r.
@@ -305,72 +203,15 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     // in every poll); thread 0 of each CTA copies a code to p.err as the CTA leaves
     int* err = MK ? mg.err_dev : p.err;
     auto report = [&]() {
-        if (MK && threadIdx.x == 0) {
-            const int e = *(volatile int*)err;
-            if (e) atomicCAS(p.err, 0, e);
-        }
+        if constexpr (MK) mk_report(err, p.err);
     };
     uint64_t deadline = 0;
     if constexpr (MK) {
-        volatile uint32_t* s_ok = s_tmem + 2;
-        if (blockIdx.x == 0) {
-            // routing of the call: top-k per token (one warp each), then the lookup, with the
-            // (still unused) stage ring as the lookup's scratch. The mapped routing record is
-            // marked as being rewritten first (the host checks the mark after reading it).
-            if (threadIdx.x == 0) {
-                st_release_sys(mg.host_wseq, mg.epoch);
-                __threadfence_system();
-            }
-            for (int t = warp; t < mg.T; t += blockDim.x >> 5)
-                topk_row<8>(mg.logits, t, mg.experts, mg.top_k, mg.idx, mg.w, mg.idx_out, mg.w_out, mg.nan_flag);
-            __syncthreads();
-            int* sc = reinterpret_cast<int*>(smem);
-            const int E = mg.experts;
-            const LookupScratch ls{sc, sc + E, sc + 2 * E, sc + 3 * E, sc + 4 * E, sc + 5 * E,
-                                   sc + 5 * E + 33, sc + 5 * E + 34};
-            lookup_block(mg.lp, ls);
-            // the scratch is stage ring memory the TMA (async proxy) writes next
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                *mg.done = 0;
-                // per-call cache counters stay on the device (read back at the handle's safe
-                // points); a NaN logit and an inconsistent cache state are reported to the host
-                const RouteCounts c = *mg.lp.rb.counts;
-                atomicAdd(mg.dstats + 0, (unsigned long long)c.n_hits);
-                atomicAdd(mg.dstats + 1, (unsigned long long)c.n_miss);
-                atomicAdd(mg.dstats + 2, (unsigned long long)c.n_bypass);
-                atomicAdd(mg.dstats + 3, (unsigned long long)c.n_evict);
-                atomicAdd(mg.dstats + 4, (unsigned long long)c.n_fill);
-                atomicAdd(mg.dstats + 5, (unsigned long long)c.n_unique);
-                atomicAdd(mg.dstats + 6, 1ull);
-                if (c.err & 1) *(volatile int*)mg.host_nan = 1;
-                if (c.err & 6) atomicCAS(err, 0, 30);
-                __threadfence_system();
-                st_release_gpu(mg.route_flag, mg.epoch);
-                st_release_sys(mg.host_seq, mg.epoch);
-            }
-        } else {
-            mk_prefetch_first_tile<BN>(mg, smem, p.hidden, p.inter);
-        }
-        if (threadIdx.x == 0) {
-            deadline = global_ns() + (uint64_t)mg.wait_ns;
-            *s_ok = wait_ge_until(mg.route_flag, mg.epoch, err, 20, deadline, 256) ? 1u : 0u;
-            // a later epoch cannot appear while this launch runs: the flag is exact
-        }
-        __syncthreads();
-        if (*s_ok == 0) { report(); return; }
-        if (threadIdx.x != 0) deadline = global_ns() + (uint64_t)mg.wait_ns;
+        if (blockIdx.x == 0) mk_route(mg, smem, err);
+        else mk_prefetch_first_tile<BN>(mg, smem, p.hidden, p.inter);
+        if (!mk_wait_route(mg, err, deadline, s_tmem + 2)) { report(); return; }
     }
-    RouteCounts rc;
-    if constexpr (MK) {
-        const int4* c4 = reinterpret_cast<const int4*>(p.counts);
-        const int4 a = __ldcg(c4), b = __ldcg(c4 + 1);
-        rc.n_unique = a.x; rc.n_hits = a.y; rc.n_miss = a.z; rc.n_fill = a.w;
-        rc.n_bypass = b.x; rc.n_evict = b.y; rc.err = b.z; rc.pad = b.w;
-    } else {
-        rc = *p.counts;
-    }
+    const RouteCounts rc = MK ? mk_counts(p.counts) : *p.counts;
     const int u_begin = MK ? 0 : (p.pass == 0 ? 0 : rc.n_hits);
     const int u_end = MK ? rc.n_unique : (p.pass == 0 ? rc.n_hits : rc.n_unique);
     const int n_entries = u_end - u_begin;
@@ -675,37 +516,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                      :: "r"(tmem_base), "r"(TMEM_COLS) : "memory");
     }
     if constexpr (MK) {
-        // combine, once every W2 tile quarter of the call is written: out[t] = sum_j w[t,j] *
-        // y[t*k + j], in rank order (the same arithmetic as the standalone combine)
-        volatile uint32_t* s_ok = s_tmem + 2;
-        if (threadIdx.x == 0)
-            *s_ok = wait_ge_until(mg.done, 4 * m2 * nt_total, err, 24, deadline, 1024) ? 1u : 0u;
-        __syncthreads();
-        if (*s_ok == 0) { report(); return; }
-        const int k = mg.top_k;
-        const int hv = H / 8;
-        const int64_t items = (int64_t)mg.T * hv;
-        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
-             i += (int64_t)gridDim.x * blockDim.x) {
-            const int t = (int)(i / hv), c = (int)(i % hv);
-            float accv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) accv[q] = 0.f;
-            for (int j = 0; j < k; ++j) {
-                const float wj = __ldcg(mg.w + (int64_t)t * k + j);
-                const float4* yr = reinterpret_cast<const float4*>(p.y + ((int64_t)t * k + j) * p.y_ld + c * 8);
-                const float4 a = __ldcg(yr), b = __ldcg(yr + 1);
-                accv[0] = fmaf(wj, a.x, accv[0]); accv[1] = fmaf(wj, a.y, accv[1]);
-                accv[2] = fmaf(wj, a.z, accv[2]); accv[3] = fmaf(wj, a.w, accv[3]);
-                accv[4] = fmaf(wj, b.x, accv[4]); accv[5] = fmaf(wj, b.y, accv[5]);
-                accv[6] = fmaf(wj, b.z, accv[6]); accv[7] = fmaf(wj, b.w, accv[7]);
-            }
-            uint4 o;
-            __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ob[q] = __floats2bfloat162_rn(accv[2 * q], accv[2 * q + 1]);
-            *reinterpret_cast<uint4*>(mg.out + (int64_t)t * H + c * 8) = o;
-        }
+        // combine, once every W2 tile quarter of the call is written
+        mk_combine(mg, p.y, p.y_ld, H, 4 * m2 * nt_total, err, deadline, s_tmem + 2);
         report();
     }
 }

@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "tc_fp4.cuh"
 #include "tc_ptx.cuh"
+#include "mk.cuh"
 #include "../../include/ftmoe.h"
 
 namespace ftmoe {
@@ -178,23 +179,13 @@ __device__ void split_row(const __nv_bfloat16* row, int K, int P, int fmt, uint8
     }
 }
 
-__device__ __forceinline__ int ld_acquire_s32(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Bounded wait until *flag >= target (written by other CTAs of this launch).
 __device__ __forceinline__ bool wait_count(const int* flag, int target, int* err, int code) {
     // back off to ~1 us between polls: many CTAs poll a few flags, and a tight loop floods
     // the L2 slice that also serves the writers
     uint32_t ns = 64;
     for (uint32_t i = 0; i < (kWaitLimit >> 4); ++i) {
-        if (ld_acquire_s32(flag) >= target) return true;
+        if (ld_acquire(flag) >= target) return true;
         if ((i & 63u) == 63u && *(volatile int*)err) return false;
         __nanosleep(ns);
         if (ns < 1024) ns <<= 1;
@@ -258,16 +249,21 @@ __device__ __forceinline__ int entry_of_row(const int* s_eoff, int u_begin, int 
     return lo;
 }
 
-template <int BN, int FMT, int P>
-__global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
-    Fp4Params p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
+// MK: the fused decode call (TcMega; one cooperative launch, 256 threads: warps 6 and 7 or 7
+// have no role besides the routing, the row split and the combine).
+template <int BN, int FMT, int P, bool MK>
+constexpr int fp4_block() { return MK ? 256 : Fp4Cfg<P, BN>::THREADS; }
+
+template <int BN, int FMT, int P, bool MK>
+__global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel(
+    Fp4Params p, TcMega mg, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr int BS = FMT == FT_W_MXFP4 ? 32 : 16;
     constexpr int APS = kStageK / (BS * 4);           // scale atoms per operand per stage
     constexpr int SF_BYTES = APS * 512;
     constexpr uint32_t SF_COL0 = 256;                 // scale-factor columns: one buffer of 64 per issuer
     constexpr int NI = Fp4Cfg<P, BN>::NI;             // MMA issuers
-    constexpr int NTH = Fp4Cfg<P, BN>::THREADS;
+    constexpr int NTH = fp4_block<BN, FMT, P, MK>();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages, STAGE = p.stage_bytes;
@@ -290,15 +286,27 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
     int* s_tvote = s_tile + kTQ;                                           // [2][4] tile-id votes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const RouteCounts rc = *p.counts;
-    const int u_begin = p.pass == 1 ? rc.n_hits : 0;
-    const int u_end = p.pass == 0 ? rc.n_hits : rc.n_unique;
-    if (u_end <= u_begin) return;
+    // the fused call's waits poll a device word and run to a %globaltimer deadline
+    int* err = MK ? mg.err_dev : p.err;
+    uint64_t deadline = 0;
+    if constexpr (MK) {
+        if (blockIdx.x == 0) mk_route(mg, smem, err);
+        if (!mk_wait_route(mg, err, deadline, s_tmem + 3)) { mk_report(err, p.err); return; }
+    }
+    const RouteCounts rc = MK ? mk_counts(p.counts) : *p.counts;
+    const int u_begin = MK ? 0 : (p.pass == 1 ? rc.n_hits : 0);
+    const int u_end = MK ? rc.n_unique : (p.pass == 0 ? rc.n_hits : rc.n_unique);
+    const int n_hits = rc.n_hits;
+    if (u_end <= u_begin) { if constexpr (MK) mk_report(err, p.err); return; }
+    auto bwait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+        if constexpr (MK) return mbar_wait_until(bar, parity, err, code, deadline);
+        else return mbar_wait(bar, parity, err, code);
+    };
     const int H = p.hidden, I = p.inter;
     const int m13 = 2 * I / 128, m2 = H / 128;
     const int ak13 = H / BS / 4, ak2 = I / BS / 4;   // scale atoms per 128-row band / per tile
 
-    for (int i = threadIdx.x; i <= u_end; i += blockDim.x) s_eoff[i] = p.entry_off[i];
+    for (int i = threadIdx.x; i <= u_end; i += blockDim.x) s_eoff[i] = ldr<MK>(p.entry_off + i);
     __syncthreads();
     for (int i = threadIdx.x; i < u_end; i += blockDim.x) s_tp[i] = (s_eoff[i + 1] - s_eoff[i] + BN - 1) / BN;
     __syncthreads();
@@ -335,7 +343,21 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
     const uint32_t tmem_base = *s_tmem;
     const int nt_pass = s_tp[u_end] - s_tp[u_begin];
     const int total = nt_pass * (m13 + m2);
-    int* err = p.err;
+    // fused call: hit entries' tiles, then miss entries' (a CTA waiting for a fill never holds
+    // back hit work)
+    const int total0 = MK ? (m13 + m2) * (s_tp[n_hits] - s_tp[0]) : 0;
+    auto tile = [&](int t) -> FTile {
+        if constexpr (MK) {
+            return t < total0 ? fp4_tile(t, s_tp, 0, n_hits, m13, m2)
+                              : fp4_tile(t - total0, s_tp, n_hits, u_end, m13, m2);
+        } else {
+            return fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
+        }
+    };
+    auto cwait = [&](const int* flag, int target, int code) -> bool {
+        if constexpr (MK) return wait_ge_until(flag, target, err, code, deadline, 1024);
+        else return wait_count(flag, target, err, code);
+    };
 
     // 1. W13 activation pieces: the launch's CTAs split the pass's token rows between them
     // (unless the caller has already written them)
@@ -345,7 +367,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
             const int u = entry_of_row(s_eoff, u_begin, u_end, r);
             const int i = r - s_eoff[u];
             const int tile = s_tp[u] + i / BN, rin = i % BN;
-            const __nv_bfloat16* src = p.x + (int64_t)(p.pairs[r] / p.top_k) * H;
+            const __nv_bfloat16* src = p.x + (int64_t)(ldr<MK>(p.pairs + r) / p.top_k) * H;
             split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
                           p.xsf + (int64_t)tile * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
                           threadIdx.x, NTH, 2, s_red);
@@ -366,20 +388,28 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
             bool ok = true;
             for (uint32_t q = 0; ok; ++q) {
                 const int ts = (int)(q % kTQ);
-                if (!mbar_wait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, err, 8)) { ok = false; break; }
+                if (!bwait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 8)) { ok = false; break; }
                 const int claimed = P > 1 ? atomicAdd(p.tile_ctr, 1) : (int)(blockIdx.x + q * gridDim.x);
                 const int t = claimed < total ? claimed : -1;
                 s_tile[ts] = t;
                 mbar_arrive(&tq_full[ts]);
                 if (t < 0) break;
-                const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
+                const FTile tl = tile(t);
                 const int K = tl.w13 ? H : I;
                 const int k_stages = K / kStageK;
                 const int ak = tl.w13 ? ak13 : ak2;
                 const CUtensorMap* mA = tl.w13 ? &tmA13 : &tmA2;
                 const CUtensorMap* mB = tl.w13 ? &tmB13 : &tmB2;
                 const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * ak * 512;
-                const int slot = p.entry_dst[tl.u];
+                const int slot = ldr<MK>(p.entry_dst + tl.u);
+                if constexpr (MK) {
+                    // a missed expert's weights are read only once its copy has landed
+                    if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
                 const uint8_t* sfa = p.arena + (int64_t)slot * p.blob_bytes + (tl.w13 ? p.off_s13 : p.off_s2) +
                                      (int64_t)tl.mt * ak * 512;
                 // the tile's rows are token-major (token i, piece pc at row i * P + pc): only the
@@ -392,19 +422,19 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
                 const int* dep = tl.w13 ? p.cnt_x + tl.u : p.cnt_w13 + tl.u;
                 const int target = tl.w13 ? (p.x_ready ? 0 : s_eoff[tl.u + 1] - s_eoff[tl.u])
                                           : m13 * (s_tp[tl.u + 1] - s_tp[tl.u]);
-                const bool ready_now = target == 0 || ld_acquire_s32(dep) >= target;
+                const bool ready_now = target == 0 || ld_acquire(dep) >= target;
                 const int npre = ready_now ? 0 : min(S, k_stages);
                 const uint32_t it0 = it;
                 for (int kb = 0; kb < npre; ++kb, ++it) {
                     const int s = it % S;
-                    if (!mbar_wait(&empty[s], ((it / S) & 1u) ^ 1u, err, 1)) { ok = false; break; }
+                    if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
                     uint8_t* st = smem + (size_t)s * STAGE;
                     mbar_expect_tx(&full[s], stage_tx);
                     tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
                     bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
                 }
                 if (!ok) break;
-                const bool ready = ready_now || wait_count(dep, target, err, tl.w13 ? 6 : 7);
+                const bool ready = ready_now || cwait(dep, target, tl.w13 ? 6 : 7);
                 fence_proxy_async_global();
                 // the armed stages expect their activation bytes: load them in any case so the
                 // ring drains if the wait ran out
@@ -418,7 +448,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
                 if (!ready) { ok = false; break; }
                 for (int kb = npre; kb < k_stages; ++kb, ++it) {
                     const int s = it % S;
-                    if (!mbar_wait(&empty[s], ((it / S) & 1u) ^ 1u, err, 1)) { ok = false; break; }
+                    if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
                     uint8_t* st = smem + (size_t)s * STAGE;
                     mbar_expect_tx(&full[s], stage_tx);
                     tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
@@ -446,21 +476,21 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
                 const int ts = (int)(tcount % kTQ);
-                if (!mbar_wait(&tq_full[ts], (tcount / kTQ) & 1u, err, 9)) break;
+                if (!bwait(&tq_full[ts], (tcount / kTQ) & 1u, 9)) break;
                 const int t = s_tile[ts];
                 mbar_arrive(&tq_empty[ts]);
                 if (t < 0) break;
-                const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
+                const FTile tl = tile(t);
                 const int k_stages = (tl.w13 ? H : I) / kStageK;
                 const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
                 const int n_mma = (P * n_valid + 15) & ~15;
                 const uint32_t acc = tcount & 1u;
-                if (!mbar_wait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, err, 2)) break;
+                if (!bwait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * (uint32_t)NC;
                 for (int kb = 0; kb < k_stages; ++kb, ++it) {
                     const int s = it % S;
-                    if (!mbar_wait(&full[s], (it / S) & 1u, err, 3)) { ok = false; break; }
+                    if (!bwait(&full[s], (it / S) & 1u, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + (size_t)s * STAGE);
                     const uint32_t ssf = sa + kABytes + B_BYTES;
@@ -490,7 +520,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
                 mma_commit(&tfull[acc]);
             }
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         const int q = warp & 3;
         const int etid = threadIdx.x - 64;                 // 0..127 over the epilogue warps
         const int row_in_tile = q * 32 + lane;
@@ -498,7 +528,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
             // the next claimed tile id; the four warps vote on the wait's outcome so that they
             // leave the loop together (they meet at named barriers below)
             const int ts = (int)(tcount % kTQ);
-            const bool have = mbar_wait(&tq_full[ts], (tcount / kTQ) & 1u, err, 10);
+            const bool have = bwait(&tq_full[ts], (tcount / kTQ) & 1u, 10);
             int* tv = s_tvote + (tcount & 1u) * 4;
             if (lane == 0) tv[q] = have ? 1 : 0;
             named_bar(1, 128);
@@ -507,7 +537,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
             __syncwarp();
             if (lane == 0) mbar_arrive(&tq_empty[ts]);
             if (t < 0) break;
-            const FTile tl = fp4_tile(t, s_tp, u_begin, u_end, m13, m2);
+            const FTile tl = tile(t);
             const int nt = tl.g - s_tp[tl.u];
             const int row_b = s_eoff[tl.u] + nt * BN;
             const int n_valid = min(BN, s_eoff[tl.u + 1] - row_b);
@@ -516,7 +546,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
             // at the same named barriers (votes are double-buffered by tile parity); after a
             // wait runs out they keep looping without work, and later waits return at once
             // because the error word is set
-            const bool mine = mbar_wait(&tfull[acc], (tcount >> 1) & 1u, err, 4);
+            const bool mine = bwait(&tfull[acc], (tcount >> 1) & 1u, 4);
             int* vote = s_got + (tcount & 1u) * 4;
             if (lane == 0) vote[q] = mine ? 1 : 0;
             named_bar(1, 128);
@@ -525,8 +555,9 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
                 tc_fence_after();
                 float ts = 1.f;
                 if (FMT == FT_W_NVFP4) {
-                    const int slot = p.entry_dst[tl.u];
-                    ts = reinterpret_cast<const float*>(p.arena + (int64_t)slot * p.blob_bytes + p.off_ts)[tl.w13 ? 0 : 1];
+                    const int slot = ldr<MK>(p.entry_dst + tl.u);
+                    const float* tsp = reinterpret_cast<const float*>(p.arena + (int64_t)slot * p.blob_bytes + p.off_ts);
+                    ts = MK ? __ldcg(tsp + (tl.w13 ? 0 : 1)) : tsp[tl.w13 ? 0 : 1];
                 }
                 const float* rsp = p.xrs + (int64_t)tl.g * BN;     // W13 only: the x rows' prescale
                 // accumulators of this tile: issuer A at (NI acc) NC, issuer B at (NI acc + 1) NC
@@ -581,7 +612,7 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
 #pragma unroll
                         for (int j = 0; j < tpc; ++j) {
                             const int i = i0 + j;
-                            if (i < n_valid) p.y[(int64_t)p.pairs[row_b + i] * H + m] = tok[j];
+                            if (i < n_valid) p.y[(int64_t)ldr<MK>(p.pairs + row_b + i) * H + m] = tok[j];
                         }
                     }
                 }
@@ -613,6 +644,11 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
                 __threadfence();
                 named_bar(1, 128);
                 if (etid == 0) atomicAdd(p.cnt_w13 + tl.u, 1);
+            } else if (MK) {
+                // this W2 tile's expert outputs are written (read by the combine)
+                __threadfence();
+                named_bar(1, 128);
+                if (etid == 0) atomicAdd(mg.done, 1);
             }
         }
     }
@@ -621,6 +657,10 @@ __global__ void __launch_bounds__(Fp4Cfg<P, BN>::THREADS, 1) fp4_ffn_kernel(
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem_base) : "memory");
+    }
+    if constexpr (MK) {
+        mk_combine(mg, p.y, H, H, m2 * nt_pass, err, deadline, s_tmem + 3);
+        mk_report(err, p.err);
     }
 }
 
@@ -733,26 +773,77 @@ int stage_bytes_for(int fmt, int bn, int pieces) {
     return fp4::kABytes + pieces * bn * 128 + 2 * aps * 512;
 }
 
+// Stages and shared memory of a launch (the same for the fused call).
 template <int BN, int FMT, int P>
-cudaError_t launch_t(const Fp4Params& p0, const Fp4Maps& m, int grid, cudaStream_t s) {
-    Fp4Params p = p0;
+cudaError_t fp4_smem(Fp4Params& p, size_t* smem) {
     p.stage_bytes = stage_bytes_for(FMT, BN, p.pieces);
     const size_t fixed = 1024 + (4 + 2 * fp4::kTQ) * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + BN * 65 * 4 + 32 +
                          (fp4::kTQ + 8) * 4 + 64;
     p.stages = (int)((kSmemLimit - fixed) / (p.stage_bytes + 16));
     if (p.stages > 8) p.stages = 8;
     if (p.stages < 2) return cudaErrorInvalidValue;
-    const size_t smem = fixed + (size_t)p.stages * (p.stage_bytes + 16);
-    if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
+    *smem = fixed + (size_t)p.stages * (p.stage_bytes + 16);
+    if (*smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+template <int BN, int FMT, int P, bool MK>
+cudaError_t fp4_attr() {
     static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(fp4::fp4_ffn_kernel<BN, FMT, P>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    fp4::fp4_ffn_kernel<BN, FMT, P><<<grid, fp4::Fp4Cfg<P, BN>::THREADS, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
+    if (attr) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fp4::fp4_ffn_kernel<BN, FMT, P, MK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e == cudaSuccess) attr = true;
+    return e;
+}
+
+template <int BN, int FMT, int P>
+cudaError_t launch_t(const Fp4Params& p0, const Fp4Maps& m, int grid, cudaStream_t s) {
+    Fp4Params p = p0;
+    size_t smem = 0;
+    cudaError_t e = fp4_smem<BN, FMT, P>(p, &smem);
+    if (e != cudaSuccess) return e;
+    e = fp4_attr<BN, FMT, P, false>();
+    if (e != cudaSuccess) return e;
+    fp4::fp4_ffn_kernel<BN, FMT, P, false><<<grid, fp4::Fp4Cfg<P, BN>::THREADS, smem, s>>>(
+        p, TcMega{}, *m.a13, *m.b13, *m.a2, *m.b2);
     return cudaGetLastError();
+}
+
+// The fused decode call: every CTA must be resident (they wait on CTA 0's routing and on
+// each other's outputs).
+template <int FMT>
+cudaError_t launch_mega_t(const Fp4Params& p0, const TcMega& mg, const Fp4Maps& m, int grid, cudaStream_t s) {
+    Fp4Params p = p0;
+    size_t smem = 0;
+    cudaError_t e = fp4_smem<16, FMT, 4>(p, &smem);
+    if (e != cudaSuccess) return e;
+    e = fp4_attr<16, FMT, 4, true>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(fp4::fp4_block<16, FMT, 4, true>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fp4::fp4_ffn_kernel<16, FMT, 4, true>, p, mg, *m.a13, *m.b13, *m.a2, *m.b2);
+}
+
+template <int FMT>
+int mega_grid_t(int num_sms) {
+    Fp4Params p{};
+    p.pieces = 4;
+    size_t smem = 0;
+    if (fp4_smem<16, FMT, 4>(p, &smem) != cudaSuccess || fp4_attr<16, FMT, 4, true>() != cudaSuccess) return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fp4::fp4_ffn_kernel<16, FMT, 4, true>,
+                                                      fp4::fp4_block<16, FMT, 4, true>(), smem) != cudaSuccess)
+        return 0;
+    return per_sm * num_sms;
 }
 
 }  // namespace
@@ -791,6 +882,22 @@ cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t fp4_launch_mega(int fmt, const Fp4Params& p, const TcMega& mg, const Fp4Maps& m, int grid,
+                            cudaStream_t s) {
+    if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1 || !p.tile_ctr ||
+        p.pieces != kFp4MaxPieces || p.x_ready || mg.experts < 1 || mg.experts > 256 || mg.epoch <= 0 || grid < 1)
+        return cudaErrorInvalidValue;
+    if (fmt == FT_W_MXFP4) return launch_mega_t<FT_W_MXFP4>(p, mg, m, grid, s);
+    if (fmt == FT_W_NVFP4) return launch_mega_t<FT_W_NVFP4>(p, mg, m, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+int fp4_mega_grid(int fmt, int num_sms) {
+    if (fmt == FT_W_MXFP4) return mega_grid_t<FT_W_MXFP4>(num_sms);
+    if (fmt == FT_W_NVFP4) return mega_grid_t<FT_W_NVFP4>(num_sms);
+    return 0;
 }
 
 cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, int grid, cudaStream_t s) {

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include "common.cuh"
+#include "tc_ffn.cuh"
 
 namespace ftmoe {
 
@@ -62,6 +63,11 @@ cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, in
                                int64_t n_slots, int64_t blob_bytes);
 cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int64_t rows, int box_rows);
 cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, int grid, cudaStream_t s);
+// the fused decode call (16-token tiles, four pieces; pass, x_ready ignored: all entries, rows
+// split in the launch); grid = the number of CTAs that fit on the device (fp4_mega_grid)
+cudaError_t fp4_launch_mega(int fmt, const Fp4Params& p, const TcMega& mg, const Fp4Maps& m, int grid,
+                            cudaStream_t s);
+int fp4_mega_grid(int fmt, int num_sms);
 // prefill: MXFP4 activations of T token rows (OCP rule), token-major codes [T][H/2] and scale
 // bytes [T][H/32]; then the routed rows gathered into the W13 N operand (one piece, bn rows
 // per tile)

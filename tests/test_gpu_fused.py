@@ -267,15 +267,15 @@ def test_fused_host_wait_timeout(ft, monkeypatch):
 
 
 def test_fused_rejects_unsupported_configs(ft):
-    cfg = W.config("elastic_nvfp4")
+    cfg = W.config("elastic_nvfp4", hidden=512, inter=256, t_max=17)
     pool = HostPool(cfg, images=4)
     with pytest.raises(ft.FtError) as e:
-        _make(ft, cfg, pool, 8, True)          # FP4 weights
+        _make(ft, cfg, pool, 8, True)          # FP4 weights, more than 16 tokens per call
     assert e.value.status == ft.FT_ERR_INVALID
     cfg = W.config("decode_mxfp4", wfmt="bf16", layers=1, hidden=64, inter=64, t_max=33)
     pool = HostPool(cfg, images=4)
     with pytest.raises(ft.FtError):
-        _make(ft, cfg, pool, 8, True)          # more than 32 tokens per call
+        _make(ft, cfg, pool, 8, True)          # BF16, more than 32 tokens per call
 
 
 def test_fused_calls_queue_without_host_waits(ft, bf16_pool):
@@ -300,3 +300,49 @@ def test_fused_calls_queue_without_host_waits(ft, bf16_pool):
     assert np.array_equal(s0[0], s1[0]) and np.array_equal(s0[1], s1[1])
     for c in caches:
         c.close()
+
+
+@pytest.mark.parametrize("name", ["decode_mxfp4", "elastic_nvfp4"])
+def test_fused_fp4_matches_default_and_simulator(ft, name):
+    """FP4 weights (block-scaled tcgen05 path) through the fused call: outputs bit-identical to
+    the default path, per-call counts and snapshots against the simulator, one call per layer
+    against the oracle. MXFP4: 4 layers of the 256-expert top-6 routing; NVFP4: resizes."""
+    cfg = W.config(name, layers=4 if name == "decode_mxfp4" else 1, hidden=512, inter=256, steps=12)
+    pool = HostPool(cfg, images=7)
+    C = W.cache_capacity(cfg)
+    runs = [Runner(_make(ft, cfg, pool, C, fused), cfg, C) for fused in (False, True)]
+    experts = OracleExperts(pool, max_cached=7)
+    worst = 0.0
+    for s, step in enumerate(W.decode_trace(cfg)):
+        if name == "elastic_nvfp4" and s in (4, 8):
+            for r in runs:
+                r.resize(C // 3 if s == 4 else C)
+        for d in step:
+            out, idx, _ = _pair_call(runs, d["layer"], d["x"], d["logits"])
+            if s % 4 == 1 and d["layer"] == 0:
+                ref, ref_idx, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
+                assert np.array_equal(idx, ref_idx)
+                worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref))
+        if s % 4 == 0:
+            for r in runs:
+                r.check_state()
+    assert worst <= TOL[cfg.wfmt], worst
+    assert runs[0].cache.stats() == runs[1].cache.stats()
+    for r in runs:
+        r.check_state()
+        r.cache.close()
+
+
+def test_fused_fp4_full_size_mxfp4(ft):
+    """The 284B-shaped MXFP4 layer at full size (H 4096, I 2048), 2 layers, 6 steps: fused and
+    default outputs bit-identical, counts against the simulator."""
+    cfg = W.config("decode_mxfp4", layers=2, steps=6)
+    pool = HostPool(cfg, images=16)
+    C = W.cache_capacity(cfg)
+    runs = [Runner(_make(ft, cfg, pool, C, fused), cfg, C) for fused in (False, True)]
+    for step in W.decode_trace(cfg):
+        for d in step:
+            _pair_call(runs, d["layer"], d["x"], d["logits"])
+    for r in runs:
+        r.check_state()
+        r.cache.close()
