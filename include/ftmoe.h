@@ -109,10 +109,15 @@ typedef enum { FT_POLICY_GLOBAL_LRU = 0, FT_POLICY_LAYER_LRU = 1, FT_POLICY_STAT
  *   from mapped memory while the kernel runs and, per miss, enqueues the copy and a
  *   stream-ordered write of a device flag on the copy stream. The results (outputs, top-k,
  *   cache state, statistics) equal those of the default path bit for bit.
- *   Requires BF16 weights, experts <= 256 and max_tokens <= 32, and a device where the
- *   kernel's CTAs can all be resident at once; ft_moe_create fails with FT_ERR_INVALID
- *   otherwise. ft_timing_t then reports the whole kernel as ffn_hit_ms (route_ms covers only
- *   the router logits, if computed; ffn_miss_ms and combine_ms stay 0). */
+ *   Requires experts <= 256, max_tokens <= 32 (BF16 weights) or <= 16 (MXFP4, NVFP4), and a
+ *   device where the kernel's CTAs can all be resident at once; ft_moe_create fails with
+ *   FT_ERR_INVALID otherwise. ft_moe_forward then never waits for the device: a host thread
+ *   of the handle reads each call's miss list and enqueues its copies. Errors found on the
+ *   device or by that thread (a NaN logit, a failed copy, a wait that ran out) are returned by
+ *   the next call on the handle or by the next safe point (ft_cache_stats, ft_cache_snapshot,
+ *   ft_cache_resize, ft_cache_pin, ft_moe_timing). ft_timing_t reports the whole kernel as
+ *   ffn_hit_ms (route_ms covers only the router logits, if computed; ffn_miss_ms and
+ *   combine_ms stay 0). */
 #define FT_FLAG_FUSED_DECODE 0x100
 
 typedef struct {
