@@ -105,6 +105,8 @@ struct ft_moe {
     int32_t* h_miss_dst = nullptr;
 
     cudaStream_t copy_stream = nullptr;
+    cudaStream_t copy_stream2 = nullptr;  // fused decode: the fill agent alternates the two
+    cudaEvent_t ev_copy2 = nullptr;
     cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_done = nullptr;
 
     ft_cache_stats_t stats{};
@@ -379,6 +381,7 @@ void free_all(ft_moe* h) {
         agent_stop(h);
     }
     if (h->copy_stream) cudaStreamSynchronize(h->copy_stream);
+    if (h->copy_stream2) cudaStreamSynchronize(h->copy_stream2);
     if (h->ev_done) cudaEventSynchronize(h->ev_done);
     cudaFree(h->d_router); cudaFree(h->d_arena); cudaFree(h->d_table); cudaFree(h->d_slot_key);
     cudaFree(h->d_order[0]); cudaFree(h->d_order[1]); cudaFree(h->d_logits); cudaFree(h->d_idx);
@@ -403,6 +406,8 @@ void free_all(ft_moe* h) {
     h->p_pending.clear();
     if (h->h_mapped) cudaFreeHost(h->h_mapped);
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+    if (h->copy_stream2) cudaStreamDestroy(h->copy_stream2);
+    if (h->ev_copy2) cudaEventDestroy(h->ev_copy2);
     if (h->ev_route) cudaEventDestroy(h->ev_route);
     if (h->ev_fill) cudaEventDestroy(h->ev_fill);
     if (h->ev_done) cudaEventDestroy(h->ev_done);
@@ -530,19 +535,28 @@ ft_status agent_handle(ft_moe* h, const ft_moe::FillAgent::Job& job, std::string
         }
     StreamWriteValue32Fn wv = stream_write_fn();
     const CUdeviceptr flags = (CUdeviceptr)(h->d_mega + 64);
-    if (job.se) cudaEventRecord(job.se->fill_begin, h->copy_stream);
+    // misses alternate between two copy streams: the memory barrier before one stream's flag
+    // write then overlaps the other stream's copy
+    cudaStream_t cs[2] = {h->copy_stream, h->copy_stream2};
+    if (job.se) {
+        cudaEventRecord(job.se->fill_begin, cs[0]);
+        cudaStreamWaitEvent(cs[1], job.se->fill_begin, 0);
+    }
     for (int j = 0; j < n_miss; ++j) {
+        cudaStream_t st = cs[j & 1];
         cudaError_t ce = cudaMemcpyAsync(h->d_arena + (size_t)dsts[(size_t)j] * h->blob_bytes,
                                          h->blobs[(size_t)keys[(size_t)j]], h->blob_bytes,
-                                         cudaMemcpyHostToDevice, h->copy_stream);
+                                         cudaMemcpyHostToDevice, st);
         if (ce != cudaSuccess) { *msg = std::string("fused decode fill: ") + cudaGetErrorString(ce); return FT_ERR_CUDA; }
-        if (wv((CUstream)h->copy_stream, flags + 4 * (CUdeviceptr)j, (cuuint32_t)epoch, 0) != CUDA_SUCCESS) {
+        if (wv((CUstream)st, flags + 4 * (CUdeviceptr)j, (cuuint32_t)epoch, 0) != CUDA_SUCCESS) {
             *msg = "fused decode fill: stream write of a fill flag failed";
             return FT_ERR_CUDA;
         }
     }
     if (job.se) {
-        cudaEventRecord(job.se->fill_end, h->copy_stream);
+        cudaEventRecord(h->ev_copy2, cs[1]);
+        cudaStreamWaitEvent(cs[0], h->ev_copy2, 0);
+        cudaEventRecord(job.se->fill_end, cs[0]);
         std::lock_guard<std::mutex> lk(h->agent->mu);
         job.se->has_fill = true;
     }
@@ -659,6 +673,7 @@ ft_status sync_handle(ft_moe* h) {
     ft_status s = wait_event(h, h->ev_done, "synchronise handle");
     if (s != FT_OK) return s;
     FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+    if (h->copy_stream2) FT_CUDA(h, cudaStreamSynchronize(h->copy_stream2));
     if (h->h_ffn_err && *(volatile int*)h->h_ffn_err) {
         h->broken = true;
         return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait (code " +
@@ -1019,6 +1034,10 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
             cuda_fail(h, cudaGetLastError(), "memset(fused decode flags)"); return bail(FT_ERR_CUDA);
         }
         h->d_dstats = (unsigned long long*)(h->d_mega + 16);
+        if (cudaStreamCreateWithFlags(&h->copy_stream2, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_copy2, cudaEventDisableTiming) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "second copy stream"); return bail(FT_ERR_CUDA);
+        }
         h->mega = true;
         h->agent.reset(new ft_moe::FillAgent());
         h->agent->th = std::thread(agent_main, h);
