@@ -179,6 +179,74 @@ __device__ __forceinline__ void mk_combine(const TcMega& mg, const float* y, int
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(const uint8_t* p, int64_t bytes) {
+    for (int64_t o = 0; o < bytes; o += 65536) {
+        const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p + o), "r"(n) : "memory");
+    }
+}
+
+// Where one 128-row weight tile of each matrix lives in a blob: the rows (codes or bf16
+// values) and, for FP4, the band's scale atoms.
+struct MkTileBytes {
+    int64_t w13_off, w13_row_bytes;     // W13 rows [2I][...]
+    int64_t w2_off, w2_row_bytes;       // W2 rows [H][...]
+    int64_t s13_off, s13_band_bytes;    // scale atoms of a 128-row W13 band (0: none)
+    int64_t s2_off, s2_band_bytes;
+    int rows13, rows2;                  // 2I, H
+};
+
+// Fused call, every CTA but the routing one: the call's top-k again (into shared memory),
+// the hit experts as the cache table shows them now, and an L2 prefetch of the weight tile
+// this CTA will process first (hits' W13 tiles, then their W2 tiles, in the FFN's order;
+// BN tokens per N tile), so the first wave of tiles streams from L2 once the routing is
+// published. A key that the concurrent lookup is inserting may be taken for a hit: that only
+// wastes a prefetch.
+template <int BN>
+__device__ void mk_prefetch_first_tile(const TcMega& mg, uint8_t* scratch, const MkTileBytes& tb) {
+    const int E = mg.experts, k = mg.top_k, P = mg.T * mg.top_k;
+    int32_t* s_idx = reinterpret_cast<int32_t*>(scratch);          // [P <= 1024]
+    float* s_w = reinterpret_cast<float*>(scratch + 4096);          // [P]
+    int* cnt = reinterpret_cast<int*>(scratch + 8192);              // [E <= 256]
+    int* s_warp = cnt + 256;                                        // [33]
+    const int warp = threadIdx.x >> 5;
+    for (int t = warp; t < mg.T; t += blockDim.x >> 5)
+        topk_row<8>(mg.logits, t, E, k, s_idx, s_w, nullptr, nullptr, nullptr);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < P; i += blockDim.x) atomicAdd(&cnt[s_idx[i]], 1);
+    __syncthreads();
+    const int e = threadIdx.x;                                      // E <= blockDim.x
+    const int c = e < E ? cnt[e] : 0;
+    int slot = -1;
+    if (c > 0) {
+        slot = __ldcg(mg.lp.table + (int64_t)mg.lp.layer * E + e);
+        if (slot >= mg.lp.capacity) slot = -1;
+    }
+    const int nt = slot >= 0 ? (c + BN - 1) / BN : 0;
+    const int m13 = (tb.rows13 + 127) / 128, m2 = (tb.rows2 + 127) / 128;
+    int tot13 = 0, tot2 = 0;
+    const int off13 = block_excl_scan(nt * m13, s_warp, &tot13);
+    const int off2 = block_excl_scan(nt * m2, s_warp, &tot2);
+    const int t = blockIdx.x;
+    if (nt > 0) {
+        const uint8_t* base = mg.arena + (int64_t)slot * mg.blob_bytes;
+        if (t >= off13 && t < off13 + nt * m13) {
+            const int mt = (t - off13) % m13;
+            const int rows = min(128, tb.rows13 - mt * 128);
+            prefetch_l2(base + tb.w13_off + (int64_t)mt * 128 * tb.w13_row_bytes, (int64_t)rows * tb.w13_row_bytes);
+            if (tb.s13_band_bytes) prefetch_l2(base + tb.s13_off + (int64_t)mt * tb.s13_band_bytes, tb.s13_band_bytes);
+        } else if (t >= tot13 && t - tot13 >= off2 && t - tot13 < off2 + nt * m2) {
+            const int mt = (t - tot13 - off2) % m2;
+            const int rows = min(128, tb.rows2 - mt * 128);
+            prefetch_l2(base + tb.w2_off + (int64_t)mt * 128 * tb.w2_row_bytes, (int64_t)rows * tb.w2_row_bytes);
+            if (tb.s2_band_bytes) prefetch_l2(base + tb.s2_off + (int64_t)mt * tb.s2_band_bytes, tb.s2_band_bytes);
+        }
+    }
+    // the scratch is stage ring memory the TMA (async proxy) writes later
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Thread 0 of a CTA leaving a fused call: an error code of the launch's device word goes to
 // the host-mapped word the handle reads.
 __device__ __forceinline__ void mk_report(const int* err_dev, int* err_host) {

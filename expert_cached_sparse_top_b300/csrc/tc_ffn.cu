@@ -119,60 +119,6 @@ __device__ __forceinline__ int entry_of_row(const int32_t* entry_off, int n_entr
     return lo;
 }
 
-__device__ __forceinline__ void prefetch_l2(const uint8_t* p, int64_t bytes) {
-    for (int64_t o = 0; o < bytes; o += 65536) {
-        const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p + o), "r"(n) : "memory");
-    }
-}
-
-// Fused call, every CTA but the routing one: the call's top-k again (into shared memory),
-// the hit experts as the cache table shows them now, and an L2 prefetch of the weight tile
-// this CTA will process first (hits' W13 tiles, then their W2 tiles, in the FFN's order),
-// so the first wave of tiles streams from L2 once the routing is published. A key that the
-// concurrent lookup is inserting may be taken for a hit: that only wastes a prefetch.
-template <int BN>
-__device__ void mk_prefetch_first_tile(const TcMega& mg, uint8_t* scratch, int H, int I) {
-    const int E = mg.experts, k = mg.top_k, P = mg.T * mg.top_k;
-    int32_t* s_idx = reinterpret_cast<int32_t*>(scratch);          // [P <= 1024]
-    float* s_w = reinterpret_cast<float*>(scratch + 4096);          // [P]
-    int* cnt = reinterpret_cast<int*>(scratch + 8192);              // [E <= 256]
-    int* s_warp = cnt + 256;                                        // [33]
-    const int warp = threadIdx.x >> 5;
-    for (int t = warp; t < mg.T; t += blockDim.x >> 5)
-        topk_row<8>(mg.logits, t, E, k, s_idx, s_w, nullptr, nullptr, nullptr);
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < P; i += blockDim.x) atomicAdd(&cnt[s_idx[i]], 1);
-    __syncthreads();
-    const int e = threadIdx.x;                                      // E <= blockDim.x
-    const int c = e < E ? cnt[e] : 0;
-    int slot = -1;
-    if (c > 0) {
-        slot = __ldcg(mg.lp.table + (int64_t)mg.lp.layer * E + e);
-        if (slot >= mg.lp.capacity) slot = -1;
-    }
-    const int nt = slot >= 0 ? (c + BN - 1) / BN : 0;
-    const int m13 = (2 * I + kBM - 1) / kBM, m2 = (H + kBM - 1) / kBM;
-    int tot13 = 0, tot2 = 0;
-    const int off13 = block_excl_scan(nt * m13, s_warp, &tot13);
-    const int off2 = block_excl_scan(nt * m2, s_warp, &tot2);
-    const int t = blockIdx.x;
-    if (nt > 0) {
-        const uint8_t* base = mg.arena + (int64_t)slot * mg.blob_bytes;
-        if (t >= off13 && t < off13 + nt * m13) {
-            const int mt = (t - off13) % m13;
-            prefetch_l2(base + mg.off_w13 + (int64_t)mt * kBM * H * 2, (int64_t)kBM * H * 2);
-        } else if (t >= tot13 && t - tot13 >= off2 && t - tot13 < off2 + nt * m2) {
-            const int mt = (t - tot13 - off2) % m2;
-            const int rows = min(kBM, H - mt * kBM);
-            prefetch_l2(base + mg.off_w2 + (int64_t)mt * kBM * I * 2, (int64_t)rows * I * 2);
-        }
-    }
-    // the scratch is stage ring memory the TMA (async proxy) writes later
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 template <int BN, bool MK>
 __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     TcParams p, TcMega mg, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
@@ -208,7 +154,11 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     uint64_t deadline = 0;
     if constexpr (MK) {
         if (blockIdx.x == 0) mk_route(mg, smem, err);
-        else mk_prefetch_first_tile<BN>(mg, smem, p.hidden, p.inter);
+        else {
+            const int64_t H2 = (int64_t)p.hidden * 2, I2 = (int64_t)p.inter * 2;
+            const MkTileBytes tb{mg.off_w13, H2, mg.off_w2, I2, 0, 0, 0, 0, 2 * p.inter, p.hidden};
+            mk_prefetch_first_tile<BN>(mg, smem, tb);
+        }
         if (!mk_wait_route(mg, err, deadline, s_tmem + 2)) { report(); return; }
     }
     const RouteCounts rc = MK ? mk_counts(p.counts) : *p.counts;
