@@ -118,9 +118,9 @@ def _peaks():
 # algorithmic bytes of the same launches, kept in a profile summary together with a hash of
 # the kernel's sources; a kernel changed since the capture reports no traffic.
 TRAFFIC = {
-    "bf16": ("tc_ffn_decode_bf16_traffic.md", ["tc_ffn.cu", "tc_ffn.cuh", "tc_ptx.cuh"]),
-    "mxfp4": ("fp4_ffn_decode_mxfp4_traffic.md", ["tc_fp4.cu", "tc_fp4.cuh", "tc_ptx.cuh"]),
-    "nvfp4": ("fp4_ffn_decode_nvfp4_traffic.md", ["tc_fp4.cu", "tc_fp4.cuh", "tc_ptx.cuh"]),
+    "bf16": ("tc_ffn_decode_bf16_traffic.md", ["tc_ffn.cu", "tc_ffn.cuh", "tc_ptx.cuh", "mk.cuh"]),
+    "mxfp4": ("fp4_ffn_decode_mxfp4_traffic.md", ["tc_fp4.cu", "tc_fp4.cuh", "tc_ptx.cuh", "mk.cuh"]),
+    "nvfp4": ("fp4_ffn_decode_nvfp4_traffic.md", ["tc_fp4.cu", "tc_fp4.cuh", "tc_ptx.cuh", "mk.cuh"]),
 }
 
 
