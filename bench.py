@@ -73,7 +73,7 @@ class Clocks:
             self.f = open(path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q, "--format=csv,noheader",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -159,7 +159,7 @@ def traffic_ratio(wfmt):
 
 # Decode workloads: name -> (metric, host images (None = the whole pool), default steps, warmup)
 DECODE = {
-    "decode_bf16": (METRIC, None, 200, 16),
+    "decode_bf16": (METRIC, None, 480, 16),
     "decode_mxfp4": ("MoE decode tokens/s through 43 MXFP4 layers (284B-shaped, one global "
                      "LRU cache 20% of pool)", 16, 24, 4),
     "elastic_nvfp4": ("MoE-layer decode tokens/s (35B-A3B-shaped NVFP4 layer, LRU cache "
