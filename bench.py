@@ -20,6 +20,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +40,12 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def clocks_path(args, rank):
+    """File for the nvidia-smi samples of the timed region (a %d in --clocks-csv takes the rank)."""
+    path = args.clocks_csv or os.path.join(tempfile.gettempdir(), "ftmoe_clocks_r%d.csv")
+    return path % rank if "%d" in path else path
 
 
 def max_over_ranks(x, device="cpu"):
@@ -360,8 +367,7 @@ def run_ours(args):
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        clk = Clocks(local, os.path.join(ROOT, "gpurun_out", "clocks_r%d.csv" % rank)) \
-            if record_clocks else None
+        clk = Clocks(local, clocks_path(args, rank)) if record_clocks else None
         t_wall = time.perf_counter()
         for j in range(K):
             i = Wm + j
@@ -382,7 +388,6 @@ def run_ours(args):
         s1 = cache.stats()
         return step_ms, t_wall, tim, s0, s1, clocks
 
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     if args.ffn_traffic:
         # the cached pass alone, every FFN launch counted from the first call (an ncu capture
         # of the FFN kernel over this run divides its DRAM bytes by these); with --all-resident
@@ -747,6 +752,9 @@ def main():
     ap.add_argument("--ffn-traffic", action="store_true",
                     help="decode: run the cached pass only and print the FFN launches and their "
                          "algorithmic bytes (the denominator of an ncu traffic capture)")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="where the nvidia-smi samples of the timed region go (a %%d takes the "
+                         "rank; default: the temp directory)")
     ap.add_argument("--all-resident", action="store_true",
                     help="with --ffn-traffic: every selected expert resident (no fills)")
     ap.add_argument("--fused", action="store_true",

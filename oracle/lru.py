@@ -8,7 +8,7 @@ cache") and is rebuilt under a revised VRAM budget at safe points without reload
 host pool ([MTP] §Three mechanisms, elastic memory management); the measured quantity is
 the fraction of "decode-time expert reads" that miss ([MTP] §Results; [LN]).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * key = (layer, expert); one global recency order over all keys of all layers;
 * the unit of counting is one unique key per forward call (the call's set S, ascending);

@@ -4,7 +4,7 @@ The pages compare the engine's global LRU ("a shared LRU expert cache spanning a
 layers ... instead of a placement frozen at load time", [MTP] §Three mechanisms) with
 engines whose expert placement does not follow the router: llama.cpp assigns MoE tensors at
 load time, KTransformers pins a "hot" subset ([MTP] §The gap it targets), and reports their
-decode miss rates ([MTP] §Results). Readings taken (listed in the design doc):
+decode miss rates ([MTP] §Results). Readings taken where the pages leave it open:
 
 * per-layer LRU: the C slots are split evenly between the L layers (layer l gets
   C // L slots, the first C % L layers one more, in layer order) and each layer runs the

@@ -2,8 +2,8 @@
 
 Every array is drawn from ``numpy.random.default_rng(SeedSequence([seed, tag, ...]))`` so
 any (config, step, layer) can be regenerated on its own. Shapes and value distributions
-follow the workload definitions; where they are not given, the choices are listed in
-DESIGN.md ("Input recipe").
+follow the workload definitions; where they are not given, the choices made are stated
+beside each generator below.
 """
 import math
 from dataclasses import dataclass, field
