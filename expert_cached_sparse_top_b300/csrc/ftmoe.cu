@@ -1091,7 +1091,7 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
     {
         // at most kFusedAhead calls whose routing the agent has not handled yet: the caller
         // never queues far ahead of the device (a full launch queue would block the caller
-        // inside the driver while the kernels wait for the agent's copies)
+        // inside the CUDA driver while the kernels wait for the agent's copies)
         auto& a = *h->agent;
         std::unique_lock<std::mutex> lk(a.mu);
         const bool ok = a.cv.wait_for(lk, std::chrono::milliseconds(h->wait_ms + 5000), [&] {
