@@ -132,11 +132,17 @@ TRAFFIC = {
 
 
 def kernel_sources_sha256(files):
+    """SHA-256 of the kernel's code: the sources with comments and whitespace removed, so a
+    comment edit keeps a capture valid and any code change voids it."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "expert_cached_sparse_top_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "expert_cached_sparse_top_b300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()
 
 
