@@ -8,15 +8,22 @@
 // gathered per expert), and the fp32 accumulator D[128 x N] lives in tensor memory. So a
 // weight tile is read from HBM once however few tokens the expert has.
 //
-//   warp 0      TMA producer: weights through a 3-D tensor map over the slot arena
-//               (K, row, slot) and activations through a 2-D map, 128-byte swizzled,
-//               into an S-stage shared-memory ring (mbarrier complete_tx).
-//   warp 1      allocates TMEM (2 accumulators of N columns) and issues tcgen05.mma
-//               (kind::f16, bf16 x bf16 -> fp32) from one lane; tcgen05.commit frees ring
-//               stages and publishes finished accumulators.
+//   warp 0      TMA producer: claims tiles from the launch's counter when it is ready for the
+//               next one and hands their ids to the other roles through an mbarrier ring;
+//               loads weights through a 3-D tensor map over the slot arena (K, row, slot)
+//               and activations through a 2-D map, 128-byte swizzled, into an S-stage
+//               shared-memory ring (mbarrier complete_tx).
+//   warp 1      allocates TMEM (2 accumulators of N columns per issuer) and issues
+//               tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) from one lane; for N <= 64 warp 6
+//               issues half of every stage's K steps into its own accumulator; tcgen05.commit
+//               frees ring stages and publishes finished accumulators.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator rows; W13 pairs gate/up rows
 //               (adjacent TMEM lanes) into silu(g)*u and writes the bf16 activation; W2
 //               writes fp32 expert outputs to their (token, rank) rows.
+//
+// The fused decode call (MK = true, 256 threads) adds CTA 0's routing, the other CTAs' L2
+// prefetch of their first weight tile, the row gather, the miss tiles' wait for their fill
+// flags and the combine (mk.cuh).
 //
 // Every mbarrier wait is bounded; a wait that runs out records an error code in global
 // memory, and all roles leave their loops, so the kernel always ends and frees its TMEM.

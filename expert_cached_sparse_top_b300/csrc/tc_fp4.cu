@@ -7,25 +7,32 @@
 // into shared memory and tcgen05.cp into tensor memory. Nothing dequantises a weight.
 //
 // The activations stay bf16-accurate although the MMA takes FP4 operands on both sides:
-// `split_kernel` writes every activation row as the sum of P E2M1 "pieces", each with its own
+// every activation row is written as the sum of P E2M1 "pieces", each with its own
 // power-of-two block scale (piece p quantises the residual left by pieces 0..p-1, its scale
 // chosen from the residual's block maximum so no code saturates). Each piece gains at least two
 // bits, so four pieces carry a bf16 row to within about 2^-9 of its block maximum. The pieces
-// of a tile's BN rows are P x BN rows of the MMA's N operand (piece-major), so one MMA per K
-// step covers all of them and the epilogue adds the P column groups of the fp32 accumulator:
-// the result equals W * (sum of pieces). A per-row power-of-two prescale keeps the piece
-// scales inside the E4M3 range; the epilogue undoes it (and applies the NVFP4 tensor scale)
-// per accumulator column.
+// of a tile's BN tokens are P x BN rows of the MMA's N operand (token-major: token i's piece p
+// is row i * P + p), so one MMA per K step covers all of them, and the epilogue adds each
+// token's P columns of the fp32 accumulator: the result equals W * (sum of pieces). A per-row
+// power-of-two prescale keeps the piece scales inside the E4M3 range; the epilogue undoes it
+// (and applies the NVFP4 tensor scale). The pieces are made inside the launch: the x rows by
+// all CTAs before their tiles (counted per entry), the SwiGLU rows by each W13 tile for its 64
+// features (counted per entry; the entry's W2 tiles wait for the count).
 //
-// Kernel roles per CTA (persistent, one CTA per SM, 6 warps):
-//   warp 0      producer: per 256-element K stage, the 128-row weight tile (3-D tensor map
-//               over the slot arena), its scale atoms (bulk copy from the slot), the tile's
-//               P x BN activation-piece rows (2-D map) and their scale atoms.
-//   warp 1      TMEM allocation; one lane copies the stage's scale atoms into tensor memory
-//               and issues 4 block-scaled MMAs (K = 64, N = P x BN); commits free ring
-//               stages and publishes finished accumulators.
-//   warps 2..5  epilogue: W13 tiles -> silu(g) * u -> bf16 activation rows; W2 tiles -> fp32
-//               expert outputs per (token, rank).
+// Kernel roles per CTA (persistent, one CTA per SM):
+//   warp 0      producer: claims tiles (decode: from the launch's counter, when it is ready for
+//               the next; prefill: a fixed round robin) and hands their ids to the other roles
+//               through an mbarrier ring; per 256-element K stage it loads the 128-row weight
+//               tile (3-D tensor map over the slot arena), its scale atoms (bulk copy from the
+//               slot), the tile's P x BN activation-piece rows (2-D map) and their scale atoms.
+//   warp 1      TMEM allocation; with warp 6 (when P x BN <= 64) it copies the stage's scale
+//               atoms into tensor memory and issues the block-scaled MMAs (K = 64, N = P x BN),
+//               each issuer two of the stage's four K steps into its own accumulator; commits
+//               free ring stages and publish finished accumulators.
+//   warps 2..5  epilogue: W13 tiles -> silu(g) * u -> bf16 activation rows and their W2
+//               pieces; W2 tiles -> fp32 expert outputs per (token, rank).
+// The fused decode call (MK = true, 256 threads) adds CTA 0's routing before the tiles, the
+// miss tiles' wait for their fill flags and the combine after them (mk.cuh).
 // Every wait is bounded; a wait that runs out records an error code and all roles leave.
 #include "common.cuh"
 #include "tc_fp4.cuh"
