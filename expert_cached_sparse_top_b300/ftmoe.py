@@ -126,6 +126,9 @@ FLAG_FUSED_DECODE = 0x100
 
 def make_config(layers, experts, hidden, inter, top_k, max_tokens, wfmt, cache_slots, device=0,
                 max_prefill_tokens=0, policy=POLICY_GLOBAL_LRU, fused_decode=False):
+    """An ft_moe_config. policy: POLICY_*; fused_decode: every forward is one cooperative
+    launch (FT_FLAG_FUSED_DECODE) and does not wait for the device; its errors surface on the
+    next call or safe point (stats, snapshot, resize, pin, timing)."""
     flags = int(policy) | (FLAG_FUSED_DECODE if fused_decode else 0)
     return FtMoeConfig(layers, experts, hidden, inter, top_k, max_tokens,
                        WFMT.get(wfmt, wfmt), device, cache_slots, flags, max_prefill_tokens)
