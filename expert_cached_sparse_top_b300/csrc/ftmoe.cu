@@ -1102,6 +1102,11 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
             return fail(h, FT_ERR_TIMEOUT, "fill agent: host wait exceeded FTMOE_WAIT_MS");
         }
     }
+    {
+        // the agent failed while this call waited: report it instead of launching
+        ft_status ar = agent_report(h);
+        if (ar != FT_OK) return ar;
+    }
     const int32_t epoch = ++h->mega_epoch;
     TcParams tp{};
     tp.counts = h->rb.counts;
