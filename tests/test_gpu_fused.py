@@ -346,3 +346,44 @@ def test_fused_fp4_full_size_mxfp4(ft):
     for r in runs:
         r.check_state()
         r.cache.close()
+
+
+@pytest.mark.parametrize("T", [17, 32])
+def test_32_token_tiles_default_and_fused(ft, bf16_pool, T):
+    """Calls of 17..32 tokens use 32-token N tiles (the BF16 kernel's second template): the
+    default and fused paths against the oracle, bit-identical to each other, cold then warm."""
+    cfg = W.config("decode_bf16", t_min=T, t_max=T)
+    C = W.cache_capacity(cfg)
+    runs = [Runner(_make(ft, cfg, bf16_pool, C, fused, max_tokens=32), cfg, C) for fused in (False, True)]
+    experts = OracleExperts(bf16_pool, max_cached=64)
+    for s, step in enumerate(W.decode_trace(cfg, steps=4)):
+        d = step[0]
+        out, idx, _ = _pair_call(runs, 0, d["x"], d["logits"])
+        if s % 2 == 0:
+            ref, ref_idx, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
+            assert np.array_equal(idx, ref_idx)
+            assert normwise_err(bf16_dev_to_f64(out), ref) <= TOL["bf16"]
+    for r in runs:
+        r.check_state()
+        r.cache.close()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+def test_fp4_32_token_tiles(ft, fmt):
+    """FP4 calls of 32 tokens use 32-token tiles (four pieces: 128 N rows, one MMA issuer) on
+    the default path: against the oracle and independent of the cache state."""
+    import torch
+    name = "decode_mxfp4" if fmt == "mxfp4" else "elastic_nvfp4"
+    cfg = W.config(name, layers=1, hidden=512, inter=256, t_min=32, t_max=32)
+    pool = HostPool(cfg, images=9)
+    experts = OracleExperts(pool, max_cached=9)
+    d = W.trace_step(cfg, 2, 0, 32)
+    ref, _, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
+    outs = []
+    for C in (W.cache_capacity(cfg), 0):
+        run = Runner(_make(ft, cfg, pool, C, False, max_tokens=32), cfg, C)
+        out, _, _ = run.call(0, d["x"], d["logits"])
+        assert normwise_err(bf16_dev_to_f64(out), ref) <= TOL[fmt]
+        outs.append(out.clone())
+        run.cache.close()
+    assert torch.equal(outs[0], outs[1])
