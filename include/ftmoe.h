@@ -270,7 +270,23 @@ FT_API ft_status ft_cache_pin(ft_moe* h, const int32_t* keys, int32_t n);
 FT_API ft_status ft_moe_set_timing(ft_moe* h, int32_t enable);
 FT_API ft_status ft_moe_timing(ft_moe* h, ft_timing_t* out, int32_t reset);
 
-/* Text of the last error on this handle (or of the last failed create when h is NULL). */
+/* Text of the last error on this handle (or of the last failed create when h is NULL).
+ *
+ * When an expert-FFN kernel ran out of a bounded wait, the text carries the code it recorded
+ * (the first wait to give up; the kernel then left every loop and ended):
+ *   1, 3     a shared-memory stage was not freed / not filled in time
+ *   2, 4     a tensor-memory accumulator was not freed / not completed in time
+ *   5        draining the issued loads after a failure
+ *   BF16 kernel: 6 a W2 tile's wait for its expert's W13 tiles; 7, 8, 9 the ring of claimed
+ *            tile ids (producer, MMA issuers, epilogue)
+ *   FP4 kernel:  6 a W13 tile's wait for its split activation rows, 7 a W2 tile's wait for
+ *            its expert's W13 tiles; 8, 9, 10 the ring of claimed tile ids
+ *   20       fused decode: the routing of CTA 0 was not published
+ *   21       fused decode: a missed expert's copy did not land (fill flag)
+ *   22       fused decode: the host abandoned the call's copies (reported with its own error)
+ *   23       fused decode: the activation rows of an entry were not gathered
+ *   24       fused decode: the expert outputs of the call were not complete for the combine
+ *   30       fused decode: the cache lookup found an inconsistent state */
 FT_API const char* ft_moe_last_error(const ft_moe* h);
 
 /* Destroy: synchronises, frees device memory, unpins what create pinned. NULL is a no-op. */
