@@ -37,21 +37,32 @@ def up_to_date():
 
 
 def build(force=False, verbose=False):
+    """Build if forced or stale. Processes that build at once (one rank per GPU) serialise on
+    a lock file; a process that got the lock after another built the library reuses it."""
     if not force and up_to_date():
         return LIB
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include"),
-           "--expt-relaxed-constexpr", "-o", LIB + ".tmp", *sources()]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd))
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc failed building libftmoe.so")
-    if verbose:
-        sys.stderr.write(r.stderr)
-    os.replace(LIB + ".tmp", LIB)
+    import fcntl
+    with open(LIB + ".lock", "w") as lk:
+        fcntl.flock(lk, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIB
+            tmp = "%s.%d.tmp" % (LIB, os.getpid())
+            cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+                   "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include"),
+                   "--expt-relaxed-constexpr", "-o", tmp, *sources()]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+                print(" ".join(cmd))
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise RuntimeError("nvcc failed building libftmoe.so")
+            if verbose:
+                sys.stderr.write(r.stderr)
+            os.replace(tmp, LIB)
+        finally:
+            fcntl.flock(lk, fcntl.LOCK_UN)
     return LIB
 
 
