@@ -24,6 +24,8 @@ Modules:
 * ``formats``  E2M1 / E8M0 / E4M3 decoding and the expert blob layout.
 * ``moe``      router logits, top-k, gate weights, SwiGLU expert FFN, combine, layer forward.
 * ``lru``      the global LRU expert-cache simulator (hits, misses, bypasses, slots, resize).
+* ``policies`` the comparator policies: per-layer LRU over an even slot split, and a static
+               resident set (misses bypassed).
 
 Parity status per function is stated in each module header; every function here is pinned
 by a ``-m "not gpu"`` test in ``tests/test_oracle_*.py`` except where a header says
