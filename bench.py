@@ -768,7 +768,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare"])
     args = ap.parse_args()
-    dflt = DECODE.get(args.workload, (None, None, 8, 3))
+    dflt = DECODE.get(args.workload, (None, None, 32 if args.workload == "policy_compare" else 8, 3))
     if args.steps is None:
         args.steps = dflt[2]
     if args.warmup is None:
