@@ -68,23 +68,85 @@ def replica_throughput(units_per_rank, seconds_per_rank, device="cpu"):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """SM clocks, power and throttle reasons sampled during the timed region.
+
+    NVML (the library nvidia-smi reads) is polled from a thread every 2 ms, so even a timed
+    region of a few tens of milliseconds holds many samples; spawning nvidia-smi takes longer
+    than such a region. Each sample is also written to `path` as a CSV line. Falls back to an
+    `nvidia-smi -lms 50` process where NVML cannot be loaded."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clocks-event-reason bits
+    BITS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+            ("sw_power_cap", 0x4))
 
-    def __init__(self, index, path):
+    def __init__(self, index, path, period_s=0.002):
+        import threading
         self.path = path
         self.proc = None
+        self.samples = []
+        self.f = open(path, "w")
+        self.nv = None
         try:
-            self.f = open(path, "w")
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.handle = self._handle(pynvml, index)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
+        except Exception:
+            self.nv = None
+        if self.nv is not None:
+            self.stop_ev = threading.Event()
+            self.period = period_s
+            self.sample()
+            self.th = threading.Thread(target=self._loop, daemon=True)
+            self.th.start()
+            return
+        try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.Q, "--format=csv,noheader",
                  "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
+    @staticmethod
+    def _handle(pynvml, index):
+        # the CUDA device's PCI bus id picks the same GPU whatever CUDA_VISIBLE_DEVICES says
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(index)
+            bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            return pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return pynvml.nvmlDeviceGetHandleByIndex(index)
+
+    def sample(self):
+        nv = self.nv
+        try:
+            sm = float(nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM))
+            rs = int(nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle))
+            pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+        except Exception:
+            return
+        self.samples.append((sm, rs))
+        self.f.write("%.1f,%.0f,%.0f,%.1f,0x%x\n" % (time.time(), sm, self.max_mhz, pw, rs))
+
+    def _loop(self):
+        while not self.stop_ev.wait(self.period):
+            self.sample()
+
     def stop(self):
+        if self.nv is not None:
+            self.stop_ev.set()
+            self.th.join(timeout=5)
+            self.sample()
+            self.f.close()
+            if not self.samples:
+                return None
+            reasons = sorted({n for _, r in self.samples for n, b in self.BITS if r & b})
+            return {"sm_mhz": float(np.median([sm for sm, _ in self.samples])), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(self.samples), "source": "NVML, 2 ms period"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -94,7 +156,7 @@ class Clocks:
             self.proc.kill()
         self.f.close()
         sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        names = [n for n, _ in self.BITS]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
@@ -110,7 +172,7 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 50 ms period"}
 
 
 def _peaks():
@@ -212,6 +274,16 @@ def W_cap(cfg, frac):
     return W.cache_capacity(cfg, frac)
 
 
+def host_cpus():
+    """The host's core count (os.cpu_count, what nproc reports without a mask) and the cores
+    this process may run on (its affinity mask), stated beside every CPU number."""
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        aff = None
+    return {"host_cpus": os.cpu_count(), "affinity_cpus": aff}
+
+
 def oracle_baseline(cfg, pool, budget_s=15.0, max_steps=64):
     """The oracle as it stands on this host's cores: LRU simulator + fp64 MoE layer over the
     first calls of the same trace until ~budget_s of CPU work. Returns tokens/s through
@@ -245,7 +317,7 @@ def oracle_baseline(cfg, pool, budget_s=15.0, max_steps=64):
             break
     dt = time.perf_counter() - t0
     return {"value": layer_tokens / cfg.layers / dt, "unit": "tokens/s", "cores": int(threads),
-            "kind": "oracle",
+            "kind": "oracle", **host_cpus(),
             "sample": "first %d layer calls (%d layer-tokens) of the same seeded trace, fp64 "
                       "numpy oracle + LRU simulator" % (calls, layer_tokens)}
 
@@ -291,7 +363,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg, W.cache_capacity(cfg), "n/a (CPU)"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": int(threads),
-                         "kind": "oracle",
+                         "kind": "oracle", **host_cpus(),
                          "sample": "steps %d..%d of the seeded trace; per step the cache "
                                    "simulator on all tokens and the fp64 layer on the first "
                                    "min(T, %d) tokens of the first %d layer(s), time scaled to "
@@ -313,6 +385,18 @@ def workload_config(cfg, C, l2):
 
 
 def run_ours(args):
+    line = decode_line(args)
+    if line is not None:
+        if not getattr(args, "no_extras", False) and args.workload == WORKLOAD and not args.tokens \
+                and not args.layers and not args.fused and line["n_gpus"] == 1:
+            line["extras"]["sub"] = sub_records(args)
+        print(json.dumps(line), flush=True)
+
+
+def decode_line(args):
+    """One decode workload on this rank's GPU; rank 0 returns the JSON line (dict), the
+    other ranks None. args.lite skips the end-to-end pass and the oracle baseline (the
+    sub-records of the default run)."""
     import torch
     import torch.distributed as dist
     import workloads as W
@@ -431,9 +515,10 @@ def run_ours(args):
     rs_ms, _, rtim, _, _, _ = timed_pass(cache_r, elastic=False)
     cache_r.close()
 
+    lite = getattr(args, "lite", False)
     # end to end through the C ABI with host buffers: H2D of x + logits, forward, D2H of out
     hx = [[(torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory(),
-            torch.from_numpy(d["logits"]).pin_memory()) for d in st] for st in trace]
+            torch.from_numpy(d["logits"]).pin_memory()) for d in st] for st in trace] if not lite else []
     oh = torch.empty((cfg.layers, cfg.t_max, cfg.hidden), dtype=torch.bfloat16).pin_memory()
     xd = torch.empty((cfg.layers, cfg.t_max, cfg.hidden), dtype=torch.bfloat16, device=dev)
     ld = torch.empty((cfg.layers, cfg.t_max, cfg.experts), dtype=torch.float32, device=dev)
@@ -441,7 +526,7 @@ def run_ours(args):
     cache_e = make(C)
     h2d = d2h = 0
     e2e_s = 0.0
-    for i in range(Wm + K):
+    for i in (range(Wm + K) if not lite else ()):
         if i in resizes:
             cache_e.resize(resizes[i])
         T = Ts[i]
@@ -466,7 +551,7 @@ def run_ours(args):
         if ws > 1:
             dist.barrier()
             dist.destroy_process_group()
-        return
+        return None
 
     peaks = _peaks()
     hbm = peaks.get("hbm_gbs")
@@ -478,7 +563,7 @@ def run_ours(args):
     misses = s1["misses"] - s0["misses"]
     hits = s1["hits"] - s0["hits"]
     fill_b = (s1["fill_bytes"] - s0["fill_bytes"]) + (s1["stage_bytes"] - s0["stage_bytes"])
-    base = oracle_baseline(cfg, pool, budget_s=args.cpu_budget)
+    base = oracle_baseline(cfg, pool, budget_s=args.cpu_budget) if not lite else None
     # q* of the pages' bandwidth-adaptive policy: of a step's m misses, about m * B_P / B_H
     # would be filled over PCIe and the rest computed in place on the CPU ([MTP] q* policy).
     # CPU execution is not built; the split is reported from the bandwidths measured here.
@@ -531,7 +616,7 @@ def run_ours(args):
                      "avg_launch_ms": ffn_ms / max(ffn_passes, 1)},
         "cpu_baseline": base,
         "e2e": {"value": tokens * ws / e2e_s, "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d // K, "d2h_bytes_per_step": d2h // K},
+                "h2d_bytes_per_step": h2d // K, "d2h_bytes_per_step": d2h // K} if not lite else None,
         "gpu_launches": int(tim["kernel_launches"]),
         "clocks": clocks,
         "extras": {
@@ -553,10 +638,10 @@ def run_ours(args):
                                                      "ffn_miss_ms", "combine_ms", "total_ms")},
         },
     }
-    print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+    return line
 
 
 def run_policy_compare(args):
@@ -637,6 +722,10 @@ def run_policy_compare(args):
 
 
 def run_prefill(args):
+    print(json.dumps(prefill_line(args)), flush=True)
+
+
+def prefill_line(args):
     """Prefill on the 35B-A3B-shaped layer (config 4's literal reading): 4096 tokens,
     near-uniform logits N(0, 0.5), ~256 tokens per expert; layers streamed double-buffered.
     Two numbers: (a) layers in order, every layer's 1.2 GB copied over PCIe (the method's
@@ -705,10 +794,15 @@ def run_prefill(args):
         # ~96 tokens per expert: the layer's weights bound it (the HBM ceiling is far below the
         # FP4 tensor peak), so the roofline is weight bytes per FFN second against HBM
         gbs = wbytes / (ffn_ms * 1e-3) / 1e9
+        fp4p = getattr(args, "fp4_peak", None) or fp4_peak_probe()
         roof = {"bound": "hbm", "kernel": "block-scaled tcgen05 grouped GEMM (MXFP4 x MXFP4: W13+SwiGLU, W2)",
                 "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs", "tflops": ffn_tflops,
-                "hbm_bound_ceiling_tflops": ceiling, "frac_of_hbm_ceiling": ffn_tflops / ceiling}
+                "hbm_bound_ceiling_tflops": ceiling, "frac_of_hbm_ceiling": ffn_tflops / ceiling,
+                "fp4_peak_tflops": fp4p["tflops"], "fp4_peak_source": fp4p["source"],
+                "frac_of_fp4_peak": ffn_tflops / fp4p["tflops"],
+                "ceiling_tflops": min(ceiling, fp4p["tflops"]),
+                "frac_of_ceiling": ffn_tflops / min(ceiling, fp4p["tflops"])}
         metric = ("MoE-layer prefill tokens/s (284B-shaped MXFP4 layer, 256 experts top-6, %d tokens, "
                   "layers streamed)" % T)
     else:
@@ -740,7 +834,92 @@ def run_prefill(args):
                    if ts["prefill_fill_ms"] > 0 else None,
                    "layer_weight_bytes": wbytes},
     }
-    print(json.dumps(line), flush=True)
+    return line
+
+
+# The FP4 tensor-core peak is not in MEASURED_PEAKS.json. It is measured here, in the same
+# process, with cuBLASLt's block-scaled NVFP4 GEMM (torch._scaled_mm, 8192^3, best of 10
+# back-to-back launches after a warm-up, CUDA events); where that call is unavailable the
+# value measured the same way on this machine earlier is reported, labelled as such.
+FP4_PEAK_EARLIER = 6740.0
+
+
+def fp4_peak_probe(n=8192, reps=10):
+    import torch
+    try:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        a = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+        b = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+        # per-16 E4M3 block scales in the swizzled 128 x 4 layout: (n / 128) x (n / 64) atoms
+        sa = torch.full((n * (n // 16),), 1.0, device=dev).to(torch.float8_e4m3fn)
+        sb = torch.full((n * (n // 16),), 1.0, device=dev).to(torch.float8_e4m3fn)
+        run = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(); run(); e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, sa, sb
+        return {"tflops": 2.0 * n ** 3 / (best * 1e-3) / 1e12,
+                "source": "measured in this run: cuBLASLt NVFP4 block-scaled GEMM (torch._scaled_mm), "
+                          "%d^3, best of %d, burst" % (n, reps)}
+    except Exception as e:  # noqa: BLE001 - the probe is optional; its absence is reported
+        return {"tflops": FP4_PEAK_EARLIER,
+                "source": "measured earlier on this pool the same way (cuBLASLt NVFP4 %d^3, burst); "
+                          "the live probe failed here: %s" % (n, str(e).splitlines()[0][:160])}
+
+
+SUB_RECORDS = (
+    # name, workload, steps, warmup, extra settings
+    ("decode_mxfp4", "decode_mxfp4", 8, 4, {}),
+    ("elastic_nvfp4", "elastic_nvfp4", 96, 16, {}),
+    ("prefill_mxfp4", "prefill_mxfp4", 8, 3, {}),
+    ("prefill_bf16", "prefill_bf16", 8, 3, {}),
+)
+
+
+def sub_records(args):
+    """The rest of the metric, measured in the default run after the headline: 43-layer MXFP4
+    decode, elastic NVFP4 decode, and MXFP4 / BF16 prefill at 4096 tokens, each with its own
+    CUDA-event timing and roofline block. Decode sub-records skip the end-to-end pass and the
+    oracle baseline (the headline carries both)."""
+    import torch
+    out = {}
+    fp4 = None
+    for name, wl, steps, warmup, extra in SUB_RECORDS:
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.steps, a.warmup, a.lite = wl, steps, warmup, True
+        a.layers, a.tokens, a.fused, a.ffn_traffic, a.all_resident = 0, 0, False, False, False
+        for k2, v in extra.items():
+            setattr(a, k2, v)
+        t0 = time.perf_counter()
+        try:
+            if wl in DECODE:
+                line = decode_line(a)
+            else:
+                if fp4 is None and wl == "prefill_mxfp4":
+                    fp4 = fp4_peak_probe()
+                a.fp4_peak = fp4
+                line = prefill_line(a)
+        except Exception as e:  # noqa: BLE001 - a failed sub-record must not hide the headline
+            out[name] = {"error": "%s: %s" % (type(e).__name__, (str(e).splitlines() or [""])[0][:200])}
+            line = None
+        try:
+            torch.cuda.synchronize()
+        except Exception:  # noqa: BLE001
+            pass
+        if line is None:
+            continue
+        for k2 in ("n_gpus", "higher_is_better", "scaling", "vs_baseline", "data", "cpu_baseline",
+                   "e2e", "clocks"):
+            line.pop(k2, None)
+        line["wall_s"] = time.perf_counter() - t0
+        out[name] = line
+    return out
 
 
 def main():
@@ -765,6 +944,8 @@ def main():
                     help="with --ffn-traffic: every selected expert resident (no fills)")
     ap.add_argument("--fused", action="store_true",
                     help="decode through the fused decode kernel (FT_FLAG_FUSED_DECODE; BF16)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default run: skip the sub-records of the other workloads")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare"])
     args = ap.parse_args()

@@ -12,6 +12,8 @@
 // tensor scale) is applied in fp32.
 #include "common.cuh"
 
+#include <atomic>
+
 namespace ftmoe {
 
 namespace {
@@ -234,16 +236,22 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) ffn_kernel(FfnParams p) {
 
 constexpr int kW2Rows = 4;
 
-int g_num_sms = 0;
+// SM count of each device, looked up once per device (relaxed atomics: concurrent first
+// lookups store the same value).
+constexpr int kMaxSmDevices = 64;
+std::atomic<int> g_num_sms[kMaxSmDevices];
 
 int grid_blocks() {
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 148;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxSmDevices) return 148 * 4;
+    int n = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+        g_num_sms[dev].store(n, std::memory_order_relaxed);
     }
-    return g_num_sms * 4;
+    return n * 4;
 }
 
 template <int FMT>

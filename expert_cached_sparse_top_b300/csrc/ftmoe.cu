@@ -457,6 +457,17 @@ ft_status encode_tc_maps(ft_moe* h) {
     return FT_OK;
 }
 
+// Back-off of the host's polling loops: spin for the first ~50 us (the lookup a decode call
+// waits for usually lands within that), then yield the core, and past ~2 ms sleep between
+// polls, so a long wait does not take a host core from the fill agent or the caller.
+void poll_backoff(std::chrono::steady_clock::time_point t0) {
+    const auto us = std::chrono::duration_cast<std::chrono::microseconds>(
+        std::chrono::steady_clock::now() - t0).count();
+    if (us < 50) return;
+    if (us < 2000) { std::this_thread::yield(); return; }
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+}
+
 // Wait for an event with a deadline (polling), so a wedged device turns into an error.
 ft_status wait_event(ft_moe* h, cudaEvent_t ev, const char* what) {
     auto t0 = std::chrono::steady_clock::now();
@@ -470,6 +481,7 @@ ft_status wait_event(ft_moe* h, cudaEvent_t ev, const char* what) {
             h->broken = true;
             return fail(h, FT_ERR_TIMEOUT, std::string(what) + ": host wait exceeded FTMOE_WAIT_MS");
         }
+        poll_backoff(t0);
     }
 }
 
@@ -503,6 +515,7 @@ ft_status agent_handle(ft_moe* h, const ft_moe::FillAgent::Job& job, std::string
             const auto dt = std::chrono::duration_cast<std::chrono::milliseconds>(
                 std::chrono::steady_clock::now() - t0).count();
             if (dt > h->wait_ms) { *msg = "fused decode routing: host wait exceeded FTMOE_WAIT_MS"; return FT_ERR_TIMEOUT; }
+            poll_backoff(t0);
         }
     }
     // a later call has routed already: this one had no misses (a call with misses holds the
@@ -1081,9 +1094,9 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
         // restart the epochs at a safe point (nothing of this handle in flight)
         ft_status ss = sync_handle(h);
         if (ss != FT_OK) return ss;
-        FT_CUDA(h, cudaMemset(h->d_mega, 0, (size_t)(16) * 4));
-        FT_CUDA(h, cudaMemset(h->d_mega + 64, 0, (size_t)h->max_u * 4));
-        FT_CUDA(h, cudaDeviceSynchronize());
+        FT_CUDA(h, cudaMemsetAsync(h->d_mega, 0, (size_t)(16) * 4, s));
+        FT_CUDA(h, cudaMemsetAsync(h->d_mega + 64, 0, (size_t)h->max_u * 4, s));
+        FT_CUDA(h, cudaStreamSynchronize(s));
         *(volatile int32_t*)h->h_seq = 0;
         *(volatile int32_t*)h->h_wseq = 0;
         h->mega_epoch = 0;

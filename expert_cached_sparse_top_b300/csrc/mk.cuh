@@ -44,6 +44,18 @@ __device__ __forceinline__ bool wait_ge_until(const int* p, int target, int* err
 
 // Fill flag of one missed expert: epoch once its blob is in place; -e with e >= epoch once
 // the host abandoned this call (and any later one) before copying it.
+//
+// The flag is written by a copy stream that the host feeds while this kernel runs, so the
+// wait depends on the GPU running that stream's copies concurrently with the cooperative
+// launch. Where GPU work is serialised (a profiler replaying one kernel at a time), the copy
+// cannot run until the kernel ends and the wait runs out. It gives up a quarter of the call's
+// wait budget before every other wait of the launch (`deadline` is the launch's common one),
+// so the code recorded first is 21 and names the missing fill, not the stage or accumulator
+// waits that stall behind it.
+__device__ __forceinline__ uint64_t fill_deadline(uint64_t deadline, int64_t wait_ns) {
+    return deadline - (uint64_t)(wait_ns / 4);
+}
+
 __device__ __forceinline__ bool wait_fill_until(const int* p, int epoch, int* err, uint64_t deadline) {
     uint32_t ns = 64;
     for (uint32_t i = 0;; ++i) {

@@ -17,6 +17,8 @@
 #include "common.cuh"
 #include "../../include/ftmoe.h"
 
+#include <atomic>
+
 namespace ftmoe {
 namespace {
 
@@ -29,8 +31,11 @@ static_assert(kNoAllocBytes > kListBytes, "scratch too small");
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
+// Device address of the array, per device, looked up on the first call there. Threads that
+// make their first calls at the same time may both look it up; they store the same value, and
+// the atomics make that benign.
 constexpr int kMaxDevices = 64;
-uint8_t* g_scratch_addr[kMaxDevices] = {nullptr};
+std::atomic<uint8_t*> g_scratch_addr[kMaxDevices];
 
 // One-entry work list: a single resident expert (slot 0) that every token visits once.
 __global__ void noalloc_list_kernel(uint8_t* scratch, int T) {
@@ -65,14 +70,15 @@ extern "C" ft_status ft_expert_ffn_noalloc(const void* blob, int32_t wfmt, int32
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FT_ERR_CUDA;
-    if (!g_scratch_addr[dev]) {
+    uint8_t* scratch = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!scratch) {
         // First call on this device: look up the array's device address (host code cannot
         // use the symbol itself as a pointer).
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FT_ERR_CUDA;
-        g_scratch_addr[dev] = static_cast<uint8_t*>(p);
+        scratch = static_cast<uint8_t*>(p);
+        g_scratch_addr[dev].store(scratch, std::memory_order_relaxed);
     }
-    uint8_t* scratch = g_scratch_addr[dev];
     cudaStream_t s = (cudaStream_t)stream;
 
     noalloc_list_kernel<<<1, 256, 0, s>>>(scratch, T);

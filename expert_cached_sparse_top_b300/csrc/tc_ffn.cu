@@ -275,7 +275,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed; W13
                     // activation rows only once the entry's rows are gathered
-                    if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err, deadline)) {
+                    if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err,
+                                                                 fill_deadline(deadline, mg.wait_ns))) {
                         ok = false;
                         break;
                     }

@@ -413,7 +413,8 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const int slot = ldr<MK>(p.entry_dst + tl.u);
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed
-                    if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err, deadline)) {
+                    if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err,
+                                                                 fill_deadline(deadline, mg.wait_ns))) {
                         ok = false;
                         break;
                     }

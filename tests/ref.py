@@ -45,9 +45,30 @@ def oracle_call(experts, layer, x_bits, logits, k, tokens=None, ffn=None):
 
 
 def normwise_err(got, ref):
+    """Normwise relative error of a whole call: ||got - ref||_F / ||ref||_F."""
     ref = np.asarray(ref, dtype=np.float64)
     den = np.linalg.norm(ref)
     return float(np.linalg.norm(np.asarray(got, dtype=np.float64) - ref) / max(den, 1e-30))
+
+
+def token_err(got, ref):
+    """Worst per-token normwise relative error: max over rows t of ||got_t - ref_t|| / ||ref_t||.
+    A few wrong tokens in a large call stay under a whole-call bound; they do not stay under
+    this one."""
+    ref = np.asarray(ref, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    ref2 = ref.reshape(ref.shape[0], -1)
+    num = np.linalg.norm(got.reshape(ref2.shape) - ref2, axis=1)
+    den = np.maximum(np.linalg.norm(ref2, axis=1), 1e-30)
+    return float((num / den).max())
+
+
+def out_err(got, ref):
+    """The error the parity tests bound by TOL: the larger of the whole-call normwise error and
+    the worst per-token normwise error (both at the same tolerance)."""
+    return max(normwise_err(got, ref), token_err(got, ref))
 
 
 def to_dev_bf16(bits):

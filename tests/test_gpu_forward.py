@@ -7,7 +7,7 @@ import pytest
 
 import workloads as W
 from workloads.host import HostPool
-from ref import (TOL, OracleExperts, Runner, bf16_dev_to_f64, normwise_err, oracle_call,
+from ref import (TOL, OracleExperts, Runner, bf16_dev_to_f64, out_err, oracle_call,
                  to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def test_tiny_layer_router_in_the_loop(ft):
         assert np.array_equal(idx, ref_idx)
         assert np.max(np.abs(w - ref_w)) <= 2e-6
         outs.append(bf16_dev_to_f64(out))
-        assert normwise_err(outs[-1], ref_out) <= TOL["bf16"]
+        assert out_err(outs[-1], ref_out) <= TOL["bf16"]
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
     st = cache.stats()
     U = len(np.unique(ref_idx))
@@ -78,7 +78,7 @@ def test_decode_bf16_trace_parity(ft, bf16_pool):
         out, idx, w = run.call(0, d["x"], d["logits"])
         ref_out, ref_idx, ref_w = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
         assert np.array_equal(idx, ref_idx)
-        worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref_out))
+        worst = max(worst, out_err(bf16_dev_to_f64(out), ref_out))
         if s % 3 == 0:
             run.check_state()
     assert worst <= TOL["bf16"], worst
@@ -104,7 +104,7 @@ def test_decode_bf16_fixed_T(ft, bf16_pool, T, path, monkeypatch):
         d = step[0]
         out, idx, w = run.call(0, d["x"], d["logits"])
         ref_out, _, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
-        assert normwise_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
+        assert out_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
     run.check_state()
     cache.close()
 
@@ -183,7 +183,7 @@ def test_elastic_nvfp4_full_size(ft):
         if s % 2 == 0:
             ref_out, ref_idx, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
             assert np.array_equal(idx, ref_idx)
-            worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref_out))
+            worst = max(worst, out_err(bf16_dev_to_f64(out), ref_out))
     assert worst <= TOL["nvfp4"], worst
     run.check_state()
     cache.close()
@@ -206,8 +206,41 @@ def test_mxfp4_43_layers_full_size(ft):
             if d["layer"] in (0, 21, 42):
                 ref_out, ref_idx, _ = oracle_call(experts, d["layer"], d["x"], d["logits"], cfg.top_k)
                 assert np.array_equal(idx, ref_idx)
-                worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref_out))
+                worst = max(worst, out_err(bf16_dev_to_f64(out), ref_out))
         run.check_state()
+    assert worst <= TOL["mxfp4"], worst
+    cache.close()
+
+
+def test_mxfp4_43_layers_full_trace_small_shape(ft):
+    """The 284B-shaped cache over its whole trace: 256 steps x 43 layers (11,008 calls) into
+    one global LRU of 2201 slots (20 % of 43 x 256 keys), at a reduced expert size (H = I =
+    256). Every call's hits, misses, bypasses and evictions are checked against the oracle's
+    LRU simulator, the full cache state every 32 steps and at the end, and sampled outputs
+    against the oracle layer."""
+    cfg = W.config("decode_mxfp4", hidden=256, inter=256)
+    pool = HostPool(cfg, images=13)
+    C = W.cache_capacity(cfg)
+    assert C == 2201
+    cache = _make(ft, cfg, pool, C)
+    run = Runner(cache, cfg, C)
+    experts = OracleExperts(pool, max_cached=13)
+    worst = 0.0
+    n = 0
+    for s, step in enumerate(W.decode_trace(cfg)):
+        for d in step:
+            out, idx, _ = run.call(d["layer"], d["x"], d["logits"])
+            n += 1
+            if s % 32 == 0 and d["layer"] in (0, 42):
+                ref_out, ref_idx, _ = oracle_call(experts, d["layer"], d["x"], d["logits"], cfg.top_k)
+                assert np.array_equal(idx, ref_idx)
+                worst = max(worst, out_err(bf16_dev_to_f64(out), ref_out))
+        if s % 32 == 31:
+            run.check_state()
+    run.check_state()
+    assert n == 256 * 43
+    st = cache.stats()
+    assert st["calls"] == n
     assert worst <= TOL["mxfp4"], worst
     cache.close()
 
@@ -226,7 +259,7 @@ def test_ragged_and_empty_calls(ft):
         out, idx, _ = run.call(0, x, logits)
         ref_out, ref_idx, _ = oracle_call(experts, 0, x, logits, cfg.top_k)
         assert np.array_equal(idx, ref_idx)
-        assert normwise_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
+        assert out_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
     run.check_state()
     before = cache.stats()
     x = to_dev_bf16(W.tiny_inputs(cfg))

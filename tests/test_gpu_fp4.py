@@ -7,7 +7,7 @@ import pytest
 
 import workloads as W
 from workloads.host import HostPool
-from ref import TOL, OracleExperts, Runner, bf16_dev_to_f64, normwise_err, oracle_call
+from ref import TOL, OracleExperts, Runner, bf16_dev_to_f64, out_err, oracle_call
 
 pytestmark = pytest.mark.gpu
 
@@ -59,12 +59,12 @@ def test_fp4_decode_fixed_T(ft, fmt, T, path, monkeypatch):
     run = Runner(cache, cfg, C)
     experts = OracleExperts(pool, max_cached=8 if fmt == "mxfp4" else 64)
     worst = 0.0
-    for step in W.decode_trace(cfg, steps=3):
+    for step in W.decode_trace(cfg, steps=8):
         d = step[0]
         out, idx, _ = run.call(0, d["x"], d["logits"])
         ref_out, ref_idx, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
         assert np.array_equal(idx, ref_idx)
-        worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref_out))
+        worst = max(worst, out_err(bf16_dev_to_f64(out), ref_out))
     run.check_state()
     cache.close()
     print("%s %s T=%d worst normwise err %.3e" % (fmt, path, T, worst))

@@ -13,7 +13,7 @@ import pytest
 import workloads as W
 from workloads.host import HostPool
 from oracle import lru, policies
-from ref import (TOL, OracleExperts, Runner, bf16_dev_to_f64, normwise_err, oracle_call, to_dev,
+from ref import (TOL, OracleExperts, Runner, bf16_dev_to_f64, out_err, oracle_call, to_dev,
                  to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -67,7 +67,7 @@ def test_fused_decode_bf16_trace_parity(ft, bf16_pool):
             ref_out, ref_idx, ref_w = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
             assert np.array_equal(idx, ref_idx)
             assert np.max(np.abs(w - ref_w)) <= 2e-6
-            worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref_out))
+            worst = max(worst, out_err(bf16_dev_to_f64(out), ref_out))
             for r in runs:
                 r.check_state()
     assert worst <= TOL["bf16"], worst
@@ -89,7 +89,7 @@ def test_fused_fixed_T_all_resident_and_cold(ft, bf16_pool, T):
     outs = []
     for _ in range(3):
         out, _, _ = _pair_call(runs, 0, d["x"], d["logits"])
-        assert normwise_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
+        assert out_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
         outs.append(out.clone())
     assert bool((outs[0] == outs[2]).all())
     st = runs[1].cache.stats()
@@ -194,7 +194,7 @@ def test_fused_router_in_the_loop_and_ragged(ft):
         lg = moe.router_logits(formats.bf16_to_f64(x), router[0])
         out, idx, _ = _pair_call(runs, 0, x, None)
         ref_out, _, _ = oracle_call(experts, 0, x, lg, cfg.top_k)
-        assert normwise_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
+        assert out_err(bf16_dev_to_f64(out), ref_out) <= TOL["bf16"]
     for r in runs:
         r.check_state()
     cache = runs[1].cache
@@ -322,7 +322,7 @@ def test_fused_fp4_matches_default_and_simulator(ft, name):
             if s % 4 == 1 and d["layer"] == 0:
                 ref, ref_idx, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
                 assert np.array_equal(idx, ref_idx)
-                worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref))
+                worst = max(worst, out_err(bf16_dev_to_f64(out), ref))
         if s % 4 == 0:
             for r in runs:
                 r.check_state()
@@ -362,7 +362,7 @@ def test_32_token_tiles_default_and_fused(ft, bf16_pool, T):
         if s % 2 == 0:
             ref, ref_idx, _ = oracle_call(experts, 0, d["x"], d["logits"], cfg.top_k)
             assert np.array_equal(idx, ref_idx)
-            assert normwise_err(bf16_dev_to_f64(out), ref) <= TOL["bf16"]
+            assert out_err(bf16_dev_to_f64(out), ref) <= TOL["bf16"]
     for r in runs:
         r.check_state()
         r.cache.close()
@@ -383,7 +383,7 @@ def test_fp4_32_token_tiles(ft, fmt):
     for C in (W.cache_capacity(cfg), 0):
         run = Runner(_make(ft, cfg, pool, C, False, max_tokens=32), cfg, C)
         out, _, _ = run.call(0, d["x"], d["logits"])
-        assert normwise_err(bf16_dev_to_f64(out), ref) <= TOL[fmt]
+        assert out_err(bf16_dev_to_f64(out), ref) <= TOL[fmt]
         outs.append(out.clone())
         run.cache.close()
     assert torch.equal(outs[0], outs[1])

@@ -8,7 +8,7 @@ import pytest
 import workloads as W
 from workloads.host import HostPool
 from oracle import lru, policies
-from ref import TOL, OracleExperts, Runner, bf16_dev_to_f64, normwise_err, oracle_call
+from ref import TOL, OracleExperts, Runner, bf16_dev_to_f64, out_err, oracle_call
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_layer_lru_matches_simulator(ft):
             if s % 6 == 0 and d["layer"] == 2:
                 ref, ref_idx, _ = oracle_call(experts, d["layer"], d["x"], d["logits"], cfg.top_k)
                 assert np.array_equal(idx, ref_idx)
-                worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref))
+                worst = max(worst, out_err(bf16_dev_to_f64(out), ref))
         if s % 4 == 0:
             run.check_state()
     run.check_state()
@@ -83,7 +83,7 @@ def test_static_set_matches_simulator(ft):
             out, idx, _ = run.call(d["layer"], d["x"], d["logits"])
             if s % 6 == 0 and d["layer"] == 1:
                 ref, _, _ = oracle_call(experts, d["layer"], d["x"], d["logits"], cfg.top_k)
-                worst = max(worst, normwise_err(bf16_dev_to_f64(out), ref))
+                worst = max(worst, out_err(bf16_dev_to_f64(out), ref))
     run.check_state()
     assert np.array_equal(cache.snapshot()[0], before)   # the resident set never changes
     st = cache.stats()

@@ -5,7 +5,7 @@ import pytest
 
 import workloads as W
 from workloads.host import HostPool
-from ref import TOL, OracleExperts, bf16_dev_to_f64, normwise_err, oracle_call, to_dev, to_dev_bf16
+from ref import TOL, OracleExperts, bf16_dev_to_f64, out_err, oracle_call, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,7 @@ def test_prefill_bf16_layers_in_order(ft):
         got = bf16_dev_to_f64(out)
         if tokens is not None:
             got = got[tokens]
-        assert normwise_err(got, ref) <= TOL["bf16"], layer
+        assert out_err(got, ref) <= TOL["bf16"], layer
     st = cache.stats()
     assert st["hits"] == 0 and st["misses"] == 0          # the LRU is not consulted
     cache.close()
@@ -76,7 +76,7 @@ def test_prefill_ragged_token_counts(ft):
         x, logits = W.prefill_inputs(cfg, layer, tokens=T)
         out = _run(cache, cfg, layer, x, logits)
         ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k)
-        assert normwise_err(bf16_dev_to_f64(out), ref) <= TOL["bf16"], (layer, T)
+        assert out_err(bf16_dev_to_f64(out), ref) <= TOL["bf16"], (layer, T)
     cache.close()
 
 
@@ -102,13 +102,13 @@ def test_prefill_mxfp4_shape(ft, path, monkeypatch):
             ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample,
                                     ffn=moe.expert_ffn_w4a4)
             plain, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample)
-            err = normwise_err(got[sample], ref)
+            err = out_err(got[sample], ref)
             print("layer %d: vs act-quant oracle %.3e, vs plain oracle %.3e (information)"
-                  % (layer, err, normwise_err(got[sample], plain)))
+                  % (layer, err, out_err(got[sample], plain)))
             assert err <= TOL["mxfp4"], (layer, err)
         else:
             ref, _, _ = oracle_call(experts, layer, x, logits, cfg.top_k, tokens=sample)
-            assert normwise_err(got[sample], ref) <= TOL["mxfp4"], layer
+            assert out_err(got[sample], ref) <= TOL["mxfp4"], layer
     cache.close()
 
 
@@ -126,7 +126,7 @@ def test_prefill_router_in_the_loop(ft):
     experts = OracleExperts(pool)
     ref, _, _ = oracle_call(experts, 0, x, ref_logits, cfg.top_k, tokens=keep)
     assert len(keep) > 48
-    assert normwise_err(bf16_dev_to_f64(out)[keep], ref) <= TOL["bf16"]
+    assert out_err(bf16_dev_to_f64(out)[keep], ref) <= TOL["bf16"]
     cache.close()
 
 

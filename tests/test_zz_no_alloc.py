@@ -5,13 +5,15 @@ output: an engine that has already handed its whole VRAM budget to its own exper
 a serving loop that forbids cudaMalloc/cudaFree after start-up because those calls can stall
 or synchronise the device in the middle of a step. Its scratch is a fixed array compiled
 into the library. This file checks, through the C ABI, that two calls in a row give the
-same result as the cached forward (ft_moe_forward) over a one-expert, top-1 layer, within
-the tolerance the other parity tests use. It is collected last on purpose.
+same result as the oracle's expert FFN (the plain SwiGLU definition in fp64 on the decoded
+blob) and as the cached forward (ft_moe_forward) over a one-expert, top-1 layer, within the
+tolerance the other parity tests use. It is collected last on purpose.
 """
 import numpy as np
 import pytest
 
 import workloads as W
+from oracle import formats, moe
 from workloads.host import HostPool
 
 pytestmark = pytest.mark.gpu
@@ -33,20 +35,21 @@ def ft():
 def _x(cfg, T, seed):
     bits = W.tiny_inputs(W.config("tiny", hidden=cfg.hidden, tokens=T, seed=seed))
     import torch
-    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    return bits, torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
 
 
 @pytest.mark.parametrize("name,H,I", [("decode_bf16", 256, 128), ("decode_mxfp4", 512, 256),
                                       ("elastic_nvfp4", 2048, 768)])
-def test_noalloc_matches_cached_forward_twice(ft, name, H, I):
+def test_noalloc_matches_oracle_and_cached_forward_twice(ft, name, H, I):
     import torch
     cfg = W.config(name, layers=1, experts=1, top_k=1, hidden=H, inter=I)
     pool = HostPool(cfg)
     blob = torch.from_numpy(pool.arr[0].copy()).cuda()
     c = ft.make_config(1, 1, H, I, 1, 16, cfg.wfmt, 1)
     cache = ft.MoECache(c, pool.ptrs, None)
+    w1, w3, w2 = formats.decode_blob(pool.blob(0), cfg.fmt, H, I)
     for call, T in enumerate((16, 7)):                  # two calls in a row
-        x = _x(cfg, T, seed=10 + call)
+        bits, x = _x(cfg, T, seed=10 + call)
         y = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
         ft.expert_ffn_noalloc(blob, cfg.wfmt, H, I, x, T, y)
         out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
@@ -54,8 +57,11 @@ def test_noalloc_matches_cached_forward_twice(ft, name, H, I):
         cache.forward(0, x, T, out, logits=logits)       # top-1 of one expert: weight 1
         torch.cuda.synchronize()
         got = y.double().cpu().numpy()
-        ref = out.double().cpu().numpy()
         assert np.isfinite(got).all()
+        want, _ = moe.expert_ffn(w1, w3, w2, formats.bf16_to_f64(bits))
+        err_oracle = np.linalg.norm(got - want) / np.linalg.norm(want)
+        assert err_oracle <= TOL[cfg.wfmt], (call, err_oracle)
+        ref = out.double().cpu().numpy()
         err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
         assert err <= TOL[cfg.wfmt], (call, err)
     cache.close()
