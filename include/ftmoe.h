@@ -115,7 +115,12 @@ typedef enum { FT_POLICY_GLOBAL_LRU = 0, FT_POLICY_LAYER_LRU = 1, FT_POLICY_STAT
  *   of the handle reads each call's miss list and enqueues its copies. Errors found on the
  *   device or by that thread (a NaN logit, a failed copy, a wait that ran out) are returned by
  *   the next call on the handle or by the next safe point (ft_cache_stats, ft_cache_snapshot,
- *   ft_cache_resize, ft_cache_pin, ft_moe_timing). ft_timing_t reports the whole kernel as
+ *   ft_cache_resize, ft_cache_pin, ft_moe_timing). A call with misses can finish only if the
+ *   GPU runs the copy stream's fills while the cooperative kernel is resident (its miss tiles
+ *   wait for them); where GPU work is serialised, e.g. under a profiler that replays kernels
+ *   one at a time, that wait runs out (after FTMOE_WAIT_MS, at most 4 s), the kernel ends, and
+ *   the next call reports FT_ERR_CUDA with code 21. Calls whose experts are all resident do
+ *   not depend on any copy. ft_timing_t reports the whole kernel as
  *   ffn_hit_ms (route_ms covers only the router logits, if computed; ffn_miss_ms and
  *   combine_ms stay 0). */
 #define FT_FLAG_FUSED_DECODE 0x100
