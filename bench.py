@@ -94,8 +94,9 @@ class Clocks:
             self.nv = pynvml
             self.handle = self._handle(pynvml, index)
             self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
-        except Exception:
+        except Exception as e:  # noqa: BLE001 - fall back to nvidia-smi, keep the reason
             self.nv = None
+            self.nvml_error = "%s: %s" % (type(e).__name__, str(e)[:120])
         if self.nv is not None:
             self.stop_ev = threading.Event()
             self.period = period_s
@@ -172,7 +173,8 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm), "source": "nvidia-smi, 50 ms period"}
+                "samples": len(sm), "source": "nvidia-smi, 50 ms period",
+                "nvml_error": getattr(self, "nvml_error", None)}
 
 
 def _peaks():
@@ -794,15 +796,25 @@ def prefill_line(args):
         # ~96 tokens per expert: the layer's weights bound it (the HBM ceiling is far below the
         # FP4 tensor peak), so the roofline is weight bytes per FFN second against HBM
         gbs = wbytes / (ffn_ms * 1e-3) / 1e9
-        fp4p = getattr(args, "fp4_peak", None) or fp4_peak_probe()
-        roof = {"bound": "hbm", "kernel": "block-scaled tcgen05 grouped GEMM (MXFP4 x MXFP4: W13+SwiGLU, W2)",
+        probe = getattr(args, "fp4_peak", None) or fp4_peak_probe()
+        # FP4 dense peak: the measured BF16 peak x the nominal FP4 / BF16 ratio (13.5 / 2.25);
+        # the activations enter the MMA as four E2M1 pieces, so the tensor pipe issues 4x the
+        # useful flops and the tensor-bound ceiling of useful flops is a quarter of that peak
+        fp4_peak = bf16 * 6.0 if bf16 else None
+        pieces = 4
+        tensor_ceiling = fp4_peak / pieces if fp4_peak else None
+        ceil = min(ceiling, tensor_ceiling) if tensor_ceiling else ceiling
+        roof = {"bound": "hbm", "kernel": "block-scaled tcgen05 grouped GEMM (%s weights x bf16 activations "
+                                          "as four E2M1 pieces: W13+SwiGLU, W2)" % cfg.wfmt.upper(),
                 "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs", "tflops": ffn_tflops,
+                "tensor_tflops_issued": ffn_tflops * pieces,
                 "hbm_bound_ceiling_tflops": ceiling, "frac_of_hbm_ceiling": ffn_tflops / ceiling,
-                "fp4_peak_tflops": fp4p["tflops"], "fp4_peak_source": fp4p["source"],
-                "frac_of_fp4_peak": ffn_tflops / fp4p["tflops"],
-                "ceiling_tflops": min(ceiling, fp4p["tflops"]),
-                "frac_of_ceiling": ffn_tflops / min(ceiling, fp4p["tflops"])}
+                "fp4_peak_tflops": fp4_peak,
+                "fp4_peak_source": "MEASURED_PEAKS.json bf16_tflops x 6 (nominal FP4 / BF16 dense ratio)",
+                "frac_of_fp4_peak": (ffn_tflops * pieces / fp4_peak) if fp4_peak else None,
+                "cublaslt_nvfp4_probe_tflops": probe["tflops"], "cublaslt_nvfp4_probe_source": probe["source"],
+                "ceiling_tflops": ceil, "frac_of_ceiling": ffn_tflops / ceil}
         metric = ("MoE-layer prefill tokens/s (284B-shaped MXFP4 layer, 256 experts top-6, %d tokens, "
                   "layers streamed)" % T)
     else:
@@ -817,7 +829,7 @@ def prefill_line(args):
         "value": T * cfg.layers / stream_s, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * stream_s / cfg.layers,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 weights x mxfp4 activations" if fp4 else "bf16",
+        "dtype": ("%s weights x bf16 activations (four E2M1 pieces)" % cfg.wfmt) if fp4 else "bf16",
         "data": "synthetic",
         "config": {"workload": args.workload, "tokens": T, "experts": cfg.experts, "top_k": cfg.top_k,
                    "hidden": cfg.hidden, "inter": cfg.inter, "layers": cfg.layers,

@@ -63,6 +63,24 @@ struct LookupParams {
     RouteHostView hv;
 };
 
+// One layer-ahead prefetch (prefetch_kernel): a predicted expert set inserted into the LRU.
+struct PrefetchParams {
+    const int32_t* expert_ids; // [n] predicted experts of `layer` (duplicates allowed)
+    int32_t n;
+    int32_t layer;
+    int32_t experts;
+    int64_t capacity;          // C
+    int64_t list_len;          // entries of the order (C)
+    int64_t protect;           // most recent entries that may not be evicted (<= list_len)
+    int32_t* table;            // [L*E]
+    int32_t* slot_key;         // [C]
+    const int32_t* order_in;   // [C] least recent first
+    int32_t* order_out;        // [C]
+    int32_t* hv_counts;        // host-mapped: inserted, evictions, skipped, error bits
+    int32_t* hv_key;           // host-mapped [max]: key of insert j
+    int32_t* hv_dst;           // host-mapped [max]: its slot
+};
+
 // Weight-section offsets inside one expert blob.
 struct BlobLayout {
     int64_t blob_bytes;
@@ -101,6 +119,7 @@ cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_
                                 float* w, int32_t* idx2, float* w2, int32_t* nan_flag,
                                 cudaStream_t s);
 cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s);
+cudaError_t launch_prefetch(const PrefetchParams& p, cudaStream_t s);
 cudaError_t launch_ffn(int fmt, const FfnParams& p, int max_tokens, cudaStream_t s,
                        int* kernels_launched);
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H,

@@ -58,6 +58,8 @@ struct StageEvents {
     bool has_fill;
     bool has_miss;
     cudaEvent_t fill_begin, fill_end;
+    cudaEvent_t pf_begin, pf_end;        // prefetch fills issued for this call (ft_cache_prefetch)
+    bool pf_wait;                        // ev[6] -> ev[7]: the call's stream waited for them
 };
 
 struct PrefillEvents {
@@ -186,11 +188,9 @@ struct ft_moe {
     CUtensorMap tmP_A13[2]{}, tmP_A2[2]{};
     CUtensorMap tmP_B13[5]{}, tmP_B2[5]{};     // per N tile width 16..256
     bool p_b_ok[5] = {false, false, false, false, false};
-    // prefill on the block-scaled tensor cores (MXFP4 weights, MXFP4 activations)
+    // prefill on the block-scaled tensor cores (FP4 weights, activations as E2M1 pieces)
     bool use_fp4_prefill = false;
     int64_t p_fp4_tiles = 0;
-    uint8_t* d_p_tq = nullptr;            // token-major activation codes [T][H/2]
-    uint8_t* d_p_tsf = nullptr;           // and scale bytes [T][H/32]
     uint8_t* d_p_fxq = nullptr;           // W13 N operand (tile-major), scale atoms, row scales
     uint8_t* d_p_fxsf = nullptr;
     float* d_p_fxrs = nullptr;
@@ -198,6 +198,17 @@ struct ft_moe {
     uint8_t* d_p_fasf = nullptr;
     CUtensorMap tmPF_A13[2]{}, tmPF_A2[2]{}, tmPF_B13{}, tmPF_B2{};
     std::vector<PrefillEvents> p_pending;
+
+    // layer-ahead prefetch (ft_cache_prefetch)
+    cudaStream_t pf_stream = nullptr;
+    cudaEvent_t ev_pf_in = nullptr, ev_pf_route = nullptr, ev_pf_fill = nullptr;
+    uint8_t* h_pf = nullptr;              // host-mapped: counts[4], keys[max_pairs], slots[max_pairs]
+    uint8_t* d_pf = nullptr;              // its device address
+    bool pf_route_pending = false;        // a prefetch since the last forward: order its lookup first
+    bool pf_fill_pending = false;         // and its copies before the next forward's expert FFN
+    int64_t protect = 0;                  // most recent LRU entries of the call in flight (+ prefetched)
+    cudaEvent_t pf_fill_begin = nullptr, pf_fill_end = nullptr;   // timing of pending prefetch fills
+    cudaEvent_t last_end_ev = nullptr;    // timing: end of the previous recorded forward (fill lead)
 
     bool timing = false;
     std::deque<StageEvents> pending;
@@ -393,7 +404,7 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
     cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
     cudaFree(h->d_p_route_mem); cudaFree(h->d_p_xp); cudaFree(h->d_p_act); cudaFree(h->d_p_y);
-    cudaFree(h->d_p_tq); cudaFree(h->d_p_tsf); cudaFree(h->d_p_fxq); cudaFree(h->d_p_fxsf);
+    cudaFree(h->d_p_fxq); cudaFree(h->d_p_fxsf);
     cudaFree(h->d_p_fxrs); cudaFree(h->d_p_faq); cudaFree(h->d_p_fasf);
     for (int b = 0; b < 2; ++b) {
         if (h->ev_buf_ready[b]) cudaEventDestroy(h->ev_buf_ready[b]);
@@ -404,7 +415,13 @@ void free_all(ft_moe* h) {
             if (ev) h->event_pool.push_back(ev);
     }
     h->p_pending.clear();
+    if (h->pf_stream) cudaStreamSynchronize(h->pf_stream);
     if (h->h_mapped) cudaFreeHost(h->h_mapped);
+    if (h->h_pf) cudaFreeHost(h->h_pf);
+    if (h->pf_stream) cudaStreamDestroy(h->pf_stream);
+    for (cudaEvent_t ev : {h->ev_pf_in, h->ev_pf_route, h->ev_pf_fill, h->pf_fill_begin, h->pf_fill_end,
+                           h->last_end_ev})
+        if (ev) cudaEventDestroy(ev);
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     if (h->copy_stream2) cudaStreamDestroy(h->copy_stream2);
     if (h->ev_copy2) cudaEventDestroy(h->ev_copy2);
@@ -415,6 +432,8 @@ void free_all(ft_moe* h) {
         for (auto ev : se.ev) h->event_pool.push_back(ev);
         h->event_pool.push_back(se.fill_begin);
         h->event_pool.push_back(se.fill_end);
+        h->event_pool.push_back(se.pf_begin);
+        h->event_pool.push_back(se.pf_end);
     }
     h->pending.clear();
     for (auto ev : h->event_pool) if (ev) cudaEventDestroy(ev);
@@ -687,6 +706,7 @@ ft_status sync_handle(ft_moe* h) {
     if (s != FT_OK) return s;
     FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
     if (h->copy_stream2) FT_CUDA(h, cudaStreamSynchronize(h->copy_stream2));
+    if (h->pf_stream) FT_CUDA(h, cudaStreamSynchronize(h->pf_stream));
     if (h->h_ffn_err && *(volatile int*)h->h_ffn_err) {
         h->broken = true;
         return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait (code " +
@@ -716,7 +736,22 @@ float ev_ms(cudaEvent_t a, cudaEvent_t b) {
 void collect_timing(ft_moe* h) {
     for (auto& se : h->pending) {
         cudaEventSynchronize(se.ev[5]);
-        h->tsum.route_ms += ev_ms(se.ev[0], se.ev[1]);
+        // fill lead: how long before the previous call ended this call's first copy started
+        // (a prefetch issued for it, else its own miss fills)
+        cudaEvent_t first = se.pf_begin ? se.pf_begin : (se.has_fill ? se.fill_begin : nullptr);
+        if (first && h->last_end_ev) {
+            if (se.pf_begin) cudaEventSynchronize(se.pf_end);
+            if (se.has_fill) cudaEventSynchronize(se.fill_end);
+            h->tsum.fill_lead_ms += ev_ms(first, h->last_end_ev);
+            h->tsum.fill_lead_calls++;
+        }
+        if (se.pf_begin) {
+            cudaEventSynchronize(se.pf_end);
+            h->tsum.prefetch_fill_ms += ev_ms(se.pf_begin, se.pf_end);
+        }
+        const double pf_wait = se.pf_wait ? ev_ms(se.ev[6], se.ev[7]) : 0.0;
+        h->tsum.prefetch_wait_ms += pf_wait;
+        h->tsum.route_ms += ev_ms(se.ev[0], se.ev[1]) - pf_wait;
         h->tsum.ffn_hit_ms += ev_ms(se.ev[1], se.ev[2]);
         if (se.has_miss) h->tsum.ffn_miss_ms += ev_ms(se.ev[3], se.ev[4]);
         h->tsum.combine_ms += ev_ms(se.ev[4], se.ev[5]);
@@ -727,9 +762,15 @@ void collect_timing(ft_moe* h) {
             h->tsum.fill_ms += f;
             h->stats.fill_ns += (uint64_t)(f * 1e6);
         }
-        for (auto ev : se.ev) h->event_pool.push_back(ev);
+        // ev[5] (the call's end) stays out of the pool until the next call's lead is taken
+        for (int i = 0; i < 8; ++i)
+            if (i != 5) h->event_pool.push_back(se.ev[i]);
+        if (h->last_end_ev) h->event_pool.push_back(h->last_end_ev);
+        h->last_end_ev = se.ev[5];
         h->event_pool.push_back(se.fill_begin);
         h->event_pool.push_back(se.fill_end);
+        if (se.pf_begin) h->event_pool.push_back(se.pf_begin);
+        if (se.pf_end) h->event_pool.push_back(se.pf_end);
     }
     h->pending.clear();
     for (auto& pe : h->p_pending) {
@@ -769,7 +810,7 @@ ft_status alloc_prefill(ft_moe* h) {
     FT_CUDA(h, dm((void**)&h->d_p_err, 64));
     FT_CUDA(h, cudaMemset(h->d_p_err, 0, 64));
     {
-        const size_t bytes = 256 + 4 * ((size_t)E + (size_t)E + (size_t)E + 1 + (size_t)npairs + (size_t)E) + 64;
+        const size_t bytes = 256 + 4 * ((size_t)E + (size_t)E + (size_t)E + 1 + (size_t)npairs + 2 * (size_t)E) + 64;
         FT_CUDA(h, dm((void**)&h->d_p_route_mem, bytes));
         uint8_t* p = h->d_p_route_mem;
         h->p_rb.counts = (RouteCounts*)p; p += 256;
@@ -778,21 +819,21 @@ ft_status alloc_prefill(ft_moe* h) {
         h->p_rb.entry_off = (int32_t*)p; p += 4 * (E + 1);
         h->p_rb.pairs = (int32_t*)p; p += 4 * (size_t)npairs;
         h->p_rb.dep = (int32_t*)p; p += 4 * E;
+        h->p_rb.dep_x = (int32_t*)p; p += 4 * E;
         h->p_rb.tile_ctr = (int32_t*)p;
     }
     FT_CUDA(h, dm((void**)&h->d_p_act, (size_t)h->p_rows * I * 2));
     FT_CUDA(h, dm((void**)&h->d_p_y, (size_t)npairs * H * 4));
-    h->use_fp4_prefill = h->use_fp4 && c.wfmt == FT_W_MXFP4;
+    h->use_fp4_prefill = h->use_fp4;
     if (h->use_fp4_prefill) {
-        const int bn = 128;
-        const int64_t T = h->max_prefill;
+        // bf16-accurate activations as four E2M1 pieces, as in decode: 32-token tiles, 128
+        // N-operand rows per tile (token-major pieces)
+        const int bn = kFp4PrefillBn, P = kFp4MaxPieces;
         h->p_fp4_tiles = E + (npairs + bn - 1) / bn;
-        const size_t xq = fp4_piece_bytes(h->p_fp4_tiles, 1, bn, (int)H);
-        const size_t aq = fp4_piece_bytes(h->p_fp4_tiles, 1, bn, (int)I);
+        const size_t xq = fp4_piece_bytes(h->p_fp4_tiles, P, bn, (int)H);
+        const size_t aq = fp4_piece_bytes(h->p_fp4_tiles, P, bn, (int)I);
         const size_t xsf = fp4_sf_bytes(h->p_fp4_tiles, (int)H, c.wfmt);
         const size_t asf = fp4_sf_bytes(h->p_fp4_tiles, (int)I, c.wfmt);
-        FT_CUDA(h, dm((void**)&h->d_p_tq, (size_t)T * H / 2));
-        FT_CUDA(h, dm((void**)&h->d_p_tsf, (size_t)T * H / 32));
         FT_CUDA(h, dm((void**)&h->d_p_fxq, xq));
         FT_CUDA(h, dm((void**)&h->d_p_fxsf, xsf));
         FT_CUDA(h, dm((void**)&h->d_p_fxrs, (size_t)h->p_fp4_tiles * bn * 4));
@@ -803,7 +844,7 @@ ft_status alloc_prefill(ft_moe* h) {
         FT_CUDA(h, cudaMemset(h->d_p_faq, 0, aq));
         FT_CUDA(h, cudaMemset(h->d_p_fxsf, 0, xsf));
         FT_CUDA(h, cudaMemset(h->d_p_fasf, 0, asf));
-        const int64_t prow = h->p_fp4_tiles * bn;
+        const int64_t prow = h->p_fp4_tiles * P * bn;
         for (int b = 0; b < 2; ++b) {
             FT_CUDA(h, fp4_encode_weights(&h->tmPF_A13[b], h->d_layerbuf[b] + h->lay.off_w13, (int)H,
                                           (int)(2 * I), E, h->lay.blob_bytes));
@@ -1021,6 +1062,24 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess) {
         cuda_fail(h, cudaGetLastError(), "stream/event create"); return bail(FT_ERR_CUDA);
     }
+    {
+        const size_t pbytes = 64 + 8 * (size_t)std::max<int32_t>(h->max_pairs, 1);
+        uint8_t* dp = nullptr;
+        if (cudaStreamCreateWithFlags(&h->pf_stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_pf_in, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_pf_route, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_pf_fill, cudaEventDisableTiming) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "prefetch stream/events"); return bail(FT_ERR_CUDA);
+        }
+        if (cudaHostAlloc((void**)&h->h_pf, pbytes, cudaHostAllocMapped) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "cudaHostAlloc(prefetch view)"); return bail(FT_ERR_OOM);
+        }
+        memset(h->h_pf, 0, pbytes);
+        if (cudaHostGetDevicePointer((void**)&dp, h->h_pf, 0) != cudaSuccess) {
+            cuda_fail(h, cudaGetLastError(), "cudaHostGetDevicePointer(prefetch view)"); return bail(FT_ERR_CUDA);
+        }
+        h->d_pf = dp;
+    }
     st = init_lru_state(h);
     if (st != FT_OK) return bail(st);
     st = encode_tc_maps(h);
@@ -1178,7 +1237,6 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
         f4.inter = c.inter;
         f4.top_k = k;
         f4.pieces = h->fp4_pieces;
-        f4.x_ready = 0;
         f4.arena = h->d_arena;
         f4.blob_bytes = h->lay.blob_bytes;
         f4.off_s13 = h->lay.off_s13;
@@ -1264,6 +1322,8 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     }
     int launches = 0;
     FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_done, 0));      // one call at a time per handle
+    // a prefetch since the last call updated the LRU state first: this call's lookup follows it
+    if (h->pf_route_pending) FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_pf_route, 0));
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[0], s));
     const float* lg = logits;
     if (!lg) {
@@ -1388,6 +1448,14 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         launches += 2;
         return tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
     };
+    // experts a prefetch inserted look resident: the FFN over resident experts waits for the
+    // prefetch's copies (the wait is timed on its own, outside the routing and FFN windows)
+    if (h->pf_fill_pending) {
+        if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[6], s));
+        FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_pf_fill, 0));
+        if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[7], s));
+        se.pf_wait = true;
+    }
     // the FFN window opens here: routing, the row gather (BF16) and parameter set-up before
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
     FT_CUDA(h, run_ffn(0));
@@ -1403,6 +1471,14 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         rc.n_bypass = vc[4]; rc.n_evict = vc[5]; rc.err = vc[6]; rc.pad = 0;
     }
     if (rc.err & 6) { h->broken = true; return fail(h, FT_ERR_STATE, "cache lookup found inconsistent state"); }
+    // the call in flight owns the most recent hits + fills of the order until it ends
+    h->protect = (int64_t)rc.n_hits + rc.n_fill;
+    h->pf_route_pending = h->pf_fill_pending = false;
+    if (h->timing) {
+        se.pf_begin = h->pf_fill_begin;
+        se.pf_end = h->pf_fill_end;
+        h->pf_fill_begin = h->pf_fill_end = nullptr;
+    }
 
     if (rc.n_miss > 0) {
         if (h->fault_fill) {
@@ -1543,12 +1619,9 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
         }
     } else if (h->use_fp4_prefill) {
-        // MXFP4 activations once per token, gathered per routed row into 128-token tiles; one
-        // launch then runs W13 + SwiGLU (+ the SwiGLU activation's MXFP4 codes) and W2
-        const int bn = 128;
-        FT_CUDA(h, fp4_quant_tokens((const __nv_bfloat16*)x, T, H, h->d_p_tq, h->d_p_tsf, s));
-        FT_CUDA(h, fp4_gather_tiles(h->p_rb.counts, h->p_rb.entry_off, h->p_rb.pairs, k, H, bn, h->d_p_tq,
-                                    h->d_p_tsf, h->d_p_fxq, h->d_p_fxsf, h->d_p_fxrs, npairs, s));
+        // one launch: the routed rows split into four E2M1 pieces (bf16-accurate, as in
+        // decode), W13 + SwiGLU (+ the SwiGLU activation's pieces) and W2, 32-token tiles
+        const int bn = kFp4PrefillBn;
         Fp4Params f4{};
         f4.counts = h->p_rb.counts;
         f4.entry_off = h->p_rb.entry_off;
@@ -1558,8 +1631,7 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.hidden = H;
         f4.inter = I;
         f4.top_k = k;
-        f4.pieces = 1;
-        f4.x_ready = 1;
+        f4.pieces = kFp4MaxPieces;
         f4.arena = h->d_layerbuf[b];
         f4.blob_bytes = h->lay.blob_bytes;
         f4.off_s13 = h->lay.off_s13;
@@ -1570,6 +1642,7 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.aq = h->d_p_faq; f4.asf = h->d_p_fasf;
         f4.act = h->d_p_act;
         f4.y = h->d_p_y;
+        f4.cnt_x = h->p_rb.dep_x;
         f4.cnt_w13 = h->p_rb.dep;
         f4.err = h->d_ffn_err;
         f4.tile_ctr = h->p_rb.tile_ctr;
@@ -1613,6 +1686,9 @@ ft_status ft_cache_resize(ft_moe* h, int64_t new_slots) {
         return fail(h, FT_ERR_INVALID, "resize supports the global LRU policy only");
     ft_status s = sync_handle(h);
     if (s != FT_OK) return s;
+    // a safe point: nothing is in flight, so no entry needs protecting from a prefetch
+    h->protect = 0;
+    h->pf_route_pending = h->pf_fill_pending = false;
     const int64_t C = h->C, C2 = new_slots;
     std::vector<int32_t> order((size_t)C), slot_key((size_t)C);
     if (C > 0) {
@@ -1716,6 +1792,101 @@ ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys) 
     return FT_OK;
 }
 
+ft_status ft_cache_prefetch(ft_moe* h, int32_t layer, const int32_t* experts, int32_t n, void* stream_) {
+    if (!h) return FT_ERR_INVALID;
+    if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
+    const ft_moe_config& c = h->cfg;
+    if (h->mega) return fail(h, FT_ERR_INVALID, "ft_cache_prefetch is not available with FT_FLAG_FUSED_DECODE");
+    if (h->policy != FT_POLICY_GLOBAL_LRU) return fail(h, FT_ERR_INVALID, "ft_cache_prefetch supports the global LRU only");
+    if (layer < 0 || layer >= c.layers) return fail(h, FT_ERR_INVALID, "layer out of range");
+    if (n < 0 || n > h->max_pairs) return fail(h, FT_ERR_INVALID, "n out of range (0 <= n <= max_tokens * top_k)");
+    if (n == 0) return FT_OK;
+    if (!experts) return fail(h, FT_ERR_INVALID, "experts is NULL");
+    cudaStream_t s = (cudaStream_t)stream_;
+    cudaSetDevice(h->dev);
+    if (*(volatile int*)h->h_ffn_err) {
+        h->broken = true;
+        return fail(h, FT_ERR_CUDA, "an expert-FFN kernel ran out of a bounded wait (code " +
+                                    std::to_string(*(volatile int*)h->h_ffn_err) + ")");
+    }
+    cudaError_t pe = cudaGetLastError();
+    if (pe != cudaSuccess) return cuda_fail(h, pe, "earlier asynchronous error");
+    // The prefetch's lookup runs on the handle's prefetch stream, after the caller's work that
+    // wrote `experts`, after the last forward call's lookup and after the last prefetch's
+    // lookup: it may overlap the rest of the call in flight, whose entries it protects.
+    FT_CUDA(h, cudaEventRecord(h->ev_pf_in, s));
+    FT_CUDA(h, cudaStreamWaitEvent(h->pf_stream, h->ev_pf_in, 0));
+    FT_CUDA(h, cudaStreamWaitEvent(h->pf_stream, h->ev_route, 0));
+    FT_CUDA(h, cudaStreamWaitEvent(h->pf_stream, h->ev_pf_route, 0));
+    PrefetchParams pp{};
+    pp.expert_ids = experts;
+    pp.n = n;
+    pp.layer = layer;
+    pp.experts = c.experts;
+    pp.capacity = h->C;
+    pp.list_len = h->C;
+    pp.protect = std::min<int64_t>(h->protect, h->stats.resident);
+    pp.table = h->d_table;
+    pp.slot_key = h->d_slot_key;
+    pp.order_in = h->d_order[h->cur];
+    pp.order_out = h->d_order[h->cur ^ 1];
+    int32_t* hv = (int32_t*)h->h_pf;
+    int32_t* dv = (int32_t*)h->d_pf;
+    pp.hv_counts = dv;
+    pp.hv_key = dv + 16;
+    pp.hv_dst = dv + 16 + h->max_pairs;
+    FT_CUDA(h, launch_prefetch(pp, h->pf_stream));
+    h->cur ^= 1;
+    FT_CUDA(h, cudaEventRecord(h->ev_pf_route, h->pf_stream));
+    h->pf_route_pending = true;
+    // the insert list is needed on the host to issue the copies
+    ft_status ws = wait_event(h, h->ev_pf_route, "prefetch lookup");
+    if (ws != FT_OK) return ws;
+    volatile int32_t* vc = hv;
+    const int n_fill = vc[0], n_evict = vc[1], n_skip = vc[2], err = vc[3];
+    if ((err & 4) || n_fill < 0 || n_fill > n || n_evict > n_fill) {
+        h->broken = true;
+        return fail(h, FT_ERR_STATE, "prefetch lookup found inconsistent state");
+    }
+    if (n_fill > 0) {
+        if (h->fault_fill) {
+            h->broken = true;
+            return fail(h, FT_ERR_CUDA, "injected fill failure (FTMOE_FAULT=fill_fail)");
+        }
+        if (h->timing && !h->pf_fill_begin) {
+            h->pf_fill_begin = get_event(h);
+            FT_CUDA(h, cudaEventRecord(h->pf_fill_begin, h->copy_stream));
+        }
+        const int nkeys = c.layers * c.experts;
+        for (int j = 0; j < n_fill; ++j) {
+            const int key = ((volatile int32_t*)hv)[16 + j];
+            const int dst = ((volatile int32_t*)hv)[16 + h->max_pairs + j];
+            if (key < 0 || key >= nkeys || dst < 0 || dst >= h->C) {
+                h->broken = true;
+                return fail(h, FT_ERR_STATE, "prefetch insert list out of range");
+            }
+            FT_CUDA(h, cudaMemcpyAsync(h->d_arena + (size_t)dst * h->blob_bytes, h->blobs[(size_t)key],
+                                       h->blob_bytes, cudaMemcpyHostToDevice, h->copy_stream));
+        }
+        FT_CUDA(h, cudaEventRecord(h->ev_pf_fill, h->copy_stream));
+        if (h->timing) {
+            if (!h->pf_fill_end) h->pf_fill_end = get_event(h);
+            FT_CUDA(h, cudaEventRecord(h->pf_fill_end, h->copy_stream));
+        }
+        h->pf_fill_pending = true;
+    }
+    ft_cache_stats_t& st = h->stats;
+    st.prefetches++;
+    st.prefetch_fills += (uint64_t)n_fill;
+    st.prefetch_evictions += (uint64_t)n_evict;
+    st.prefetch_skipped += (uint64_t)n_skip;
+    st.prefetch_bytes += (uint64_t)n_fill * h->blob_bytes;
+    st.resident += n_fill - n_evict;
+    h->protect += n_fill;            // inserted at the most recent end: protected from later prefetches
+    if (err & 1) return fail(h, FT_ERR_INVALID, "prefetch: expert id out of range (ignored)");
+    return FT_OK;
+}
+
 ft_status ft_cache_pin(ft_moe* h, const int32_t* keys, int32_t n) {
     if (!h) return FT_ERR_INVALID;
     if (h->broken) return fail(h, FT_ERR_STATE, "handle is unusable after an earlier failure");
@@ -1725,6 +1896,8 @@ ft_status ft_cache_pin(ft_moe* h, const int32_t* keys, int32_t n) {
         if (keys[i] < 0 || keys[i] >= nkeys) return fail(h, FT_ERR_INVALID, "key out of range");
     ft_status s = sync_handle(h);
     if (s != FT_OK) return s;
+    h->protect = 0;
+    h->pf_route_pending = h->pf_fill_pending = false;
     const int64_t C = h->C;
     std::vector<int32_t> table((size_t)nkeys), sk((size_t)C), order;
     FT_CUDA(h, cudaMemcpy(table.data(), h->d_table, (size_t)nkeys * 4, cudaMemcpyDeviceToHost));
@@ -1764,6 +1937,12 @@ ft_status ft_cache_pin(ft_moe* h, const int32_t* keys, int32_t n) {
 
 ft_status ft_moe_set_timing(ft_moe* h, int32_t enable) {
     if (!h) return FT_ERR_INVALID;
+    if ((enable != 0) != h->timing) {
+        // a change of mode starts a new sequence: no lead is taken against a call recorded
+        // before it, and prefetch events recorded under the old mode are dropped
+        for (cudaEvent_t* ev : {&h->last_end_ev, &h->pf_fill_begin, &h->pf_fill_end})
+            if (*ev) { h->event_pool.push_back(*ev); *ev = nullptr; }
+    }
     h->timing = enable != 0;
     return FT_OK;
 }

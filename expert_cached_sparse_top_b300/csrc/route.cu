@@ -2,10 +2,10 @@
 // gate softmax, and the single-CTA cache lookup that updates the global LRU on the device
 // and groups (token, rank) pairs by expert.
 //
-// Method: the router is left exactly as the model defines it ("Meet FreeToken: An
-// Edge-Native MoE Serving Engine ...", section "Key Takeaways": no router changes), and
-// the expert cache is one LRU over all MoE layers that follows the router (same page,
-// section "Three mechanisms", semantic-aware caching).
+// Method: the router is used exactly as the model defines it ("Meet FreeToken: An
+// Edge-Native MoE Serving Engine ...", section "Key Takeaways"), and the expert cache is one
+// LRU over all MoE layers that follows the router's choices (same page, section "Three
+// mechanisms", semantic-aware caching).
 #include "common.cuh"
 #include "route_dev.cuh"
 
@@ -89,6 +89,104 @@ __global__ void __launch_bounds__(kLookupThreads, 1) lookup_kernel(LookupParams 
 
 cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
     lookup_kernel<<<1, kLookupThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------------------
+// Layer-ahead prefetch: insert a predicted expert set of one layer into the global LRU
+// (one CTA). Keys of the set already resident stay where they are. Each missing key, in
+// ascending expert order, takes a victim from the unprotected part of the order
+// (positions [0, list_len - protect): free slots first, then the least recent key outside
+// the set); the protected tail (the forward call still in flight) is never touched. The new
+// order is [unprotected part minus victims] ++ [protected tail] ++ [victims, in the order
+// of the keys inserted], which equals inserting each key at the most recent end. Missing
+// keys beyond the available victims are skipped. The insert list goes to host-mapped
+// memory: hv[0] inserted, hv[1] evictions, hv[2] skipped, hv[3] error bits (1: expert out
+// of range, 4: table/slot inconsistency), then keys [max] and slots [max].
+// ----------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kLookupThreads, 1) prefetch_kernel(PrefetchParams p) {
+    __shared__ int s_present[kMaxExperts];
+    __shared__ int s_miss_e[kMaxExperts];
+    __shared__ int s_warp[33];
+    __shared__ int s_evict, s_err;
+    const int tid = threadIdx.x;
+    const int E = p.experts;
+    const int64_t C = p.capacity, NL = p.list_len;
+    const int64_t NA = NL - p.protect;        // unprotected part of the order
+    const int key0 = p.layer * E;
+    for (int e = tid; e < E; e += blockDim.x) s_present[e] = 0;
+    if (tid == 0) { s_evict = 0; s_err = 0; }
+    __syncthreads();
+    for (int i = tid; i < p.n; i += blockDim.x) {
+        const int e = p.expert_ids[i];
+        if (e < 0 || e >= E) atomicOr(&s_err, 1);
+        else s_present[e] = 1;
+    }
+    __syncthreads();
+    const int e = tid;                        // E <= blockDim.x (checked by the launcher)
+    int slot = -1;
+    if (e < E && s_present[e]) {
+        slot = p.table[key0 + e];
+        if (slot >= C) { atomicOr(&s_err, 4); slot = -1; }
+    }
+    const int missing = (e < E && s_present[e] && slot < 0) ? 1 : 0;
+    int n_missing = 0;
+    const int mrank = block_excl_scan(missing, s_warp, &n_missing);
+    if (missing) s_miss_e[mrank] = e;
+    __syncthreads();
+    // victims: the first n_fill entries of the unprotected part whose key is not in the set
+    int n_cand = 0;
+    int64_t per = 0, i0 = 0, i1 = 0;
+    int cnt = 0;
+    if (NA > 0) {
+        per = (NA + blockDim.x - 1) / blockDim.x;
+        i0 = (int64_t)tid * per;
+        i1 = (i0 + per < NA) ? i0 + per : NA;
+        for (int64_t i = i0; i < i1; ++i) {
+            const int k = p.slot_key[p.order_in[i]];
+            cnt += !(k >= key0 && k < key0 + E && s_present[k - key0]);
+        }
+    }
+    const int base = block_excl_scan(cnt, s_warp, &n_cand);
+    const int n_fill = n_missing < n_cand ? n_missing : n_cand;
+    if (NA > 0) {
+        int r = base;
+        for (int64_t i = i0; i < i1; ++i) {
+            const int s = p.order_in[i];
+            const int k = p.slot_key[s];
+            const bool inS = k >= key0 && k < key0 + E && s_present[k - key0];
+            if (!inS && r < n_fill) {
+                const int j = r;
+                if (k >= 0) { p.table[k] = -1; atomicAdd(&s_evict, 1); }
+                const int nk = key0 + s_miss_e[j];
+                p.table[nk] = s;
+                p.slot_key[s] = nk;
+                p.hv_key[j] = nk;
+                p.hv_dst[j] = s;
+                p.order_out[NL - n_fill + j] = s;
+            } else {
+                // victims before this entry: min(candidates before it, n_fill)
+                const int vb = r < n_fill ? r : n_fill;
+                p.order_out[i - vb] = s;
+            }
+            r += !inS;
+        }
+    }
+    for (int64_t i = (NA > 0 ? NA : 0) + tid; i < NL; i += blockDim.x) p.order_out[i - n_fill] = p.order_in[i];
+    __syncthreads();
+    if (tid == 0) {
+        p.hv_counts[0] = n_fill;
+        p.hv_counts[1] = s_evict;
+        p.hv_counts[2] = n_missing - n_fill;
+        p.hv_counts[3] = s_err;
+        __threadfence_system();
+    }
+}
+
+cudaError_t launch_prefetch(const PrefetchParams& p, cudaStream_t s) {
+    if (p.experts < 1 || p.experts > kLookupThreads || p.protect < 0 || p.protect > p.list_len)
+        return cudaErrorInvalidValue;
+    prefetch_kernel<<<1, kLookupThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

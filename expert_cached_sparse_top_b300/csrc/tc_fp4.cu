@@ -20,8 +20,8 @@
 // features (counted per entry; the entry's W2 tiles wait for the count).
 //
 // Kernel roles per CTA (persistent, one CTA per SM):
-//   warp 0      producer: claims tiles (decode: from the launch's counter, when it is ready for
-//               the next; prefill: a fixed round robin) and hands their ids to the other roles
+//   warp 0      producer: claims tiles from the launch's counter when it is ready for the
+//               next one, and hands their ids to the other roles
 //               through an mbarrier ring; per 256-element K stage it loads the 128-row weight
 //               tile (3-D tensor map over the slot arena), its scale atoms (bulk copy from the
 //               slot), the tile's P x BN activation-piece rows (2-D map) and their scale atoms.
@@ -46,9 +46,9 @@ namespace fp4 {
 using namespace tc;
 
 constexpr int kStageK = 256;                 // K elements per stage: 128 bytes of E2M1
-// Tiles whose MMA has N <= 64 (decode) get two MMA-issuing warps (warps 1 and 6): a single
-// thread issuing every small-N tcgen05.mma / cp cannot keep up with the weight stream. Larger
-// tiles (prefill, N = 128) keep one issuer.
+// Tiles whose MMA has N <= 64 (16-token tiles) get two MMA-issuing warps (warps 1 and 6): a
+// single thread issuing every small-N tcgen05.mma / cp cannot keep up with the weight stream.
+// 32-token tiles (N = 128) keep one issuer.
 template <int P, int BN> struct Fp4Cfg {
     static constexpr int NI = P * BN <= 64 ? 2 : 1;
     static constexpr int THREADS = NI == 2 ? 224 : 192;
@@ -92,10 +92,7 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
 // share one scale block; all 32 lanes of the warp must call this together. Piece pc's codes go
 // to codes0 + pc * piece_stride (4 bytes); the block's scale byte of piece pc is written by the
 // group's first lane into the tile's atom at N-operand row n0 + pc, block jb.
-//
-// OCP = true is the single-piece MXFP4 activation quantisation of the FP4 prefill path:
-// scale exponent floor(log2(block max)) - 2 and codes saturating at +-6 (OCP Microscaling).
-template <int G, bool OCP = false>
+template <int G>
 __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* codes0, int64_t piece_stride,
                                        uint8_t* sf_atom, int n0, int jb, bool store, bool lead) {
     for (int pc = 0; pc < P; ++pc) {
@@ -107,10 +104,7 @@ __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* c
         const int be = exp_of(bmax);
         int e;
         uint8_t sfb;
-        if (OCP) {
-            e = be <= -1000 ? -126 : max(-126, min(126, be - 2));
-            sfb = (uint8_t)(e + 127);
-        } else if (fmt == FT_W_MXFP4) {
+        if (fmt == FT_W_MXFP4) {
             e = be <= -1000 ? -126 : max(-126, min(126, be - 1));
             sfb = (uint8_t)(e + 127);
         } else {
@@ -123,11 +117,9 @@ __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* c
         for (int j = 0; j < 4; ++j) {
             const uint32_t byte = e2m1x2(v[2 * j] * inv, v[2 * j + 1] * inv);
             word |= byte << (8 * j);
-            if (!OCP) {
-                const float2 q = e2m1x2_decode(byte);
-                v[2 * j] -= q.x * step;
-                v[2 * j + 1] -= q.y * step;
-            }
+            const float2 q = e2m1x2_decode(byte);
+            v[2 * j] -= q.x * step;
+            v[2 * j + 1] -= q.y * step;
         }
         if (store) {
             *reinterpret_cast<uint32_t*>(codes0 + pc * piece_stride) = word;
@@ -369,36 +361,31 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     };
 
     // 1. W13 activation pieces: the launch's CTAs split the pass's token rows between them
-    // (unless the caller has already written them)
-    if (!p.x_ready) {
-        const int r0 = s_eoff[u_begin], r1 = s_eoff[u_end];
-        for (int r = r0 + blockIdx.x; r < r1; r += gridDim.x) {
-            const int u = entry_of_row(s_eoff, u_begin, u_end, r);
-            const int i = r - s_eoff[u];
-            const int tile = s_tp[u] + i / BN, rin = i % BN;
-            const __nv_bfloat16* src = p.x + (int64_t)(ldr<MK>(p.pairs + r) / p.top_k) * H;
-            split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
-                          p.xsf + (int64_t)tile * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
-                          threadIdx.x, NTH, 2, s_red);
-            fence_proxy_async_global();
-            __threadfence();
-            named_bar(2, NTH);
-            if (threadIdx.x == 0) atomicAdd(p.cnt_x + u, 1);
-        }
+    const int r0 = s_eoff[u_begin], r1 = s_eoff[u_end];
+    for (int r = r0 + blockIdx.x; r < r1; r += gridDim.x) {
+        const int u = entry_of_row(s_eoff, u_begin, u_end, r);
+        const int i = r - s_eoff[u];
+        const int tile = s_tp[u] + i / BN, rin = i % BN;
+        const __nv_bfloat16* src = p.x + (int64_t)(ldr<MK>(p.pairs + r) / p.top_k) * H;
+        split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
+                      p.xsf + (int64_t)tile * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
+                      threadIdx.x, NTH, 2, s_red);
+        fence_proxy_async_global();
+        __threadfence();
+        named_bar(2, NTH);
+        if (threadIdx.x == 0) atomicAdd(p.cnt_x + u, 1);
     }
 
     if (warp == 0) {
         if (lane == 0) {
-            // decode: tiles are claimed from the launch's counter when the producer is ready for
-            // the next one; prefill (one piece, ~25 tiles per CTA): a fixed round robin, which
-            // measured faster there. Either way they reach the MMA issuers and the epilogue in
-            // claim order.
+            // tiles are claimed from the launch's counter when the producer is ready for the next
+            // one; they reach the MMA issuers and the epilogue in claim order
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t q = 0; ok; ++q) {
                 const int ts = (int)(q % kTQ);
                 if (!bwait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 8)) { ok = false; break; }
-                const int claimed = P > 1 ? atomicAdd(p.tile_ctr, 1) : (int)(blockIdx.x + q * gridDim.x);
+                const int claimed = atomicAdd(p.tile_ctr, 1);
                 const int t = claimed < total ? claimed : -1;
                 s_tile[ts] = t;
                 mbar_arrive(&tq_full[ts]);
@@ -430,7 +417,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 // weights (and their scales) of the first stages go out before the activation
                 // pieces of this entry are known to be ready (if they are not ready yet)
                 const int* dep = tl.w13 ? p.cnt_x + tl.u : p.cnt_w13 + tl.u;
-                const int target = tl.w13 ? (p.x_ready ? 0 : s_eoff[tl.u + 1] - s_eoff[tl.u])
+                const int target = tl.w13 ? s_eoff[tl.u + 1] - s_eoff[tl.u]
                                           : m13 * (s_tp[tl.u + 1] - s_tp[tl.u]);
                 const bool ready_now = target == 0 || ld_acquire(dep) >= target;
                 const int npre = ready_now ? 0 : min(S, k_stages);
@@ -638,7 +625,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                         for (int j = 0; j < 8; ++j) v[j] = s_stage[i * 65 + f8 + j];
                         const int f0 = tl.mt * 64 + f8;             // first feature of the 8
                         const int jb = f0 / BS;                     // scale block along K = I
-                        split8<G, P == 1>(v, P, FMT, p.aq + ((int64_t)tl.g * NC + i * P) * (I / 2) + f0 / 2, I / 2,
+                        split8<G>(v, P, FMT, p.aq + ((int64_t)tl.g * NC + i * P) * (I / 2) + f0 / 2, I / 2,
                                   p.asf + ((int64_t)tl.g * ak2 + jb / 4) * 512, i * P, jb, i < n_valid,
                                   (f8 % BS) == 0);
                     }
@@ -671,83 +658,6 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     if constexpr (MK) {
         mk_combine(mg, p.y, H, H, m2 * nt_pass, err, deadline, s_tmem + 3);
         mk_report(err, p.err);
-    }
-}
-
-// Prefill activations, MXFP4 (single piece, OCP rule), token-major: codes [T][H/2], scale
-// bytes [T][H/32]. Thread = 8 consecutive elements, 4 lanes per 32-element block.
-__global__ void __launch_bounds__(128) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int H,
-                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
-    const int t = blockIdx.x;
-    const int c = blockIdx.y * 1024 + threadIdx.x * 8;       // H % 256 == 0: warp-uniform
-    if (c >= H) return;
-    const uint4 u4 = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * H + c));
-    const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
-    float v[8];
-    float bmax = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        v[2 * q] = __uint_as_float(w4[q] << 16);
-        v[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
-        bmax = fmaxf(bmax, fmaxf(fabsf(v[2 * q]), fabsf(v[2 * q + 1])));
-    }
-    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
-    const int be = exp_of(bmax);
-    const int e = be <= -1000 ? -126 : max(-126, min(126, be - 2));
-    const float inv = pow2(-e);
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) word |= e2m1x2(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * j);
-    *reinterpret_cast<uint32_t*>(codes + (int64_t)t * (H / 2) + c / 2) = word;
-    if ((threadIdx.x & 3) == 0) sf[(int64_t)t * (H / 32) + c / 32] = (uint8_t)(e + 127);
-}
-
-// Routed rows -> the W13 N operand of the single-piece MMA: row r (entry u, position i) takes
-// token pairs[r] / top_k's codes into tile tp[u] + i / bn, row i % bn, and scatters its scale
-// bytes into that tile's atoms; its row scale is 1. One warp per row.
-__global__ void __launch_bounds__(256) gather_tiles_kernel(const RouteCounts* __restrict__ counts,
-                                                           const int32_t* __restrict__ entry_off,
-                                                           const int32_t* __restrict__ pairs, int top_k, int H,
-                                                           int bn, const uint8_t* __restrict__ tcodes,
-                                                           const uint8_t* __restrict__ tsf, uint8_t* __restrict__ xq,
-                                                           uint8_t* __restrict__ xsf, float* __restrict__ xrs) {
-    __shared__ int s_eoff[kMaxExperts + 1];
-    __shared__ int s_tp[kMaxExperts + 1];
-    const int U = counts->n_unique;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i <= U; i += blockDim.x) s_eoff[i] = entry_off[i];
-    __syncthreads();
-    for (int i = threadIdx.x; i < U; i += blockDim.x) s_tp[i] = (s_eoff[i + 1] - s_eoff[i] + bn - 1) / bn;
-    __syncthreads();
-    if (warp == 0) {
-        const int per = (U + 31) / 32;
-        const int i0 = lane * per, i1 = min(U, i0 + per);
-        int local = 0;
-        for (int i = i0; i < i1; ++i) local += s_tp[i];
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - local;
-        for (int i = i0; i < i1; ++i) { const int t = s_tp[i]; s_tp[i] = run; run += t; }
-    }
-    __syncthreads();
-    const int rows = s_eoff[U];
-    const int nblk = H / 32, atoms = nblk / 4;
-    for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
-        const int u = entry_of_row(s_eoff, 0, U, r);
-        const int i = r - s_eoff[u];
-        const int tile = s_tp[u] + i / bn, rin = i % bn;
-        const int64_t tok = pairs[r] / top_k;
-        const uint4* src = reinterpret_cast<const uint4*>(tcodes + tok * (H / 2));
-        uint4* dst = reinterpret_cast<uint4*>(xq + ((int64_t)tile * bn + rin) * (H / 2));
-        for (int c = lane; c < H / 32; c += 32) dst[c] = __ldg(src + c);
-        uint8_t* atom0 = xsf + (int64_t)tile * atoms * 512 + (rin & 31) * 16 + (rin >> 5) * 4;
-        for (int j = lane; j < nblk; j += 32) atom0[(j >> 2) * 512 + (j & 3)] = __ldg(tsf + tok * nblk + j);
-        if (lane == 0) xrs[(int64_t)tile * bn + rin] = 1.f;
     }
 }
 
@@ -897,7 +807,7 @@ cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int
 cudaError_t fp4_launch_mega(int fmt, const Fp4Params& p, const TcMega& mg, const Fp4Maps& m, int grid,
                             cudaStream_t s) {
     if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1 || !p.tile_ctr ||
-        p.pieces != kFp4MaxPieces || p.x_ready || mg.experts < 1 || mg.experts > 256 || mg.epoch <= 0 || grid < 1)
+        p.pieces != kFp4MaxPieces || mg.experts < 1 || mg.experts > 256 || mg.epoch <= 0 || grid < 1)
         return cudaErrorInvalidValue;
     if (fmt == FT_W_MXFP4) return launch_mega_t<FT_W_MXFP4>(p, mg, m, grid, s);
     if (fmt == FT_W_NVFP4) return launch_mega_t<FT_W_NVFP4>(p, mg, m, grid, s);
@@ -914,31 +824,12 @@ cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, in
     if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1 || !p.tile_ctr) return cudaErrorInvalidValue;
     if (fmt != FT_W_MXFP4 && fmt != FT_W_NVFP4) return cudaErrorInvalidValue;
     const bool mx = fmt == FT_W_MXFP4;
-    // decode: four pieces, 16- or 32-token tiles; prefill: one MXFP4 piece, 128-token tiles
+    // four pieces; 16-token tiles (decode), 32-token tiles (decode with more tokens, prefill)
     if (p.pieces == kFp4MaxPieces && bn == 16)
         return mx ? launch_t<16, FT_W_MXFP4, 4>(p, m, grid, s) : launch_t<16, FT_W_NVFP4, 4>(p, m, grid, s);
     if (p.pieces == kFp4MaxPieces && bn == 32)
         return mx ? launch_t<32, FT_W_MXFP4, 4>(p, m, grid, s) : launch_t<32, FT_W_NVFP4, 4>(p, m, grid, s);
-    if (p.pieces == 1 && bn == 128 && mx && p.x_ready) return launch_t<128, FT_W_MXFP4, 1>(p, m, grid, s);
     return cudaErrorInvalidValue;
-}
-
-cudaError_t fp4_quant_tokens(const __nv_bfloat16* x, int T, int H, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
-    if (T <= 0) return cudaSuccess;
-    if (H % fp4::kStageK) return cudaErrorInvalidValue;
-    fp4::quant_tokens_kernel<<<dim3(T, (H + 1023) / 1024), 128, 0, s>>>(x, H, codes, sf);
-    return cudaGetLastError();
-}
-
-cudaError_t fp4_gather_tiles(const RouteCounts* counts, const int32_t* entry_off, const int32_t* pairs,
-                             int top_k, int H, int bn, const uint8_t* tcodes, const uint8_t* tsf,
-                             uint8_t* xq, uint8_t* xsf, float* xrs, int rows_max, cudaStream_t s) {
-    if (rows_max <= 0) return cudaSuccess;
-    int blocks = (rows_max + 7) / 8;
-    if (blocks > 148 * 8) blocks = 148 * 8;
-    fp4::gather_tiles_kernel<<<blocks, 256, 0, s>>>(counts, entry_off, pairs, top_k, H, bn, tcodes, tsf, xq,
-                                                   xsf, xrs);
-    return cudaGetLastError();
 }
 
 }  // namespace ftmoe

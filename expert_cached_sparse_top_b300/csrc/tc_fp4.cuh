@@ -7,6 +7,7 @@
 namespace ftmoe {
 
 constexpr int kFp4MaxPieces = 4;
+constexpr int kFp4PrefillBn = 32;   // tokens per tile of the prefill FFN (P * BN = 128 N rows)
 
 // One launch computes a pass of the call (hit entries, miss entries, or all of them):
 //   1. every CTA splits some of the pass's activation rows x[pairs[r] / top_k] into P E2M1
@@ -26,8 +27,7 @@ struct Fp4Params {
     int32_t pass;                // 0: entries [0, n_hits), 1: [n_hits, n_unique), 2: all
     int32_t hidden, inter;       // multiples of 256
     int32_t top_k;
-    int32_t pieces;              // P, with P * bn <= 128 (4 for decode; 1 for prefill)
-    int32_t x_ready;             // nonzero: xq / xsf / xrs were written before the launch
+    int32_t pieces;              // P, with P * bn <= 128 (always four)
     int32_t stages;              // set by the launcher
     int32_t stage_bytes;         // set by the launcher
     const uint8_t* arena;        // weight slots (scale atoms and tensor scales are read here)
@@ -63,17 +63,9 @@ cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, in
                                int64_t n_slots, int64_t blob_bytes);
 cudaError_t fp4_encode_pieces(CUtensorMap* map, const void* base, int k_dim, int64_t rows, int box_rows);
 cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, int grid, cudaStream_t s);
-// the fused decode call (16-token tiles, four pieces; pass, x_ready ignored: all entries, rows
-// split in the launch); grid = the number of CTAs that fit on the device (fp4_mega_grid)
+// the fused decode call (16-token tiles, four pieces; pass ignored: all entries, rows split
+// in the launch); grid = the number of CTAs that fit on the device (fp4_mega_grid)
 cudaError_t fp4_launch_mega(int fmt, const Fp4Params& p, const TcMega& mg, const Fp4Maps& m, int grid,
                             cudaStream_t s);
 int fp4_mega_grid(int fmt, int num_sms);
-// prefill: MXFP4 activations of T token rows (OCP rule), token-major codes [T][H/2] and scale
-// bytes [T][H/32]; then the routed rows gathered into the W13 N operand (one piece, bn rows
-// per tile)
-cudaError_t fp4_quant_tokens(const __nv_bfloat16* x, int T, int H, uint8_t* codes, uint8_t* sf, cudaStream_t s);
-cudaError_t fp4_gather_tiles(const RouteCounts* counts, const int32_t* entry_off, const int32_t* pairs,
-                             int top_k, int H, int bn, const uint8_t* tcodes, const uint8_t* tsf,
-                             uint8_t* xq, uint8_t* xsf, float* xrs, int rows_max, cudaStream_t s);
-
 }  // namespace ftmoe

@@ -21,6 +21,7 @@ EXPORTS = (
     "ft_cache_resize", "ft_cache_stats", "ft_cache_snapshot", "ft_moe_set_timing",
     "ft_moe_timing", "ft_moe_last_error", "ft_moe_destroy", "ft_router_logits",
     "ft_topk_softmax", "ft_expert_ffn_noalloc", "ft_moe_prefill", "ft_cache_pin",
+    "ft_cache_prefetch",
 )
 
 
@@ -38,7 +39,10 @@ class FtCacheStats(ctypes.Structure):
                 ("misses", ctypes.c_uint64), ("bypassed", ctypes.c_uint64),
                 ("evictions", ctypes.c_uint64), ("fill_bytes", ctypes.c_uint64),
                 ("stage_bytes", ctypes.c_uint64), ("fill_ns", ctypes.c_uint64),
-                ("capacity", ctypes.c_int64), ("resident", ctypes.c_int64)]
+                ("capacity", ctypes.c_int64), ("resident", ctypes.c_int64),
+                ("prefetches", ctypes.c_uint64), ("prefetch_fills", ctypes.c_uint64),
+                ("prefetch_evictions", ctypes.c_uint64), ("prefetch_skipped", ctypes.c_uint64),
+                ("prefetch_bytes", ctypes.c_uint64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -52,7 +56,9 @@ class FtTiming(ctypes.Structure):
                 ("ffn_weight_bytes", ctypes.c_uint64), ("kernel_launches", ctypes.c_uint64),
                 ("prefill_calls", ctypes.c_uint64), ("prefill_fill_ms", ctypes.c_double),
                 ("prefill_compute_ms", ctypes.c_double), ("prefill_ffn_ms", ctypes.c_double),
-                ("prefill_flops", ctypes.c_double), ("prefill_fill_bytes", ctypes.c_uint64)]
+                ("prefill_flops", ctypes.c_double), ("prefill_fill_bytes", ctypes.c_uint64),
+                ("prefetch_fill_ms", ctypes.c_double), ("prefetch_wait_ms", ctypes.c_double),
+                ("fill_lead_ms", ctypes.c_double), ("fill_lead_calls", ctypes.c_uint64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -88,6 +94,7 @@ def lib():
         "ft_expert_ffn_noalloc": (I32, [P, I32, I32, I32, P, I32, P, P]),
         "ft_moe_prefill": (I32, [VP, I32, P, I32, P, P, P]),
         "ft_cache_pin": (I32, [VP, P, I32]),
+        "ft_cache_prefetch": (I32, [VP, I32, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -185,6 +192,12 @@ class MoECache:
     def prefill_status(self, layer, x, T, out, logits=None, stream=None):
         return lib().ft_moe_prefill(self.h, int(layer), _ptr(x), int(T), _ptr(logits), _ptr(out),
                                     _stream(stream))
+
+    def prefetch(self, layer, experts, n=None, stream=None):
+        """Layer-ahead prefetch of `layer`'s predicted experts (dev int32 tensor); `stream` is
+        the stream they are produced on."""
+        n = int(experts.numel()) if n is None else int(n)
+        check(lib().ft_cache_prefetch(self.h, int(layer), _ptr(experts), n, _stream(stream)), self.h)
 
     def pin(self, keys):
         """Place keys (layer * experts + expert) into the cache, first key least recent."""

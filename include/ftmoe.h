@@ -150,6 +150,11 @@ typedef struct {
     uint64_t fill_ns;     /* device time of the copy batches (timing enabled only) */
     int64_t capacity;     /* current C */
     int64_t resident;     /* keys resident now */
+    uint64_t prefetches;         /* ft_cache_prefetch calls with n >= 1 */
+    uint64_t prefetch_fills;     /* predicted keys inserted (copied into a slot) */
+    uint64_t prefetch_evictions; /* resident keys displaced by a prefetch */
+    uint64_t prefetch_skipped;   /* predicted keys not inserted: no unprotected victim */
+    uint64_t prefetch_bytes;     /* host->device bytes copied by prefetches */
 } ft_cache_stats_t;
 
 /* Accumulated device time per stage, in milliseconds, measured with CUDA events on the
@@ -174,6 +179,13 @@ typedef struct {
     double prefill_ffn_ms;     /* the two grouped-GEMM launches (W13+SwiGLU, W2) */
     double prefill_flops;      /* 6 * T * k * H * I per call (dense-equivalent FFN flops) */
     uint64_t prefill_fill_bytes;
+    /* layer-ahead prefetch (ft_cache_prefetch) */
+    double prefetch_fill_ms;   /* copy-stream time of the prefetches' copies */
+    double prefetch_wait_ms;   /* time forward calls' streams waited for those copies */
+    double fill_lead_ms;       /* sum over recorded forward calls with copies of (end of the previous
+                                  call - start of this call's first copy, the prefetch's if any): how
+                                  far ahead of the previous call's end this call's copies started */
+    uint64_t fill_lead_calls;  /* calls in fill_lead_ms */
 } ft_timing_t;
 
 typedef struct ft_moe ft_moe;
@@ -258,6 +270,38 @@ FT_API ft_status ft_cache_stats(ft_moe* h, ft_cache_stats_t* out);
  *                (FT_POLICY_LAYER_LRU: layer 0's list, then layer 1's, ..., then the pad).
  * Either pointer may be NULL. */
 FT_API ft_status ft_cache_snapshot(ft_moe* h, int32_t* slot_of_key, int32_t* lru_keys);
+
+/* Layer-ahead prefetch: start copying the experts a later forward call of `layer` is
+ * expected to select, before that call is made. The pages describe decode as following the
+ * router with one LRU cache over all layers ("Three mechanisms", semantic-aware caching);
+ * they do not describe fetching ahead of the router. This call is the reading taken here of
+ * starting a layer's copies as soon as its experts are predicted: the caller predicts them
+ * (for instance the next layer's router applied to the current layer's input, with
+ * ft_router_logits and ft_topk_softmax), and the cache inserts what is missing so that the
+ * forward call finds those experts resident. Outputs never depend on it (a wrong prediction
+ * costs PCIe bytes only).
+ *   layer    0 <= layer < layers: the layer whose experts are predicted.
+ *   experts  dev int32 [n]: predicted expert ids (any order, duplicates allowed), valid once
+ *            the work enqueued so far on `stream` has run.
+ *   n        0 <= n <= max_tokens * top_k (n = 0 returns FT_OK).
+ *   stream   the stream `experts` is produced on (only an event is recorded there). To let
+ *            the copies start while a forward call is still computing, produce `experts` on a
+ *            stream other than the one that call runs on.
+ * Cache semantics: each predicted key not resident, in ascending expert order, takes the
+ * lowest free slot, else the least recently used key that is neither predicted nor one of
+ * the entries the last forward call used (its hits and fills, the most recent entries of the
+ * order) or a key an earlier prefetch since that call inserted; it is inserted at the most
+ * recent end. Predicted keys already resident are left in place. A key with no such victim is
+ * skipped. The copies go on the handle's copy stream after those already issued; the next
+ * ft_moe_forward orders its cache lookup after this prefetch's and its expert FFN after these
+ * copies. The call blocks the host until its own cache update has run on the device (it needs
+ * the insert list to issue the copies), which does not wait for the forward call in flight.
+ * Counted in ft_cache_stats_t's prefetch fields, not in hits/misses. Global LRU policy only,
+ * and not with FT_FLAG_FUSED_DECODE (FT_ERR_INVALID). Errors: FT_ERR_INVALID (arguments; an
+ * expert id out of range is ignored and reported after the valid ones were prefetched),
+ * FT_ERR_TIMEOUT, FT_ERR_CUDA, FT_ERR_STATE. */
+FT_API ft_status ft_cache_prefetch(ft_moe* h, int32_t layer, const int32_t* experts, int32_t n,
+                                   void* stream);
 
 /* Place keys (layer * experts + expert, host int32[n]) into the cache at a safe point, the
  * first key least recent: a key already resident moves to the most recent end; a missing key

@@ -1,12 +1,12 @@
 """Global LRU expert-cache simulator: which (layer, expert) keys hit, miss, get bypassed,
 and which GPU slot each resident key occupies.
 
-What the pages fix: during decode "a shared LRU expert cache spanning all MoE layers
-follows the router instead of a placement frozen at load time" ([MTP] §Three mechanisms,
-semantic-aware caching); the cache starts cold ("the first request is served with a cold
-cache") and is rebuilt under a revised VRAM budget at safe points without reloading the
-host pool ([MTP] §Three mechanisms, elastic memory management); the measured quantity is
-the fraction of "decode-time expert reads" that miss ([MTP] §Results; [LN]).
+What the pages fix: during decode one LRU cache of experts is shared by every MoE layer and
+follows the router's actual choices, not a placement decided at load time ([MTP] §Three
+mechanisms, semantic-aware caching); the cache is empty when the first request arrives, and
+it is rebuilt under a changed VRAM budget at safe points without the host pool being read
+again ([MTP] §Three mechanisms, elastic memory management); the quantity the pages measure is
+the fraction of expert reads during decode that miss ([MTP] §Results; [LN]).
 
 Readings taken where the pages are silent:
 
@@ -21,6 +21,14 @@ Readings taken where the pages are silent:
 * resize to C': keep the min(C', resident) most recently used keys, in order. A survivor
   whose slot is < C' keeps it; the others move, in ascending old-slot order, to the lowest
   free slots < C'. Growth only adds free slots.
+* layer-ahead prefetch (the engine's ft_cache_prefetch; the pages describe no such step, it
+  is the reading of "start a layer's fills once its experts are known" taken here): a
+  prefetch of ``layer`` with a predicted expert set S' inserts each non-resident key of S',
+  in ascending expert order, exactly as a miss would (lowest free slot, else the least
+  recently used key outside S'), at the MRU end; keys of S' already resident are left where
+  they are (a prediction is not a use). The ``protect`` most recently used keys are never
+  victims: they belong to the forward call still in flight. A key that finds no victim is
+  skipped (nothing is staged). Prefetches count separately from forward calls.
 
 Comparator policies (the engine's FT_POLICY_LAYER_LRU / FT_POLICY_STATIC) are in
 ``policies.py``: per-layer LRU is one of these caches per layer; a static resident set is
@@ -47,6 +55,17 @@ class CallResult:
         self.slot_of = {}     # expert -> slot for hits and filled misses
 
 
+class PrefetchResult:
+    """Outcome of one prefetch."""
+
+    __slots__ = ("inserted", "evicted", "skipped")
+
+    def __init__(self):
+        self.inserted = []    # [(expert, slot)] ascending expert
+        self.evicted = []     # [(old_key, slot)] in the order the evictions happened
+        self.skipped = []     # predicted experts with no victim available, ascending
+
+
 class LRUCache:
     """List-based simulator. Keys are ints key = layer * experts + expert."""
 
@@ -59,7 +78,8 @@ class LRUCache:
         self.order = OrderedDict()            # key -> slot, least recent first
         self.key_of_slot = [None] * self.capacity
         self.free = list(range(self.capacity))   # min-heap of free slot indices
-        self.stats = dict(calls=0, hits=0, misses=0, bypassed=0, evictions=0)
+        self.stats = dict(calls=0, hits=0, misses=0, bypassed=0, evictions=0,
+                          prefetches=0, prefetch_fills=0, prefetch_evictions=0, prefetch_skipped=0)
 
     # -- queries -----------------------------------------------------------------------
     def resident(self):
@@ -117,6 +137,44 @@ class LRUCache:
         st["misses"] += len(res.misses) + len(res.bypassed)
         st["bypassed"] += len(res.bypassed)
         st["evictions"] += len(res.evicted)
+        return res
+
+    def prefetch(self, layer, experts, protect=0):
+        """Layer-ahead prefetch of ``layer``'s predicted ``experts`` (any order/dups); the
+        ``protect`` most recent keys cannot be evicted (clamped to the resident count)."""
+        S = sorted(set(int(e) for e in experts))
+        in_S = {layer * self.experts + e for e in S}
+        keys = list(self.order.keys())
+        protect = max(0, min(int(protect), len(keys)))
+        protected = set(keys[len(keys) - protect:])
+        res = PrefetchResult()
+        for e in S:
+            key = layer * self.experts + e
+            if key in self.order:
+                continue                      # resident: left in place
+            if self.no_insert:
+                res.skipped.append(e)
+                continue
+            slot = self._free_slot()
+            if slot is None:
+                victim = None
+                for k in self.order:          # least recent first
+                    if k not in in_S and k not in protected:
+                        victim = k
+                        break
+                if victim is None:
+                    res.skipped.append(e)
+                    continue
+                slot = self.order.pop(victim)
+                res.evicted.append((victim, slot))
+            self.order[key] = slot
+            self.key_of_slot[slot] = key
+            res.inserted.append((e, slot))
+        st = self.stats
+        st["prefetches"] += 1
+        st["prefetch_fills"] += len(res.inserted)
+        st["prefetch_evictions"] += len(res.evicted)
+        st["prefetch_skipped"] += len(res.skipped)
         return res
 
     def pin(self, keys):

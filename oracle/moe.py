@@ -1,10 +1,10 @@
 """The routed MoE layer forward, written out as its plain definition in fp64.
 
-What the method computes: the pages insist the cached-expert engine returns exactly the
-model's own MoE output. "Expert output stays bit-exact — no router changes, no expert
-substitution, no precision relaxation" ([MTP] §Key Takeaways), and the GPU and CPU halves
-of a step "merge exactly ... no router modification" ([MTP] §Three mechanisms, q* policy).
-So the oracle is the plain routed-MoE definition, independent of where an expert lives:
+What the method computes: the pages state that the cached-expert engine returns exactly the
+model's own MoE output: the router is left as it is, no expert is replaced by another and no
+step runs at reduced precision ([MTP] §Key Takeaways); the parts of a step computed on the GPU
+and on the CPU are summed without approximation ([MTP] §Three mechanisms, q* policy). So the
+oracle is the plain routed-MoE definition, independent of where an expert lives:
 
 1. router logits      l[t,e] = sum_h x[t,h] * Wr[e,h]                  (x is bf16, Wr fp32)
 2. top-k              the k experts with the largest logits, in rank order
@@ -21,9 +21,8 @@ Pins (tests/test_oracle_moe.py): top-k against brute force over all C(E,k) subse
 inputs and crafted ties; gate weights against the closed forms (k=1 gives 1, equal logits
 give 1/k) and the sum-to-one invariant; the FFN at E=1, k=1 against
 torch.nn.functional.silu-based SwiGLU in fp64 (library routine); k=E with all experts
-equal to the dense weighted sum; a hand-worked 3-expert example (tests/golden/); the
-MXFP4 act-quant step (FP4 prefill reading) against hand-worked blocks, a brute-force nearest-
-even search on random blocks and its fixed points; bf16 rounding against torch's bfloat16.
+equal to the dense weighted sum; a hand-worked 3-expert example (tests/golden/); bf16
+rounding against torch's bfloat16.
 """
 import numpy as np
 
@@ -80,43 +79,6 @@ def bf16_round(v):
     u = f.view(np.uint32).astype(np.uint64)
     u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
-
-
-def mx_act_quant(v, block=32):
-    """MXFP4 quantisation of activations along the last axis (the act-quant step of the FP4
-    prefill reading): per block of 32 consecutive values, shared scale 2^s with
-    s = floor(log2(max |v|)) - 2 (E2M1's largest exponent), each value divided by 2^s and
-    rounded to the nearest E2M1 magnitude {0, 0.5, 1, 1.5, 2, 3, 4, 6} with ties to the even
-    code, saturating at 6 (OCP Microscaling v1.0, conversion to MX). An all-zero block stays
-    zero. Returns the dequantised values (fp64)."""
-    v = np.asarray(v, dtype=np.float64)
-    shp = v.shape
-    b = v.reshape(-1, block)
-    amax = np.abs(b).max(axis=1, keepdims=True)
-    with np.errstate(divide="ignore"):
-        s = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0.0)
-    scale = 2.0 ** s
-    m = np.abs(b) / scale
-    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
-    # nearest grid point; on a tie take the even code (codes 0, 2, 4, 6: 0, 1, 2, 4)
-    d = np.abs(m[..., None] - grid)
-    best = d.min(axis=-1, keepdims=True)
-    cand = d == best
-    even = (np.arange(8) % 2) == 0
-    pick = np.where((cand & even).any(axis=-1), np.argmax(cand & even, axis=-1), np.argmax(cand, axis=-1))
-    q = grid[pick] * np.sign(b) * scale
-    return q.reshape(shp)
-
-
-def expert_ffn_w4a4(w1, w3, w2, x):
-    """Step 4 for the FP4 prefill reading (weights FP4, activations MXFP4): x is
-    act-quantised, the SwiGLU activation is rounded to bf16 (the precision the kernel keeps
-    it in) and act-quantised, then y = W2 a_q. Returns y [n][H]."""
-    xq = mx_act_quant(np.asarray(x, dtype=np.float64))
-    g = xq @ w1.T
-    u = xq @ w3.T
-    a = mx_act_quant(bf16_round(silu(g) * u))
-    return a @ w2.T
 
 
 def combine(w, y):

@@ -32,7 +32,7 @@ class OracleExperts:
 
 def oracle_call(experts, layer, x_bits, logits, k, tokens=None, ffn=None):
     """Expected (out, idx, w) for one forward call; ``tokens`` restricts to a sample; ``ffn``
-    replaces the plain expert FFN (e.g. moe.expert_ffn_w4a4 for the FP4 prefill reading)."""
+    replaces the plain expert FFN (moe.expert_ffn)."""
     E = experts.cfg.experts
     x = formats.bf16_to_f64(x_bits)
     l = np.asarray(logits, dtype=np.float64)

@@ -58,6 +58,13 @@ def test_hand_traces(trace):
             assert r.misses == _pairs(_field(misses)), op
             assert r.bypassed == _ints(_field(byp)), op
             assert r.evicted == _pairs(_field(ev)), op
+        elif op.startswith("prefetch"):
+            head, ins, ev, skip = [p.strip() for p in op.split("|")]
+            _, layer, S, prot = head.split()
+            r = c.prefetch(int(layer), _ints(S), protect=int(prot.split("=")[1]))
+            assert r.inserted == _pairs(_field(ins)), op
+            assert r.evicted == _pairs(_field(ev)), op
+            assert r.skipped == _ints(_field(skip)), op
         elif op.startswith("final"):
             slots, lru, counts = [p.strip() for p in op.split("|")]
             E, C = trace["experts"], c.capacity
@@ -200,3 +207,44 @@ def test_pin_order_and_capacity():
         raise AssertionError("pin into a full cache must fail")
     except ValueError:
         pass
+
+
+def test_prefetch_properties():
+    """Layer-ahead prefetch pins: (1) with nothing of S' resident and nothing protected it
+    leaves the same state as a forward call of S' (same victims, same order); (2) it never
+    reorders the keys it keeps; (3) protected keys and resident keys of S' are never evicted;
+    (4) with every resident key protected only free slots are used; (5) slot table stays a
+    bijection within capacity."""
+    rng = np.random.default_rng(21)
+    for trial in range(300):
+        C, E, L = int(rng.integers(1, 9)), int(rng.integers(2, 7)), int(rng.integers(1, 4))
+        a, b = LRUCache(C, E), LRUCache(C, E)
+        for _ in range(int(rng.integers(0, 6))):
+            layer = int(rng.integers(0, L))
+            S = rng.integers(0, E, size=int(rng.integers(1, E + 1)))
+            a.call(layer, S)
+            b.call(layer, S)
+        layer = int(rng.integers(0, L))
+        S = sorted(set(int(e) for e in rng.integers(0, E, size=int(rng.integers(1, E + 1)))))
+        keys = [layer * E + e for e in S]
+        before = a.lru_keys()
+        protect = int(rng.integers(0, len(before) + 2))
+        r = a.prefetch(layer, S, protect=protect)
+        after = a.lru_keys()
+        protected = set(before[len(before) - min(protect, len(before)):])
+        evicted = {k for k, _ in r.evicted}
+        assert not (evicted & protected)
+        assert not (evicted & set(keys))
+        kept = [k for k in before if k not in evicted]
+        assert after[:len(kept)] == kept                       # (2) kept keys keep their order
+        assert after[len(kept):] == [layer * E + e for e, _ in r.inserted]
+        if protect >= len(before):
+            assert not r.evicted                                # (4) free slots only
+        sok, _ = a.snapshot(L * E)
+        live = [s for s in sok if s >= 0]
+        assert len(live) == len(set(live)) == a.resident() <= C  # (5)
+        if protect == 0 and not any(k in before for k in keys):
+            rb = b.call(layer, S)                               # (1) same as a forward call
+            assert [(e, s) for e, s in rb.misses] == r.inserted
+            assert rb.evicted == r.evicted and rb.bypassed == r.skipped
+            assert b.lru_keys() == after and b.snapshot(L * E) == a.snapshot(L * E)

@@ -147,68 +147,6 @@ def test_plausible_mistakes_fail_a_pin():
     assert not np.allclose(y_ok, y_swapped)
 
 
-# ---- act-quant step of the FP4 prefill reading (MXFP4 activations) ----------------------
-def _e2m1_nearest_even_bruteforce(m):
-    """Reference by enumeration: nearest of the 8 magnitudes, ties to the even code."""
-    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
-    if m >= 6.0:
-        return 6.0
-    best = min(abs(m - g) for g in grid)
-    ties = [i for i, g in enumerate(grid) if abs(m - g) == best]
-    even = [i for i in ties if i % 2 == 0]
-    return grid[(even or ties)[0]]
-
-
-def test_mx_act_quant_hand_values():
-    # block max 3 -> s = floor(log2 3) - 2 = -1 -> scale 0.5; values / 0.5 rounded on the grid
-    blk = np.zeros(32)
-    blk[:8] = [3.0, -3.0, 0.125, 0.375, 0.625, 1.1, -2.2, 2.9]
-    # 3/0.5 = 6 -> 6 -> 3; 0.125/0.5 = 0.25 -> tie 0 / 0.5 -> even code 0 -> 0;
-    # 0.375/0.5 = 0.75 -> tie 0.5 / 1 -> even (1.0) -> 0.5; 0.625/0.5 = 1.25 -> tie 1 / 1.5
-    # -> 1.0 -> 0.5; 1.1/0.5 = 2.2 -> 2 -> 1.0; 2.2/0.5 = 4.4 -> 4 -> 2.0; 2.9/0.5 = 5.8 -> 6 -> 3.0
-    want = [3.0, -3.0, 0.0, 0.5, 0.5, 1.0, -2.0, 3.0]
-    assert np.array_equal(moe.mx_act_quant(blk)[:8], want)
-    # block max 7 -> s = 0, 7 saturates to 6; 5 is a tie between 4 and 6 -> 4
-    blk = np.zeros(32)
-    blk[:3] = [7.0, 5.0, -0.75]
-    assert np.array_equal(moe.mx_act_quant(blk)[:3], [6.0, 4.0, -1.0])
-    assert np.array_equal(moe.mx_act_quant(np.zeros(64)), np.zeros(64))
-
-
-def test_mx_act_quant_bruteforce_and_invariants():
-    rng = np.random.default_rng(7)
-    v = rng.standard_normal((6, 64)) * np.array([1e-3, 0.1, 1, 10, 1e3, 3e5])[:, None]
-    q = moe.mx_act_quant(v)
-    for r in range(v.shape[0]):
-        for b0 in range(0, 64, 32):
-            blk = v[r, b0:b0 + 32]
-            amax = np.abs(blk).max()
-            s = 2.0 ** (np.floor(np.log2(amax)) - 2)
-            for j in range(32):
-                m = abs(blk[j]) / s
-                assert q[r, b0 + j] == np.sign(blk[j]) * _e2m1_nearest_even_bruteforce(m) * s
-    # quantised values are fixed points, and every block keeps its largest magnitude's binade
-    assert np.array_equal(moe.mx_act_quant(q), q)
-    assert np.all(np.abs(q).reshape(-1, 32).max(axis=1) > 0)
-
-
-def test_w4a4_ffn_reduces_to_plain_ffn_on_grid_values():
-    """With inputs already on the MXFP4 grid and a SwiGLU output that bf16 and MXFP4 represent
-    exactly, the W4A4 expert equals the plain expert."""
-    rng = np.random.default_rng(3)
-    H, I = 64, 32
-    x = moe.mx_act_quant(rng.standard_normal((3, H)))
-    w1 = rng.standard_normal((I, H)) * 0.1
-    w3 = rng.standard_normal((I, H)) * 0.1
-    w2 = rng.standard_normal((H, I)) * 0.1
-    ref, a = moe.expert_ffn(w1, w3, w2, x)
-    got = moe.expert_ffn_w4a4(w1, w3, w2, x)
-    # the only differences come from rounding a (bf16 then MXFP4): bounded by the MX step
-    aq = moe.mx_act_quant(moe.bf16_round(a))
-    assert np.allclose(got, aq @ w2.T, rtol=0, atol=1e-12)
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 0.25
-
-
 def test_bf16_round_matches_torch():
     import torch
     rng = np.random.default_rng(11)
