@@ -723,6 +723,123 @@ def run_policy_compare(args):
     print(json.dumps(line), flush=True)
 
 
+def chained_line(args):
+    """Chained decode through 8 layers of the 35B-A3B shape: each layer's input is the previous
+    layer's input plus its output (bf16), every layer's router runs on the device inside the
+    forward call, and one global LRU (37 % of the pool) serves all layers. Run twice on the same
+    inputs: plain, and with the layer-ahead prefetch, where the next layer's router is applied
+    to the current layer's input on a side stream (a predictor of its routing) and
+    ft_cache_prefetch starts those experts' copies while the current layer still computes.
+    Reports tokens/s through all layers, the fill lead (how long before the previous layer's
+    end a layer's first copy starts) and the cache counts of both runs."""
+    import torch
+    import workloads as W
+    from workloads.host import HostPool
+    from expert_cached_sparse_top_b300 import build as b
+    b.build()
+    from expert_cached_sparse_top_b300 import ftmoe
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    ov = {"layers": args.layers} if args.layers else {}
+    cfg = W.config("decode_chained", **ov)
+    C = W.cache_capacity(cfg)
+    pool = HostPool(cfg, images=cfg.experts)           # key -> blob key % E (PCIe bytes real)
+    router = W.router_weights(cfg)
+    wr = torch.from_numpy(router).to(dev)
+    K, Wm = args.steps, args.warmup
+    trace = list(W.decode_trace(cfg, steps=Wm + K))
+    x0 = [torch.from_numpy(st[0]["x"].view(np.int16)).view(torch.bfloat16).to(dev) for st in trace]
+    Ts = [st[0]["T"] for st in trace]
+    L, E, k, H = cfg.layers, cfg.experts, cfg.top_k, cfg.hidden
+    s = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    lib = ftmoe.lib()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def run(prefetch):
+        c = ftmoe.make_config(L, E, H, cfg.inter, k, cfg.t_max, cfg.wfmt, C)
+        cache = ftmoe.MoECache(c, pool.ptrs, router)
+        out = torch.empty((cfg.t_max, H), dtype=torch.bfloat16, device=dev)
+        xs = torch.empty((L + 1, cfg.t_max, H), dtype=torch.bfloat16, device=dev)
+        lg = torch.empty((cfg.t_max, E), dtype=torch.float32, device=dev)
+        pidx = torch.empty((cfg.t_max * k,), dtype=torch.int32, device=dev)
+        pw = torch.empty((cfg.t_max * k,), dtype=torch.float32, device=dev)
+        ready = torch.cuda.Event()
+
+        def step(i):
+            T = Ts[i]
+            xs[0, :T].copy_(x0[i])
+            for l in range(L):
+                if prefetch and l + 1 < L:
+                    # the next layer's router on this layer's input, on the side stream
+                    ready.record(s)
+                    side.wait_event(ready)
+                    check = lib.ft_router_logits(xs[l].data_ptr(), T, H, wr[l + 1].data_ptr(), E,
+                                                 lg.data_ptr(), side.cuda_stream)
+                    check |= lib.ft_topk_softmax(lg.data_ptr(), T, E, k, pidx.data_ptr(), pw.data_ptr(),
+                                                 side.cuda_stream)
+                    if check:
+                        raise RuntimeError("stage call failed")
+                cache.forward(l, xs[l], T, out, stream=s)
+                if prefetch and l + 1 < L:
+                    cache.prefetch(l + 1, pidx, n=T * k, stream=side)
+                torch.add(xs[l, :T], out[:T], out=xs[l + 1, :T])
+
+        for i in range(Wm):
+            step(i)
+        torch.cuda.synchronize()
+        s0 = cache.stats()
+        cache.set_timing(True)
+        cache.timing(reset=True)
+        evs = []
+        for j in range(K):
+            flush.zero_()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            step(Wm + j)
+            e.record(s)
+            evs.append((a, e))
+        torch.cuda.synchronize()
+        tim = cache.timing(reset=True)
+        s1 = cache.stats()
+        cache.close()
+        sec = sum(a.elapsed_time(e) for a, e in evs) / 1e3
+        d = {k2: s1[k2] - s0[k2] for k2 in ("hits", "misses", "bypassed", "fill_bytes", "stage_bytes",
+                                              "prefetch_fills", "prefetch_bytes", "prefetch_skipped")}
+        return {"tokens_per_s": sum(Ts[Wm:]) / sec, "ms_per_step": 1e3 * sec / K,
+                "misses_per_step": d["misses"] / K, "hits_per_step": d["hits"] / K,
+                "prefetch_fills_per_step": d["prefetch_fills"] / K,
+                "pcie_GB_per_step": (d["fill_bytes"] + d["stage_bytes"] + d["prefetch_bytes"]) / K / 1e9,
+                "fill_lead_us": 1e3 * tim["fill_lead_ms"] / max(tim["fill_lead_calls"], 1),
+                "fill_lead_calls": int(tim["fill_lead_calls"]),
+                "fill_ms_per_step": (tim["fill_ms"] + tim["prefetch_fill_ms"]) / K,
+                "prefetch_wait_ms_per_step": tim["prefetch_wait_ms"] / K,
+                "ffn_GBps": tim["ffn_weight_bytes"] / ((tim["ffn_hit_ms"] + tim["ffn_miss_ms"]) * 1e-3) / 1e9
+                if tim["ffn_hit_ms"] + tim["ffn_miss_ms"] > 0 else None,
+                "kernel_launches": int(tim["kernel_launches"])}
+
+    plain = run(False)
+    ahead = run(True)
+    peaks = _peaks()
+    hbm = peaks.get("hbm_gbs")
+    return {
+        "metric": "MoE decode tokens/s through %d chained 35B-A3B-shaped BF16 layers (router in the "
+                  "loop, one global LRU at 37%% of pool) with layer-ahead prefetch" % L,
+        "value": ahead["tokens_per_s"], "unit": "tokens/s", "steps": K, "warmup": Wm,
+        "ms_per_step": ahead["ms_per_step"], "dtype": "bf16",
+        "config": {"workload": "decode_chained", "layers": L, "hidden": H, "experts": E,
+                   "inter": cfg.inter, "top_k": k, "cache_slots": C,
+                   "tokens_per_step": "%d..%d (seeded mix)" % (cfg.t_min, cfg.t_max),
+                   "predictor": "next layer's router on the current layer's input (side stream)",
+                   "pool": "pinned host, %d keys on %d blobs" % (cfg.keys, pool.images)},
+        "roofline": {"bound": "hbm", "kernel": "expert FFN (tcgen05 grouped GEMM), per pass",
+                     "achieved": ahead["ffn_GBps"], "peak": hbm, "unit": "GB/s",
+                     "frac": ahead["ffn_GBps"] / hbm if (ahead["ffn_GBps"] and hbm) else None},
+        "extras": {"with_prefetch": ahead, "without_prefetch": plain,
+                   "speedup": ahead["tokens_per_s"] / plain["tokens_per_s"]},
+    }
+
+
 def run_prefill(args):
     print(json.dumps(prefill_line(args)), flush=True)
 
@@ -891,6 +1008,7 @@ SUB_RECORDS = (
     ("elastic_nvfp4", "elastic_nvfp4", 96, 16, {}),
     ("prefill_mxfp4", "prefill_mxfp4", 8, 3, {}),
     ("prefill_bf16", "prefill_bf16", 8, 3, {}),
+    ("decode_chained", "decode_chained", 16, 4, {}),
 )
 
 
@@ -912,6 +1030,8 @@ def sub_records(args):
         try:
             if wl in DECODE:
                 line = decode_line(a)
+            elif wl == "decode_chained":
+                line = chained_line(a)
             else:
                 if fp4 is None and wl == "prefill_mxfp4":
                     fp4 = fp4_peak_probe()
@@ -959,9 +1079,11 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="default run: skip the sub-records of the other workloads")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare"])
+                    choices=list(DECODE) + ["prefill_bf16", "prefill_mxfp4", "policy_compare",
+                                            "decode_chained"])
     args = ap.parse_args()
-    dflt = DECODE.get(args.workload, (None, None, 32 if args.workload == "policy_compare" else 8, 3))
+    dflt = DECODE.get(args.workload, (None, None, {"policy_compare": 32, "decode_chained": 16}.get(
+        args.workload, 8), 3 if args.workload != "decode_chained" else 4))
     if args.steps is None:
         args.steps = dflt[2]
     if args.warmup is None:
@@ -970,6 +1092,8 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     if args.workload == "policy_compare":
         run_policy_compare(args)
+    elif args.workload == "decode_chained":
+        print(json.dumps(chained_line(args)), flush=True)
     elif args.workload not in DECODE:
         run_prefill(args)
     elif args.impl == "reference":

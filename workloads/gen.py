@@ -14,7 +14,7 @@ import numpy as np
 FMT_IDS = {"bf16": 0, "mxfp4": 1, "nvfp4": 2}
 
 # Stream tags, so that draws for different purposes never share a generator.
-_T_POOL, _T_ROUTER, _T_PERM, _T_TRACE, _T_X, _T_LEN, _T_PREFILL, _T_TINY = range(1, 9)
+_T_POOL, _T_ROUTER, _T_PERM, _T_TRACE, _T_X, _T_LEN, _T_PREFILL, _T_TINY, _T_PRED = range(1, 10)
 
 
 def _rng(*tags):
@@ -66,6 +66,10 @@ CONFIGS = {
     # Prefill at the 256-expert top-6 shape (~96 tokens per expert), MXFP4.
     "prefill_mxfp4": WorkloadConfig("prefill_mxfp4", 4, 256, 4096, 2048, 6, "mxfp4", seed=4,
                                     tokens=4096),
+    # Chained decode through 8 layers of the 35B-A3B shape (x_{l+1} = x_l + out_l), one global
+    # LRU at 37% of the pool, 1..16 tokens per step: the layer-ahead prefetch workload.
+    "decode_chained": WorkloadConfig("decode_chained", 8, 128, 2048, 768, 8, "bf16", seed=6,
+                                     steps=128, t_min=1, t_max=16, cache_frac=0.37),
     # Elastic NVFP4 decode, cache 40% -> 15% -> 30% at steps 0 / 341 / 682.
     "elastic_nvfp4": WorkloadConfig("elastic_nvfp4", 1, 128, 2048, 768, 8, "nvfp4", seed=5,
                                     steps=1024, t_min=1, t_max=16, cache_frac=0.40,
@@ -348,6 +352,17 @@ def decode_trace(cfg, steps=None):
 def trace_step(cfg, step, layer, T):
     """Stand-alone draw of one (step, layer) with no reuse history (tests of a single call)."""
     return DecodeTrace(cfg).layer(step, layer, T)
+
+
+def predicted_picks(cfg, step, layer, picks, accuracy):
+    """A stand-in for a predictor of ``layer``'s routing at ``step``: each of the layer's true
+    picks [T][k] is kept with probability ``accuracy`` and otherwise replaced by a uniformly
+    drawn expert (duplicates possible). Returns int32 [T * k]."""
+    rng = _rng(cfg.seed, _T_PRED, step, layer)
+    p = np.asarray(picks, dtype=np.int32).reshape(-1).copy()
+    swap = rng.random(p.size) >= accuracy
+    p[swap] = rng.integers(0, cfg.experts, size=int(swap.sum()))
+    return p
 
 
 def tiny_inputs(cfg):
