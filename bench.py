@@ -747,9 +747,9 @@ def chained_line(args):
     router = W.router_weights(cfg)
     wr = torch.from_numpy(router).to(dev)
     K, Wm = args.steps, args.warmup
-    trace = list(W.decode_trace(cfg, steps=Wm + K))
-    x0 = [torch.from_numpy(st[0]["x"].view(np.int16)).view(torch.bfloat16).to(dev) for st in trace]
-    Ts = [st[0]["T"] for st in trace]
+    xin = W.chained_inputs(cfg, Wm + K)
+    x0 = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in xin]
+    Ts = [x.shape[0] for x in xin]
     L, E, k, H = cfg.layers, cfg.experts, cfg.top_k, cfg.hidden
     s = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(dev)
@@ -831,6 +831,7 @@ def chained_line(args):
                    "inter": cfg.inter, "top_k": k, "cache_slots": C,
                    "tokens_per_step": "%d..%d (seeded mix)" % (cfg.t_min, cfg.t_max),
                    "predictor": "next layer's router on the current layer's input (side stream)",
+                   "inputs": "first-layer inputs AR(1) across steps, correlation %.2f" % cfg.x_corr,
                    "pool": "pinned host, %d keys on %d blobs" % (cfg.keys, pool.images)},
         "roofline": {"bound": "hbm", "kernel": "expert FFN (tcgen05 grouped GEMM), per pass",
                      "achieved": ahead["ffn_GBps"], "peak": hbm, "unit": "GB/s",

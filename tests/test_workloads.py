@@ -72,3 +72,23 @@ def test_aliased_pool_keeps_keys_distinct_in_address_only():
     assert pool.image_of(0) == pool.image_of(3) and pool.image_of(0) != pool.image_of(1)
     assert bytes(pool.blob(0)) == bytes(pool.blob(3))
     assert bytes(pool.blob(0)) != bytes(pool.blob(1))
+
+
+def test_chained_inputs_and_predicted_picks():
+    import numpy as np
+    from oracle import formats
+    cfg = W.config("decode_chained")
+    a = W.chained_inputs(cfg, 6)
+    b = W.chained_inputs(cfg, 6)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))             # seeded
+    assert all(1 <= x.shape[0] <= 16 and x.shape[1] == cfg.hidden for x in a)
+    x0, x1 = formats.bf16_to_f64(a[0]), formats.bf16_to_f64(a[1])
+    n = min(x0.shape[0], x1.shape[0])
+    r = np.corrcoef(x0[:n].ravel(), x1[:n].ravel())[0, 1]
+    assert abs(r - cfg.x_corr) < 0.05                                  # AR(1) correlation
+    picks = np.arange(64, dtype=np.int32).reshape(8, 8) % cfg.experts
+    p1 = W.predicted_picks(cfg, 3, 2, picks, 1.0)
+    assert np.array_equal(p1, picks.reshape(-1))
+    p2 = W.predicted_picks(cfg, 3, 2, picks, 0.5)
+    kept = (p2 == picks.reshape(-1)).mean()
+    assert 0.3 < kept < 0.8 and p2.min() >= 0 and p2.max() < cfg.experts

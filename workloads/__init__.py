@@ -7,7 +7,7 @@ CUDA path and the oracle consume exactly the arrays produced here.
 """
 from .gen import (  # noqa: F401
     CONFIGS, WorkloadConfig, config, expert_pool, router_weights, decode_trace,
-    trace_step, tiny_inputs, prefill_inputs, predicted_picks, pack_blob_bf16, pack_blob_fp4,
+    trace_step, tiny_inputs, prefill_inputs, predicted_picks, chained_inputs, pack_blob_bf16, pack_blob_fp4,
     f32_to_bf16_bits,
     cache_capacity, blob_layout,
 )

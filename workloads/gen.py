@@ -40,6 +40,7 @@ class WorkloadConfig:
     zipf_s: float = 1.1
     resize: Tuple[Tuple[int, float], ...] = field(default_factory=tuple)
     logit_std: float = 0.5              # prefill router logits N(0, logit_std)
+    x_corr: float = 0.0                 # chained decode: step-to-step correlation of a token's input
 
     @property
     def fmt(self):
@@ -69,7 +70,7 @@ CONFIGS = {
     # Chained decode through 8 layers of the 35B-A3B shape (x_{l+1} = x_l + out_l), one global
     # LRU at 37% of the pool, 1..16 tokens per step: the layer-ahead prefetch workload.
     "decode_chained": WorkloadConfig("decode_chained", 8, 128, 2048, 768, 8, "bf16", seed=6,
-                                     steps=128, t_min=1, t_max=16, cache_frac=0.37),
+                                     steps=128, t_min=1, t_max=16, cache_frac=0.37, x_corr=0.9),
     # Elastic NVFP4 decode, cache 40% -> 15% -> 30% at steps 0 / 341 / 682.
     "elastic_nvfp4": WorkloadConfig("elastic_nvfp4", 1, 128, 2048, 768, 8, "nvfp4", seed=5,
                                     steps=1024, t_min=1, t_max=16, cache_frac=0.40,
@@ -352,6 +353,23 @@ def decode_trace(cfg, steps=None):
 def trace_step(cfg, step, layer, T):
     """Stand-alone draw of one (step, layer) with no reuse history (tests of a single call)."""
     return DecodeTrace(cfg).layer(step, layer, T)
+
+
+def chained_inputs(cfg, steps):
+    """First-layer inputs of a chained decode, one [T][H] bf16 array per step. Token slot i
+    follows an AR(1) process across steps, s_t = c s_{t-1} + sqrt(1 - c^2) e_t with
+    c = cfg.x_corr and e_t ~ N(0, 1) (a decoding sequence's hidden state drifts from one step
+    to the next, so its routing repeats in part); step t uses the first T_t slots."""
+    c = float(cfg.x_corr)
+    state = _rng(cfg.seed, _T_X, 0).standard_normal((cfg.t_max, cfg.hidden), dtype=np.float32)
+    out = []
+    for step in range(steps):
+        if step:
+            e = _rng(cfg.seed, _T_X, step).standard_normal((cfg.t_max, cfg.hidden), dtype=np.float32)
+            state = np.float32(c) * state + np.float32(math.sqrt(max(0.0, 1.0 - c * c))) * e
+        T = DecodeTrace(cfg).tokens(step)
+        out.append(f32_to_bf16_bits(state[:T]))
+    return out
 
 
 def predicted_picks(cfg, step, layer, picks, accuracy):
