@@ -67,6 +67,53 @@ def replica_throughput(units_per_rank, seconds_per_rank, device="cpu"):
     return units_per_rank * ws / max_over_ranks(seconds_per_rank, device)
 
 
+class _CtypesNvml:
+    """The few read-only NVML queries the clock sampler makes, through ctypes on the driver's
+    libnvidia-ml.so.1 (used where the pynvml module is not installed)."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _ok(self, r, what):
+        if r != 0:
+            raise RuntimeError("%s returned %d" % (what, r))
+
+    def nvmlInit(self):
+        self._ok(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.c.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), self.c.byref(h)), "handle by bus id")
+        return h
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self.c.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(self.c.c_uint(i), self.c.byref(h)), "handle by index")
+        return h
+
+    def _uint(self, fn, h, *args):
+        v = self.c.c_uint()
+        self._ok(getattr(self.lib, fn)(h, *args, self.c.byref(v)), fn)
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._uint("nvmlDeviceGetClockInfo", h, self.c.c_int(kind))
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._uint("nvmlDeviceGetMaxClockInfo", h, self.c.c_int(kind))
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint("nvmlDeviceGetPowerUsage", h)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.c.c_ulonglong()
+        self._ok(self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.c.byref(v)), "clock reasons")
+        return v.value
+
+
 class Clocks:
     """SM clocks, power and throttle reasons sampled during the timed region.
 
@@ -89,7 +136,10 @@ class Clocks:
         self.f = open(path, "w")
         self.nv = None
         try:
-            import pynvml
+            try:
+                import pynvml
+            except ImportError:
+                pynvml = _CtypesNvml()
             pynvml.nvmlInit()
             self.nv = pynvml
             self.handle = self._handle(pynvml, index)

@@ -828,12 +828,12 @@ ft_status alloc_prefill(ft_moe* h) {
     if (h->use_fp4_prefill) {
         // bf16-accurate activations as four E2M1 pieces, as in decode: 32-token tiles, 128
         // N-operand rows per tile (token-major pieces)
-        const int bn = kFp4PrefillBn, P = kFp4MaxPieces;
+        const int bn = fp4_prefill_bn(c.wfmt), P = kFp4MaxPieces;
         h->p_fp4_tiles = E + (npairs + bn - 1) / bn;
         const size_t xq = fp4_piece_bytes(h->p_fp4_tiles, P, bn, (int)H);
         const size_t aq = fp4_piece_bytes(h->p_fp4_tiles, P, bn, (int)I);
-        const size_t xsf = fp4_sf_bytes(h->p_fp4_tiles, (int)H, c.wfmt);
-        const size_t asf = fp4_sf_bytes(h->p_fp4_tiles, (int)I, c.wfmt);
+        const size_t xsf = fp4_sf_bytes(h->p_fp4_tiles, (int)H, c.wfmt, P, bn);
+        const size_t asf = fp4_sf_bytes(h->p_fp4_tiles, (int)I, c.wfmt, P, bn);
         FT_CUDA(h, dm((void**)&h->d_p_fxq, xq));
         FT_CUDA(h, dm((void**)&h->d_p_fxsf, xsf));
         FT_CUDA(h, dm((void**)&h->d_p_fxrs, (size_t)h->p_fp4_tiles * bn * 4));
@@ -851,8 +851,9 @@ ft_status alloc_prefill(ft_moe* h) {
             FT_CUDA(h, fp4_encode_weights(&h->tmPF_A2[b], h->d_layerbuf[b] + h->lay.off_w2, (int)I, (int)H,
                                           E, h->lay.blob_bytes));
         }
-        FT_CUDA(h, fp4_encode_pieces(&h->tmPF_B13, h->d_p_fxq, (int)H, prow, 16));
-        FT_CUDA(h, fp4_encode_pieces(&h->tmPF_B2, h->d_p_faq, (int)I, prow, 16));
+        // prefill tiles (two scale bands) load their whole N operand with one box per stage
+        FT_CUDA(h, fp4_encode_pieces(&h->tmPF_B13, h->d_p_fxq, (int)H, prow, P * bn));
+        FT_CUDA(h, fp4_encode_pieces(&h->tmPF_B2, h->d_p_faq, (int)I, prow, P * bn));
     }
     if (h->use_tc) {
         FT_CUDA(h, dm((void**)&h->d_p_xp, (size_t)h->p_rows * H * 2));
@@ -1002,7 +1003,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         const int bn = h->fp4_bn;
         h->fp4_tiles = (int64_t)h->max_u + (h->max_pairs + bn - 1) / bn;
         const size_t xq = fp4_piece_bytes(h->fp4_tiles, P, bn, H), aq = fp4_piece_bytes(h->fp4_tiles, P, bn, I);
-        const size_t xsf = fp4_sf_bytes(h->fp4_tiles, H, cfg->wfmt), asf = fp4_sf_bytes(h->fp4_tiles, I, cfg->wfmt);
+        const size_t xsf = fp4_sf_bytes(h->fp4_tiles, H, cfg->wfmt, P, bn);
+        const size_t asf = fp4_sf_bytes(h->fp4_tiles, I, cfg->wfmt, P, bn);
         const size_t rs = (size_t)h->fp4_tiles * bn * 4;
         if (!dmalloc((void**)&h->d_xq, xq) || !dmalloc((void**)&h->d_aq, aq) ||
             !dmalloc((void**)&h->d_xsf, xsf) || !dmalloc((void**)&h->d_asf, asf) ||
@@ -1621,7 +1623,7 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     } else if (h->use_fp4_prefill) {
         // one launch: the routed rows split into four E2M1 pieces (bf16-accurate, as in
         // decode), W13 + SwiGLU (+ the SwiGLU activation's pieces) and W2, 32-token tiles
-        const int bn = kFp4PrefillBn;
+        const int bn = fp4_prefill_bn(c.wfmt);
         Fp4Params f4{};
         f4.counts = h->p_rb.counts;
         f4.entry_off = h->p_rb.entry_off;

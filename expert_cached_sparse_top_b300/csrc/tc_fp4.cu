@@ -91,10 +91,11 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
 // P pieces of 8 consecutive elements held by this thread. G adjacent lanes (G = block / 8)
 // share one scale block; all 32 lanes of the warp must call this together. Piece pc's codes go
 // to codes0 + pc * piece_stride (4 bytes); the block's scale byte of piece pc is written by the
-// group's first lane into the tile's atom at N-operand row n0 + pc, block jb.
+// group's first lane into the tile's scale atoms (sf_tile: ak atoms per 128-row band, bands in
+// row order) at N-operand row n0 + pc, block jb.
 template <int G>
 __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* codes0, int64_t piece_stride,
-                                       uint8_t* sf_atom, int n0, int jb, bool store, bool lead) {
+                                       uint8_t* sf_tile, int ak, int n0, int jb, bool store, bool lead) {
     for (int pc = 0; pc < P; ++pc) {
         float bmax = 0.f;
 #pragma unroll
@@ -125,7 +126,7 @@ __device__ __forceinline__ void split8(float (&v)[8], int P, int fmt, uint8_t* c
             *reinterpret_cast<uint32_t*>(codes0 + pc * piece_stride) = word;
             if (lead) {
                 const int n = n0 + pc;
-                sf_atom[(n & 31) * 16 + (n >> 5) * 4 + (jb & 3)] = sfb;
+                sf_tile[((int64_t)(n >> 7) * ak + (jb >> 2)) * 512 + (n & 31) * 16 + ((n & 127) >> 5) * 4 + (jb & 3)] = sfb;
             }
         }
     }
@@ -173,8 +174,7 @@ __device__ void split_row(const __nv_bfloat16* row, int K, int P, int fmt, uint8
             v[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u) * pre;
         }
         const int jb = c / G;
-        split8<G>(v, P, fmt, codes_row + c * 4, piece_stride, sf_tile + (jb / 4) * 512, n0, jb, true,
-                  (c % G) == 0);
+        split8<G>(v, P, fmt, codes_row + c * 4, piece_stride, sf_tile, K / BS / 4, n0, jb, true, (c % G) == 0);
     }
 }
 
@@ -258,16 +258,22 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     Fp4Params p, TcMega mg, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr int BS = FMT == FT_W_MXFP4 ? 32 : 16;
-    constexpr int APS = kStageK / (BS * 4);           // scale atoms per operand per stage
+    constexpr int APS = kStageK / (BS * 4);           // scale atoms per operand (per band) per stage
     constexpr int SF_BYTES = APS * 512;
-    constexpr uint32_t SF_COL0 = 256;                 // scale-factor columns: one buffer of 64 per issuer
     constexpr int NI = Fp4Cfg<P, BN>::NI;             // MMA issuers
     constexpr int NTH = fp4_block<BN, FMT, P, MK>();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages, STAGE = p.stage_bytes;
     constexpr int NC = P * BN;                        // rows of a tile's N operand: BN tokens x P pieces
+    constexpr int NB = (NC + 127) / 128;              // its 128-row scale bands
     constexpr int B_BYTES = NC * 128;
+    constexpr int HA = APS / NI;                      // weight scale atoms per stage per issuer
+    // tensor memory: NI accumulators of NC columns, double-buffered, then per issuer and
+    // stage parity SFP columns of scale factors (weights' atoms, then the bands' atoms)
+    constexpr uint32_t SF_COL0 = 2u * NI * NC;
+    constexpr uint32_t SFP = 4u * HA * (1 + NB);
+    static_assert(SF_COL0 + 2u * NI * SFP <= 512u, "tensor memory");
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
         const int tile = s_tp[u] + i / BN, rin = i % BN;
         const __nv_bfloat16* src = p.x + (int64_t)(ldr<MK>(p.pairs + r) / p.top_k) * H;
         split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
-                      p.xsf + (int64_t)tile * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
+                      p.xsf + (int64_t)tile * NB * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
                       threadIdx.x, NTH, 2, s_red);
         fence_proxy_async_global();
         __threadfence();
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const int ak = tl.w13 ? ak13 : ak2;
                 const CUtensorMap* mA = tl.w13 ? &tmA13 : &tmA2;
                 const CUtensorMap* mB = tl.w13 ? &tmB13 : &tmB2;
-                const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * ak * 512;
+                const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * NB * ak * 512;
                 const int slot = ldr<MK>(p.entry_dst + tl.u);
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed
@@ -410,10 +416,14 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const uint8_t* sfa = p.arena + (int64_t)slot * p.blob_bytes + (tl.w13 ? p.off_s13 : p.off_s2) +
                                      (int64_t)tl.mt * ak * 512;
                 // the tile's rows are token-major (token i, piece pc at row i * P + pc): only the
-                // first P * n_valid rows carry data, loaded as 16-row boxes
+                // first P * n_valid rows carry data. Tiles of up to 128 rows (decode) load just
+                // those, as 16-row boxes; wider tiles (prefill, mostly full) load all NC rows
+                // with one box (their piece tensor maps are encoded with that box height), so
+                // the producer issues a handful of copies per stage instead of up to NC / 16
                 const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
-                const int nbox = (P * n_valid + 15) / 16;
-                const uint32_t stage_tx = (uint32_t)(kABytes + 2 * SF_BYTES + nbox * 2048);
+                const int nbox = NB > 1 ? 1 : (P * n_valid + 15) / 16;
+                constexpr int kBoxBytes = NB > 1 ? NC * 128 : 2048;
+                const uint32_t stage_tx = (uint32_t)(kABytes + (1 + NB) * SF_BYTES + nbox * kBoxBytes);
                 // weights (and their scales) of the first stages go out before the activation
                 // pieces of this entry are known to be ready (if they are not ready yet)
                 const int* dep = tl.w13 ? p.cnt_x + tl.u : p.cnt_w13 + tl.u;
@@ -440,7 +450,10 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                     uint64_t* fb = &full[(it0 + kb) % S];
                     for (int bx = 0; bx < nbox; ++bx)
                         tma_load_2d(st + kABytes + bx * 2048, mB, fb, kb * 128, tl.g * NC + bx * 16);
-                    bulk_load(st + kABytes + B_BYTES + SF_BYTES, bsf + (int64_t)kb * SF_BYTES, SF_BYTES, fb);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        bulk_load(st + kABytes + B_BYTES + (1 + b) * SF_BYTES,
+                                  bsf + ((int64_t)b * ak * 512 + (int64_t)kb * SF_BYTES), SF_BYTES, fb);
                 }
                 if (!ready) { ok = false; break; }
                 for (int kb = npre; kb < k_stages; ++kb, ++it) {
@@ -452,7 +465,10 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                     bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
                     for (int bx = 0; bx < nbox; ++bx)
                         tma_load_2d(st + kABytes + bx * 2048, mB, &full[s], kb * 128, tl.g * NC + bx * 16);
-                    bulk_load(st + kABytes + B_BYTES + SF_BYTES, bsf + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        bulk_load(st + kABytes + B_BYTES + (1 + b) * SF_BYTES,
+                                  bsf + ((int64_t)b * ak * 512 + (int64_t)kb * SF_BYTES), SF_BYTES, &full[s]);
                 }
             }
             if (!ok) {
@@ -466,9 +482,12 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
         // two. One thread issuing every tcgen05.mma / cp of a decode tile (N = 16) cannot keep
         // up with the weight stream; two can.
         const uint32_t par = warp == 6 ? 1u : 0u;
-        constexpr int HA = APS / NI;                  // scale atoms per operand per issuer
         constexpr int KK = 4 / NI;                    // K steps per stage per issuer
         if (lane == 0) {
+            // descriptors of stage 0; a stage, a K step or an atom only adds a constant to the
+            // start-address field, so the loop below does no descriptor arithmetic
+            const uint64_t dsw0 = smem_desc_sw128(smem_u32(smem));
+            const uint64_t dsf0 = smem_desc_sf(smem_u32(smem) + kABytes + B_BYTES);
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
@@ -481,6 +500,8 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const int k_stages = (tl.w13 ? H : I) / kStageK;
                 const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
                 const int n_mma = (P * n_valid + 15) & ~15;
+                const uint32_t idesc0 = idesc_fp4<FMT>(n_mma, 0);
+                const uint32_t idesc2 = FMT == FT_W_MXFP4 ? idesc_fp4<FMT>(n_mma, 2) : idesc0;
                 const uint32_t acc = tcount & 1u;
                 if (!bwait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, 2)) break;
                 tc_fence_after();
@@ -489,16 +510,20 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                     const int s = it % S;
                     if (!bwait(&full[s], (it / S) & 1u, 3)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * STAGE);
-                    const uint32_t ssf = sa + kABytes + B_BYTES;
-                    // this issuer's scale atoms -> TMEM (double-buffered by stage parity):
-                    // weights at tsf + 4a, activation pieces at tsf + 4 (HA + a)
-                    const uint32_t tsf = tmem_base + SF_COL0 + par * 64u + (it & 1u) * 32u;
+                    const uint64_t so = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
+                    const uint64_t dA = dsw0 + so, dB = dA + (kABytes >> 4), dS = dsf0 + so;
+                    // this issuer's scale atoms -> TMEM (double-buffered by stage parity): the
+                    // weights' atom a at tsf + 4a, band b of the activations' atom a at
+                    // tsf + 4 HA + 4 (a NB + b)
+                    const uint32_t tsf = tmem_base + SF_COL0 + (par * 2u + (it & 1u)) * SFP;
 #pragma unroll
                     for (int a = 0; a < HA; ++a) {
-                        const int ga = (int)par * HA + a;     // atom within the stage
-                        tmem_cp_sf(tsf + (uint32_t)(4 * a), smem_desc_sf(ssf + ga * 512));
-                        tmem_cp_sf(tsf + (uint32_t)(4 * (HA + a)), smem_desc_sf(ssf + (APS + ga) * 512));
+                        const uint64_t ga = (uint64_t)((int)par * HA + a) * 32u;     // atom within the stage
+                        tmem_cp_sf(tsf + (uint32_t)(4 * a), dS + ga);
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            tmem_cp_sf(tsf + (uint32_t)(4 * HA + 4 * (a * NB + b)),
+                                       dS + (uint64_t)((1 + b) * SF_BYTES / 16) + ga);
                     }
 #pragma unroll
                     for (int k2 = 0; k2 < KK; ++k2) {
@@ -506,10 +531,9 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                         // MXFP4: one atom (4 blocks of 32) per two K steps, byte pair 0 or 2;
                         // NVFP4: one atom (4 blocks of 16) per K step
                         const int ai = (FMT == FT_W_MXFP4 ? (kk >> 1) : kk) - (int)par * HA;
-                        const uint32_t id = FMT == FT_W_MXFP4 ? (uint32_t)((kk & 1) * 2) : 0u;
-                        mma_bs<FMT>(d_tmem, smem_desc_sw128(sa + kk * 32),
-                                    smem_desc_sw128(sa + kABytes + kk * 32), idesc_fp4<FMT>(n_mma, id),
-                                    tsf + 4 * ai, tsf + 4 * (HA + ai), (kb == 0 && k2 == 0) ? 0u : 1u);
+                        const bool odd = FMT == FT_W_MXFP4 && (kk & 1);
+                        mma_bs<FMT>(d_tmem, dA + (uint64_t)(kk * 2), dB + (uint64_t)(kk * 2), odd ? idesc2 : idesc0,
+                                    tsf + 4 * ai, tsf + 4 * HA + 4 * NB * ai, (kb == 0 && k2 == 0) ? 0u : 1u);
                     }
                     mma_commit(&empty[s]);
                 }
@@ -626,7 +650,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                         const int f0 = tl.mt * 64 + f8;             // first feature of the 8
                         const int jb = f0 / BS;                     // scale block along K = I
                         split8<G>(v, P, FMT, p.aq + ((int64_t)tl.g * NC + i * P) * (I / 2) + f0 / 2, I / 2,
-                                  p.asf + ((int64_t)tl.g * ak2 + jb / 4) * 512, i * P, jb, i < n_valid,
+                                  p.asf + (int64_t)tl.g * NB * ak2 * 512, ak2, i * P, jb, i < n_valid,
                                   (f8 % BS) == 0);
                     }
                     named_bar(1, 128);
@@ -688,9 +712,11 @@ EncodeTiledFn encode_fn() {
 constexpr int kSmemLimit = 227 * 1024;
 
 int stage_bytes_for(int fmt, int bn, int pieces) {
-    // weights tile + P * bn activation rows + weight and activation scale atoms
+    // weights tile + P * bn activation rows + weight scale atoms + the activations' scale
+    // atoms, one set per 128-row band
     const int aps = fmt == FT_W_MXFP4 ? 2 : 4;
-    return fp4::kABytes + pieces * bn * 128 + 2 * aps * 512;
+    const int bands = (pieces * bn + 127) / 128;
+    return fp4::kABytes + pieces * bn * 128 + (1 + bands) * aps * 512;
 }
 
 // Stages and shared memory of a launch (the same for the fused call).
@@ -772,9 +798,10 @@ size_t fp4_piece_bytes(int64_t tiles, int pieces, int bn, int K) {
     return (size_t)tiles * pieces * bn * (K / 2);
 }
 
-size_t fp4_sf_bytes(int64_t tiles, int K, int fmt) {
+size_t fp4_sf_bytes(int64_t tiles, int K, int fmt, int pieces, int bn) {
     const int bs = fmt == FT_W_MXFP4 ? 32 : 16;
-    return (size_t)tiles * (K / bs / 4) * 512;
+    const int bands = (pieces * bn + 127) / 128;
+    return (size_t)tiles * bands * (K / bs / 4) * 512;
 }
 
 cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, int rows,
@@ -824,11 +851,16 @@ cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, in
     if (p.hidden % fp4::kStageK || p.inter % fp4::kStageK || p.top_k < 1 || !p.tile_ctr) return cudaErrorInvalidValue;
     if (fmt != FT_W_MXFP4 && fmt != FT_W_NVFP4) return cudaErrorInvalidValue;
     const bool mx = fmt == FT_W_MXFP4;
-    // four pieces; 16-token tiles (decode), 32-token tiles (decode with more tokens, prefill)
-    if (p.pieces == kFp4MaxPieces && bn == 16)
+    // four pieces; 16- or 32-token tiles (decode), the prefill width (two scale bands)
+    if (p.pieces != kFp4MaxPieces) return cudaErrorInvalidValue;
+    if (bn == 16)
         return mx ? launch_t<16, FT_W_MXFP4, 4>(p, m, grid, s) : launch_t<16, FT_W_NVFP4, 4>(p, m, grid, s);
-    if (p.pieces == kFp4MaxPieces && bn == 32)
+    if (bn == 32)
         return mx ? launch_t<32, FT_W_MXFP4, 4>(p, m, grid, s) : launch_t<32, FT_W_NVFP4, 4>(p, m, grid, s);
+    if (mx && bn == fp4_prefill_bn(FT_W_MXFP4))
+        return launch_t<fp4_prefill_bn(FT_W_MXFP4), FT_W_MXFP4, 4>(p, m, grid, s);
+    if (!mx && bn == fp4_prefill_bn(FT_W_NVFP4))
+        return launch_t<fp4_prefill_bn(FT_W_NVFP4), FT_W_NVFP4, 4>(p, m, grid, s);
     return cudaErrorInvalidValue;
 }
 

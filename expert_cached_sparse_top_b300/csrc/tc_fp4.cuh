@@ -7,7 +7,9 @@
 namespace ftmoe {
 
 constexpr int kFp4MaxPieces = 4;
-constexpr int kFp4PrefillBn = 32;   // tokens per tile of the prefill FFN (P * BN = 128 N rows)
+// Tokens per tile of the prefill FFN: P * BN N-operand rows in one MMA (two 128-row scale
+// bands), as many as tensor memory holds double-buffered with the stage's scale factors.
+__host__ __device__ constexpr int fp4_prefill_bn(int fmt) { return fmt == 1 ? 56 : 48; }
 
 // One launch computes a pass of the call (hit entries, miss entries, or all of them):
 //   1. every CTA splits some of the pass's activation rows x[pairs[r] / top_k] into P E2M1
@@ -57,7 +59,7 @@ struct Fp4Maps {
 
 // bytes of one tile-major piece buffer (codes) / scale-atom buffer for `tiles` tiles
 size_t fp4_piece_bytes(int64_t tiles, int pieces, int bn, int K);
-size_t fp4_sf_bytes(int64_t tiles, int K, int fmt);
+size_t fp4_sf_bytes(int64_t tiles, int K, int fmt, int pieces, int bn);
 
 cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, int rows,
                                int64_t n_slots, int64_t blob_bytes);
