@@ -910,6 +910,8 @@ def prefill_line(args):
     ov = {"layers": args.layers} if args.layers else {}
     if args.tokens:
         ov["tokens"] = args.tokens
+    if getattr(args, "experts", 0):
+        ov["experts"] = args.experts
     cfg = W.config(args.workload, **ov)
     torch.cuda.set_device(0)
     fp4 = cfg.wfmt != "bf16"
@@ -1074,7 +1076,7 @@ def sub_records(args):
     for name, wl, steps, warmup, extra in SUB_RECORDS:
         a = argparse.Namespace(**vars(args))
         a.workload, a.steps, a.warmup, a.lite = wl, steps, warmup, True
-        a.layers, a.tokens, a.fused, a.ffn_traffic, a.all_resident = 0, 0, False, False, False
+        a.layers, a.tokens, a.fused, a.ffn_traffic, a.all_resident, a.experts = 0, 0, False, False, False, 0
         for k2, v in extra.items():
             setattr(a, k2, v)
         t0 = time.perf_counter()
@@ -1127,6 +1129,9 @@ def main():
                     help="with --ffn-traffic: every selected expert resident (no fills)")
     ap.add_argument("--fused", action="store_true",
                     help="decode through the fused decode kernel (FT_FLAG_FUSED_DECODE; BF16)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="prefill: fewer experts per layer (a small case of the same kernel for "
+                         "profiler captures; with --tokens keeping the tokens per expert)")
     ap.add_argument("--no-extras", action="store_true",
                     help="default run: skip the sub-records of the other workloads")
     ap.add_argument("--workload", default=WORKLOAD,
