@@ -40,9 +40,88 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
     if (lane == 0) logits[(size_t)t * E + e] = acc;
 }
 
+// Router logits for many tokens (prefill): a CTA computes a 32-token x 64-expert tile of
+// logits, staging 64-wide K chunks of x (converted to fp32) and of Wr in shared memory, so a
+// Wr row is read once per 32 tokens and an x row once per 64 experts (the one-warp-per-pair
+// kernel reads both for every pair). Each thread accumulates 2 tokens x 4 experts in fp32,
+// in ascending h.
+constexpr int kRtT = 32, kRtE = 64, kRtK = 64;
+
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(
+    const __nv_bfloat16* __restrict__ x, int T, int H, const float* __restrict__ wr, int E,
+    float* __restrict__ logits) {
+    __shared__ float sx[kRtT][kRtK + 1];
+    __shared__ float sw[kRtE][kRtK + 1];
+    const int t0 = blockIdx.x * kRtT, e0 = blockIdx.y * kRtE;
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    float acc[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    for (int k0 = 0; k0 < H; k0 += kRtK) {
+        // x chunk: 32 rows x 64 bf16 (8 per thread, 16-byte loads)
+        {
+            const int r = tid >> 3, c8 = (tid & 7) * 8;
+            const int t = t0 + r;
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (t < T) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * H + k0 + c8));
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __bfloat1622float2(b2[q]);
+                    v[2 * q] = f.x;
+                    v[2 * q + 1] = f.y;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sx[r][c8 + q] = v[q];
+        }
+        // Wr chunk: 64 rows x 64 fp32 (16 per thread, 16-byte loads)
+#pragma unroll
+        for (int rep = 0; rep < 4; ++rep) {
+            const int idx = tid + rep * 256;              // 0..1023 float4 slots
+            const int r = idx >> 4, c4 = (idx & 15) * 4;
+            const int e = e0 + r;
+            float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < E) w4 = __ldg(reinterpret_cast<const float4*>(wr + (int64_t)e * H + k0 + c4));
+            sw[r][c4] = w4.x; sw[r][c4 + 1] = w4.y; sw[r][c4 + 2] = w4.z; sw[r][c4 + 3] = w4.w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < kRtK; ++k) {
+            const float xa = sx[ty][k], xb = sx[ty + 16][k];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float w = sw[tx + 16 * b][k];
+                acc[0][b] = fmaf(xa, w, acc[0][b]);
+                acc[1][b] = fmaf(xb, w, acc[1][b]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        const int t = t0 + ty + 16 * a;
+        if (t >= T) continue;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int e = e0 + tx + 16 * b;
+            if (e < E) logits[(int64_t)t * E + e] = acc[a][b];
+        }
+    }
+}
+
 cudaError_t launch_router_logits(const __nv_bfloat16* x, int T, int H, const float* wr, int E,
                                  float* logits, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
+    if (T >= 64 && H % kRtK == 0) {
+        // many tokens: the tiled kernel (Wr read once per 32 tokens)
+        const dim3 grid((T + kRtT - 1) / kRtT, (E + kRtE - 1) / kRtE);
+        router_logits_tiled_kernel<<<grid, 256, 0, s>>>(x, T, H, wr, E, logits);
+        return cudaGetLastError();
+    }
     long warps = (long)T * E;
     int blocks = (int)((warps + 7) / 8);
     router_logits_kernel<<<blocks, 256, 0, s>>>(x, T, H, wr, E, logits);

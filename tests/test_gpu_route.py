@@ -30,8 +30,11 @@ def _logits_gpu(ft, x_bits, wr):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 16), ("decode_bf16", 13), ("decode_mxfp4", 8)])
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("decode_bf16", 13), ("decode_mxfp4", 8),
+                                    ("decode_bf16", 64), ("decode_mxfp4", 1000), ("prefill_mxfp4", 4096)])
 def test_router_logits_parity(ft, name, T):
+    """Decode sizes (one warp per token-expert pair) and prefill sizes (the tiled kernel,
+    T >= 64, ragged token tiles) against the oracle's fp64 logits."""
     cfg = W.config(name)
     wr = W.router_weights(cfg, layers=1)[0]
     x = W.tiny_inputs(W.config("tiny", hidden=cfg.hidden, tokens=T))
