@@ -1247,7 +1247,6 @@ ft_status forward_fused(ft_moe* h, const void* x, int T, const float* lg, void* 
         f4.x = (const __nv_bfloat16*)x;
         f4.xq = h->d_xq; f4.xsf = h->d_xsf; f4.xrs = h->d_xrs;
         f4.aq = h->d_aq; f4.asf = h->d_asf;
-        f4.act = h->d_act;
         f4.y = h->d_y;
         f4.cnt_x = h->rb.dep_x;
         f4.cnt_w13 = h->rb.dep;
@@ -1413,7 +1412,6 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.x = (const __nv_bfloat16*)x;
         f4.xq = h->d_xq; f4.xsf = h->d_xsf; f4.xrs = h->d_xrs;
         f4.aq = h->d_aq; f4.asf = h->d_asf;
-        f4.act = h->d_act;
         f4.y = h->d_y;
         f4.cnt_x = h->rb.dep_x;
         f4.cnt_w13 = h->rb.dep;
@@ -1642,7 +1640,6 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.x = (const __nv_bfloat16*)x;
         f4.xq = h->d_p_fxq; f4.xsf = h->d_p_fxsf; f4.xrs = h->d_p_fxrs;
         f4.aq = h->d_p_faq; f4.asf = h->d_p_fasf;
-        f4.act = h->d_p_act;
         f4.y = h->d_p_y;
         f4.cnt_x = h->p_rb.dep_x;
         f4.cnt_w13 = h->p_rb.dep;

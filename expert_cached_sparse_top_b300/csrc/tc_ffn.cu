@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tq_empty + kTQ);
     int* s_tile = reinterpret_cast<int*>(s_tmem + 4);  // [kTQ]
     int* s_nt = s_tile + kTQ;                          // [kMaxExperts + 1] N-tile prefix
+    int* s_off = s_nt + (kMaxExperts + 1);             // [kMaxExperts + 1] entry row offsets
+    int* s_dst = s_off + (kMaxExperts + 1);            // [kMaxExperts] weight slot per entry
+    uint8_t* s_rdy = reinterpret_cast<uint8_t*>(s_dst + kMaxExperts);   // [kMaxExperts] W13 done, seen
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the fused call's waits poll a device word (the host-mapped p.err would put a PCIe read
@@ -197,10 +200,13 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     }
 
     // N-tile prefix over this launch's entries: counts in parallel, then one warp scans
-    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
-        const int n = ldr<MK>(p.entry_off + u_begin + i + 1) - ldr<MK>(p.entry_off + u_begin + i);
-        s_nt[i] = (n + BN - 1) / BN;
-    }
+    // (the launch's entries' row offsets and weight slots are kept in shared memory: the roles
+    // read them per tile, and a global load there sits on the producer's critical path)
+    for (int i = threadIdx.x; i <= n_entries; i += blockDim.x) s_off[i] = ldr<MK>(p.entry_off + u_begin + i);
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) s_dst[i] = ldr<MK>(p.entry_dst + u_begin + i);
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) s_rdy[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) s_nt[i] = (s_off[i + 1] - s_off[i] + BN - 1) / BN;
     __syncthreads();
     if (warp == 0) {
         const int per = (n_entries + 31) / 32;
@@ -252,15 +258,25 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
 
     if (warp == 0) {
         if (lane == 0) {
-            // tiles are claimed from the launch's counter when the producer is ready for the
-            // next one (claiming ahead would hand two tiles to one CTA while others idle) and
-            // handed to the MMA and epilogue warps in claim order
+            // tiles are claimed from the launch's counter and handed to the MMA and epilogue
+            // warps in claim order. With few tiles per CTA (decode) a tile is claimed when the
+            // producer is ready for it (claiming ahead would park a tile on a busy CTA while
+            // others idle); with many (prefill) the next claim goes out as the current tile
+            // starts, so its round trip overlaps the current tile's loads
+            const bool ahead = total >= 8 * (int)gridDim.x;
+            int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t q = 0; ok; ++q) {
                 const int ts = (int)(q % kTQ);
                 if (!bar_wait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 7)) { ok = false; break; }
-                const int claimed = atomicAdd(p.tile_ctr, 1);
+                int claimed;
+                if (ahead) {
+                    claimed = next;
+                    if (claimed < total) next = atomicAdd(p.tile_ctr, 1);
+                } else {
+                    claimed = atomicAdd(p.tile_ctr, 1);
+                }
                 const int t = claimed < total ? claimed : -1;
                 s_tile[ts] = t;
                 mbar_arrive(&tq_full[ts]);
@@ -270,8 +286,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 const CUtensorMap* mA = w13 ? &tmA13 : &tmA2;
                 const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
                 const int k_steps = (w13 ? H : I) / kBK;
-                const int slot = ldr<MK>(p.entry_dst + tl.u);
-                const int row_b = ldr<MK>(p.entry_off + tl.u) + tl.nt * BN;
+                const int slot = s_dst[tl.ent_rel];
+                const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed; W13
                     // activation rows only once the entry's rows are gathered
@@ -281,15 +297,17 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                         break;
                     }
                     if (w13) {
-                        const int rows = ldr<MK>(p.entry_off + tl.u + 1) - ldr<MK>(p.entry_off + tl.u);
+                        const int rows = s_off[tl.ent_rel + 1] - s_off[tl.ent_rel];
                         if (!wait_ge_until(mg.dep_x + tl.u, rows, err, 23, deadline, 256)) { ok = false; break; }
                     }
                     fence_proxy_async_global();
                 }
                 int kb0 = 0;
                 const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
-                if (!w13 && fused && ld_acquire(p.dep + tl.u) >= target) {
-                    // the entry's activation rows are already published: stream A and B together
+                if (!w13 && fused && (s_rdy[tl.ent_rel] || ld_acquire(p.dep + tl.u) >= target)) {
+                    // the entry's activation rows are already published (seen once, remembered):
+                    // stream A and B together
+                    s_rdy[tl.ent_rel] = 1;
                     fence_proxy_async_global();
                 } else if (!w13 && fused) {
                     // stream this tile's first weight stages while the entry's W13 tiles finish
@@ -316,6 +334,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                         ok = false;
                         break;
                     }
+                    s_rdy[tl.ent_rel] = 1;
                     fence_proxy_async_global();
                     for (int kb = 0; kb < npre; ++kb) {
                         const int s = (it0 + kb) % S;
@@ -355,8 +374,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 const int k_steps = (tl.phase == 13 ? H : I) / kBK;
                 // N of this tile: its token count rounded up to 16 (a tail tile does no
                 // padded work); the accumulator keeps BN columns
-                const int row_b = ldr<MK>(p.entry_off + tl.u) + tl.nt * BN;
-                const int n_valid = min(BN, ldr<MK>(p.entry_off + tl.u + 1) - row_b);
+                const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
+                const int n_valid = min(BN, s_off[tl.ent_rel + 1] - row_b);
                 const uint32_t idesc = idesc_bf16(min(BN, (n_valid + 15) & ~15));
                 const uint32_t acc = tcount & 1u;
                 const uint32_t aph = (tcount >> 1) & 1u;
@@ -396,8 +415,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             const Tile tl = tile(t);
             const bool w13 = tl.phase == 13;
             const int m_rows = w13 ? 2 * I : H;
-            const int row_b = ldr<MK>(p.entry_off + tl.u) + tl.nt * BN;
-            const int n_valid = min(BN, ldr<MK>(p.entry_off + tl.u + 1) - row_b);
+            const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
+            const int n_valid = min(BN, s_off[tl.ent_rel + 1] - row_b);
             const uint32_t acc = tcount & 1u;
             const uint32_t aph = (tcount >> 1) & 1u;
             if (!bar_wait(&tfull[acc], aph, 4)) break;
@@ -530,7 +549,7 @@ template <int BN>
 size_t smem_for(int stages) {
     const size_t stage = 128 * 64 * 2 + BN * 64 * 2;
     return 1024 + stages * stage + (2 * stages + 4 + 2 * tc::kTQ) * 8 + 16 + tc::kTQ * 4 +
-           (kMaxExperts + 1) * 4;
+           3 * (kMaxExperts + 1) * 4 + kMaxExperts;
 }
 
 template <int BN>

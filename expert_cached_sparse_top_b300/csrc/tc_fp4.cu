@@ -29,8 +29,8 @@
 //               atoms into tensor memory and issues the block-scaled MMAs (K = 64, N = P x BN),
 //               each issuer two of the stage's four K steps into its own accumulator; commits
 //               free ring stages and publish finished accumulators.
-//   warps 2..5  epilogue: W13 tiles -> silu(g) * u -> bf16 activation rows and their W2
-//               pieces; W2 tiles -> fp32 expert outputs per (token, rank).
+//   warps 2..5  epilogue: W13 tiles -> silu(g) * u rounded to bf16 (in shared memory) -> their
+//               W2 pieces; W2 tiles -> fp32 expert outputs per (token, rank).
 // The fused decode call (MK = true, 256 threads) adds CTA 0's routing before the tiles, the
 // miss tiles' wait for their fill flags and the combine after them (mk.cuh).
 // Every wait is bounded; a wait that runs out records an error code and all roles leave.
@@ -284,11 +284,16 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     int* s_flag = reinterpret_cast<int*>(s_tmem + 1);
     int* s_eoff = reinterpret_cast<int*>(s_tmem + 4);          // [kMaxExperts + 1]
     int* s_tp = s_eoff + (kMaxExperts + 1);                      // [kMaxExperts + 1]
-    float* s_red = reinterpret_cast<float*>(s_tp + (kMaxExperts + 1));   // [8]
+    int* s_dst = s_tp + (kMaxExperts + 1);                       // [kMaxExperts] weight slot per entry
+    float* s_red = reinterpret_cast<float*>(s_dst + kMaxExperts);         // [8]
     float* s_stage = s_red + 8;                                          // [BN][65] SwiGLU values
     int* s_got = reinterpret_cast<int*>(s_stage + BN * 65);                // [2][4] epilogue votes
     int* s_tile = s_got + 8;                                               // [kTQ] tile ids
     int* s_tvote = s_tile + kTQ;                                           // [2][4] tile-id votes
+    float* s_tok = reinterpret_cast<float*>(s_tvote + 8);                  // [BN] per-token row scale
+                                                                           // (W13) or pair id (W2)
+    uint8_t* s_ready = reinterpret_cast<uint8_t*>(s_tok + BN);             // [kMaxExperts] producer's
+                                                                           // readiness marks per entry
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the fused call's waits poll a device word and run to a %globaltimer deadline
@@ -314,6 +319,8 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     const int ak13 = H / BS / 4, ak2 = I / BS / 4;   // scale atoms per 128-row band / per tile
 
     for (int i = threadIdx.x; i <= u_end; i += blockDim.x) s_eoff[i] = ldr<MK>(p.entry_off + i);
+    for (int i = threadIdx.x; i < u_end; i += blockDim.x) s_dst[i] = ldr<MK>(p.entry_dst + i);
+    for (int i = threadIdx.x; i < u_end; i += blockDim.x) s_ready[i] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < u_end; i += blockDim.x) s_tp[i] = (s_eoff[i + 1] - s_eoff[i] + BN - 1) / BN;
     __syncthreads();
@@ -384,14 +391,26 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
 
     if (warp == 0) {
         if (lane == 0) {
-            // tiles are claimed from the launch's counter when the producer is ready for the next
-            // one; they reach the MMA issuers and the epilogue in claim order
+            // tiles are claimed from the launch's counter and reach the MMA issuers and the
+            // epilogue in claim order. A launch with few tiles per CTA (decode) claims each
+            // tile when the producer is ready for it: claiming ahead would park a tile on a
+            // busy CTA while others idle. A launch with many (prefill) claims the next tile
+            // as soon as it starts the current one, so the claim's round trip to L2 overlaps
+            // the current tile's loads instead of stalling between tiles.
+            const bool ahead = total >= 8 * (int)gridDim.x;
+            int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t q = 0; ok; ++q) {
                 const int ts = (int)(q % kTQ);
                 if (!bwait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 8)) { ok = false; break; }
-                const int claimed = atomicAdd(p.tile_ctr, 1);
+                int claimed;
+                if (ahead) {
+                    claimed = next;
+                    if (claimed < total) next = atomicAdd(p.tile_ctr, 1);
+                } else {
+                    claimed = atomicAdd(p.tile_ctr, 1);
+                }
                 const int t = claimed < total ? claimed : -1;
                 s_tile[ts] = t;
                 mbar_arrive(&tq_full[ts]);
@@ -403,7 +422,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const CUtensorMap* mA = tl.w13 ? &tmA13 : &tmA2;
                 const CUtensorMap* mB = tl.w13 ? &tmB13 : &tmB2;
                 const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * NB * ak * 512;
-                const int slot = ldr<MK>(p.entry_dst + tl.u);
+                const int slot = s_dst[tl.u];
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed
                     if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err,
@@ -424,12 +443,17 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const int nbox = NB > 1 ? 1 : (P * n_valid + 15) / 16;
                 constexpr int kBoxBytes = NB > 1 ? NC * 128 : 2048;
                 const uint32_t stage_tx = (uint32_t)(kABytes + (1 + NB) * SF_BYTES + nbox * kBoxBytes);
-                // weights (and their scales) of the first stages go out before the activation
-                // pieces of this entry are known to be ready (if they are not ready yet)
+                // the entry's activation pieces must be ready (its rows split for W13, its W13
+                // tiles done for W2). Once the producer has seen an entry ready it remembers that
+                // (s_ready bit 0: x rows, bit 1: W13 tiles) and later tiles of the entry skip the
+                // round trip; when they are not ready yet, the weights (and their scales) of the
+                // first stages go out before the wait
                 const int* dep = tl.w13 ? p.cnt_x + tl.u : p.cnt_w13 + tl.u;
                 const int target = tl.w13 ? s_eoff[tl.u + 1] - s_eoff[tl.u]
                                           : m13 * (s_tp[tl.u + 1] - s_tp[tl.u]);
-                const bool ready_now = target == 0 || ld_acquire(dep) >= target;
+                const int rbit = tl.w13 ? 1 : 2;
+                const bool ready_now = target == 0 || (s_ready[tl.u] & rbit) || ld_acquire(dep) >= target;
+                if (ready_now) s_ready[tl.u] |= rbit;
                 const int npre = ready_now ? 0 : min(S, k_stages);
                 const uint32_t it0 = it;
                 for (int kb = 0; kb < npre; ++kb, ++it) {
@@ -442,6 +466,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 }
                 if (!ok) break;
                 const bool ready = ready_now || cwait(dep, target, tl.w13 ? 6 : 7);
+                if (ready) s_ready[tl.u] |= rbit;
                 fence_proxy_async_global();
                 // the armed stages expect their activation bytes: load them in any case so the
                 // ring drains if the wait ran out
@@ -576,11 +601,18 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 tc_fence_after();
                 float ts = 1.f;
                 if (FMT == FT_W_NVFP4) {
-                    const int slot = ldr<MK>(p.entry_dst + tl.u);
+                    const int slot = s_dst[tl.u];
                     const float* tsp = reinterpret_cast<const float*>(p.arena + (int64_t)slot * p.blob_bytes + p.off_ts);
                     ts = MK ? __ldcg(tsp + (tl.w13 ? 0 : 1)) : tsp[tl.w13 ? 0 : 1];
                 }
-                const float* rsp = p.xrs + (int64_t)tl.g * BN;     // W13 only: the x rows' prescale
+                // the tile's per-token values, once per tile into shared memory (an L2 load per
+                // token in the loop below would stall every chunk): W13 tiles the x rows'
+                // prescale, W2 tiles the (token, rank) pair each output row goes to
+                if (etid < n_valid) {
+                    if (tl.w13) s_tok[etid] = __ldcg(p.xrs + (int64_t)tl.g * BN + etid);
+                    else s_tok[etid] = __int_as_float(ldr<MK>(p.pairs + row_b + etid));
+                }
+                named_bar(1, 128);
                 // accumulators of this tile: issuer A at (NI acc) NC, issuer B at (NI acc + 1) NC
                 const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)(NI * NC);
                 const int m = tl.mt * 128 + row_in_tile;
@@ -608,7 +640,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                         float sum = 0.f;
 #pragma unroll
                         for (int pc = 0; pc < P; ++pc) sum += __uint_as_float(r[j * P + pc]);
-                        tok[j] = sum * (tl.w13 ? ts * __ldcg(rsp + min(i0 + j, BN - 1)) : ts);
+                        tok[j] = sum * (tl.w13 ? ts * s_tok[min(i0 + j, BN - 1)] : ts);
                     }
                     if (tl.w13) {
                         // lanes 2f / 2f+1 hold the gate / up rows of feature f: the even lane
@@ -626,14 +658,13 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                             const int i = i0 + (odd ? jj + half : jj);
                             const float a = g / (1.f + __expf(-g)) * uu;
                             const __nv_bfloat16 ab = __float2bfloat16_rn(a);
-                            if (i < n_valid) p.act[(int64_t)(row_b + i) * I + feat] = ab;
                             s_stage[i * 65 + lf] = __bfloat162float(ab);
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < tpc; ++j) {
                             const int i = i0 + j;
-                            if (i < n_valid) p.y[(int64_t)ldr<MK>(p.pairs + row_b + i) * H + m] = tok[j];
+                            if (i < n_valid) p.y[(int64_t)__float_as_int(s_tok[i]) * H + m] = tok[j];
                         }
                     }
                 }
@@ -723,7 +754,8 @@ int stage_bytes_for(int fmt, int bn, int pieces) {
 template <int BN, int FMT, int P>
 cudaError_t fp4_smem(Fp4Params& p, size_t* smem) {
     p.stage_bytes = stage_bytes_for(FMT, BN, p.pieces);
-    const size_t fixed = 1024 + (4 + 2 * fp4::kTQ) * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 32 + BN * 65 * 4 + 32 +
+    const size_t fixed = 1024 + (4 + 2 * fp4::kTQ) * 8 + 16 + 3 * (kMaxExperts + 1) * 4 + 32 + BN * 65 * 4 + BN * 4 +
+                         kMaxExperts + 32 +
                          (fp4::kTQ + 8) * 4 + 64;
     p.stages = (int)((kSmemLimit - fixed) / (p.stage_bytes + 16));
     if (p.stages > 8) p.stages = 8;

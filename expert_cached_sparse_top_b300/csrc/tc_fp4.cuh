@@ -16,8 +16,8 @@ __host__ __device__ constexpr int fp4_prefill_bn(int fmt) { return fmt == 1 ? 56
 //      pieces (tile-major: row r of entry u at position i goes to tile tp[u] + i / bn as its
 //      token i % bn; token j's piece pc is row j * P + pc of the tile's P * bn rows) and counts
 //      the rows per entry in cnt_x;
-//   2. W13 tiles (after cnt_x[u] reaches the entry's row count) -> SwiGLU -> bf16 act rows,
-//      and each tile splits its own 64 features of those rows into the W2 pieces (the block
+//   2. W13 tiles (after cnt_x[u] reaches the entry's row count) -> SwiGLU, rounded to bf16 in
+//      shared memory; each tile splits its own 64 features of those rows into the W2 pieces (the block
 //      scale of a piece comes from its block alone); every finished tile counts in cnt_w13;
 //   3. W2 tiles (after cnt_w13[u] reaches the entry's W13 tile count) -> fp32 expert
 //      outputs y[pair].
@@ -42,7 +42,6 @@ struct Fp4Params {
     float* xrs;                  // their row scales 2^-t: [tile * bn + row]
     uint8_t* aq;                 // W2 pieces and scale atoms (K = inter), written per W13 tile
     uint8_t* asf;
-    __nv_bfloat16* act;          // [grouped row][inter] bf16 SwiGLU activation
     float* y;                    // [pair][hidden] fp32 expert outputs
     int32_t* cnt_x;              // [entry] rows split (zeroed by the routing kernels)
     int32_t* cnt_w13;            // [entry] W13 tiles finished (zeroed by the routing kernels)
