@@ -191,6 +191,9 @@ struct ft_moe {
     // prefill on the block-scaled tensor cores (FP4 weights, activations as E2M1 pieces)
     bool use_fp4_prefill = false;
     int64_t p_fp4_tiles = 0;
+    uint8_t* d_p_tq = nullptr;            // every token's pieces once: codes [T][P][H/2],
+    uint8_t* d_p_tsf = nullptr;           // their scale atoms,
+    float* d_p_trs = nullptr;             // their row scales [T]
     uint8_t* d_p_fxq = nullptr;           // W13 N operand (tile-major), scale atoms, row scales
     uint8_t* d_p_fxsf = nullptr;
     float* d_p_fxrs = nullptr;
@@ -404,6 +407,7 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
     cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
     cudaFree(h->d_p_route_mem); cudaFree(h->d_p_xp); cudaFree(h->d_p_act); cudaFree(h->d_p_y);
+    cudaFree(h->d_p_tq); cudaFree(h->d_p_tsf); cudaFree(h->d_p_trs);
     cudaFree(h->d_p_fxq); cudaFree(h->d_p_fxsf);
     cudaFree(h->d_p_fxrs); cudaFree(h->d_p_faq); cudaFree(h->d_p_fasf);
     for (int b = 0; b < 2; ++b) {
@@ -834,6 +838,15 @@ ft_status alloc_prefill(ft_moe* h) {
         const size_t aq = fp4_piece_bytes(h->p_fp4_tiles, P, bn, (int)I);
         const size_t xsf = fp4_sf_bytes(h->p_fp4_tiles, (int)H, c.wfmt, P, bn);
         const size_t asf = fp4_sf_bytes(h->p_fp4_tiles, (int)I, c.wfmt, P, bn);
+        {
+            // every token's pieces once (split), then gathered per routed row into the tiles
+            const int64_t T = h->max_prefill;
+            const int bs = c.wfmt == FT_W_MXFP4 ? 32 : 16;
+            const int64_t bands = (T * P + 127) / 128;
+            FT_CUDA(h, dm((void**)&h->d_p_tq, (size_t)T * P * (H / 2)));
+            FT_CUDA(h, dm((void**)&h->d_p_tsf, (size_t)bands * (H / bs / 4) * 512));
+            FT_CUDA(h, dm((void**)&h->d_p_trs, (size_t)T * 4));
+        }
         FT_CUDA(h, dm((void**)&h->d_p_fxq, xq));
         FT_CUDA(h, dm((void**)&h->d_p_fxsf, xsf));
         FT_CUDA(h, dm((void**)&h->d_p_fxrs, (size_t)h->p_fp4_tiles * bn * 4));
@@ -1619,10 +1632,15 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
         }
     } else if (h->use_fp4_prefill) {
-        // one launch: the routed rows split into four E2M1 pieces (bf16-accurate, as in
-        // decode), W13 + SwiGLU (+ the SwiGLU activation's pieces) and W2, 32-token tiles
+        // every token split once into four E2M1 pieces (bf16-accurate, as in decode), the
+        // routed rows gathered into the tiles, then one launch: W13 + SwiGLU (+ the SwiGLU
+        // activation's pieces) and W2
         const int bn = fp4_prefill_bn(c.wfmt);
+        FT_CUDA(h, fp4_split_tokens(c.wfmt, (const __nv_bfloat16*)x, T, H, h->d_p_tq, h->d_p_tsf, h->d_p_trs, s));
+        FT_CUDA(h, fp4_gather_tiles(c.wfmt, h->p_rb.counts, h->p_rb.entry_off, h->p_rb.pairs, k, H, bn, h->d_p_tq,
+                                    h->d_p_tsf, h->d_p_trs, h->d_p_fxq, h->d_p_fxsf, h->d_p_fxrs, npairs, s));
         Fp4Params f4{};
+        f4.x_ready = 1;
         f4.counts = h->p_rb.counts;
         f4.entry_off = h->p_rb.entry_off;
         f4.entry_dst = h->p_rb.entry_dst;

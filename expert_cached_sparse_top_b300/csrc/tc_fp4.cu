@@ -20,11 +20,13 @@
 // features (counted per entry; the entry's W2 tiles wait for the count).
 //
 // Kernel roles per CTA (persistent, one CTA per SM):
-//   warp 0      producer: claims tiles from the launch's counter when it is ready for the
-//               next one, and hands their ids to the other roles
-//               through an mbarrier ring; per 256-element K stage it loads the 128-row weight
-//               tile (3-D tensor map over the slot arena), its scale atoms (bulk copy from the
-//               slot), the tile's P x BN activation-piece rows (2-D map) and their scale atoms.
+//   warp 0      producer A: claims tiles from the launch's counter and hands their ids to the
+//               other roles through an mbarrier ring; per 256-element K stage it loads the
+//               128-row weight tile (3-D tensor map over the slot arena) and its scale atoms
+//               (bulk copy from the slot).
+//   warp 6 or 7 producer B (warp 7 when there are two MMA issuers): per stage the tile's P x BN
+//               activation-piece rows (2-D map) and their scale atoms, once the entry's pieces
+//               are ready. A stage is full when both producers' bytes have landed.
 //   warp 1      TMEM allocation; with warp 6 (when P x BN <= 64) it copies the stage's scale
 //               atoms into tensor memory and issues the block-scaled MMAs (K = 64, N = P x BN),
 //               each issuer two of the stage's four K steps into its own accumulator; commits
@@ -51,7 +53,7 @@ constexpr int kStageK = 256;                 // K elements per stage: 128 bytes 
 // 32-token tiles (N = 128) keep one issuer.
 template <int P, int BN> struct Fp4Cfg {
     static constexpr int NI = P * BN <= 64 ? 2 : 1;
-    static constexpr int THREADS = NI == 2 ? 224 : 192;
+    static constexpr int THREADS = NI == 2 ? 256 : 224;   // + producer B's warp
 };
 constexpr int kABytes = 128 * 128;           // one 128-row weight tile of a stage
 constexpr int kTQ = 4;                        // claimed-tile ring depth
@@ -248,8 +250,8 @@ __device__ __forceinline__ int entry_of_row(const int* s_eoff, int u_begin, int 
     return lo;
 }
 
-// MK: the fused decode call (TcMega; one cooperative launch, 256 threads: warps 6 and 7 or 7
-// have no role besides the routing, the row split and the combine).
+// MK: the fused decode call (TcMega; one cooperative launch, 256 threads: warps 6 and 7 take
+// part in the routing, the row split and the combine besides their roles).
 template <int BN, int FMT, int P, bool MK>
 constexpr int fp4_block() { return MK ? 256 : Fp4Cfg<P, BN>::THREADS; }
 
@@ -262,6 +264,8 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     constexpr int SF_BYTES = APS * 512;
     constexpr int NI = Fp4Cfg<P, BN>::NI;             // MMA issuers
     constexpr int NTH = fp4_block<BN, FMT, P, MK>();
+    constexpr int kPBWarp = NI == 2 ? 7 : 6;           // producer B (activation pieces)
+    static_assert(kPBWarp * 32 < NTH, "producer B's warp");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages, STAGE = p.stage_bytes;
@@ -340,10 +344,11 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
         if (lane == 31) s_tp[u_end] = incl;
     }
     if (warp == 0 && lane == 0) {
-        // a stage is free, and an accumulator full, once every MMA issuer has committed
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NI); }
+        // a stage is full once both producers' bytes landed; free, and an accumulator full,
+        // once every MMA issuer has committed
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], NI); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
-        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 4); }
+        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 5); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -374,29 +379,34 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     };
 
     // 1. W13 activation pieces: the launch's CTAs split the pass's token rows between them
-    const int r0 = s_eoff[u_begin], r1 = s_eoff[u_end];
-    for (int r = r0 + blockIdx.x; r < r1; r += gridDim.x) {
-        const int u = entry_of_row(s_eoff, u_begin, u_end, r);
-        const int i = r - s_eoff[u];
-        const int tile = s_tp[u] + i / BN, rin = i % BN;
-        const __nv_bfloat16* src = p.x + (int64_t)(ldr<MK>(p.pairs + r) / p.top_k) * H;
-        split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
-                      p.xsf + (int64_t)tile * NB * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
-                      threadIdx.x, NTH, 2, s_red);
-        fence_proxy_async_global();
-        __threadfence();
-        named_bar(2, NTH);
-        if (threadIdx.x == 0) atomicAdd(p.cnt_x + u, 1);
+    // (unless the caller has gathered them already). Warps 2 and up do it; the producer
+    // (warp 0) goes straight to its first tile and streams that tile's first weight stages
+    // while the rows are being split, and the MMA warp waits for them as usual.
+    if (warp >= 2 && !p.x_ready) {
+        const int r0 = s_eoff[u_begin], r1 = s_eoff[u_end];
+        for (int r = r0 + blockIdx.x; r < r1; r += gridDim.x) {
+            const int u = entry_of_row(s_eoff, u_begin, u_end, r);
+            const int i = r - s_eoff[u];
+            const int tile = s_tp[u] + i / BN, rin = i % BN;
+            const __nv_bfloat16* src = p.x + (int64_t)(ldr<MK>(p.pairs + r) / p.top_k) * H;
+            split_row<BS>(src, H, P, FMT, p.xq + ((int64_t)tile * NC + rin * P) * (H / 2), H / 2,
+                          p.xsf + (int64_t)tile * NB * ak13 * 512, rin * P, p.xrs + (int64_t)tile * BN + rin,
+                          threadIdx.x - 64, NTH - 64, 2, s_red);
+            fence_proxy_async_global();
+            __threadfence();
+            named_bar(2, NTH - 64);
+            if (threadIdx.x == 64) atomicAdd(p.cnt_x + u, 1);
+        }
     }
 
     if (warp == 0) {
         if (lane == 0) {
-            // tiles are claimed from the launch's counter and reach the MMA issuers and the
-            // epilogue in claim order. A launch with few tiles per CTA (decode) claims each
-            // tile when the producer is ready for it: claiming ahead would park a tile on a
-            // busy CTA while others idle. A launch with many (prefill) claims the next tile
-            // as soon as it starts the current one, so the claim's round trip to L2 overlaps
-            // the current tile's loads instead of stalling between tiles.
+            // Producer A: claims tiles and streams their weights (codes and scale atoms). Tiles
+            // reach producer B, the MMA issuers and the epilogue in claim order. A launch with
+            // few tiles per CTA (decode) claims each tile when the producer is ready for it:
+            // claiming ahead would park a tile on a busy CTA while others idle. A launch with
+            // many (prefill) claims the next tile as soon as it starts the current one, so the
+            // claim's round trip to L2 overlaps the current tile's loads.
             const bool ahead = total >= 8 * (int)gridDim.x;
             int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
             uint32_t it = 0;
@@ -416,12 +426,9 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 mbar_arrive(&tq_full[ts]);
                 if (t < 0) break;
                 const FTile tl = tile(t);
-                const int K = tl.w13 ? H : I;
-                const int k_stages = K / kStageK;
+                const int k_stages = (tl.w13 ? H : I) / kStageK;
                 const int ak = tl.w13 ? ak13 : ak2;
                 const CUtensorMap* mA = tl.w13 ? &tmA13 : &tmA2;
-                const CUtensorMap* mB = tl.w13 ? &tmB13 : &tmB2;
-                const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * NB * ak * 512;
                 const int slot = s_dst[tl.u];
                 if constexpr (MK) {
                     // a missed expert's weights are read only once its copy has landed
@@ -434,60 +441,66 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 }
                 const uint8_t* sfa = p.arena + (int64_t)slot * p.blob_bytes + (tl.w13 ? p.off_s13 : p.off_s2) +
                                      (int64_t)tl.mt * ak * 512;
+                constexpr uint32_t a_tx = (uint32_t)(kABytes + SF_BYTES);
+                for (int kb = 0; kb < k_stages; ++kb, ++it) {
+                    const int s = it % S;
+                    if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
+                    uint8_t* st = smem + (size_t)s * STAGE;
+                    mbar_expect_tx(&full[s], a_tx);
+                    tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
+                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
+                }
+            }
+            if (!ok) {
+                for (uint32_t j = (it > (uint32_t)S ? it - S : 0); j < it; ++j)
+                    mbar_wait(&full[j % S], (j / S) & 1u, err, 5);
+            }
+        }
+    } else if (warp == kPBWarp) {
+        if (lane == 0) {
+            // Producer B: the activation pieces (codes and scale atoms) of every stage, tile by
+            // tile in claim order, once the entry's pieces are ready (its rows split for W13,
+            // its W13 tiles done for W2). Two threads issuing the stage copies move about twice
+            // the bytes per SM that one does, and the weight stream never waits on the
+            // readiness of the activations. Once an entry has been seen ready, that is
+            // remembered (s_ready bit 0: x rows, bit 1: W13 tiles) and its later tiles skip the
+            // round trip.
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const int ts = (int)(tcount % kTQ);
+                if (!bwait(&tq_full[ts], (tcount / kTQ) & 1u, 11)) { ok = false; break; }
+                const int t = s_tile[ts];
+                mbar_arrive(&tq_empty[ts]);
+                if (t < 0) break;
+                const FTile tl = tile(t);
+                const int k_stages = (tl.w13 ? H : I) / kStageK;
+                const int ak = tl.w13 ? ak13 : ak2;
+                const CUtensorMap* mB = tl.w13 ? &tmB13 : &tmB2;
+                const uint8_t* bsf = (tl.w13 ? p.xsf : p.asf) + (int64_t)tl.g * NB * ak * 512;
                 // the tile's rows are token-major (token i, piece pc at row i * P + pc): only the
                 // first P * n_valid rows carry data. Tiles of up to 128 rows (decode) load just
                 // those, as 16-row boxes; wider tiles (prefill, mostly full) load all NC rows
-                // with one box (their piece tensor maps are encoded with that box height), so
-                // the producer issues a handful of copies per stage instead of up to NC / 16
+                // with one box (their piece tensor maps are encoded with that box height)
                 const int n_valid = min(BN, s_eoff[tl.u + 1] - s_eoff[tl.u] - (tl.g - s_tp[tl.u]) * BN);
                 const int nbox = NB > 1 ? 1 : (P * n_valid + 15) / 16;
                 constexpr int kBoxBytes = NB > 1 ? NC * 128 : 2048;
-                const uint32_t stage_tx = (uint32_t)(kABytes + (1 + NB) * SF_BYTES + nbox * kBoxBytes);
-                // the entry's activation pieces must be ready (its rows split for W13, its W13
-                // tiles done for W2). Once the producer has seen an entry ready it remembers that
-                // (s_ready bit 0: x rows, bit 1: W13 tiles) and later tiles of the entry skip the
-                // round trip; when they are not ready yet, the weights (and their scales) of the
-                // first stages go out before the wait
+                const uint32_t b_tx = (uint32_t)(nbox * kBoxBytes + NB * SF_BYTES);
                 const int* dep = tl.w13 ? p.cnt_x + tl.u : p.cnt_w13 + tl.u;
-                const int target = tl.w13 ? s_eoff[tl.u + 1] - s_eoff[tl.u]
+                const int target = tl.w13 ? (p.x_ready ? 0 : s_eoff[tl.u + 1] - s_eoff[tl.u])
                                           : m13 * (s_tp[tl.u + 1] - s_tp[tl.u]);
                 const int rbit = tl.w13 ? 1 : 2;
-                const bool ready_now = target == 0 || (s_ready[tl.u] & rbit) || ld_acquire(dep) >= target;
-                if (ready_now) s_ready[tl.u] |= rbit;
-                const int npre = ready_now ? 0 : min(S, k_stages);
-                const uint32_t it0 = it;
-                for (int kb = 0; kb < npre; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
-                    uint8_t* st = smem + (size_t)s * STAGE;
-                    mbar_expect_tx(&full[s], stage_tx);
-                    tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
-                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
-                }
-                if (!ok) break;
-                const bool ready = ready_now || cwait(dep, target, tl.w13 ? 6 : 7);
+                const bool ready = target == 0 || (s_ready[tl.u] & rbit) || ld_acquire(dep) >= target ||
+                                   cwait(dep, target, tl.w13 ? 6 : 7);
                 if (ready) s_ready[tl.u] |= rbit;
                 fence_proxy_async_global();
-                // the armed stages expect their activation bytes: load them in any case so the
-                // ring drains if the wait ran out
-                for (int kb = 0; kb < npre; ++kb) {
-                    uint8_t* st = smem + (size_t)((it0 + kb) % S) * STAGE;
-                    uint64_t* fb = &full[(it0 + kb) % S];
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(st + kABytes + bx * 2048, mB, fb, kb * 128, tl.g * NC + bx * 16);
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-                        bulk_load(st + kABytes + B_BYTES + (1 + b) * SF_BYTES,
-                                  bsf + ((int64_t)b * ak * 512 + (int64_t)kb * SF_BYTES), SF_BYTES, fb);
-                }
-                if (!ready) { ok = false; break; }
-                for (int kb = npre; kb < k_stages; ++kb, ++it) {
+                // the stages producer A arms expect these bytes: they are loaded even after a
+                // wait ran out, so the ring drains
+                for (int kb = 0; kb < k_stages; ++kb, ++it) {
                     const int s = it % S;
                     if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
                     uint8_t* st = smem + (size_t)s * STAGE;
-                    mbar_expect_tx(&full[s], stage_tx);
-                    tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
-                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
+                    mbar_expect_tx(&full[s], b_tx);
                     for (int bx = 0; bx < nbox; ++bx)
                         tma_load_2d(st + kABytes + bx * 2048, mB, &full[s], kb * 128, tl.g * NC + bx * 16);
 #pragma unroll
@@ -495,6 +508,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                         bulk_load(st + kABytes + B_BYTES + (1 + b) * SF_BYTES,
                                   bsf + ((int64_t)b * ak * 512 + (int64_t)kb * SF_BYTES), SF_BYTES, &full[s]);
                 }
+                if (!ready) ok = false;
             }
             if (!ok) {
                 for (uint32_t j = (it > (uint32_t)S ? it - S : 0); j < it; ++j)
@@ -716,6 +730,74 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     }
 }
 
+// Prefill: one token's P pieces (128 threads; the same split as inside the FFN launch, done
+// once per token instead of once per routed row).
+template <int BS>
+__global__ void __launch_bounds__(128) split_tokens_kernel(const __nv_bfloat16* __restrict__ x, int H, int P, int fmt,
+                                                           uint8_t* __restrict__ tq, uint8_t* __restrict__ tsf,
+                                                           float* __restrict__ trs) {
+    __shared__ float s_red[8];
+    const int t = blockIdx.x;
+    split_row<BS>(x + (int64_t)t * H, H, P, fmt, tq + (int64_t)t * P * (H / 2), H / 2, tsf, t * P, trs + t,
+                  threadIdx.x, 128, 2, s_red);
+}
+
+// Byte offset of (row n, block j) in an operand's scale atoms (128-row bands of ak atoms).
+__device__ __forceinline__ int64_t atom_byte(int64_t n, int j, int ak) {
+    return ((n >> 7) * ak + (j >> 2)) * 512 + (n & 31) * 16 + ((n & 127) >> 5) * 4 + (j & 3);
+}
+
+// Prefill: routed row r -> its tile rows (one warp per row): P piece rows of codes, their
+// scale bytes, the row scale.
+__global__ void __launch_bounds__(256) gather_tiles_kernel(
+    const RouteCounts* __restrict__ counts, const int32_t* __restrict__ entry_off, const int32_t* __restrict__ pairs,
+    int top_k, int H, int bs, int bn, int P, const uint8_t* __restrict__ tq, const uint8_t* __restrict__ tsf,
+    const float* __restrict__ trs, uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, float* __restrict__ xrs) {
+    __shared__ int s_eoff[kMaxExperts + 1];
+    __shared__ int s_tp[kMaxExperts + 1];
+    const int U = counts->n_unique;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= U; i += blockDim.x) s_eoff[i] = entry_off[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < U; i += blockDim.x) s_tp[i] = (s_eoff[i + 1] - s_eoff[i] + bn - 1) / bn;
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (U + 31) / 32;
+        const int i0 = lane * per, i1 = min(U, i0 + per);
+        int local = 0;
+        for (int i = i0; i < i1; ++i) local += s_tp[i];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int i = i0; i < i1; ++i) { const int t = s_tp[i]; s_tp[i] = run; run += t; }
+    }
+    __syncthreads();
+    const int rows = s_eoff[U];
+    const int nc = P * bn;                      // N-operand rows per tile
+    const int nb = (nc + 127) / 128;            // its scale bands
+    const int nblk = H / bs, ak = nblk / 4;
+    const int64_t piece_bytes = H / 2;
+    for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
+        const int u = entry_of_row(s_eoff, 0, U, r);
+        const int i = r - s_eoff[u];
+        const int tile = s_tp[u] + i / bn, rin = i % bn;
+        const int64_t tok = pairs[r] / top_k;
+        const uint4* src = reinterpret_cast<const uint4*>(tq + tok * P * piece_bytes);
+        uint4* dst = reinterpret_cast<uint4*>(xq + ((int64_t)tile * nc + (int64_t)rin * P) * piece_bytes);
+        for (int c = lane; c < (int)(P * piece_bytes / 16); c += 32) dst[c] = __ldg(src + c);
+        uint8_t* dsf = xsf + (int64_t)tile * nb * ak * 512;
+        for (int q = lane; q < P * nblk; q += 32) {
+            const int pc = q / nblk, j = q % nblk;
+            dsf[atom_byte(rin * P + pc, j, ak)] = __ldg(tsf + atom_byte(tok * P + pc, j, ak));
+        }
+        if (lane == 0) xrs[(int64_t)tile * bn + rin] = __ldg(trs + tok);
+    }
+}
+
 }  // namespace fp4
 
 // ----------------------------------------------------------------------------------------
@@ -894,6 +976,31 @@ cudaError_t fp4_launch(int fmt, int bn, const Fp4Params& p, const Fp4Maps& m, in
     if (!mx && bn == fp4_prefill_bn(FT_W_NVFP4))
         return launch_t<fp4_prefill_bn(FT_W_NVFP4), FT_W_NVFP4, 4>(p, m, grid, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t fp4_split_tokens(int fmt, const __nv_bfloat16* x, int T, int H, uint8_t* tq, uint8_t* tsf, float* trs,
+                             cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    if (H % fp4::kStageK) return cudaErrorInvalidValue;
+    if (fmt == FT_W_MXFP4)
+        fp4::split_tokens_kernel<32><<<T, 128, 0, s>>>(x, H, kFp4MaxPieces, fmt, tq, tsf, trs);
+    else if (fmt == FT_W_NVFP4)
+        fp4::split_tokens_kernel<16><<<T, 128, 0, s>>>(x, H, kFp4MaxPieces, fmt, tq, tsf, trs);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t fp4_gather_tiles(int fmt, const RouteCounts* counts, const int32_t* entry_off, const int32_t* pairs,
+                             int top_k, int H, int bn, const uint8_t* tq, const uint8_t* tsf, const float* trs,
+                             uint8_t* xq, uint8_t* xsf, float* xrs, int rows_max, cudaStream_t s) {
+    if (rows_max <= 0) return cudaSuccess;
+    const int bs = fmt == FT_W_MXFP4 ? 32 : 16;
+    int blocks = (rows_max + 7) / 8;
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    fp4::gather_tiles_kernel<<<blocks, 256, 0, s>>>(counts, entry_off, pairs, top_k, H, bs, bn, kFp4MaxPieces,
+                                                    tq, tsf, trs, xq, xsf, xrs);
+    return cudaGetLastError();
 }
 
 }  // namespace ftmoe

@@ -29,7 +29,9 @@ struct Fp4Params {
     int32_t pass;                // 0: entries [0, n_hits), 1: [n_hits, n_unique), 2: all
     int32_t hidden, inter;       // multiples of 256
     int32_t top_k;
-    int32_t pieces;              // P, with P * bn <= 128 (always four)
+    int32_t pieces;              // P (always four)
+    int32_t x_ready;             // nonzero: xq / xsf / xrs were written before the launch
+                                 // (prefill: split once per token, then gathered into tiles)
     int32_t stages;              // set by the launcher
     int32_t stage_bytes;         // set by the launcher
     const uint8_t* arena;        // weight slots (scale atoms and tensor scales are read here)
@@ -58,6 +60,16 @@ struct Fp4Maps {
 
 // bytes of one tile-major piece buffer (codes) / scale-atom buffer for `tiles` tiles
 size_t fp4_piece_bytes(int64_t tiles, int pieces, int bn, int K);
+// Prefill: the pieces of every token once, then the routed rows gathered into tiles.
+//   fp4_split_tokens: x [T][H] bf16 -> codes [T][P][H/2], scale atoms (row t * P + pc of a
+//   [T * P]-row operand, 128-row bands of H / bs / 4 atoms), row scales [T].
+//   fp4_gather_tiles: routed row r (entry u, position i) -> tile tp[u] + i / bn, rows
+//   (i % bn) * P .. + P - 1 of the tile's N operand (codes, scale atoms, row scale).
+cudaError_t fp4_split_tokens(int fmt, const __nv_bfloat16* x, int T, int H, uint8_t* tq, uint8_t* tsf, float* trs,
+                             cudaStream_t s);
+cudaError_t fp4_gather_tiles(int fmt, const RouteCounts* counts, const int32_t* entry_off, const int32_t* pairs,
+                             int top_k, int H, int bn, const uint8_t* tq, const uint8_t* tsf, const float* trs,
+                             uint8_t* xq, uint8_t* xsf, float* xrs, int rows_max, cudaStream_t s);
 size_t fp4_sf_bytes(int64_t tiles, int K, int fmt, int pieces, int bn);
 
 cudaError_t fp4_encode_weights(CUtensorMap* map, const void* base, int k_dim, int rows,

@@ -176,7 +176,8 @@ typedef struct {
     uint64_t prefill_calls;
     double prefill_fill_ms;    /* full-layer H2D copies (copy stream) */
     double prefill_compute_ms; /* routing + grouping + FFN + combine on the caller's stream */
-    double prefill_ffn_ms;     /* the two grouped-GEMM launches (W13+SwiGLU, W2) */
+    double prefill_ffn_ms;     /* the expert FFN: the grouped-GEMM launch (W13+SwiGLU, W2); FP4 adds
+                                  the activation split and its gather into tiles */
     double prefill_flops;      /* 6 * T * k * H * I per call (dense-equivalent FFN flops) */
     uint64_t prefill_fill_bytes;
     /* layer-ahead prefetch (ft_cache_prefetch) */
