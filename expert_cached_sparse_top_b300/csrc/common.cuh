@@ -36,7 +36,7 @@ struct RouteBuffers {
     int32_t* dep;          // [max_u] per-entry W13 completion counters of the fused FFN (zeroed here)
     int32_t* dep_x;        // [max_u] per-entry split-row counters of the fused FP4 FFN (zeroed here)
     int32_t* dep_a;        // [max_u] per-entry W2-pieces-ready flags of the fused FP4 FFN (zeroed here)
-    int32_t* tile_ctr;     // [4] tile-claim counters of the BF16 FFN launches of a call (zeroed here)
+    int32_t* tile_ctr;     // [8] tile-claim counters of the FFN launches of a call (zeroed here)
 };
 
 // Host-mapped mirror of the fill list (the host issues one copy per miss).
@@ -81,6 +81,19 @@ struct PrefetchParams {
     int32_t* hv_dst;           // host-mapped [max]: its slot
 };
 
+// Entries one expert-FFN pass covers: 0 the hits [0, n_hits), 1 the misses [n_hits, n_unique),
+// 2 all of them, 3 the misses [n_hits + miss_lo, n_hits + min(miss_hi, n_miss)) (a group of
+// misses run once their copies have landed).
+__host__ __device__ __forceinline__ void pass_range(int pass, const RouteCounts& rc, int miss_lo, int miss_hi,
+                                                    int* u_begin, int* u_end) {
+    if (pass == 0) { *u_begin = 0; *u_end = rc.n_hits; return; }
+    if (pass == 1) { *u_begin = rc.n_hits; *u_end = rc.n_unique; return; }
+    if (pass == 2) { *u_begin = 0; *u_end = rc.n_unique; return; }
+    const int hi = miss_hi < rc.n_miss ? miss_hi : rc.n_miss;
+    *u_begin = rc.n_hits + miss_lo;
+    *u_end = rc.n_hits + (hi > miss_lo ? hi : miss_lo);
+}
+
 // Weight-section offsets inside one expert blob.
 struct BlobLayout {
     int64_t blob_bytes;
@@ -106,7 +119,8 @@ struct FfnParams {
     const int32_t* entry_dst;
     const int32_t* entry_off;
     const int32_t* pairs;
-    int32_t pass;                // 0: entries [0, n_hits), 1: entries [n_hits, n_unique)
+    int32_t pass;                // see pass_range
+    int32_t miss_lo, miss_hi;    // pass 3: misses [miss_lo, miss_hi)
     const __nv_bfloat16* x;      // [T][H]
     __nv_bfloat16* act;          // [T*k][I]  SwiGLU activation, bf16
     float* y;                    // [T*k][H]  expert outputs, fp32

@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) ffn_kernel(FfnParams p) {
     constexpr int SEG = FmtTraits<FMT>::kSeg;
     const int lane = threadIdx.x & 31;
     const RouteCounts rc = *p.counts;
-    const int u_begin = p.pass == 0 ? 0 : rc.n_hits;
-    const int u_end = p.pass == 0 ? rc.n_hits : rc.n_unique;
+    int u_begin, u_end;
+    pass_range(p.pass, rc, p.miss_lo, p.miss_hi, &u_begin, &u_end);
     if (u_end <= u_begin) return;
     const int H = p.hidden, I = p.inter, k = p.top_k;
     const int K = (MODE == 13) ? H : I;

@@ -54,9 +54,10 @@ StreamWriteValue32Fn stream_write_fn() {
 }
 
 struct StageEvents {
-    cudaEvent_t ev[8];
+    cudaEvent_t ev[10];
     bool has_fill;
     bool has_miss;
+    bool has_miss2;                      // ev[8] -> ev[9]: the second group of misses
     cudaEvent_t fill_begin, fill_end;
     cudaEvent_t pf_begin, pf_end;        // prefetch fills issued for this call (ft_cache_prefetch)
     bool pf_wait;                        // ev[6] -> ev[7]: the call's stream waited for them
@@ -110,6 +111,8 @@ struct ft_moe {
     cudaStream_t copy_stream2 = nullptr;  // fused decode: the fill agent alternates the two
     cudaEvent_t ev_copy2 = nullptr;
     cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_fill_a = nullptr;      // all misses of a call but the last copied
+    bool miss_groups = true;              // FTMOE_MISS_GROUPS=0: one FFN pass over all misses
 
     ft_cache_stats_t stats{};
     bool broken = false;
@@ -431,6 +434,7 @@ void free_all(ft_moe* h) {
     if (h->ev_copy2) cudaEventDestroy(h->ev_copy2);
     if (h->ev_route) cudaEventDestroy(h->ev_route);
     if (h->ev_fill) cudaEventDestroy(h->ev_fill);
+    if (h->ev_fill_a) cudaEventDestroy(h->ev_fill_a);
     if (h->ev_done) cudaEventDestroy(h->ev_done);
     for (auto& se : h->pending) {
         for (auto ev : se.ev) h->event_pool.push_back(ev);
@@ -758,7 +762,8 @@ void collect_timing(ft_moe* h) {
         h->tsum.route_ms += ev_ms(se.ev[0], se.ev[1]) - pf_wait;
         h->tsum.ffn_hit_ms += ev_ms(se.ev[1], se.ev[2]);
         if (se.has_miss) h->tsum.ffn_miss_ms += ev_ms(se.ev[3], se.ev[4]);
-        h->tsum.combine_ms += ev_ms(se.ev[4], se.ev[5]);
+        if (se.has_miss2) h->tsum.ffn_miss_ms += ev_ms(se.ev[8], se.ev[9]);
+        h->tsum.combine_ms += ev_ms(se.has_miss2 ? se.ev[9] : se.ev[4], se.ev[5]);
         h->tsum.total_ms += ev_ms(se.ev[0], se.ev[5]);
         if (se.has_fill) {
             cudaEventSynchronize(se.fill_end);
@@ -767,7 +772,7 @@ void collect_timing(ft_moe* h) {
             h->stats.fill_ns += (uint64_t)(f * 1e6);
         }
         // ev[5] (the call's end) stays out of the pool until the next call's lead is taken
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 10; ++i)
             if (i != 5) h->event_pool.push_back(se.ev[i]);
         if (h->last_end_ev) h->event_pool.push_back(h->last_end_ev);
         h->last_end_ev = se.ev[5];
@@ -956,6 +961,7 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         h->fault_fill = strstr(f, "fill_fail") != nullptr;
     }
     if (const char* w = getenv("FTMOE_WAIT_MS")) h->wait_ms = std::max<int64_t>(1, atoll(w));
+    if (const char* g = getenv("FTMOE_MISS_GROUPS")) h->miss_groups = atoi(g) != 0;
 
     auto bail = [&](ft_status s) {
         g_create_error = h->err;
@@ -1074,6 +1080,7 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
     if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_route, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fill_a, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess) {
         cuda_fail(h, cudaGetLastError(), "stream/event create"); return bail(FT_ERR_CUDA);
     }
@@ -1430,23 +1437,28 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.cnt_w13 = h->rb.dep;
         f4.err = h->d_ffn_err;
     }
-    auto run_ffn = [&](int pass) -> cudaError_t {
+    // pass: see pass_range; ctr: which pair of the call's tile-claim counters the launch uses;
+    // lo, hi: the group of misses of pass 3
+    auto run_ffn = [&](int pass, int ctr, int lo, int hi) -> cudaError_t {
         if (h->use_fp4) {
             // one launch: activation pieces, W13 + SwiGLU, W2 pieces, W2
             f4.pass = pass;
-            f4.tile_ctr = h->rb.tile_ctr + 2 * pass;
+            f4.miss_lo = lo; f4.miss_hi = hi;
+            f4.tile_ctr = h->rb.tile_ctr + 2 * ctr;
             launches += 1;
             const Fp4Maps maps{&h->tmF_A13, &h->tmF_B13, &h->tmF_A2, &h->tmF_B2};
             return fp4_launch(c.wfmt, h->fp4_bn, f4, maps, h->num_sms, s);
         }
         if (!h->use_tc) {
             fp.pass = pass;
+            fp.miss_lo = lo; fp.miss_hi = hi;
             return launch_ffn(c.wfmt, fp, c.max_tokens, s, &launches);
         }
         tp.pass = pass;
+        tp.miss_lo = lo; tp.miss_hi = hi;
         tp.hidden = H; tp.inter = c.inter;
         const TcMaps maps{&h->tmA13, &h->tmB13, &h->tmA2, &h->tmB2};
-        tp.tile_ctr = h->rb.tile_ctr + 2 * pass;
+        tp.tile_ctr = h->rb.tile_ctr + 2 * ctr;
         if (h->tc_fused) {
             tp.phases = 3; tp.dep = h->rb.dep;
             launches += 1;
@@ -1457,7 +1469,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         cudaError_t e = tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
         if (e != cudaSuccess) return e;
         tp.phases = 2;
-        tp.tile_ctr = h->rb.tile_ctr + 2 * pass + 1;
+        tp.tile_ctr = h->rb.tile_ctr + 2 * ctr + 1;
         launches += 2;
         return tc_launch(h->tc_bn, tp, maps, h->num_sms, s);
     };
@@ -1471,7 +1483,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
     }
     // the FFN window opens here: routing, the row gather (BF16) and parameter set-up before
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[1], s));
-    FT_CUDA(h, run_ffn(0));
+    FT_CUDA(h, run_ffn(0, 0, 0, 0));
     if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[2], s));
 
     // The one host wait: the miss list of this call.
@@ -1498,28 +1510,47 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             h->broken = true;
             return fail(h, FT_ERR_CUDA, "injected fill failure (FTMOE_FAULT=fill_fail)");
         }
+        // Two groups when there are at least two misses: all but the last one run once their
+        // copies have landed, while the last copy is still on the link; the last one runs
+        // after it. Only one expert's FFN then follows the final copy instead of every miss's.
+        const int n = rc.n_miss;
+        const bool grouped = h->miss_groups && n >= 2;
         if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_begin, h->copy_stream));
-        for (int j = 0; j < rc.n_miss; ++j) {
+        for (int j = 0; j < n; ++j) {
             const int key = h->h_miss_key[j];
             const int dst = h->h_miss_dst[j];
             if (key < 0 || key >= c.layers * E || dst < 0 || dst >= h->C + h->n_stage) {
                 h->broken = true;
                 return fail(h, FT_ERR_STATE, "miss list out of range");
             }
+            if (grouped && j == n - 1) FT_CUDA(h, cudaEventRecord(h->ev_fill_a, h->copy_stream));
             FT_CUDA(h, cudaMemcpyAsync(h->d_arena + (size_t)dst * h->blob_bytes, h->blobs[(size_t)key],
                                        h->blob_bytes, cudaMemcpyHostToDevice, h->copy_stream));
         }
         FT_CUDA(h, cudaEventRecord(h->ev_fill, h->copy_stream));
         if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_end, h->copy_stream));
-        FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_fill, 0));
-        if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[3], s));
-        FT_CUDA(h, run_ffn(1));
+        if (grouped) {
+            FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_fill_a, 0));
+            if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[3], s));
+            FT_CUDA(h, run_ffn(3, 1, 0, n - 1));
+            if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[4], s));
+            FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_fill, 0));
+            if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[8], s));
+            FT_CUDA(h, run_ffn(3, 2, n - 1, n));
+            if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[9], s));
+            se.has_miss2 = true;
+        } else {
+            FT_CUDA(h, cudaStreamWaitEvent(s, h->ev_fill, 0));
+            if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[3], s));
+            FT_CUDA(h, run_ffn(1, 1, 0, 0));
+            if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[4], s));
+        }
         se.has_miss = true;
         se.has_fill = true;
     } else if (h->timing) {
         FT_CUDA(h, cudaEventRecord(se.ev[3], s));
+        FT_CUDA(h, cudaEventRecord(se.ev[4], s));
     }
-    if (h->timing) FT_CUDA(h, cudaEventRecord(se.ev[4], s));
     FT_CUDA(h, launch_combine(h->d_y, h->d_w, T, k, H, (__nv_bfloat16*)out, s));
     ++launches;
     FT_CUDA(h, cudaEventRecord(h->ev_done, s));
@@ -1527,7 +1558,7 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         FT_CUDA(h, cudaEventRecord(se.ev[5], s));
         h->pending.push_back(se);
         h->tsum.forwards++;
-        h->tsum.ffn_launches += rc.n_miss > 0 ? 2 : 1;
+        h->tsum.ffn_launches += rc.n_miss > 0 ? (se.has_miss2 ? 3 : 2) : 1;
         uint64_t wbytes = (uint64_t)rc.n_unique * (uint64_t)(h->lay.blob_bytes);
         h->tsum.ffn_weight_bytes += wbytes;
         h->tsum.kernel_launches += (uint64_t)launches;

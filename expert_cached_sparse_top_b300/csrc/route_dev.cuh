@@ -148,7 +148,7 @@ __device__ __forceinline__ void lookup_block(const LookupParams& p, const Lookup
 
     for (int e = tid; e < E; e += blockDim.x) s_present[e] = 0;
     if (tid == 0) { s_evict = 0; s_err = (p.nan_flag && *p.nan_flag) ? 1 : 0; }
-    if (tid < 4 && p.rb.tile_ctr) p.rb.tile_ctr[tid] = 0;
+    if (tid < 8 && p.rb.tile_ctr) p.rb.tile_ctr[tid] = 0;
     __syncthreads();
     for (int i = tid; i < p.n_pairs; i += blockDim.x) {
         int e = p.idx[i];

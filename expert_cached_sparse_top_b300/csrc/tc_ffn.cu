@@ -90,7 +90,8 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
 // small-N tcgen05.mma cannot keep up with the weight stream.
 template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
 constexpr int kTQ = 4;             // claimed-tile ring depth
-template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 32 : kThreads; }
+// warps: producer A (weights), MMA issuer(s), four epilogue warps, producer B (activations)
+template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 64 : kThreads + 32; }
 
 template <int BN, bool MK> constexpr int tc_block() { return MK ? 256 : tc_threads<BN>(); }
 
@@ -132,6 +133,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
     constexpr bool DUAL = TcDual<BN>::value;
     constexpr int NI = DUAL ? 2 : 1;                  // MMA issuers
+    constexpr int kPBWarp = DUAL ? 7 : 6;             // producer B (activation rows)
+    static_assert(kPBWarp * 32 < tc_block<BN, MK>(), "producer B's warp");
     constexpr int A_BYTES = kBM * kBK * 2;            // 16 KB
     constexpr int B_BYTES = BN * kBK * 2;
     constexpr int STAGE = A_BYTES + B_BYTES;
@@ -172,8 +175,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         if (!mk_wait_route(mg, err, deadline, s_tmem + 2)) { report(); return; }
     }
     const RouteCounts rc = MK ? mk_counts(p.counts) : *p.counts;
-    const int u_begin = MK ? 0 : (p.pass == 0 ? 0 : rc.n_hits);
-    const int u_end = MK ? rc.n_unique : (p.pass == 0 ? rc.n_hits : rc.n_unique);
+    int u_begin = 0, u_end = rc.n_unique;
+    if (!MK) pass_range(p.pass, rc, p.miss_lo, p.miss_hi, &u_begin, &u_end);
     const int n_entries = u_end - u_begin;
     if (n_entries <= 0) { report(); return; }
     const int H = p.hidden, I = p.inter;
@@ -224,9 +227,10 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         if (lane == 31) s_nt[n_entries] = incl;
     }
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], NI); }
+        // a stage is full once both producers' bytes landed
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], NI); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
-        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 4); }
+        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 5); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -284,75 +288,76 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 const Tile tl = tile(t);
                 const bool w13 = tl.phase == 13;
                 const CUtensorMap* mA = w13 ? &tmA13 : &tmA2;
-                const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
                 const int k_steps = (w13 ? H : I) / kBK;
                 const int slot = s_dst[tl.ent_rel];
-                const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
                 if constexpr (MK) {
-                    // a missed expert's weights are read only once its copy has landed; W13
-                    // activation rows only once the entry's rows are gathered
+                    // a missed expert's weights are read only once its copy has landed
                     if (tl.u >= n_hits && !wait_fill_until(mg.fill_flag + (tl.u - n_hits), mg.epoch, err,
                                                                  fill_deadline(deadline, mg.wait_ns))) {
                         ok = false;
                         break;
                     }
-                    if (w13) {
-                        const int rows = s_off[tl.ent_rel + 1] - s_off[tl.ent_rel];
-                        if (!wait_ge_until(mg.dep_x + tl.u, rows, err, 23, deadline, 256)) { ok = false; break; }
-                    }
                     fence_proxy_async_global();
                 }
-                int kb0 = 0;
-                const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
-                if (!w13 && fused && (s_rdy[tl.ent_rel] || ld_acquire(p.dep + tl.u) >= target)) {
-                    // the entry's activation rows are already published (seen once, remembered):
-                    // stream A and B together
-                    s_rdy[tl.ent_rel] = 1;
-                    fence_proxy_async_global();
-                } else if (!w13 && fused) {
-                    // stream this tile's first weight stages while the entry's W13 tiles finish
-                    const int npre = min(S, k_steps);
-                    const uint32_t it0 = it;
-                    for (int kb = 0; kb < npre; ++kb, ++it) {
-                        const int s = it % S;
-                        if (!bar_wait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
-                        mbar_expect_tx(&full[s], STAGE);
-                        tma_load_3d(smem + s * STAGE, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
-                    }
-                    if (!ok) break;
-                    bool dep_ok;
-                    if constexpr (MK) dep_ok = wait_ge_until(p.dep + tl.u, target, err, 6, deadline, 1024);
-                    else dep_ok = wait_dep(p.dep + tl.u, target, err);
-                    if (!dep_ok) {
-                        // the stages armed above still expect their activation bytes: load
-                        // them (rows already written or not) so the ring can drain
-                        fence_proxy_async_global();
-                        for (int kb = 0; kb < npre; ++kb) {
-                            const int s = (it0 + kb) % S;
-                            tma_load_2d(smem + s * STAGE + A_BYTES, mB, &full[s], kb * kBK, row_b);
-                        }
-                        ok = false;
-                        break;
-                    }
-                    s_rdy[tl.ent_rel] = 1;
-                    fence_proxy_async_global();
-                    for (int kb = 0; kb < npre; ++kb) {
-                        const int s = (it0 + kb) % S;
-                        tma_load_2d(smem + s * STAGE + A_BYTES, mB, &full[s], kb * kBK, row_b);
-                    }
-                    kb0 = npre;
-                }
-                for (int kb = kb0; kb < k_steps; ++kb, ++it) {
+                for (int kb = 0; kb < k_steps; ++kb, ++it) {
                     const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
-                    if (!bar_wait(&empty[s], ph ^ 1u, 1)) { ok = false; break; }
-                    uint8_t* sa = smem + s * STAGE;
-                    mbar_expect_tx(&full[s], STAGE);
-                    tma_load_3d(sa, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
-                    tma_load_2d(sa + A_BYTES, mB, &full[s], kb * kBK, row_b);
+                    if (!bar_wait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
+                    mbar_expect_tx(&full[s], A_BYTES);
+                    tma_load_3d(smem + s * STAGE, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
                 }
             }
             // drain: every issued stage must land before the CTA may exit
+            if (!ok) {
+                for (uint32_t j = (it > (uint32_t)S ? it - S : 0); j < it; ++j)
+                    mbar_wait(&full[j % S], (j / S) & 1u, err, 5);
+            }
+        }
+    } else if (warp == kPBWarp) {
+        if (lane == 0) {
+            // Producer B: the activation rows of every stage, tile by tile in claim order, once
+            // they are ready (fused call: the entry's rows gathered for W13; the entry's W13
+            // tiles done for W2, seen once and remembered). Two threads issuing the stage
+            // copies move about twice the bytes per SM that one does, and the weight stream
+            // never waits on the activations.
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const int ts = (int)(tcount % kTQ);
+                if (!bar_wait(&tq_full[ts], (tcount / kTQ) & 1u, 10)) { ok = false; break; }
+                const int t = s_tile[ts];
+                mbar_arrive(&tq_empty[ts]);
+                if (t < 0) break;
+                const Tile tl = tile(t);
+                const bool w13 = tl.phase == 13;
+                const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
+                const int k_steps = (w13 ? H : I) / kBK;
+                const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
+                bool ready = true;
+                if constexpr (MK) {
+                    if (w13) {
+                        const int rows = s_off[tl.ent_rel + 1] - s_off[tl.ent_rel];
+                        ready = wait_ge_until(mg.dep_x + tl.u, rows, err, 23, deadline, 256);
+                    }
+                }
+                if (!w13 && fused && !s_rdy[tl.ent_rel]) {
+                    const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
+                    if (ld_acquire(p.dep + tl.u) < target) {
+                        if constexpr (MK) ready = wait_ge_until(p.dep + tl.u, target, err, 6, deadline, 1024);
+                        else ready = wait_dep(p.dep + tl.u, target, err);
+                    }
+                    if (ready) s_rdy[tl.ent_rel] = 1;
+                }
+                fence_proxy_async_global();
+                // the stages producer A arms expect these bytes: they are loaded even after a
+                // wait ran out (rows written or not), so the ring drains
+                for (int kb = 0; kb < k_steps; ++kb, ++it) {
+                    const int s = it % S;
+                    if (!bar_wait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
+                    mbar_expect_tx(&full[s], B_BYTES);
+                    tma_load_2d(smem + s * STAGE + A_BYTES, mB, &full[s], kb * kBK, row_b);
+                }
+                if (!ready) ok = false;
+            }
             if (!ok) {
                 for (uint32_t j = (it > (uint32_t)S ? it - S : 0); j < it; ++j)
                     mbar_wait(&full[j % S], (j / S) & 1u, err, 5);

@@ -10,7 +10,8 @@ struct TcParams {
     const int32_t* entry_off;    // grouped-row offsets per entry
     const int32_t* entry_dst;    // weight slot (index into the 3-D weight map) per entry
     const int32_t* pairs;        // grouped row -> (token, rank) pair
-    int32_t pass;
+    int32_t pass;                // see pass_range (common.cuh)
+    int32_t miss_lo, miss_hi;
     int32_t hidden;              // H: W13 is [2I][H], W2 is [H][I]; multiples of 64
     int32_t inter;               // I
     int32_t phases;              // 1: W13 tiles, 2: W2 tiles, 3: both in one launch

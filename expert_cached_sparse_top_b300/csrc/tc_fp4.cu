@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
         if (!mk_wait_route(mg, err, deadline, s_tmem + 3)) { mk_report(err, p.err); return; }
     }
     const RouteCounts rc = MK ? mk_counts(p.counts) : *p.counts;
-    const int u_begin = MK ? 0 : (p.pass == 1 ? rc.n_hits : 0);
-    const int u_end = MK ? rc.n_unique : (p.pass == 0 ? rc.n_hits : rc.n_unique);
+    int u_begin = 0, u_end = rc.n_unique;
+    if (!MK) pass_range(p.pass, rc, p.miss_lo, p.miss_hi, &u_begin, &u_end);
     const int n_hits = rc.n_hits;
     if (u_end <= u_begin) { if constexpr (MK) mk_report(err, p.err); return; }
     auto bwait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {

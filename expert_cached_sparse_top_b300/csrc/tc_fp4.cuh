@@ -26,7 +26,8 @@ struct Fp4Params {
     const int32_t* entry_off;
     const int32_t* entry_dst;    // weight slot per entry (index into the 3-D weight maps)
     const int32_t* pairs;
-    int32_t pass;                // 0: entries [0, n_hits), 1: [n_hits, n_unique), 2: all
+    int32_t pass;                // see pass_range (common.cuh)
+    int32_t miss_lo, miss_hi;
     int32_t hidden, inter;       // multiples of 256
     int32_t top_k;
     int32_t pieces;              // P (always four)

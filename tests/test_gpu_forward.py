@@ -340,3 +340,27 @@ def test_host_wait_timeout(ft, monkeypatch):
     torch.cuda.synchronize()
     assert cache.forward_status(0, x, 16, out, logits=lg) == ft.FT_ERR_STATE
     cache.close()
+
+
+def test_miss_groups_match_single_miss_pass(ft, monkeypatch):
+    """Misses run in two groups (all but the last copied, then the last) by default; the
+    outputs are bit-identical to one FFN pass over all misses (FTMOE_MISS_GROUPS=0), and
+    cache counts equal the oracle's."""
+    import torch
+    cfg = W.config("decode_bf16", hidden=512, inter=256, t_min=16, t_max=16)
+    pool = HostPool(cfg)
+    C = W.cache_capacity(cfg)
+    outs = {}
+    for groups in ("1", "0"):
+        monkeypatch.setenv("FTMOE_MISS_GROUPS", groups)
+        cache = _make(ft, cfg, pool, C)
+        run = Runner(cache, cfg, C)
+        outs[groups] = []
+        for step in W.decode_trace(cfg, steps=12):
+            d = step[0]
+            out, _, _ = run.call(0, d["x"], d["logits"])
+            outs[groups].append(out.clone())
+        run.check_state()
+        assert cache.stats()["misses"] > 2 * 12        # several misses per call: two groups
+        cache.close()
+    assert all(torch.equal(a, b) for a, b in zip(outs["1"], outs["0"]))
