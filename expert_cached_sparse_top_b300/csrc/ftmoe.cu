@@ -112,7 +112,7 @@ struct ft_moe {
     cudaEvent_t ev_copy2 = nullptr;
     cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_done = nullptr;
     cudaEvent_t ev_fill_a = nullptr;      // all misses of a call but the last copied
-    bool miss_groups = true;              // FTMOE_MISS_GROUPS=0: one FFN pass over all misses
+    bool miss_groups = false;             // FTMOE_MISS_GROUPS=1: misses in two FFN groups
 
     ft_cache_stats_t stats{};
     bool broken = false;
@@ -1510,9 +1510,10 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
             h->broken = true;
             return fail(h, FT_ERR_CUDA, "injected fill failure (FTMOE_FAULT=fill_fail)");
         }
-        // Two groups when there are at least two misses: all but the last one run once their
-        // copies have landed, while the last copy is still on the link; the last one runs
-        // after it. Only one expert's FFN then follows the final copy instead of every miss's.
+        // With FTMOE_MISS_GROUPS=1, two groups when there are at least two misses: all but the
+        // last one run once their copies have landed, while the last copy is still on the link;
+        // the last one runs after it. Only one expert's FFN then follows the final copy instead
+        // of every miss's, at the price of a second, small FFN launch.
         const int n = rc.n_miss;
         const bool grouped = h->miss_groups && n >= 2;
         if (h->timing) FT_CUDA(h, cudaEventRecord(se.fill_begin, h->copy_stream));

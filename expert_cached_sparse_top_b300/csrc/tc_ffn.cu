@@ -428,18 +428,25 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * NI * BN;
             const int m = tl.mt * kBM + row_in_tile;
+            // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
+            uint32_t la[16], lb[16];
+            tmem_ld16(tbase, la);
+            if (DUAL) tmem_ld16(tbase + BN, lb);
 #pragma unroll 1
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t r[16];
-                tmem_ld16(tbase + c0, r);
                 if (DUAL) {
-                    uint32_t r2[16];
-                    tmem_ld16(tbase + BN + c0, r2);
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs(la, lb);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(la[j]) + __uint_as_float(lb[j]));
                 } else {
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs(la);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = la[j];
+                }
+                if (c0 + 16 < n_valid) {
+                    tmem_ld16(tbase + c0 + 16, la);
+                    if (DUAL) tmem_ld16(tbase + BN + c0 + 16, lb);
                 }
                 if (w13) {
                     // lanes 2i / 2i+1 hold the gate / up rows of output feature i

@@ -144,14 +144,25 @@ __device__ void split_row(const __nv_bfloat16* row, int K, int P, int fmt, uint8
                           int64_t piece_stride, uint8_t* sf_tile, int n0, float* rs_out, int tid, int nt,
                           int bar, float* s_red) {
     constexpr int G = BS / 8;
+    // The row is read once: each thread keeps its (up to kMaxC) 8-element chunks in registers
+    // across the maximum and the split (a second read would add an L2 round trip per row).
+    // Rows with more chunks per thread than that read the rest again.
+    constexpr int kMaxC = 4;
+    uint4 keep[kMaxC];
     float amax = 0.f;
-    for (int c = tid; c < K / 8; c += nt) {
-        const uint4 u4 = __ldcg(reinterpret_cast<const uint4*>(row) + c);
-        const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
+    {
+        int n = 0;
+        for (int c = tid; c < K / 8; c += nt, ++n) {
+            const uint4 u4 = __ldcg(reinterpret_cast<const uint4*>(row) + c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] & 0xffff0000u)));
+            for (int m = 0; m < kMaxC; ++m)
+                if (n == m) keep[m] = u4;
+            const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] << 16)));
+                amax = fmaxf(amax, fabsf(__uint_as_float(w4[q] & 0xffff0000u)));
+            }
         }
     }
 #pragma unroll
@@ -166,8 +177,18 @@ __device__ void split_row(const __nv_bfloat16* row, int K, int P, int fmt, uint8
     const float pre = pow2(t);
     if (tid == 0) *rs_out = pow2(-t);
     // K / 8 is a multiple of 32, so every warp runs the same number of iterations
-    for (int c = tid; c < K / 8; c += nt) {
-        const uint4 u4 = __ldcg(reinterpret_cast<const uint4*>(row) + c);
+    int n = 0;
+    for (int c = tid; c < K / 8; c += nt, ++n) {
+        uint4 u4;
+        if (n < kMaxC) {
+            // (a runtime index into `keep` would put it in local memory: select it instead)
+            u4 = keep[0];
+#pragma unroll
+            for (int m = 1; m < kMaxC; ++m)
+                if (n == m) u4 = keep[m];
+        } else {
+            u4 = __ldcg(reinterpret_cast<const uint4*>(row) + c);
+        }
         const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
         float v[8];
 #pragma unroll
@@ -634,18 +655,25 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 // so a 16-column load holds 16 / P whole tokens
                 constexpr int tpc = 16 / P;
                 const int ncols = (P * n_valid + 15) & ~15;
+                // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
+                uint32_t la[16], lb[16];
+                tmem_ld16(tbase, la);
+                if (NI == 2) tmem_ld16(tbase + NC, lb);
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 16) {
                     uint32_t r[16];
-                    tmem_ld16(tbase + c0, r);
                     if (NI == 2) {
-                        uint32_t r2[16];
-                        tmem_ld16(tbase + NC + c0, r2);
-                        tmem_wait_ld();
+                        tmem_wait_ld_regs(la, lb);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(la[j]) + __uint_as_float(lb[j]));
                     } else {
-                        tmem_wait_ld();
+                        tmem_wait_ld_regs(la);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) r[j] = la[j];
+                    }
+                    if (c0 + 16 < ncols) {
+                        tmem_ld16(tbase + c0 + 16, la);
+                        if (NI == 2) tmem_ld16(tbase + NC + c0 + 16, lb);
                     }
                     const int i0 = c0 / P;                     // first token of the chunk
                     float tok[tpc];

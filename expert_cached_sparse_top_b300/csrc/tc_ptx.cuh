@@ -119,6 +119,28 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Wait for this thread's outstanding tcgen05.ld, with the destination registers of the loads
+// it waits for as operands: no use of those registers can be scheduled before the wait (a
+// plain wait orders memory, not register reads).
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :: "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[16], uint32_t (&r2)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                   "+r"(r2[0]), "+r"(r2[1]), "+r"(r2[2]), "+r"(r2[3]), "+r"(r2[4]), "+r"(r2[5]), "+r"(r2[6]),
+                   "+r"(r2[7]), "+r"(r2[8]), "+r"(r2[9]), "+r"(r2[10]), "+r"(r2[11]), "+r"(r2[12]),
+                   "+r"(r2[13]), "+r"(r2[14]), "+r"(r2[15])
+                 :: "memory");
+}
+
 
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
