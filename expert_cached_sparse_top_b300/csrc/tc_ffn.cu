@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             const bool ahead = total >= 8 * (int)gridDim.x;
             int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
             uint32_t it = 0;
+            Ring rg;
             bool ok = true;
             for (uint32_t q = 0; ok; ++q) {
                 const int ts = (int)(q % kTQ);
@@ -299,11 +300,10 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                     }
                     fence_proxy_async_global();
                 }
-                for (int kb = 0; kb < k_steps; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!bar_wait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
-                    mbar_expect_tx(&full[s], A_BYTES);
-                    tma_load_3d(smem + s * STAGE, mA, &full[s], kb * kBK, tl.mt * kBM, slot);
+                for (int kb = 0; kb < k_steps; ++kb, ++it, rg.next(S)) {
+                    if (!bar_wait(&empty[rg.s], rg.ph ^ 1u, 1)) { ok = false; break; }
+                    mbar_expect_tx(&full[rg.s], A_BYTES);
+                    tma_load_3d(smem + rg.s * STAGE, mA, &full[rg.s], kb * kBK, tl.mt * kBM, slot);
                 }
             }
             // drain: every issued stage must land before the CTA may exit
@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             // copies move about twice the bytes per SM that one does, and the weight stream
             // never waits on the activations.
             uint32_t it = 0;
+            Ring rg;
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
                 const int ts = (int)(tcount % kTQ);
@@ -350,11 +351,10 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 fence_proxy_async_global();
                 // the stages producer A arms expect these bytes: they are loaded even after a
                 // wait ran out (rows written or not), so the ring drains
-                for (int kb = 0; kb < k_steps; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!bar_wait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
-                    mbar_expect_tx(&full[s], B_BYTES);
-                    tma_load_2d(smem + s * STAGE + A_BYTES, mB, &full[s], kb * kBK, row_b);
+                for (int kb = 0; kb < k_steps; ++kb, ++it, rg.next(S)) {
+                    if (!bar_wait(&empty[rg.s], rg.ph ^ 1u, 1)) { ok = false; break; }
+                    mbar_expect_tx(&full[rg.s], B_BYTES);
+                    tma_load_2d(smem + rg.s * STAGE + A_BYTES, mB, &full[rg.s], kb * kBK, row_b);
                 }
                 if (!ready) ok = false;
             }
@@ -367,7 +367,12 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         const int par = warp == 6 ? 1 : 0;
         constexpr int KK = 4 / NI;                    // K steps per stage for this issuer
         if (lane == 0) {
-            uint32_t it = 0;
+            // descriptors of stage 0: a stage or a K step only adds a constant to the
+            // start-address field, so the per-stage path does no descriptor arithmetic
+            const uint64_t dA0 = smem_desc_sw128(smem_u32(smem));
+            const uint64_t dB0 = dA0 + (uint64_t)(A_BYTES >> 4);
+            Ring rg;
+            uint64_t so = 0;                          // the ring slot's offset in 16-byte units
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
                 const int ts = (int)(tcount % kTQ);
@@ -387,20 +392,17 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 if (!bar_wait(&tempty[acc], aph ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * BN;
-                for (int kb = 0; kb < k_steps; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
-                    if (!bar_wait(&full[s], ph, 3)) { ok = false; break; }
+                for (int kb = 0; kb < k_steps; ++kb) {
+                    if (!bar_wait(&full[rg.s], rg.ph, 3)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * STAGE);
-                    const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int k2 = 0; k2 < KK; ++k2) {
-                        const int kk = par * KK + k2;
-                        mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
-                                 idesc, (kb | k2) ? 1u : 0u);
+                        const uint64_t kd = so + (uint64_t)((par * KK + k2) * 2);   // 32 bytes per K step
+                        mma_bf16(d_tmem, dA0 + kd, dB0 + kd, idesc, (kb | k2) ? 1u : 0u);
                     }
-                    mma_commit(&empty[s]);
+                    mma_commit(&empty[rg.s]);
+                    rg.next(S);
+                    so = rg.s == 0 ? 0 : so + (uint64_t)(STAGE >> 4);
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);

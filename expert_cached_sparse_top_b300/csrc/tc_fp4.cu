@@ -431,6 +431,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             const bool ahead = total >= 8 * (int)gridDim.x;
             int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
             uint32_t it = 0;
+            Ring rg;
             bool ok = true;
             for (uint32_t q = 0; ok; ++q) {
                 const int ts = (int)(q % kTQ);
@@ -463,13 +464,12 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const uint8_t* sfa = p.arena + (int64_t)slot * p.blob_bytes + (tl.w13 ? p.off_s13 : p.off_s2) +
                                      (int64_t)tl.mt * ak * 512;
                 constexpr uint32_t a_tx = (uint32_t)(kABytes + SF_BYTES);
-                for (int kb = 0; kb < k_stages; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
-                    uint8_t* st = smem + (size_t)s * STAGE;
-                    mbar_expect_tx(&full[s], a_tx);
-                    tma_load_3d(st, mA, &full[s], kb * 128, tl.mt * 128, slot);
-                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[s]);
+                for (int kb = 0; kb < k_stages; ++kb, ++it, rg.next(S)) {
+                    if (!bwait(&empty[rg.s], rg.ph ^ 1u, 1)) { ok = false; break; }
+                    uint8_t* st = smem + (size_t)rg.s * STAGE;
+                    mbar_expect_tx(&full[rg.s], a_tx);
+                    tma_load_3d(st, mA, &full[rg.s], kb * 128, tl.mt * 128, slot);
+                    bulk_load(st + kABytes + B_BYTES, sfa + (int64_t)kb * SF_BYTES, SF_BYTES, &full[rg.s]);
                 }
             }
             if (!ok) {
@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             // remembered (s_ready bit 0: x rows, bit 1: W13 tiles) and its later tiles skip the
             // round trip.
             uint32_t it = 0;
+            Ring rg;
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
                 const int ts = (int)(tcount % kTQ);
@@ -517,17 +518,16 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 fence_proxy_async_global();
                 // the stages producer A arms expect these bytes: they are loaded even after a
                 // wait ran out, so the ring drains
-                for (int kb = 0; kb < k_stages; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!bwait(&empty[s], ((it / S) & 1u) ^ 1u, 1)) { ok = false; break; }
-                    uint8_t* st = smem + (size_t)s * STAGE;
-                    mbar_expect_tx(&full[s], b_tx);
+                for (int kb = 0; kb < k_stages; ++kb, ++it, rg.next(S)) {
+                    if (!bwait(&empty[rg.s], rg.ph ^ 1u, 1)) { ok = false; break; }
+                    uint8_t* st = smem + (size_t)rg.s * STAGE;
+                    mbar_expect_tx(&full[rg.s], b_tx);
                     for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(st + kABytes + bx * 2048, mB, &full[s], kb * 128, tl.g * NC + bx * 16);
+                        tma_load_2d(st + kABytes + bx * 2048, mB, &full[rg.s], kb * 128, tl.g * NC + bx * 16);
 #pragma unroll
                     for (int b = 0; b < NB; ++b)
                         bulk_load(st + kABytes + B_BYTES + (1 + b) * SF_BYTES,
-                                  bsf + ((int64_t)b * ak * 512 + (int64_t)kb * SF_BYTES), SF_BYTES, &full[s]);
+                                  bsf + ((int64_t)b * ak * 512 + (int64_t)kb * SF_BYTES), SF_BYTES, &full[rg.s]);
                 }
                 if (!ready) ok = false;
             }
@@ -549,6 +549,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             const uint64_t dsw0 = smem_desc_sw128(smem_u32(smem));
             const uint64_t dsf0 = smem_desc_sf(smem_u32(smem) + kABytes + B_BYTES);
             uint32_t it = 0;
+            Ring rg;
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
                 const int ts = (int)(tcount % kTQ);
@@ -566,9 +567,9 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 if (!bwait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * (uint32_t)NC;
-                for (int kb = 0; kb < k_stages; ++kb, ++it) {
-                    const int s = it % S;
-                    if (!bwait(&full[s], (it / S) & 1u, 3)) { ok = false; break; }
+                for (int kb = 0; kb < k_stages; ++kb, ++it, rg.next(S)) {
+                    const int s = rg.s;
+                    if (!bwait(&full[s], rg.ph, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t so = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
                     const uint64_t dA = dsw0 + so, dB = dA + (kABytes >> 4), dS = dsf0 + so;

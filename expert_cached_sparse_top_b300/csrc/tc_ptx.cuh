@@ -13,6 +13,16 @@ constexpr int kBK = 64;                // K per stage: 64 bf16 = one 128-byte sw
 constexpr int kBM = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
+// Position in an S-stage shared-memory ring (slot and phase parity), advanced one stage at a
+// time: no division by the runtime stage count on the per-stage path.
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int S) {
+        if (++s == S) { s = 0; ph ^= 1u; }
+    }
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
