@@ -8,8 +8,8 @@ pool (47 slots); the pool sits in pinned host memory and misses are filled over 
 One step = one forward call of the layer on one decode step of the trace: top-k, cache
 lookup + LRU update, expert FFN on resident experts, miss fills (copy stream), expert FFN
 on filled / staged experts, combine. Inputs (x, logits of every timed step) are resident in
-HBM before timing starts; L2 is flushed (256 MB write) before every step, outside the
-per-step CUDA-event bracket.
+HBM before timing starts; L2 is flushed before every step, outside the per-step CUDA-event
+bracket: a 256 MB buffer is written and then read back (see `l2_flush`).
 
 Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -112,6 +112,26 @@ class _CtypesNvml:
         v = self.c.c_ulonglong()
         self._ok(self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.c.byref(v)), "clock reasons")
         return v.value
+
+
+FLUSH_MODES = ("write-read", "write")
+
+
+def l2_flush(buf, mode="write-read"):
+    """Evict every line of the previous step from L2 (126 MB) before a timed step: write
+    `buf`, twice the size of L2, and in the default mode read it back. The read evicts the
+    flush's own dirty lines while the clock is stopped, so L2 is left holding clean lines of
+    the flush buffer; a write-only flush leaves ~126 MB of dirty lines that the next step's
+    reads must first write back to HBM, traffic the workload itself does not have. Mode
+    "write" keeps the write-only flush, for comparison."""
+    import torch
+    buf.zero_()
+    if mode == "write-read":
+        buf.view(torch.int64).sum()
+
+
+FLUSH_TEXT = {"write-read": "flushed (256 MB written, then read back) before every step, outside the step's events",
+              "write": "flushed (256 MB write) before every step, outside the step's events"}
 
 
 class Clocks:
@@ -515,7 +535,7 @@ def decode_line(args):
             i = Wm + j
             if elastic and i in resizes:
                 cache.resize(resizes[i])
-            flush.zero_()
+            l2_flush(flush, args.flush)
             evs[j][0].record(stream)
             run_step(cache, i)
             evs[j][1].record(stream)
@@ -582,7 +602,7 @@ def decode_line(args):
         if i in resizes:
             cache_e.resize(resizes[i])
         T = Ts[i]
-        flush.zero_()
+        l2_flush(flush, args.flush)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for li, (xh, lh) in enumerate(hx[i]):
@@ -648,8 +668,7 @@ def decode_line(args):
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": Wm, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.wfmt, "data": "synthetic",
-        "config": dict(workload_config(cfg, C, "flushed (256 MB write) before every step, "
-                                                "outside the step's events"),
+        "config": dict(workload_config(cfg, C, FLUSH_TEXT[args.flush]),
                        pool="pinned host, %d keys on %d blobs x %d B" % (cfg.keys, pool.images,
                                                                         pool.blob_bytes),
                        resizes={str(k2): v for k2, v in resizes.items()} or None,
@@ -843,7 +862,7 @@ def chained_line(args):
         cache.timing(reset=True)
         evs = []
         for j in range(K):
-            flush.zero_()
+            l2_flush(flush, args.flush)
             a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(s)
             step(Wm + j)
@@ -947,7 +966,7 @@ def prefill_line(args):
     cache.timing(reset=True)
     evs = []
     for _ in range(args.steps):
-        flush.zero_()
+        l2_flush(flush, args.flush)
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(); cache.prefill(last, xs[last], T, out, logits=ls[last]); e.record()
         evs.append((a, e))
@@ -1132,6 +1151,9 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="prefill: fewer experts per layer (a small case of the same kernel for "
                          "profiler captures; with --tokens keeping the tokens per expert)")
+    ap.add_argument("--flush", choices=FLUSH_MODES, default="write-read",
+                    help="L2 flush between timed steps: write a 256 MB buffer and read it back "
+                         "(default), or only write it")
     ap.add_argument("--no-extras", action="store_true",
                     help="default run: skip the sub-records of the other workloads")
     ap.add_argument("--workload", default=WORKLOAD,

@@ -15,7 +15,7 @@
 //               shared-memory ring (mbarrier complete_tx).
 //   warp 1      allocates TMEM (2 accumulators of N columns per issuer) and issues
 //               tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) from one lane; for N <= 64 warp 6
-//               issues half of every stage's K steps into its own accumulator; tcgen05.commit
+//               issues every other stage into its own accumulator; tcgen05.commit
 //               frees ring stages and publishes finished accumulators.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator rows; W13 pairs gate/up rows
 //               (adjacent TMEM lanes) into silu(g)*u and writes the bf16 activation; W2
@@ -85,9 +85,10 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
     return r;
 }
 
-// Decode-sized tiles (N <= 64) are issued by two MMA warps, each taking two of a stage's four
-// K steps into its own accumulator (the epilogue adds them): a single thread issuing every
-// small-N tcgen05.mma cannot keep up with the weight stream.
+// Decode-sized tiles (N <= 64) are issued by two MMA warps, each taking every other stage of
+// the tile into its own accumulator (the epilogue adds them): a single thread issuing every
+// small-N tcgen05.mma, with a barrier wait and a commit per stage, cannot keep up with the
+// weight stream.
 template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
 constexpr int kTQ = 4;             // claimed-tile ring depth
 // warps: producer A (weights), MMA issuer(s), four epilogue warps, producer B (activations)
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     }
     if (warp == 0 && lane == 0) {
         // a stage is full once both producers' bytes landed
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], NI); }
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
         for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 5); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -365,7 +366,6 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         }
     } else if (warp == 1 || (DUAL && warp == 6)) {
         const int par = warp == 6 ? 1 : 0;
-        constexpr int KK = 4 / NI;                    // K steps per stage for this issuer
         if (lane == 0) {
             // descriptors of stage 0: a stage or a K step only adds a constant to the
             // start-address field, so the per-stage path does no descriptor arithmetic
@@ -392,15 +392,22 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 if (!bar_wait(&tempty[acc], aph ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * BN;
+                // with two issuers, each takes every other stage of the tile (all four K steps)
+                // into its own accumulator: a stage costs an issuer one barrier wait and one
+                // commit, and the two issue stages concurrently
+                bool first = true;
                 for (int kb = 0; kb < k_steps; ++kb) {
-                    if (!bar_wait(&full[rg.s], rg.ph, 3)) { ok = false; break; }
-                    tc_fence_after();
+                    if (!DUAL || (kb & 1) == par) {
+                        if (!bar_wait(&full[rg.s], rg.ph, 3)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int k2 = 0; k2 < KK; ++k2) {
-                        const uint64_t kd = so + (uint64_t)((par * KK + k2) * 2);   // 32 bytes per K step
-                        mma_bf16(d_tmem, dA0 + kd, dB0 + kd, idesc, (kb | k2) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t kd = so + (uint64_t)(kk * 2);   // 32 bytes per K step
+                            mma_bf16(d_tmem, dA0 + kd, dB0 + kd, idesc, (first && kk == 0) ? 0u : 1u);
+                        }
+                        first = false;
+                        mma_commit(&empty[rg.s]);
                     }
-                    mma_commit(&empty[rg.s]);
                     rg.next(S);
                     so = rg.s == 0 ? 0 : so + (uint64_t)(STAGE >> 4);
                 }
@@ -430,14 +437,16 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * NI * BN;
             const int m = tl.mt * kBM + row_in_tile;
+            // the second issuer's accumulator holds the odd stages: none when K is one stage
+            const bool two = DUAL && (w13 ? H : I) > kBK;
             // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
             uint32_t la[16], lb[16];
             tmem_ld16(tbase, la);
-            if (DUAL) tmem_ld16(tbase + BN, lb);
+            if (two) tmem_ld16(tbase + BN, lb);
 #pragma unroll 1
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t r[16];
-                if (DUAL) {
+                if (two) {
                     tmem_wait_ld_regs(la, lb);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(la[j]) + __uint_as_float(lb[j]));
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 }
                 if (c0 + 16 < n_valid) {
                     tmem_ld16(tbase + c0 + 16, la);
-                    if (DUAL) tmem_ld16(tbase + BN + c0 + 16, lb);
+                    if (two) tmem_ld16(tbase + BN + c0 + 16, lb);
                 }
                 if (w13) {
                     // lanes 2i / 2i+1 hold the gate / up rows of output feature i
