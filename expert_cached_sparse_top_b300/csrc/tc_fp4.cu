@@ -293,11 +293,10 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     constexpr int NC = P * BN;                        // rows of a tile's N operand: BN tokens x P pieces
     constexpr int NB = (NC + 127) / 128;              // its 128-row scale bands
     constexpr int B_BYTES = NC * 128;
-    constexpr int HA = APS / NI;                      // weight scale atoms per stage per issuer
-    // tensor memory: NI accumulators of NC columns, double-buffered, then per issuer and
-    // stage parity SFP columns of scale factors (weights' atoms, then the bands' atoms)
+    // tensor memory: NI accumulators of NC columns, double-buffered, then per issuer two
+    // buffers of SFP columns of scale factors (a stage's weight atoms, then its bands' atoms)
     constexpr uint32_t SF_COL0 = 2u * NI * NC;
-    constexpr uint32_t SFP = 4u * HA * (1 + NB);
+    constexpr uint32_t SFP = 4u * APS * (1 + NB);
     static_assert(SF_COL0 + 2u * NI * SFP <= 512u, "tensor memory");
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
     uint64_t* empty = full + S;
@@ -367,7 +366,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
     if (warp == 0 && lane == 0) {
         // a stage is full once both producers' bytes landed; free, and an accumulator full,
         // once every MMA issuer has committed
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], NI); }
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
         for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 5); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -537,18 +536,18 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             }
         }
     } else if (warp == 1 || (NI == 2 && warp == 6)) {
-        // Two issuers: in every stage warp 1 issues K steps 0-1 and warp 6 K steps 2-3 (with the
-        // scale atoms those steps read), each into its own accumulator; the epilogue adds the
-        // two. One thread issuing every tcgen05.mma / cp of a decode tile (N = 16) cannot keep
-        // up with the weight stream; two can.
+        // Two issuers (decode): warp 1 issues the even stages of a tile and warp 6 the odd
+        // ones, each with all four K steps and the stage's scale atoms, into its own
+        // accumulator; the epilogue adds the two. A stage costs an issuer one barrier wait and
+        // one commit, and the two issue stages concurrently: one thread issuing every
+        // tcgen05.mma / cp of a decode tile (N = 16) cannot keep up with the weight stream.
         const uint32_t par = warp == 6 ? 1u : 0u;
-        constexpr int KK = 4 / NI;                    // K steps per stage per issuer
         if (lane == 0) {
             // descriptors of stage 0; a stage, a K step or an atom only adds a constant to the
             // start-address field, so the loop below does no descriptor arithmetic
             const uint64_t dsw0 = smem_desc_sw128(smem_u32(smem));
             const uint64_t dsf0 = smem_desc_sf(smem_u32(smem) + kABytes + B_BYTES);
-            uint32_t it = 0;
+            uint32_t mine = 0;                        // stages this issuer has issued
             Ring rg;
             bool ok = true;
             for (uint32_t tcount = 0; ok; ++tcount) {
@@ -567,35 +566,38 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 if (!bwait(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * (uint32_t)NC;
-                for (int kb = 0; kb < k_stages; ++kb, ++it, rg.next(S)) {
+                bool first = true;
+                for (int kb = 0; kb < k_stages; ++kb, rg.next(S)) {
+                    if (NI == 2 && (uint32_t)(kb & 1) != par) continue;
                     const int s = rg.s;
                     if (!bwait(&full[s], rg.ph, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t so = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
                     const uint64_t dA = dsw0 + so, dB = dA + (kABytes >> 4), dS = dsf0 + so;
-                    // this issuer's scale atoms -> TMEM (double-buffered by stage parity): the
-                    // weights' atom a at tsf + 4a, band b of the activations' atom a at
-                    // tsf + 4 HA + 4 (a NB + b)
-                    const uint32_t tsf = tmem_base + SF_COL0 + (par * 2u + (it & 1u)) * SFP;
+                    // the stage's scale atoms -> TMEM (two buffers per issuer, alternating by
+                    // the issuer's own stages): the weights' atom a at tsf + 4a, band b of the
+                    // activations' atom a at tsf + 4 APS + 4 (a NB + b)
+                    const uint32_t tsf = tmem_base + SF_COL0 + (par * 2u + (mine & 1u)) * SFP;
+                    ++mine;
 #pragma unroll
-                    for (int a = 0; a < HA; ++a) {
-                        const uint64_t ga = (uint64_t)((int)par * HA + a) * 32u;     // atom within the stage
+                    for (int a = 0; a < APS; ++a) {
+                        const uint64_t ga = (uint64_t)a * 32u;     // atom within the stage
                         tmem_cp_sf(tsf + (uint32_t)(4 * a), dS + ga);
 #pragma unroll
                         for (int b = 0; b < NB; ++b)
-                            tmem_cp_sf(tsf + (uint32_t)(4 * HA + 4 * (a * NB + b)),
+                            tmem_cp_sf(tsf + (uint32_t)(4 * APS + 4 * (a * NB + b)),
                                        dS + (uint64_t)((1 + b) * SF_BYTES / 16) + ga);
                     }
 #pragma unroll
-                    for (int k2 = 0; k2 < KK; ++k2) {
-                        const int kk = (int)par * KK + k2;
+                    for (int kk = 0; kk < 4; ++kk) {
                         // MXFP4: one atom (4 blocks of 32) per two K steps, byte pair 0 or 2;
                         // NVFP4: one atom (4 blocks of 16) per K step
-                        const int ai = (FMT == FT_W_MXFP4 ? (kk >> 1) : kk) - (int)par * HA;
+                        const int ai = FMT == FT_W_MXFP4 ? (kk >> 1) : kk;
                         const bool odd = FMT == FT_W_MXFP4 && (kk & 1);
                         mma_bs<FMT>(d_tmem, dA + (uint64_t)(kk * 2), dB + (uint64_t)(kk * 2), odd ? idesc2 : idesc0,
-                                    tsf + 4 * ai, tsf + 4 * HA + 4 * NB * ai, (kb == 0 && k2 == 0) ? 0u : 1u);
+                                    tsf + 4 * ai, tsf + 4 * APS + 4 * NB * ai, (first && kk == 0) ? 0u : 1u);
                     }
+                    first = false;
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
@@ -657,13 +659,15 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 constexpr int tpc = 16 / P;
                 const int ncols = (P * n_valid + 15) & ~15;
                 // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
+                // the second issuer's accumulator holds the odd stages: none when K is one stage
+                const bool two = NI == 2 && (tl.w13 ? H : I) > kStageK;
                 uint32_t la[16], lb[16];
                 tmem_ld16(tbase, la);
-                if (NI == 2) tmem_ld16(tbase + NC, lb);
+                if (two) tmem_ld16(tbase + NC, lb);
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 16) {
                     uint32_t r[16];
-                    if (NI == 2) {
+                    if (two) {
                         tmem_wait_ld_regs(la, lb);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(la[j]) + __uint_as_float(lb[j]));
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                     }
                     if (c0 + 16 < ncols) {
                         tmem_ld16(tbase + c0 + 16, la);
-                        if (NI == 2) tmem_ld16(tbase + NC + c0 + 16, lb);
+                        if (two) tmem_ld16(tbase + NC + c0 + 16, lb);
                     }
                     const int i0 = c0 / P;                     // first token of the chunk
                     float tok[tpc];
