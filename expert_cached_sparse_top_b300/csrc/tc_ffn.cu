@@ -85,10 +85,13 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
     return r;
 }
 
-// Decode-sized tiles (N <= 64) are issued by two MMA warps, each taking every other stage of
-// the tile into its own accumulator (the epilogue adds them): a single thread issuing every
-// small-N tcgen05.mma, with a barrier wait and a commit per stage, cannot keep up with the
-// weight stream.
+// Decode-sized tiles (N <= 64) are issued by two MMA warps, each into its own accumulator (the
+// epilogue adds them): a single thread issuing every small-N tcgen05.mma, with a barrier wait
+// and a commit per stage, cannot keep up with the weight stream. Issuer i takes the stages
+// that land in ring slots of parity i (the ring has an even number of slots), so each slot
+// is only ever consumed by one issuer, which waits on its phases in order: an issuer that
+// waited for a slot another issuer had not yet drained could ask for a phase two ahead of
+// the barrier's, and an mbarrier parity wait cannot tell that from the phase before.
 template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
 constexpr int kTQ = 4;             // claimed-tile ring depth
 // warps: producer A (weights), MMA issuer(s), four epilogue warps, producer B (activations)
@@ -392,12 +395,12 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 if (!bar_wait(&tempty[acc], aph ^ 1u, 2)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * BN;
-                // with two issuers, each takes every other stage of the tile (all four K steps)
-                // into its own accumulator: a stage costs an issuer one barrier wait and one
-                // commit, and the two issue stages concurrently
+                // with two issuers, each takes the stages of its ring-slot parity (all four K
+                // steps) into its own accumulator: a stage costs an issuer one barrier wait and
+                // one commit, and the two issue stages concurrently
                 bool first = true;
                 for (int kb = 0; kb < k_steps; ++kb) {
-                    if (!DUAL || (kb & 1) == par) {
+                    if (!DUAL || (rg.s & 1) == par) {
                         if (!bar_wait(&full[rg.s], rg.ph, 3)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
@@ -419,6 +422,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
+        uint32_t ring_it = 0;                         // the ring position of the tile's first stage
         for (uint32_t tcount = 0;; ++tcount) {
             const int ts = (int)(tcount % kTQ);
             if (!bar_wait(&tq_full[ts], (tcount / kTQ) & 1u, 9)) break;
@@ -437,11 +441,15 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * NI * BN;
             const int m = tl.mt * kBM + row_in_tile;
-            // the second issuer's accumulator holds the odd stages: none when K is one stage
-            const bool two = DUAL && (w13 ? H : I) > kBK;
+            // issuer i's accumulator holds the stages of ring-slot parity i: a tile of one stage
+            // fills only the accumulator of its slot's parity
+            const int k_steps = (w13 ? H : I) / kBK;
+            const bool two = DUAL && k_steps > 1;
+            const uint32_t a0 = (DUAL && !two && (ring_it & 1u)) ? (uint32_t)BN : 0u;
+            ring_it += (uint32_t)k_steps;
             // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
             uint32_t la[16], lb[16];
-            tmem_ld16(tbase, la);
+            tmem_ld16(tbase + a0, la);
             if (two) tmem_ld16(tbase + BN, lb);
 #pragma unroll 1
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                     for (int j = 0; j < 16; ++j) r[j] = la[j];
                 }
                 if (c0 + 16 < n_valid) {
-                    tmem_ld16(tbase + c0 + 16, la);
+                    tmem_ld16(tbase + a0 + c0 + 16, la);
                     if (two) tmem_ld16(tbase + BN + c0 + 16, lb);
                 }
                 if (w13) {
@@ -565,7 +573,9 @@ template <int BN>
 int stages_for() {
     const int stage = 128 * 64 * 2 + BN * 64 * 2;
     int s = (212 * 1024) / stage;
-    return s > 11 ? 11 : s;
+    s = s > 11 ? 11 : s;
+    // two issuers own the ring's even and odd slots: the ring has an even number of them
+    return tc::TcDual<BN>::value ? (s & ~1) : s;
 }
 
 template <int BN>

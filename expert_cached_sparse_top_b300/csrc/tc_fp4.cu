@@ -536,11 +536,15 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             }
         }
     } else if (warp == 1 || (NI == 2 && warp == 6)) {
-        // Two issuers (decode): warp 1 issues the even stages of a tile and warp 6 the odd
-        // ones, each with all four K steps and the stage's scale atoms, into its own
-        // accumulator; the epilogue adds the two. A stage costs an issuer one barrier wait and
-        // one commit, and the two issue stages concurrently: one thread issuing every
-        // tcgen05.mma / cp of a decode tile (N = 16) cannot keep up with the weight stream.
+        // Two issuers (decode): warp 1 issues the stages in even ring slots and warp 6 those in
+        // odd ones (the ring has an even number of slots), each with all four K steps and the
+        // stage's scale atoms, into its own accumulator; the epilogue adds the two. A stage
+        // costs an issuer one barrier wait and one commit, and the two issue stages
+        // concurrently: one thread issuing every tcgen05.mma / cp of a decode tile (N = 16)
+        // cannot keep up with the weight stream. Each slot is only ever consumed by one
+        // issuer, which waits on its phases in order: an issuer waiting on a slot that the
+        // other had not yet drained could ask for a phase two ahead of the barrier's, which a
+        // parity wait cannot tell from the phase before.
         const uint32_t par = warp == 6 ? 1u : 0u;
         if (lane == 0) {
             // descriptors of stage 0; a stage, a K step or an atom only adds a constant to the
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const uint32_t d_tmem = tmem_base + (acc * NI + par) * (uint32_t)NC;
                 bool first = true;
                 for (int kb = 0; kb < k_stages; ++kb, rg.next(S)) {
-                    if (NI == 2 && (uint32_t)(kb & 1) != par) continue;
+                    if (NI == 2 && (uint32_t)(rg.s & 1) != par) continue;
                     const int s = rg.s;
                     if (!bwait(&full[s], rg.ph, 3)) { ok = false; break; }
                     tc_fence_after();
@@ -608,6 +612,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
         const int q = warp & 3;
         const int etid = threadIdx.x - 64;                 // 0..127 over the epilogue warps
         const int row_in_tile = q * 32 + lane;
+        uint32_t ring_it = 0;                              // the ring position of the tile's first stage
         for (uint32_t tcount = 0;; ++tcount) {
             // the next claimed tile id; the four warps vote on the wait's outcome so that they
             // leave the loop together (they meet at named barriers below)
@@ -622,6 +627,9 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             if (lane == 0) mbar_arrive(&tq_empty[ts]);
             if (t < 0) break;
             const FTile tl = tile(t);
+            const int k_st = (tl.w13 ? H : I) / kStageK;
+            const uint32_t tile_it = ring_it;
+            ring_it += (uint32_t)k_st;
             const int nt = tl.g - s_tp[tl.u];
             const int row_b = s_eoff[tl.u] + nt * BN;
             const int n_valid = min(BN, s_eoff[tl.u + 1] - row_b);
@@ -659,10 +667,12 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 constexpr int tpc = 16 / P;
                 const int ncols = (P * n_valid + 15) & ~15;
                 // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
-                // the second issuer's accumulator holds the odd stages: none when K is one stage
-                const bool two = NI == 2 && (tl.w13 ? H : I) > kStageK;
+                // issuer i's accumulator holds the stages of ring-slot parity i: a tile of one
+                // stage fills only the accumulator of its slot's parity
+                const bool two = NI == 2 && k_st > 1;
+                const uint32_t a0 = (NI == 2 && !two && (tile_it & 1u)) ? (uint32_t)NC : 0u;
                 uint32_t la[16], lb[16];
-                tmem_ld16(tbase, la);
+                tmem_ld16(tbase + a0, la);
                 if (two) tmem_ld16(tbase + NC, lb);
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 16) {
@@ -677,7 +687,7 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                         for (int j = 0; j < 16; ++j) r[j] = la[j];
                     }
                     if (c0 + 16 < ncols) {
-                        tmem_ld16(tbase + c0 + 16, la);
+                        tmem_ld16(tbase + a0 + c0 + 16, la);
                         if (two) tmem_ld16(tbase + NC + c0 + 16, lb);
                     }
                     const int i0 = c0 / P;                     // first token of the chunk
@@ -874,6 +884,8 @@ cudaError_t fp4_smem(Fp4Params& p, size_t* smem) {
                          (fp4::kTQ + 8) * 4 + 64;
     p.stages = (int)((kSmemLimit - fixed) / (p.stage_bytes + 16));
     if (p.stages > 8) p.stages = 8;
+    // two issuers own the ring's even and odd slots: the ring has an even number of them
+    if (fp4::Fp4Cfg<P, BN>::NI == 2) p.stages &= ~1;
     if (p.stages < 2) return cudaErrorInvalidValue;
     *smem = fixed + (size_t)p.stages * (p.stage_bytes + 16);
     if (*smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
