@@ -95,7 +95,12 @@ __device__ __forceinline__ Tile tile_at(int t, const int* s_nt, int n_entries, i
 template <int BN> struct TcDual { static constexpr bool value = BN <= 64; };
 constexpr int kTQ = 4;             // claimed-tile ring depth
 // warps: producer A (weights), MMA issuer(s), four epilogue warps, producer B (activations)
-template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 64 : kThreads + 32; }
+// Prefill-sized tiles (N >= 128) take two groups of four epilogue warps (warps 2-5 and 7-10),
+// each group taking every other 16-column chunk: one warp per sub-partition left the
+// epilogue of a 128 x 256 tile as long as its MMAs, so the double-buffered accumulator could
+// not hide it.
+template <int BN, bool MK> constexpr int tc_epi_warps() { return (!TcDual<BN>::value && !MK) ? 8 : 4; }
+template <int BN> constexpr int tc_threads() { return TcDual<BN>::value ? kThreads + 64 : kThreads + 32 + 128; }
 
 template <int BN, bool MK> constexpr int tc_block() { return MK ? 256 : tc_threads<BN>(); }
 
@@ -138,6 +143,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     constexpr bool DUAL = TcDual<BN>::value;
     constexpr int NI = DUAL ? 2 : 1;                  // MMA issuers
     constexpr int kPBWarp = DUAL ? 7 : 6;             // producer B (activation rows)
+    constexpr int NE = tc_epi_warps<BN, MK>();        // epilogue warps
     static_assert(kPBWarp * 32 < tc_block<BN, MK>(), "producer B's warp");
     constexpr int A_BYTES = kBM * kBK * 2;            // 16 KB
     constexpr int B_BYTES = BN * kBK * 2;
@@ -233,8 +239,8 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     if (warp == 0 && lane == 0) {
         // a stage is full once both producers' bytes landed
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], 4); }
-        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 5); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], NI); mbar_init(&tempty[a], NE); }
+        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], NI + 1 + NE); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                     }
                 }
                 if (!w13 && fused && !s_rdy[tl.ent_rel]) {
-                    const int target = 4 * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
+                    const int target = NE * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
                     if (ld_acquire(p.dep + tl.u) < target) {
                         if constexpr (MK) ready = wait_ge_until(p.dep + tl.u, target, err, 6, deadline, 1024);
                         else ready = wait_dep(p.dep + tl.u, target, err);
@@ -418,9 +424,12 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 mma_commit(&tfull[acc]);
             }
         }
-    } else if (warp >= 2 && warp <= 5) {
-        // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
+    } else if ((warp >= 2 && warp <= 5) || (NE == 8 && warp >= 7 && warp <= 10)) {
+        // epilogue warps 2..5 (and 7..10) -> TMEM lane quarter (warp % 4); group g takes the
+        // 16-column chunks g, g + NE / 4, ...
         const int q = warp & 3;
+        const int g = warp >= 7 ? 1 : 0;
+        constexpr int CSTEP = 16 * (NE / 4);
         const int row_in_tile = q * 32 + lane;
         uint32_t ring_it = 0;                         // the ring position of the tile's first stage
         for (uint32_t tcount = 0;; ++tcount) {
@@ -447,12 +456,16 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             const bool two = DUAL && k_steps > 1;
             const uint32_t a0 = (DUAL && !two && (ring_it & 1u)) ? (uint32_t)BN : 0u;
             ring_it += (uint32_t)k_steps;
-            // the chunk loads are pipelined: chunk c + 16 is in flight while chunk c is processed
+            // the chunk loads are pipelined: the group's next chunk is in flight while one is
+            // processed
             uint32_t la[16], lb[16];
-            tmem_ld16(tbase + a0, la);
-            if (two) tmem_ld16(tbase + BN, lb);
+            const int cfirst = g * 16;
+            if (cfirst < n_valid) {
+                tmem_ld16(tbase + a0 + cfirst, la);
+                if (two) tmem_ld16(tbase + BN + cfirst, lb);
+            }
 #pragma unroll 1
-            for (int c0 = 0; c0 < n_valid; c0 += 16) {
+            for (int c0 = cfirst; c0 < n_valid; c0 += CSTEP) {
                 uint32_t r[16];
                 if (two) {
                     tmem_wait_ld_regs(la, lb);
@@ -463,9 +476,9 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
 #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = la[j];
                 }
-                if (c0 + 16 < n_valid) {
-                    tmem_ld16(tbase + a0 + c0 + 16, la);
-                    if (two) tmem_ld16(tbase + BN + c0 + 16, lb);
+                if (c0 + CSTEP < n_valid) {
+                    tmem_ld16(tbase + a0 + c0 + CSTEP, la);
+                    if (two) tmem_ld16(tbase + BN + c0 + CSTEP, lb);
                 }
                 if (w13) {
                     // lanes 2i / 2i+1 hold the gate / up rows of output feature i
