@@ -75,6 +75,7 @@ __device__ __forceinline__ bool wait_fill_until(const int* p, int epoch, int* er
 
 __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, int* err, int code,
                                                 uint64_t deadline) {
+    if (mbar_test_wait(bar, parity)) return true;
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 1023u) == 1023u) {
