@@ -191,6 +191,9 @@ struct ft_moe {
     CUtensorMap tmP_A13[2]{}, tmP_A2[2]{};
     CUtensorMap tmP_B13[5]{}, tmP_B2[5]{};     // per N tile width 16..256
     bool p_b_ok[5] = {false, false, false, false, false};
+    CUtensorMap tmP_B13h{}, tmP_B2h{};            // 128-row boxes: half of a 256-row N tile
+    bool p_bh_ok = false;
+    bool pair_prefill = true;                      // FTMOE_PAIR=0 turns the CTA-pair kernel off
     // prefill on the block-scaled tensor cores (FP4 weights, activations as E2M1 pieces)
     bool use_fp4_prefill = false;
     int64_t p_fp4_tiles = 0;
@@ -1005,6 +1008,8 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         const bool simt = ffn && strcmp(ffn, "simt") == 0;
         h->use_tc = cfg->wfmt == FT_W_BF16 && !simt;
         h->use_fp4 = cfg->wfmt != FT_W_BF16 && !simt && H % 256 == 0 && I % 256 == 0;
+        const char* pz = getenv("FTMOE_PAIR");
+        h->pair_prefill = !(pz && strcmp(pz, "0") == 0);
         const char* fz = getenv("FTMOE_TC_FUSED");
         h->tc_fused = !(fz && strcmp(fz, "0") == 0);
         h->tc_bn = tc_pick_bn(cfg->max_tokens);
@@ -1653,7 +1658,18 @@ ft_status ft_moe_prefill(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         tp.hidden = H; tp.inter = I;
         const TcMaps maps{&h->tmP_A13[b], &h->tmP_B13[bi], &h->tmP_A2[b], &h->tmP_B2[bi]};
         tp.tile_ctr = h->p_rb.tile_ctr;
-        if (h->tc_fused) {
+        // 256-token tiles on CTA pairs: two 128-row weight tiles of one N tile per cluster
+        const bool pair = h->pair_prefill && h->tc_fused && bn == 256 && H % 256 == 0 && (2 * I) % 256 == 0;
+        if (pair) {
+            if (!h->p_bh_ok) {
+                FT_CUDA(h, tc_encode_acts(&h->tmP_B13h, h->d_p_xp, H, (int)h->p_rows, 128));
+                FT_CUDA(h, tc_encode_acts(&h->tmP_B2h, h->d_p_act, I, (int)h->p_rows, 128));
+                h->p_bh_ok = true;
+            }
+            const TcMaps pm{&h->tmP_A13[b], &h->tmP_B13h, &h->tmP_A2[b], &h->tmP_B2h};
+            tp.phases = 3; tp.dep = h->p_rb.dep;
+            FT_CUDA(h, tc_launch_pair(tp, pm, h->num_sms, s));
+        } else if (h->tc_fused) {
             tp.phases = 3; tp.dep = h->p_rb.dep;
             FT_CUDA(h, tc_launch(bn, tp, maps, h->num_sms, s));
         } else {

@@ -136,6 +136,45 @@ __device__ __forceinline__ int entry_of_row(const int32_t* entry_off, int n_entr
     return lo;
 }
 
+// Epilogue of one 16-column chunk of an accumulator row (this lane's weight row m of the tile,
+// token columns c0 .. c0 + 15 of the tile's N-tile starting at grouped row row_b): W13 pairs
+// gate/up rows (adjacent lanes) into silu(g) * u and writes the bf16 activation; W2 writes the
+// fp32 expert outputs to their (token, rank) rows.
+template <bool MK>
+__device__ __forceinline__ void epi_store_chunk(const TcParams& p, const uint32_t (&r)[16], bool w13, int c0,
+                                                int n_valid, int m, int m_rows, int row_b, int lane) {
+    if (w13) {
+        // lanes 2i / 2i+1 hold the gate / up rows of output feature i
+        float own[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) own[j] = __uint_as_float(r[j]);
+        const bool odd = lane & 1;
+        const int feat = m >> 1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // even lane computes columns c0+j, odd lane columns c0+8+j
+            const float send = odd ? own[j] : own[j + 8];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float g = odd ? recv : own[j];
+            const float uu = odd ? own[j + 8] : recv;
+            const int n = c0 + (odd ? 8 + j : j);
+            if (n < n_valid && m < m_rows) {
+                const float a = g / (1.f + __expf(-g)) * uu;
+                p.act[(int64_t)(row_b + n) * p.act_ld + feat] = __float2bfloat16_rn(a);
+            }
+        }
+    } else {
+        // the chunk's 16 (token, rank) pairs: one load per lane, then broadcast
+        const int my_pair = (lane < 16 && c0 + lane < n_valid) ? ldr<MK>(p.pairs + row_b + c0 + lane) : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int n = c0 + j;
+            const int pair = __shfl_sync(0xffffffffu, my_pair, j);
+            if (n < n_valid && m < m_rows) p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
+        }
+    }
+}
+
 template <int BN, bool MK>
 __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     TcParams p, TcMega mg, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
@@ -480,36 +519,7 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                     tmem_ld16(tbase + a0 + c0 + CSTEP, la);
                     if (two) tmem_ld16(tbase + BN + c0 + CSTEP, lb);
                 }
-                if (w13) {
-                    // lanes 2i / 2i+1 hold the gate / up rows of output feature i
-                    float own[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) own[j] = __uint_as_float(r[j]);
-                    const bool odd = lane & 1;
-                    const int feat = m >> 1;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        // even lane computes columns c0+j, odd lane columns c0+8+j
-                        const float send = odd ? own[j] : own[j + 8];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                        const float g = odd ? recv : own[j];
-                        const float uu = odd ? own[j + 8] : recv;
-                        const int n = c0 + (odd ? 8 + j : j);
-                        if (n < n_valid && m < m_rows) {
-                            const float a = g / (1.f + __expf(-g)) * uu;
-                            p.act[(int64_t)(row_b + n) * p.act_ld + feat] = __float2bfloat16_rn(a);
-                        }
-                    }
-                } else {
-                    // the chunk's 16 (token, rank) pairs: one load per lane, then broadcast
-                    const int my_pair = (lane < 16 && c0 + lane < n_valid) ? ldr<MK>(p.pairs + row_b + c0 + lane) : 0;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = c0 + j;
-                        const int pair = __shfl_sync(0xffffffffu, my_pair, j);
-                        if (n < n_valid && m < m_rows) p.y[(int64_t)pair * p.y_ld + m] = __uint_as_float(r[j]);
-                    }
-                }
+                epi_store_chunk<MK>(p, r, w13, c0, n_valid, m, m_rows, row_b, lane);
             }
             tc_fence_before();
             if (w13 && fused) {
@@ -540,6 +550,296 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
         // combine, once every W2 tile quarter of the call is written
         mk_combine(mg, p.y, p.y_ld, H, 4 * m2 * nt_total, err, deadline, s_tmem + 2);
         report();
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Prefill tiles on CTA pairs. A 128 x 256 tile needs 48 KB of shared-memory stages per 4 MMAs
+// (16 KB of weights, 32 KB of token rows), and 148 SMs streaming that from L2 run the MMAs at
+// about two thirds of their rate. Here a cluster of two CTAs takes two adjacent 128-row weight
+// tiles of the same N-tile as one 256 x 256 tile: each CTA loads its own 128 weight rows and
+// half of the token rows (32 KB per stage), and the even CTA issues tcgen05.mma.cta_group::2,
+// which reads the A rows and the B halves of both CTAs and leaves each CTA's 128 accumulator
+// rows in its own tensor memory.
+//
+//   warp 0      producer A: the even CTA claims pair tiles from the launch's counter and hands
+//               each id to the odd CTA (shared-memory store + release arrive across the
+//               cluster); both load their weight rows; every load of the pair completes on
+//               the even CTA's stage barrier, which expects the pair's bytes
+//   warp 1      (even CTA) MMA issuer: M = 256, N = the tile's token count rounded up to 64,
+//               128 or 256;
+//               commits arrive on both CTAs' barriers (stage free, accumulator full)
+//   warps 2..5, 7..10  epilogue of this CTA's 128 rows, as in tc_ffn_kernel; it reports the
+//               accumulator drained to the even CTA
+//   warp 6      producer B: this CTA's half of the token rows (rows from rank * N / 2)
+//
+// Barriers that the other CTA arrives on are waited with cluster-scope acquire; all waits are
+// bounded. Both CTAs meet at a cluster barrier before either frees its tensor memory or exits.
+constexpr int kPairBN = 256;
+constexpr int kPairStages = 6;
+constexpr int kPairThreads = 352;
+
+// N of a pair MMA for a tile of n valid token rows: 64, 128 or 256 (each CTA supplies N / 2).
+__device__ __forceinline__ int pair_n(int n) { return n <= 64 ? 64 : n <= 128 ? 128 : 256; }
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1) tc_pair_kernel(
+    TcParams p, const __grid_constant__ CUtensorMap tmA13, const __grid_constant__ CUtensorMap tmB13,
+    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2) {
+    constexpr int BN = kPairBN, S = kPairStages, NE = 8;
+    constexpr int A_BYTES = kBM * kBK * 2;            // this CTA's 128 weight rows: 16 KB
+    constexpr int B_BYTES = (BN / 2) * kBK * 2;       // this CTA's half of the token rows: 16 KB
+    constexpr int STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators of 256 columns
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);   // used in the even CTA
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;       // [2]
+    uint64_t* tempty = tfull + 2;      // [2] used in the even CTA
+    uint64_t* tq_full = tempty + 2;    // [kTQ]
+    uint64_t* tq_empty = tq_full + kTQ;   // [kTQ] used in the even CTA
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tq_empty + kTQ);
+    int* s_tile = reinterpret_cast<int*>(s_tmem + 4);  // [kTQ]
+    int* s_nt = s_tile + kTQ;                          // [kMaxExperts + 1]
+    int* s_off = s_nt + (kMaxExperts + 1);             // [kMaxExperts + 1]
+    int* s_dst = s_off + (kMaxExperts + 1);            // [kMaxExperts]
+    uint8_t* s_rdy = reinterpret_cast<uint8_t*>(s_dst + kMaxExperts);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool lead = rank == 0;
+    int* err = p.err;
+    // both CTAs read the same routing, so both leave here or neither does
+    const RouteCounts rc = *p.counts;
+    int u_begin = 0, u_end = rc.n_unique;
+    pass_range(p.pass, rc, p.miss_lo, p.miss_hi, &u_begin, &u_end);
+    const int n_entries = u_end - u_begin;
+    if (n_entries <= 0) return;
+    const int H = p.hidden, I = p.inter;
+    const int m13 = (2 * I) / kBM, m2 = H / kBM;      // both even (checked by the launcher)
+    const bool fused = p.dep != nullptr;
+
+    for (int i = threadIdx.x; i <= n_entries; i += blockDim.x) s_off[i] = p.entry_off[u_begin + i];
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) s_dst[i] = p.entry_dst[u_begin + i];
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) s_rdy[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) s_nt[i] = (s_off[i + 1] - s_off[i] + BN - 1) / BN;
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (n_entries + 31) / 32;
+        const int i0 = lane * per, i1 = min(n_entries, i0 + per);
+        int local = 0;
+        for (int i = i0; i < i1; ++i) local += s_nt[i];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int i = i0; i < i1; ++i) { const int t = s_nt[i]; s_nt[i] = run; run += t; }
+        if (lane == 31) s_nt[n_entries] = incl;
+    }
+    if (warp == 0 && lane == 0) {
+        // the even CTA's stage barrier: one arrive (its producer A, expecting both CTAs' bytes)
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 2 * NE); }
+        // tile-id slot consumers of both CTAs: the odd CTA's producer A, both producers B, the
+        // MMA issuer, both CTAs' epilogue warps
+        for (int a = 0; a < kTQ; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], 1 + 2 + 1 + 2 * NE); }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(s_tmem)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                // the other CTA's barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int nt_total = s_nt[n_entries];
+    const int total = (m13 + m2) * nt_total;          // 128-row tiles (W13 then W2)
+    const int total_pairs = total / 2;
+    auto tile = [&](int t) -> Tile { return tile_at(t, s_nt, n_entries, u_begin, m13, m2, 3); };
+    // arrive on a barrier of the even CTA
+    auto arrive_lead = [&](uint64_t* bar) {
+        if (lead) mbar_arrive(bar);
+        else mbar_arrive_cluster(cluster_addr(bar, 0));
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const bool ahead = total_pairs >= 8 * (int)(gridDim.x / 2);
+            int next = (lead && ahead) ? atomicAdd(p.tile_ctr, 1) : 0;
+            uint32_t it = 0;
+            Ring rg;
+            bool ok = true;
+            for (uint32_t q = 0; ok; ++q) {
+                const int ts = (int)(q % kTQ);
+                int tp = -1;
+                if (lead) {
+                    if (!mbar_wait_cluster(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, err, 7)) { ok = false; break; }
+                    int claimed;
+                    if (ahead) {
+                        claimed = next;
+                        if (claimed < total_pairs) next = atomicAdd(p.tile_ctr, 1);
+                    } else {
+                        claimed = atomicAdd(p.tile_ctr, 1);
+                    }
+                    tp = claimed < total_pairs ? claimed : -1;
+                    s_tile[ts] = tp;
+                    st_cluster_u32(cluster_addr(&s_tile[ts], 1), tp);
+                    mbar_arrive(&tq_full[ts]);
+                    mbar_arrive_cluster(cluster_addr(&tq_full[ts], 1));
+                } else {
+                    if (!mbar_wait_cluster(&tq_full[ts], (q / kTQ) & 1u, err, 7)) { ok = false; break; }
+                    tp = s_tile[ts];
+                    mbar_arrive_cluster(cluster_addr(&tq_empty[ts], 0));
+                }
+                if (tp < 0) break;
+                const Tile tl = tile(2 * tp + (int)rank);
+                const bool w13 = tl.phase == 13;
+                const CUtensorMap* mA = w13 ? &tmA13 : &tmA2;
+                const int k_steps = (w13 ? H : I) / kBK;
+                const int slot = s_dst[tl.ent_rel];
+                for (int kb = 0; kb < k_steps; ++kb, ++it, rg.next(S)) {
+                    if (!mbar_wait(&empty[rg.s], rg.ph ^ 1u, err, 1)) { ok = false; break; }
+                    if (lead) mbar_expect_tx(&full[rg.s], 2 * STAGE);
+                    tma_load_3d_pair(smem + rg.s * STAGE, mA, cluster_addr(&full[rg.s], 0), kb * kBK, tl.mt * kBM, slot);
+                }
+            }
+            // the last stages' releases (commits of the even CTA's MMAs) arrive on this CTA's
+            // barriers: they must have landed before the CTA leaves
+            for (uint32_t j = (it > (uint32_t)S ? it - S : 0); j < it; ++j)
+                mbar_wait(&empty[j % S], (j / S) & 1u, err, 11);
+            if (!ok) __nanosleep(20000);   // copies in flight after a failed wait land first
+        }
+    } else if (warp == 6) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            Ring rg;
+            bool ok = true;
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const int ts = (int)(tcount % kTQ);
+                if (!mbar_wait_cluster(&tq_full[ts], (tcount / kTQ) & 1u, err, 10)) { ok = false; break; }
+                const int tp = s_tile[ts];
+                arrive_lead(&tq_empty[ts]);
+                if (tp < 0) break;
+                const Tile tl = tile(2 * tp + (int)rank);
+                const bool w13 = tl.phase == 13;
+                const CUtensorMap* mB = w13 ? &tmB13 : &tmB2;
+                const int k_steps = (w13 ? H : I) / kBK;
+                const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
+                const int n_valid = min(BN, s_off[tl.ent_rel + 1] - row_b);
+                const int row_h = row_b + (int)rank * (pair_n(n_valid) / 2);
+                bool ready = true;
+                if (!w13 && fused && !s_rdy[tl.ent_rel]) {
+                    const int target = NE * m13 * (s_nt[tl.ent_rel + 1] - s_nt[tl.ent_rel]);
+                    if (ld_acquire(p.dep + tl.u) < target) ready = wait_dep(p.dep + tl.u, target, err);
+                    if (ready) s_rdy[tl.ent_rel] = 1;
+                }
+                fence_proxy_async_global();
+                for (int kb = 0; kb < k_steps; ++kb, ++it, rg.next(S)) {
+                    if (!mbar_wait(&empty[rg.s], rg.ph ^ 1u, err, 1)) { ok = false; break; }
+                    tma_load_2d_pair(smem + rg.s * STAGE + A_BYTES, mB, cluster_addr(&full[rg.s], 0), kb * kBK, row_h);
+                }
+                if (!ready) ok = false;
+            }
+            if (!ok) __nanosleep(20000);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && lead) {
+            const uint64_t dA0 = smem_desc_sw128(smem_u32(smem));
+            const uint64_t dB0 = dA0 + (uint64_t)(A_BYTES >> 4);
+            Ring rg;
+            uint64_t so = 0;
+            bool ok = true;
+            for (uint32_t tcount = 0; ok; ++tcount) {
+                const int ts = (int)(tcount % kTQ);
+                if (!mbar_wait(&tq_full[ts], (tcount / kTQ) & 1u, err, 8)) break;
+                const int tp = s_tile[ts];
+                mbar_arrive(&tq_empty[ts]);
+                if (tp < 0) break;
+                const Tile tl = tile(2 * tp);
+                const int k_steps = (tl.phase == 13 ? H : I) / kBK;
+                const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
+                const int n_valid = min(BN, s_off[tl.ent_rel + 1] - row_b);
+                const uint32_t idesc = idesc_bf16_mn(2 * kBM, pair_n(n_valid));
+                const uint32_t acc = tcount & 1u;
+                if (!mbar_wait_cluster(&tempty[acc], ((tcount >> 1) & 1u) ^ 1u, err, 2)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < k_steps; ++kb) {
+                    if (!mbar_wait(&full[rg.s], rg.ph, err, 3)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t kd = so + (uint64_t)(kk * 2);
+                        mma_bf16_pair(d_tmem, dA0 + kd, dB0 + kd, idesc, (kb | kk) ? 1u : 0u);
+                    }
+                    mma_commit_pair(&empty[rg.s]);
+                    rg.next(S);
+                    so = rg.s == 0 ? 0 : so + (uint64_t)(STAGE >> 4);
+                }
+                if (!ok) break;
+                mma_commit_pair(&tfull[acc]);
+            }
+        }
+    } else if ((warp >= 2 && warp <= 5) || (warp >= 7 && warp <= 10)) {
+        const int q = warp & 3;
+        const int g = warp >= 7 ? 1 : 0;
+        constexpr int CSTEP = 32;
+        const int row_in_tile = q * 32 + lane;
+        for (uint32_t tcount = 0;; ++tcount) {
+            const int ts = (int)(tcount % kTQ);
+            if (!mbar_wait_cluster(&tq_full[ts], (tcount / kTQ) & 1u, err, 9)) break;
+            const int tp = s_tile[ts];
+            __syncwarp();
+            if (lane == 0) arrive_lead(&tq_empty[ts]);
+            if (tp < 0) break;
+            const Tile tl = tile(2 * tp + (int)rank);
+            const bool w13 = tl.phase == 13;
+            const int m_rows = w13 ? 2 * I : H;
+            const int row_b = s_off[tl.ent_rel] + tl.nt * BN;
+            const int n_valid = min(BN, s_off[tl.ent_rel + 1] - row_b);
+            const uint32_t acc = tcount & 1u;
+            if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1u, err, 4)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            const int m = tl.mt * kBM + row_in_tile;
+            uint32_t la[16];
+            const int cfirst = g * 16;
+            if (cfirst < n_valid) tmem_ld16(tbase + cfirst, la);
+#pragma unroll 1
+            for (int c0 = cfirst; c0 < n_valid; c0 += CSTEP) {
+                uint32_t r[16];
+                tmem_wait_ld_regs(la);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) r[j] = la[j];
+                if (c0 + CSTEP < n_valid) tmem_ld16(tbase + c0 + CSTEP, la);
+                epi_store_chunk<false>(p, r, w13, c0, n_valid, m, m_rows, row_b, lane);
+            }
+            tc_fence_before();
+            if (w13 && fused) {
+                // publish this warp's activation rows to the entry's W2 tiles (TMA readers)
+                __threadfence();
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.dep + tl.u, 1);
+            }
+            __syncwarp();
+            if (lane == 0) arrive_lead(&tempty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "r"(TMEM_COLS) : "memory");
     }
 }
 
@@ -719,6 +1019,22 @@ cudaError_t tc_launch_mega(int bn, const TcParams& p, const TcMega& mg, const Tc
     if (bn == 16) return launch_mega<16>(p, mg, m, grid, s);
     if (bn == 32) return launch_mega<32>(p, mg, m, grid, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_launch_pair(const TcParams& p, const TcMaps& m, int grid, cudaStream_t s) {
+    if (!p.tile_ctr || !p.dep || p.hidden % (2 * tc::kBM) || (2 * p.inter) % (2 * tc::kBM) || grid < 2)
+        return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)tc::kPairStages * (2 * tc::kBM * tc::kBK * 2) +
+                        (2 * tc::kPairStages + 4 + 2 * tc::kTQ) * 8 + 16 + tc::kTQ * 4 + 3 * (kMaxExperts + 1) * 4 +
+                        kMaxExperts;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc::tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    tc::tc_pair_kernel<<<grid & ~1, tc::kPairThreads, smem, s>>>(p, *m.a13, *m.b13, *m.a2, *m.b2);
+    return cudaGetLastError();
 }
 
 int tc_mega_grid(int bn, int num_sms) {

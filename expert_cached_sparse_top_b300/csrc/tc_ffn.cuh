@@ -77,6 +77,9 @@ cudaError_t tc_encode_weights(CUtensorMap* map, const void* base, int k_dim, int
                               int64_t n_slots, int64_t blob_bytes);
 cudaError_t tc_encode_acts(CUtensorMap* map, const void* base, int k_dim, int rows, int box_rows);
 cudaError_t tc_launch(int bn, const TcParams& p, const TcMaps& m, int grid, cudaStream_t s);
+// prefill tiles (N = 256) on CTA pairs: W13 and W2 in one launch (p.dep set); H and 2I
+// multiples of 256; the B maps' boxes are 128 rows (each CTA loads half of a tile's rows)
+cudaError_t tc_launch_pair(const TcParams& p, const TcMaps& m, int grid, cudaStream_t s);
 // the fused decode call (BN = 16 or 32); grid = the number of CTAs that fit on the device
 cudaError_t tc_launch_mega(int bn, const TcParams& p, const TcMega& mg, const TcMaps& m, int grid,
                            cudaStream_t s);
