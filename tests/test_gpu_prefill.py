@@ -189,3 +189,27 @@ def test_prefill_errors(ft):
     assert cache.prefill_status(1, x, 16, out, logits=lg) == ft.FT_ERR_INVALID
     assert cache.prefill_status(0, x, 0, out, logits=lg) == ft.FT_OK
     cache.close()
+
+
+def test_prefill_bf16_pair_and_single_cta_kernels(ft, monkeypatch):
+    """The 4096-token 35B-A3B-shaped layer through the CTA-pair kernel (256 x 256 tiles over
+    two CTAs, the default) and through the one-CTA kernel (FTMOE_PAIR=0): both within the
+    normwise tolerance of the oracle on a token sample, and within it of each other."""
+    import torch
+    cfg = W.config("prefill_bf16", layers=1)
+    pool = HostPool(cfg, images=131)
+    experts = OracleExperts(pool, max_cached=131)
+    x, logits = W.prefill_inputs(cfg, 0)
+    outs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("FTMOE_PAIR", mode)
+        cache = _make(ft, cfg, pool, cfg.tokens)
+        outs[mode] = _run(cache, cfg, 0, x, logits).clone()
+        cache.close()
+    tokens = np.arange(0, cfg.tokens, 5)
+    ref, _, _ = oracle_call(experts, 0, x, logits, cfg.top_k, tokens=tokens)
+    for mode, out in outs.items():
+        assert out_err(bf16_dev_to_f64(out)[tokens], ref) <= TOL["bf16"], mode
+    a, b = bf16_dev_to_f64(outs["1"]), bf16_dev_to_f64(outs["0"])
+    assert out_err(a, b) <= TOL["bf16"]
+    assert torch.isfinite(outs["1"].float()).all()
