@@ -137,10 +137,13 @@ FLUSH_TEXT = {"write-read": "flushed (256 MB written, then read back) before eve
 class Clocks:
     """SM clocks, power and throttle reasons sampled during the timed region.
 
-    NVML (the library nvidia-smi reads) is polled from a thread every 2 ms, so even a timed
-    region of a few tens of milliseconds holds many samples; spawning nvidia-smi takes longer
-    than such a region. Each sample is also written to `path` as a CSV line. Falls back to an
-    `nvidia-smi -lms 50` process where NVML cannot be loaded."""
+    NVML (the library nvidia-smi reads) is polled from a thread every 10 ms, so a timed region
+    of a few tens of milliseconds still holds several samples; spawning nvidia-smi takes
+    longer than such a region. The power draw is read on every fifth sample only: each NVML
+    query takes a driver lock that the timed loop's CUDA calls also take, and at a 2 ms period
+    with every query the host loop ran up to 70 ms per 1 ms step on some boxes. Each sample is
+    also written to `path` as a CSV line. Falls back to an `nvidia-smi -lms 50` process where
+    NVML cannot be loaded."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -148,7 +151,7 @@ class Clocks:
     BITS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
             ("sw_power_cap", 0x4))
 
-    def __init__(self, index, path, period_s=0.002):
+    def __init__(self, index, path, period_s=0.010):
         import threading
         self.path = path
         self.proc = None
@@ -197,7 +200,9 @@ class Clocks:
         try:
             sm = float(nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM))
             rs = int(nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle))
-            pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+            if len(self.samples) % 5 == 0 or not hasattr(self, "pw"):
+                self.pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+            pw = self.pw
         except Exception:
             return
         self.samples.append((sm, rs))
@@ -217,7 +222,7 @@ class Clocks:
                 return None
             reasons = sorted({n for _, r in self.samples for n, b in self.BITS if r & b})
             return {"sm_mhz": float(np.median([sm for sm, _ in self.samples])), "sm_max_mhz": self.max_mhz,
-                    "reasons": reasons, "samples": len(self.samples), "source": "NVML, 2 ms period"}
+                    "reasons": reasons, "samples": len(self.samples), "source": "NVML, %d ms period" % round(self.period * 1e3)}
         if self.proc is None:
             return None
         self.proc.terminate()
