@@ -139,11 +139,9 @@ class Clocks:
 
     NVML (the library nvidia-smi reads) is polled from a thread every 10 ms, so a timed region
     of a few tens of milliseconds still holds several samples; spawning nvidia-smi takes
-    longer than such a region. The power draw is read on every fifth sample only: each NVML
-    query takes a driver lock that the timed loop's CUDA calls also take, and at a 2 ms period
-    with every query the host loop ran up to 70 ms per 1 ms step on some boxes. Each sample is
-    also written to `path` as a CSV line. Falls back to an `nvidia-smi -lms 50` process where
-    NVML cannot be loaded."""
+    longer than such a region. The power draw (the slowest query) is read on every fifth
+    sample. Each sample is also written to `path` as a CSV line. Falls back to an
+    `nvidia-smi -lms 50` process where NVML cannot be loaded."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -531,6 +529,9 @@ def decode_line(args):
         cache.timing(reset=True)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
+        # the flush's kernels are loaded on their first launch (about a second): not inside
+        # the timed loop's wall clock
+        l2_flush(flush, args.flush)
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize()

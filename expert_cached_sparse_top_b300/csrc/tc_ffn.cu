@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
     uint8_t* s_rdy = reinterpret_cast<uint8_t*>(s_dst + kMaxExperts);   // [kMaxExperts] W13 done, seen
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA13); prefetch_tmap(&tmB13); prefetch_tmap(&tmA2); prefetch_tmap(&tmB2);
+    }
     // the fused call's waits poll a device word (the host-mapped p.err would put a PCIe read
     // in every poll); thread 0 of each CTA copies a code to p.err as the CTA leaves
     int* err = MK ? mg.err_dev : p.err;
@@ -317,7 +320,10 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
             // others idle); with many (prefill) the next claim goes out as the current tile
             // starts, so its round trip overlaps the current tile's loads
             const bool ahead = total >= 8 * (int)gridDim.x;
-            int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
+            // every CTA's first tile is its own index (no round trip to the counter before
+            // the first load); the launch's counter hands out the rest
+            auto claim = [&]() { return atomicAdd(p.tile_ctr, 1) + (int)gridDim.x; };
+            int next = ahead ? claim() : 0;
             uint32_t it = 0;
             Ring rg;
             bool ok = true;
@@ -325,11 +331,13 @@ __global__ void __launch_bounds__(tc_block<BN, MK>(), 1) tc_ffn_kernel(
                 const int ts = (int)(q % kTQ);
                 if (!bar_wait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 7)) { ok = false; break; }
                 int claimed;
-                if (ahead) {
+                if (q == 0) {
+                    claimed = (int)blockIdx.x;
+                } else if (ahead) {
                     claimed = next;
-                    if (claimed < total) next = atomicAdd(p.tile_ctr, 1);
+                    if (claimed < total) next = claim();
                 } else {
-                    claimed = atomicAdd(p.tile_ctr, 1);
+                    claimed = claim();
                 }
                 const int t = claimed < total ? claimed : -1;
                 s_tile[ts] = t;
@@ -606,6 +614,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1) tc_
     uint8_t* s_rdy = reinterpret_cast<uint8_t*>(s_dst + kMaxExperts);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA13); prefetch_tmap(&tmB13); prefetch_tmap(&tmA2); prefetch_tmap(&tmB2);
+    }
     const uint32_t rank = cluster_rank();
     const bool lead = rank == 0;
     int* err = p.err;
@@ -672,7 +683,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1) tc_
     if (warp == 0) {
         if (lane == 0) {
             const bool ahead = total_pairs >= 8 * (int)(gridDim.x / 2);
-            int next = (lead && ahead) ? atomicAdd(p.tile_ctr, 1) : 0;
+            // every cluster's first pair tile is its own index; the counter hands out the rest
+            auto claim = [&]() { return atomicAdd(p.tile_ctr, 1) + (int)(gridDim.x / 2); };
+            int next = (lead && ahead) ? claim() : 0;
             uint32_t it = 0;
             Ring rg;
             bool ok = true;
@@ -682,11 +695,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1) tc_
                 if (lead) {
                     if (!mbar_wait_cluster(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, err, 7)) { ok = false; break; }
                     int claimed;
-                    if (ahead) {
+                    if (q == 0) {
+                        claimed = (int)(blockIdx.x / 2);
+                    } else if (ahead) {
                         claimed = next;
-                        if (claimed < total_pairs) next = atomicAdd(p.tile_ctr, 1);
+                        if (claimed < total_pairs) next = claim();
                     } else {
-                        claimed = atomicAdd(p.tile_ctr, 1);
+                        claimed = claim();
                     }
                     tp = claimed < total_pairs ? claimed : -1;
                     s_tile[ts] = tp;

@@ -320,6 +320,9 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                                                                            // readiness marks per entry
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA13); prefetch_tmap(&tmB13); prefetch_tmap(&tmA2); prefetch_tmap(&tmB2);
+    }
     // the fused call's waits poll a device word and run to a %globaltimer deadline
     int* err = MK ? mg.err_dev : p.err;
     uint64_t deadline = 0;
@@ -428,7 +431,10 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
             // many (prefill) claims the next tile as soon as it starts the current one, so the
             // claim's round trip to L2 overlaps the current tile's loads.
             const bool ahead = total >= 8 * (int)gridDim.x;
-            int next = ahead ? atomicAdd(p.tile_ctr, 1) : 0;
+            // every CTA's first tile is its own index (no round trip to the counter before
+            // the first load); the launch's counter hands out the rest
+            auto claim = [&]() { return atomicAdd(p.tile_ctr, 1) + (int)gridDim.x; };
+            int next = ahead ? claim() : 0;
             uint32_t it = 0;
             Ring rg;
             bool ok = true;
@@ -436,11 +442,13 @@ __global__ void __launch_bounds__(fp4_block<BN, FMT, P, MK>(), 1) fp4_ffn_kernel
                 const int ts = (int)(q % kTQ);
                 if (!bwait(&tq_empty[ts], ((q / kTQ) & 1u) ^ 1u, 8)) { ok = false; break; }
                 int claimed;
-                if (ahead) {
+                if (q == 0) {
+                    claimed = (int)blockIdx.x;
+                } else if (ahead) {
                     claimed = next;
-                    if (claimed < total) next = atomicAdd(p.tile_ctr, 1);
+                    if (claimed < total) next = claim();
                 } else {
-                    claimed = atomicAdd(p.tile_ctr, 1);
+                    claimed = claim();
                 }
                 const int t = claimed < total ? claimed : -1;
                 s_tile[ts] = t;

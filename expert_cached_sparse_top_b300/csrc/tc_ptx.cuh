@@ -91,6 +91,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
            "r"(c0), "r"(c1) : "memory");
 }
 
+// Fetch a tensor map (kernel parameter) into the descriptor cache ahead of its first TMA.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
