@@ -68,7 +68,7 @@ def replica_throughput(units_per_rank, seconds_per_rank, device="cpu"):
 
 
 class _CtypesNvml:
-    """The few read-only NVML queries the clock sampler makes, through ctypes on the driver's
+    """The few read-only NVML queries the clock sampler makes, through ctypes on the NVIDIA
     libnvidia-ml.so.1 (used where the pynvml module is not installed)."""
     NVML_CLOCK_SM = 1
 
