@@ -5,17 +5,20 @@
  * What the calls compute. The pages describing the edge-native MoE serving engine
  * ("Meet FreeToken: An Edge-Native MoE Serving Engine that Runs 753B GLM-5.2 on a Single
  * Workstation GPU", MarkTechPost) state the problem this library serves:
- *   - "The gap it targets": the expert pool does not fit the GPU, so inactive experts sit
- *     in host memory and enter the execution path on demand; prefill routes thousands of
- *     tokens to nearly every expert.
- *   - "Three mechanisms", semantic-aware caching: during decode one shared LRU expert cache
- *     spans all MoE layers and follows the router; during prefill, full layers are double
- *     buffered (layer l+1 streams while layer l computes).
- *   - "Three mechanisms", elastic memory management: experts are read into their final host
- *     layout and then pinned; the GPU cache is rebuilt under a revised VRAM budget at safe
- *     points without reloading the host pool; the first request is served cold.
- *   - "Key Takeaways": expert output is exact — no router changes, no expert substitution,
- *     no precision relaxation. Where an expert's bytes live never changes the result.
+ *   - "The gap it targets": all the experts together exceed GPU memory, so the ones not in
+ *     use wait in host memory and are brought in when a token is routed to them; a prefill
+ *     batch reaches almost every expert.
+ *   - "Three mechanisms", semantic-aware caching: in decode, a single LRU set of resident
+ *     experts serves every MoE layer and is driven by the router's choices; in prefill, two
+ *     whole-layer buffers alternate, the next layer's weights arriving while the current
+ *     one computes.
+ *   - "Three mechanisms", elastic memory management: each expert is laid out once in host
+ *     memory in the form the GPU copies, and that memory is page-locked; when the VRAM
+ *     budget changes, the GPU-side cache is rebuilt between calls with the host pool left
+ *     as it is; the first request starts from an empty cache.
+ *   - "Key Takeaways": caching changes where an expert's weights are read from, never what
+ *     the layer computes: the router's choice, the experts applied and the arithmetic's
+ *     precision are those of the model itself.
  * The CPU-side execution of misses (the pages' q* split) is not part of this library;
  * every miss is filled over PCIe and its bytes are reported in the statistics.
  *
@@ -362,7 +365,9 @@ FT_API ft_status ft_topk_softmax(const float* logits, int32_t T, int32_t E, int3
 #define FT_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* One expert's SwiGLU FFN, y = W2 (silu(W1 x) * (W3 x)), with no device allocation at all.
- * The pages have no counterpart to this call: it exists for callers that cannot allocate
+ * It computes what the routed layer computes for one expert (the expert step of the decode
+ * path in "Three mechanisms"), outside any cache. The pages have no counterpart to this
+ * call as such: it exists for callers that cannot allocate
  * device memory when they need an expert's output — an engine that has given its whole
  * VRAM budget to its own expert arena, a serving loop that forbids cudaMalloc/cudaFree
  * after start-up because they can stall or synchronise the device mid-step, or a host whose
