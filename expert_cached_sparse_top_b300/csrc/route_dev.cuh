@@ -3,9 +3,9 @@
 // warp), and the cache lookup + LRU update + pair grouping of one call (one CTA).
 //
 // Method: the router is left exactly as the model defines it ("Meet FreeToken: An
-// Edge-Native MoE Serving Engine ...", section "Key Takeaways": no router changes), and
-// the expert cache is one LRU over all MoE layers that follows the router (same page,
-// section "Three mechanisms", semantic-aware caching).
+// Edge-Native MoE Serving Engine ...", section "Key Takeaways": caching never alters what
+// the layer computes), and the expert cache is one LRU over all MoE layers that follows the
+// router (same page, section "Three mechanisms", semantic-aware caching).
 #pragma once
 #include "common.cuh"
 

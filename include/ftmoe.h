@@ -33,7 +33,7 @@
  *     it; ft_moe_last_error() returns the text.
  *   - A handle is not thread-safe: one host thread at a time.
  *
- * Expert blob layout (one contiguous blob per (layer, expert), the "final host layout";
+ * Expert blob layout (one contiguous blob per (layer, expert), as laid out in host memory;
  * each section starts on a 256-byte boundary, the blob size is rounded up to 256 bytes):
  *     section          BF16             MXFP4                  NVFP4
  *     s0 W13           [2I][H] bf16     [2I][H/2] E2M1 x2      [2I][H/2] E2M1 x2

@@ -2,10 +2,11 @@
 
 The pages name three weight precisions for the served models: BF16 (35B-A3B on the RTX
 5090), MXFP4 (DeepSeek-V4-Flash) and NVFP4 (35B on the 8 GB laptop GPU) ([MTP] §Results;
-[LN]). They also say experts are read "straight into their final host layout, then pinned"
-([MTP] §Three mechanisms, elastic memory management). The pages do not print a layout; the
-one decoded here is this library's own final host layout (one contiguous blob per expert,
-so that one DMA fills one cache slot):
+[LN]). They also say each expert is laid out in host memory once, in the form that is
+copied to the GPU, and that memory is page-locked ([MTP] §Three mechanisms, elastic
+memory management). The pages do not print a layout; the one decoded here is this
+library's own host layout (one contiguous blob per expert, so that one DMA fills one cache
+slot):
 
     section            BF16               MXFP4                 NVFP4
     s0  W13            [2I][H] bf16       [2I][H/2] E2M1 x2     [2I][H/2] E2M1 x2

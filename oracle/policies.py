@@ -1,8 +1,8 @@
 """The comparator cache policies of the pages' evaluation, as plain simulators.
 
-The pages compare the engine's global LRU ("a shared LRU expert cache spanning all MoE
-layers ... instead of a placement frozen at load time", [MTP] §Three mechanisms) with
-engines whose expert placement does not follow the router: llama.cpp assigns MoE tensors at
+The pages compare the engine's global LRU (one LRU set of experts over every MoE layer that
+moves with the router, where other engines fix placement when the model loads; [MTP]
+§Three mechanisms) with engines whose expert placement does not follow the router: llama.cpp assigns MoE tensors at
 load time, KTransformers pins a "hot" subset ([MTP] §The gap it targets), and reports their
 decode miss rates ([MTP] §Results). Readings taken where the pages leave it open:
 

@@ -103,7 +103,7 @@ def f32_to_bf16_bits(a):
 
 
 # ---------------------------------------------------------------------------------------
-# Blob layout (the library's final host layout; see include/ftmoe.h)
+# Blob layout (the library's host layout of an expert; see include/ftmoe.h)
 # ---------------------------------------------------------------------------------------
 def _up(n, a=256):
     return (n + a - 1) // a * a
