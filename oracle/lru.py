@@ -21,8 +21,8 @@ Readings taken where the pages are silent:
 * resize to C': keep the min(C', resident) most recently used keys, in order. A survivor
   whose slot is < C' keeps it; the others move, in ascending old-slot order, to the lowest
   free slots < C'. Growth only adds free slots.
-* layer-ahead prefetch (the engine's ft_cache_prefetch; the pages describe no such step, it
-  is the reading of "start a layer's fills once its experts are known" taken here): a
+* layer-ahead prefetch (the engine's ft_cache_prefetch; the pages describe no such step:
+  the reading taken here starts a layer's fills as soon as its experts are predicted): a
   prefetch of ``layer`` with a predicted expert set S' inserts each non-resident key of S',
   in ascending expert order, exactly as a miss would (lowest free slot, else the least
   recently used key outside S'), at the MRU end; keys of S' already resident are left where
