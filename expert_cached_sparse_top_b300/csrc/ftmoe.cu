@@ -135,6 +135,9 @@ struct ft_moe {
     uint8_t* d_xq = nullptr;              // W13 activation pieces (codes), tile-major
     uint8_t* d_xsf = nullptr;             // their scale atoms
     float* d_xrs = nullptr;               // their row scales
+    uint8_t* d_tq = nullptr;              // decode: every token's pieces once, codes [T][P][H/2],
+    uint8_t* d_tsf = nullptr;             // their scale atoms (row t * P + pc)
+    float* d_trs = nullptr;               // and row scales [T], gathered into the tiles per call
     uint8_t* d_aq = nullptr;              // W2 activation pieces and scale atoms
     uint8_t* d_asf = nullptr;
     CUtensorMap tmF_A13{}, tmF_A2{}, tmF_B13{}, tmF_B2{};
@@ -409,6 +412,7 @@ void free_all(ft_moe* h) {
     cudaFree(h->d_w); cudaFree(h->d_nan); cudaFree(h->d_route_mem); cudaFree(h->d_act);
     cudaFree(h->d_y); cudaFree(h->d_xp);
     cudaFree(h->d_xq); cudaFree(h->d_xsf); cudaFree(h->d_xrs);
+    cudaFree(h->d_tq); cudaFree(h->d_tsf); cudaFree(h->d_trs);
     cudaFree(h->d_aq); cudaFree(h->d_asf);
     cudaFree(h->d_layerbuf[0]); cudaFree(h->d_layerbuf[1]); cudaFree(h->d_p_logits);
     cudaFree(h->d_p_idx); cudaFree(h->d_p_w); cudaFree(h->d_p_chunk); cudaFree(h->d_p_err);
@@ -1033,6 +1037,14 @@ ft_status ft_moe_create(const ft_moe_config* cfg, const void* const* expert_blob
         if (!dmalloc((void**)&h->d_xq, xq) || !dmalloc((void**)&h->d_aq, aq) ||
             !dmalloc((void**)&h->d_xsf, xsf) || !dmalloc((void**)&h->d_asf, asf) ||
             !dmalloc((void**)&h->d_xrs, rs)) return bail(FT_ERR_OOM);
+        {
+            const int64_t Tm = cfg->max_tokens;
+            const int bs = cfg->wfmt == FT_W_MXFP4 ? 32 : 16;
+            const int64_t bands = (Tm * P + 127) / 128;
+            if (!dmalloc((void**)&h->d_tq, (size_t)Tm * P * (H / 2)) ||
+                !dmalloc((void**)&h->d_tsf, (size_t)bands * (H / bs / 4) * 512) ||
+                !dmalloc((void**)&h->d_trs, (size_t)Tm * 4)) return bail(FT_ERR_OOM);
+        }
         // rows of a tile past its last token are read by the MMA and ignored; start them at zero
         if (cudaMemset(h->d_xq, 0, xq) != cudaSuccess || cudaMemset(h->d_aq, 0, aq) != cudaSuccess ||
             cudaMemset(h->d_xsf, 0, xsf) != cudaSuccess || cudaMemset(h->d_asf, 0, asf) != cudaSuccess ||
@@ -1441,6 +1453,14 @@ ft_status ft_moe_forward(ft_moe* h, int32_t layer, const void* x, int32_t T, con
         f4.cnt_x = h->rb.dep_x;
         f4.cnt_w13 = h->rb.dep;
         f4.err = h->d_ffn_err;
+        // every token split once into its pieces, then the call's routed rows gathered into
+        // the tiles of both passes (as the BF16 path gathers its rows here), so the FFN
+        // launches start on ready activations
+        FT_CUDA(h, fp4_split_tokens(c.wfmt, (const __nv_bfloat16*)x, T, H, h->d_tq, h->d_tsf, h->d_trs, s));
+        FT_CUDA(h, fp4_gather_tiles(c.wfmt, h->rb.counts, h->rb.entry_off, h->rb.pairs, k, H, h->fp4_bn, h->d_tq,
+                                    h->d_tsf, h->d_trs, h->d_xq, h->d_xsf, h->d_xrs, T * k, s));
+        launches += 2;
+        f4.x_ready = 1;
     }
     // pass: see pass_range; ctr: which pair of the call's tile-claim counters the launch uses;
     // lo, hi: the group of misses of pass 3
