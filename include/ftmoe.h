@@ -52,11 +52,11 @@
  *   The expert computes y = W2 (silu(W1 x) * (W3 x)) with fp32 accumulation; the SwiGLU
  *   activation is rounded to bf16 before W2, the combined output to bf16.
  *   FP4 weights feed the block-scaled tensor-core MMA as stored (E2M1 codes plus the scale
- *   atoms above). In ft_moe_forward the bf16 activations enter that MMA as four E2M1 pieces
- *   with power-of-two block scales, whose sum carries the bf16 value (the error stays below
- *   the bf16 rounding of the SwiGLU activation). In ft_moe_prefill with MXFP4 weights, the
- *   activations (x and the bf16 SwiGLU activation) are quantised to MXFP4 (E8M0 exponent
- *   floor(log2 max) - 2 per 32, round to nearest even, saturating at +-6): a W4A4 product.
+ *   atoms above). In ft_moe_forward and ft_moe_prefill the bf16 activations (x and the bf16
+ *   SwiGLU activation) enter that MMA as four E2M1 pieces with power-of-two block scales,
+ *   whose sum carries the bf16 value (the error stays below the bf16 rounding of the SwiGLU
+ *   activation); each token is split once per call and its pieces gathered into the tiles
+ *   (the fused decode call splits its routed rows inside its one launch).
  *   For NVFP4 the SwiGLU pieces' scales are powers of two within E4M3's range: SwiGLU
  *   magnitudes beyond ~1500 saturate. Setting FTMOE_FFN=simt selects the CUDA-core FFN, which
  *   dequantises FP4 weights exactly and keeps bf16 activations.
@@ -164,7 +164,8 @@ typedef struct {
  * stream each stage runs on (ft_moe_set_timing(h, 1) enables recording). */
 typedef struct {
     double route_ms;      /* router logits (if computed) + top-k + cache lookup/permute
-                             (+ the BF16 path's activation-row gather) */
+                             (+ the BF16 path's activation-row gather, or the FP4 path's
+                             token split into pieces and their gather into tiles) */
     double ffn_hit_ms;    /* expert FFN kernel over entries resident at call start */
     double fill_ms;       /* H2D miss copies on the copy stream */
     double ffn_miss_ms;   /* expert FFN over filled / staged entries */
