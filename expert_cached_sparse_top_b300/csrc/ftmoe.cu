@@ -842,8 +842,8 @@ ft_status alloc_prefill(ft_moe* h) {
     FT_CUDA(h, dm((void**)&h->d_p_y, (size_t)npairs * H * 4));
     h->use_fp4_prefill = h->use_fp4;
     if (h->use_fp4_prefill) {
-        // bf16-accurate activations as four E2M1 pieces, as in decode: 32-token tiles, 128
-        // N-operand rows per tile (token-major pieces)
+        // bf16-accurate activations as four E2M1 pieces, as in decode: tiles of 56 (MXFP4) or
+        // 48 (NVFP4) tokens, 224 or 192 N-operand rows (token-major pieces)
         const int bn = fp4_prefill_bn(c.wfmt), P = kFp4MaxPieces;
         h->p_fp4_tiles = E + (npairs + bn - 1) / bn;
         const size_t xq = fp4_piece_bytes(h->p_fp4_tiles, P, bn, (int)H);
