@@ -47,3 +47,52 @@ def test_clocks_path_takes_the_rank():
     assert bench.clocks_path(a, 3) == "out/clocks.csv"
     a = argparse.Namespace(clocks_csv=None)
     assert bench.clocks_path(a, 1).endswith("ftmoe_clocks_r1.csv")
+
+
+def test_traffic_summaries_match_the_current_kernels():
+    """The committed DRAM-traffic summaries were captured on the kernels as they are now (a
+    kernel change voids them: the bench then reports no traffic until they are recaptured)."""
+    for wfmt in ("bf16", "mxfp4", "nvfp4"):
+        assert bench.traffic_ratio(wfmt) is not None, wfmt
+
+
+def test_l2_flush_writes_the_whole_buffer_in_every_mode():
+    import torch
+    for mode in bench.FLUSH_MODES:
+        buf = torch.full((4096,), 7, dtype=torch.uint8)
+        bench.l2_flush(buf, mode)
+        assert int(buf.sum()) == 0
+        assert mode in bench.FLUSH_TEXT
+
+
+def _bench(*args, timeout=240):
+    import subprocess
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_warmup_below_three_is_refused():
+    r = _bench("--impl", "reference", "--steps", "1", "--warmup", "2", timeout=120)
+    assert r.returncode != 0 and "--warmup must be >= 3" in r.stderr
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm is the oracle as it stands, timed on the host cores: one JSON line with
+    the headline's metric and unit, an end-to-end block without device copies and a
+    cpu_baseline that says what it timed."""
+    import json
+    r = _bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.DECODE[bench.WORKLOAD][0]
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == bench.WORKLOAD
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
